@@ -1,0 +1,175 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
+
+This module holds none of the attention arithmetic: it draws random numbers,
+rounds them to bf16 bit patterns and builds packed-sequence offsets.  The same
+bits are uploaded to the GPU and widened to fp64 for the oracle, so both sides
+see identical inputs.
+
+Seed recipe: tensor seed = 1000 * workload + 10 * variant + tensor index, with
+tensor index Q=0, K=1, V=2, dO=3, sinks=4, lengths=5.  Every draw uses numpy's
+``Generator(PCG64(seed))``.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+Q, K, V, DO, SINKS, LENGTHS = range(6)
+
+
+def seed_of(workload: int, variant: int, tensor: int) -> int:
+    return 1000 * workload + 10 * variant + tensor
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def bf16_bits(x) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest, ties to even); returns uint16 bit patterns."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = (u + 0x7FFF + lsb) >> 16
+    return r.astype(np.uint16)
+
+
+def bf16_to_f32(bits) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    return bf16_to_f32(bits).astype(np.float64)
+
+
+def normal_bf16(seed: int, shape) -> np.ndarray:
+    """i.i.d. N(0, 1) draws in fp32, rounded to bf16 bit patterns."""
+    return bf16_bits(rng(seed).standard_normal(size=shape, dtype=np.float32))
+
+
+def normal_f32(seed: int, shape) -> np.ndarray:
+    return rng(seed).standard_normal(size=shape, dtype=np.float32)
+
+
+def varlen_lengths(seed: int, n: int = 256, total: int = 32768, median: float = 64.0,
+                   sigma: float = 1.5, zero_frac: float = 0.10) -> np.ndarray:
+    """Packed-batch sequence lengths.
+
+    Log-normal draws (median ``median``, log-sd ``sigma``); round(zero_frac * n)
+    slots, picked by a seeded permutation, are forced to 0; the rest are scaled
+    to sum to ``total``, floored, clamped to at least 1, and the remainder goes
+    to the largest fractional parts (taken back from the smallest fractional
+    parts if the clamp overshot).
+    """
+    g = rng(seed)
+    raw = g.lognormal(mean=math.log(median), sigma=sigma, size=n)
+    n_zero = int(round(zero_frac * n))
+    zero_idx = g.permutation(n)[:n_zero]
+    keep = np.ones(n, bool)
+    keep[zero_idx] = False
+    lengths = np.zeros(n, np.int64)
+    idx = np.nonzero(keep)[0]
+    if len(idx) == 0:
+        if total != 0:
+            raise ValueError("no non-empty slot to hold the tokens")
+        return lengths.astype(np.int32)
+    scaled = raw[idx] * (total / raw[idx].sum())
+    fl = np.maximum(np.floor(scaled).astype(np.int64), 1)
+    frac = scaled - np.floor(scaled)
+    rem = total - int(fl.sum())
+    if rem > 0:
+        order = np.argsort(-frac, kind="stable")
+        fl[order[:rem]] += 1
+    elif rem < 0:
+        order = np.argsort(frac, kind="stable")
+        for t in order:
+            if rem == 0:
+                break
+            if fl[t] > 1:
+                fl[t] -= 1
+                rem += 1
+    lengths[idx] = fl
+    assert int(lengths.sum()) == total
+    return lengths.astype(np.int32)
+
+
+def cu_seqlens(lengths) -> np.ndarray:
+    """int32 offsets [N+1] from 0 to the token count."""
+    lengths = np.asarray(lengths, dtype=np.int64)
+    cu = np.zeros(len(lengths) + 1, np.int64)
+    cu[1:] = np.cumsum(lengths)
+    return cu.astype(np.int32)
+
+
+# ----------------------------------------------------------------------------------------------
+# The workloads.  Each is a dict of problem sizes; ``make`` draws its tensors.
+# ----------------------------------------------------------------------------------------------
+
+def workload(name: str, **over) -> dict:
+    """Problem sizes of a named workload (keyword overrides allowed)."""
+    w = dict(WORKLOADS[name])
+    w.update(over)
+    w.setdefault("name", name)
+    return w
+
+
+WORKLOADS = {
+    # tiny forward+backward
+    "tiny": dict(wid=1, B=1, s_q=128, s_kv=128, h_q=2, h_kv=2, d=64, causal=False,
+                 window=(-1, -1), sinks=False, varlen=False),
+    "tiny_causal": dict(wid=1, variant=1, B=1, s_q=128, s_kv=128, h_q=2, h_kv=2, d=64,
+                        causal=True, window=(-1, -1), sinks=False, varlen=False),
+    # dense sweep (fixed 16k tokens); the headline is s=8192 causal
+    **{f"sweep_s{s}{'_causal' if c else ''}": dict(
+        wid=2, variant=(2 * i + (1 if c else 0)), B=16384 // s, s_q=s, s_kv=s, h_q=16, h_kv=16,
+        d=128, causal=c, window=(-1, -1), sinks=False, varlen=False)
+       for i, s in enumerate((512, 1024, 2048, 4096, 8192, 16384)) for c in (False, True)},
+    # grouped-query heads with sliding windows and sinks
+    "gqa_window_causal": dict(wid=3, variant=0, B=2, s_q=4096, s_kv=4096, h_q=64, h_kv=8, d=64,
+                              causal=True, window=(127, 0), sinks=True, varlen=False),
+    "gqa_window_2sided": dict(wid=3, variant=1, B=2, s_q=4096, s_kv=4096, h_q=64, h_kv=8, d=64,
+                              causal=False, window=(128, 128), sinks=True, varlen=False),
+    # packed varlen
+    "varlen": dict(wid=4, variant=0, B=256, T=32768, h_q=32, h_kv=32, d=128, causal=True,
+                   window=(-1, -1), sinks=False, varlen=True),
+    # decode / chunked prefill against a long cache
+    **{f"decode_d{d}_sq{sq}": dict(wid=5, variant=(0 if d == 128 else 2) + (0 if sq == 1 else 1),
+                                   B=64, s_q=sq, s_kv=32768, h_q=32, h_kv=8, d=d, causal=True,
+                                   window=(-1, -1), sinks=False, varlen=False)
+       for d in (128, 256) for sq in (1, 64)},
+}
+
+
+def make(w: dict) -> dict:
+    """Draw the bf16 bit patterns (uint16) and side inputs of workload ``w``.
+
+    Returns q, k, v, dout (uint16, [B,S,H,D] or packed [T,H,D]), sinks (fp32 or
+    None), cu_q / cu_k (int32 or None), and the sizes.
+    """
+    wid, var = w["wid"], w.get("variant", 0)
+    h_q, h_kv, d = w["h_q"], w["h_kv"], w["d"]
+    out = dict(w)
+    if w.get("varlen"):
+        if "lengths" in w:
+            lq = np.asarray(w["lengths"], np.int32)
+            lk = np.asarray(w.get("lengths_k", lq), np.int32)
+        else:
+            lq = varlen_lengths(seed_of(wid, var, LENGTHS), n=w["B"], total=w["T"])
+            lk = lq
+        cu_q, cu_k = cu_seqlens(lq), cu_seqlens(lk)
+        Tq, Tk = int(cu_q[-1]), int(cu_k[-1])
+        qshape, kshape = (Tq, h_q, d), (Tk, h_kv, d)
+        out.update(cu_q=cu_q, cu_k=cu_k, B=len(lq), s_q=Tq, s_kv=Tk)
+    else:
+        qshape = (w["B"], w["s_q"], h_q, d)
+        kshape = (w["B"], w["s_kv"], h_kv, d)
+        out.update(cu_q=None, cu_k=None)
+    out["q"] = normal_bf16(seed_of(wid, var, Q), qshape)
+    out["k"] = normal_bf16(seed_of(wid, var, K), kshape)
+    out["v"] = normal_bf16(seed_of(wid, var, V), kshape)
+    out["dout"] = normal_bf16(seed_of(wid, var, DO), qshape)
+    out["sinks"] = normal_f32(seed_of(wid, var, SINKS), (h_q,)) if w.get("sinks") else None
+    out.setdefault("scale", 1.0 / math.sqrt(d))
+    return out
