@@ -1,0 +1,326 @@
+#!/usr/bin/env python3
+"""Benchmark: exact attention forward + backward on one GB300 (or N independent replicas).
+
+One step = fa_fwd + fa_bwd (preprocess, main, postprocess) over the dense causal
+workload B=2, s=8192, h=16, d=128, bf16 — the shape the throughput target is quoted on.
+The metric is attention TFLOPS of the forward+backward pass with the pages' convention:
+4 * d FLOPs per allowed (query, key) pair for the forward, 2.5x that for the backward,
+3.5x for both.  Inputs are seeded synthetic draws already resident in HBM; L2 is flushed
+(a 256 MiB write) between timed steps.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+Under torchrun every rank runs its own replica (the path has no exchange step); the
+step time is the maximum over ranks and the value counts all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_bwd_gb300 import inputs, metrics  # noqa: E402
+
+METRIC = "attention TFLOPS fwd+bwd (bf16, d=128, causal)"
+UNIT = "TFLOP/s"
+WORKLOAD = "sweep_s8192_causal"
+# dram__bytes_read.sum + dram__bytes_write.sum of one bwd_main launch, from the ncu
+# capture summarised in profiles/ (None until a capture of the current kernel exists)
+BWD_MAIN_DRAM_BYTES = None
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"], src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                mx = float(parts[2].split()[0])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.out.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from exact_attention_bwd_gb300 import binding as fa
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = inputs.make(inputs.workload(args.workload))
+    fl_fwd = metrics.fwd_flops(w)
+    fl_bwd = metrics.bwd_flops(w)
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v, dout = up(w["q"]), up(w["k"]), up(w["v"]), up(w["dout"])
+    kw = dict(causal=w["causal"], window=w["window"], softmax_scale=w["scale"])
+    o, lse, ws_f = fa.forward(q, k, v, **kw)
+    dq, dk, dv, _, ws_b = fa.backward(q, k, v, o, lse, dout, **kw)
+    grads = (dq, dk, dv, None)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.forward(q, k, v, **kw, out=o, lse=lse, workspace=ws_f)
+        fa.backward(q, k, v, o, lse, dout, **kw, workspace=ws_b, grads=grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status(ws_f) != 0 or fa.device_status(ws_b) != 0:
+        raise RuntimeError("device status nonzero after warm-up")
+
+    fa.fa_profile_enable(True)
+    kern = {n: [] for n in ("fwd", "bwd_pre", "bwd_main", "bwd_post")}
+    times = []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            ev0.record(stream)
+            step()
+            ev1.record(stream)
+            ev1.synchronize()
+            times.append(ev0.elapsed_time(ev1))
+            for n in kern:
+                rc, ms = fa.fa_profile_read(n)
+                if rc == 0:
+                    kern[n].append(ms)
+    torch.cuda.synchronize()
+    fa.fa_profile_enable(False)
+    clocks = clk.summary()
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * (fl_fwd + fl_bwd) * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs in, results out, through the same public API ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dout))
+        outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, dq, dk, dv)]
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in outs) + lse_h.numel() * 4
+        e2e_ms = []
+        for it in range(args.warmup + args.steps):
+            flush.zero_()
+            ev0.record(stream)
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            dout.copy_(hdo, non_blocking=True)
+            step()
+            for hdst, src in zip(outs, (o, dq, dk, dv)):
+                hdst.copy_(src, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            ev1.record(stream)
+            ev1.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(ev0.elapsed_time(ev1))
+        tot = sum(e2e_ms)
+        if world > 1:
+            t = torch.tensor([tot], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            tot = float(t.item())
+        e2e = {"value": world * (fl_fwd + fl_bwd) * len(e2e_ms) / (tot * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": tot / len(e2e_ms)}
+
+    pk = peaks()
+    main_ms = statistics.mean(kern["bwd_main"]) if kern["bwd_main"] else None
+    fwd_ms = statistics.mean(kern["fwd"]) if kern["fwd"] else None
+    long_region = total_ms > 1000.0
+    peak = pk["bf16_sus"] if long_region else pk["bf16"]
+    roof = None
+    if main_ms:
+        ach = fl_bwd / (main_ms * 1e-3) / 1e12
+        roof = {"kernel": "bwd_main", "bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": BWD_MAIN_DRAM_BYTES,
+                "peak_kind": f"{pk['src']} bf16 {'sustained' if long_region else 'burst'}",
+                "algorithmic_flops": fl_bwd}
+    per_kernel = {n: round(statistics.mean(x), 4) for n, x in kern.items() if x}
+    fwd_tf = fl_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": args.workload, "B": w["B"], "s_q": w["s_q"], "s_kv": w["s_kv"], "h_q": w["h_q"],
+                   "h_kv": w["h_kv"], "d": w["d"], "causal": w["causal"], "window": list(w["window"]),
+                   "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "fwd_tflops": round(fwd_tf, 1) if fwd_tf else None,
+        "fwd_frac_of_peak": round(fwd_tf / pk["bf16"], 4) if fwd_tf else None,
+        "kernel_ms": per_kernel,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "step_ms": {"median": statistics.median(times), "mean": statistics.mean(times),
+                    "std": statistics.pstdev(times), "min": min(times), "max": max(times)},
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = oracle_sample(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------------------
+# the oracle on a bounded sample of the workload
+# ----------------------------------------------------------------------------------------------
+
+def oracle_sample(w, rows=256):
+    """fp64 oracle fwd+bwd on the last `rows` query rows of batch element 0 (all heads,
+    every key they see), timed on the host cores; TFLOPS with the same convention."""
+    import oracle
+    b = 0
+    s_q, s_kv = w["s_q"], w["s_kv"]
+    i0 = s_q - rows
+    q = inputs.bf16_to_f64(w["q"][b:b + 1, i0:])
+    kend = s_kv if not w["causal"] else s_kv  # the last rows see every key up to s_kv
+    k = inputs.bf16_to_f64(w["k"][b:b + 1, :kend])
+    v = inputs.bf16_to_f64(w["v"][b:b + 1, :kend])
+    do = inputs.bf16_to_f64(w["dout"][b:b + 1, i0:])
+    kw = dict(scale=w["scale"], causal=w["causal"], window=w["window"])
+    sub = dict(w, B=1, s_q=rows, s_kv=kend, cu_q=None, cu_k=None, varlen=False)
+    flops = 3.5 * metrics.fwd_flops(sub)
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, **kw)
+    oracle.bwd(q, k, v, do, **kw)
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"batch 0, all {w['h_q']} heads, last {rows} of {s_q} query rows with all keys they see "
+                      f"(fwd+bwd, fp64, {flops / 1e9:.1f} GFLOP)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = inputs.make(inputs.workload(args.workload))
+    vals = []
+    cb = None
+    for it in range(args.warmup + args.steps):
+        r = oracle_sample(w, rows=64)
+        if it >= args.warmup:
+            vals.append(r["value"])
+            cb = r
+    val = statistics.mean(vals)
+    cb = dict(cb, value=round(val, 6))
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": args.workload, "B": w["B"], "s_q": w["s_q"], "s_kv": w["s_kv"],
+                       "h_q": w["h_q"], "h_kv": w["h_kv"], "d": w["d"], "causal": w["causal"]},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(val, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

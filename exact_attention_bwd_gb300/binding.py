@@ -1,0 +1,220 @@
+"""ctypes binding of libfa_gb300.so (include/fa.h): argument marshalling only.
+
+The functions named like the C entry points (``fa_fwd``, ``fa_bwd``, ...) pass raw
+device pointers straight through.  ``forward`` / ``backward`` are conveniences that
+take torch CUDA tensors, allocate the outputs and the workspace with torch and call
+the same entry points on torch's current stream.  Every step of the computation runs
+in the library's kernels; there is no CPU path.  Loading fails loudly when the
+library is missing or cannot be built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_WORKSPACE = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+FA_ERR_DEVICE_CHECK = 6
+
+FA_FLAG_VALIDATE_CU = 1
+FA_FLAG_NO_SPLIT = 2
+
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_read_device_status",
+           "fa_status_string", "fa_profile_enable", "fa_profile_read", "fa_version")
+
+
+class FaParams(ctypes.Structure):
+    """Mirror of ``fa_params``."""
+    _fields_ = [
+        ("B", ctypes.c_int), ("s_q", ctypes.c_int), ("s_kv", ctypes.c_int),
+        ("h_q", ctypes.c_int), ("h_kv", ctypes.c_int), ("d", ctypes.c_int),
+        ("softmax_scale", ctypes.c_float), ("causal", ctypes.c_int),
+        ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+        ("sinks", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("max_seqlen_q", ctypes.c_int), ("max_seqlen_k", ctypes.c_int), ("flags", ctypes.c_uint),
+    ]
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {fa_status_string(code)} (status {code})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Loads (building first if stale) the CUDA library; raises if that is impossible."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing:
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"CUDA library {_build.LIB} is missing; run exact_attention_bwd_gb300/build.py")
+        lib = ctypes.CDLL(_build.LIB)
+        P = ctypes.POINTER(FaParams)
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.fa_fwd.restype = ctypes.c_int
+        lib.fa_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.fa_bwd.restype = ctypes.c_int
+        lib.fa_fwd_workspace_size.argtypes = [P]
+        lib.fa_fwd_workspace_size.restype = sz
+        lib.fa_bwd_workspace_size.argtypes = [P]
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_read_device_status.argtypes = [vp, vp]
+        lib.fa_read_device_status.restype = ctypes.c_int
+        lib.fa_status_string.argtypes = [ctypes.c_int]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_profile_enable.argtypes = [ctypes.c_int]
+        lib.fa_profile_enable.restype = ctypes.c_int
+        lib.fa_profile_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_float)]
+        lib.fa_profile_read.restype = ctypes.c_int
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+# ----------------------------------------------------------------------------------------------
+# raw entry points (same names as the C ABI)
+# ----------------------------------------------------------------------------------------------
+
+def fa_fwd(params: FaParams, q, k, v, o, lse, workspace, workspace_bytes, stream) -> int:
+    return load().fa_fwd(ctypes.byref(params), q, k, v, o, lse, workspace, workspace_bytes, stream)
+
+
+def fa_bwd(params: FaParams, q, k, v, o, lse, dout, dq, dk, dv, dsinks, workspace, workspace_bytes,
+           stream) -> int:
+    return load().fa_bwd(ctypes.byref(params), q, k, v, o, lse, dout, dq, dk, dv, dsinks, workspace,
+                         workspace_bytes, stream)
+
+
+def fa_fwd_workspace_size(params: FaParams) -> int:
+    return int(load().fa_fwd_workspace_size(ctypes.byref(params)))
+
+
+def fa_bwd_workspace_size(params: FaParams) -> int:
+    return int(load().fa_bwd_workspace_size(ctypes.byref(params)))
+
+
+def fa_read_device_status(workspace, stream) -> int:
+    return load().fa_read_device_status(workspace, stream)
+
+
+def fa_status_string(code: int) -> str:
+    return load().fa_status_string(code).decode()
+
+
+def fa_profile_enable(on: bool) -> int:
+    return load().fa_profile_enable(1 if on else 0)
+
+
+def fa_profile_read(kernel: str):
+    ms = ctypes.c_float(0.0)
+    rc = load().fa_profile_read(kernel.encode(), ctypes.byref(ms))
+    return rc, float(ms.value)
+
+
+def fa_version() -> str:
+    return load().fa_version().decode()
+
+
+# ----------------------------------------------------------------------------------------------
+# torch conveniences: allocation and stream plumbing only
+# ----------------------------------------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None,
+                cu_k=None, flags=0) -> FaParams:
+    """fa_params from tensor shapes: [B,S,H,D] dense or [T,H,D] packed (with cu_q / cu_k)."""
+    if cu_q is None:
+        B, s_q, h_q, d = q.shape
+        _, s_kv, h_kv, _ = k.shape
+    else:
+        T_q, h_q, d = q.shape
+        T_k, h_kv, _ = k.shape
+        B, s_q, s_kv = cu_q.numel() - 1, T_q, T_k
+    p = FaParams()
+    p.B, p.s_q, p.s_kv, p.h_q, p.h_kv, p.d = B, s_q, s_kv, h_q, h_kv, d
+    p.softmax_scale = float(softmax_scale) if softmax_scale else 0.0
+    p.causal = 1 if causal else 0
+    p.window_left, p.window_right = int(window[0]), int(window[1])
+    p.sinks = None if sinks is None else sinks.data_ptr()
+    p.cu_seqlens_q = None if cu_q is None else cu_q.data_ptr()
+    p.cu_seqlens_k = None if cu_k is None else cu_k.data_ptr()
+    p.max_seqlen_q = p.max_seqlen_k = 0
+    p.flags = flags
+    return p
+
+
+def _stream():
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None, cu_k=None,
+            flags=0, out=None, lse=None, workspace=None):
+    """Runs fa_fwd on torch CUDA tensors; returns (o, lse, workspace)."""
+    import torch
+    p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
+                    cu_k=cu_k, flags=flags)
+    nbytes = fa_fwd_workspace_size(p)
+    if nbytes == 0:
+        raise FaError(FA_ERR_UNSUPPORTED, "fa_fwd_workspace_size")
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        shape = (p.B, p.h_q, p.s_q) if cu_q is None else (p.h_q, p.s_q)
+        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+    rc = fa_fwd(p, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream())
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse, workspace
+
+
+def backward(q, k, v, o, lse, dout, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None,
+             cu_q=None, cu_k=None, flags=0, workspace=None, grads=None):
+    """Runs fa_bwd on torch CUDA tensors; returns (dq, dk, dv, dsinks, workspace)."""
+    import torch
+    p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
+                    cu_k=cu_k, flags=flags)
+    nbytes = fa_bwd_workspace_size(p)
+    if nbytes == 0:
+        raise FaError(FA_ERR_UNSUPPORTED, "fa_bwd_workspace_size")
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if grads is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dsinks = None if sinks is None else torch.empty_like(sinks)
+    else:
+        dq, dk, dv, dsinks = grads
+    rc = fa_bwd(p, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                _ptr(dsinks), _ptr(workspace), workspace.numel(), _stream())
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv, dsinks, workspace
+
+
+def device_status(workspace) -> int:
+    return fa_read_device_status(_ptr(workspace), _stream())

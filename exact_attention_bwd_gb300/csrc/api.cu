@@ -1,0 +1,493 @@
+// C ABI of the library (include/fa.h): argument checks, planning, TMA descriptors and
+// launches on the caller's stream.  Nothing here allocates device memory: every
+// scratch buffer is carved out of the caller's workspace.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "kernels.h"
+
+namespace fa {
+namespace {
+
+// ------------------------------------------------------------------------------------------
+// device properties and the driver's tensor-map encoder
+// ------------------------------------------------------------------------------------------
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 4-D bf16 tensor map over [b][s][h][d] (innermost first: d, h, s, b) with a
+// (64, box_h, box_s, 1) box and 128-byte swizzle.  Out-of-range rows read as zero.
+bool encode_bhsd(CUtensorMap* m, const void* base, int d, int h, int s, int b, int box_h, int box_s) {
+    auto fn = encoder();
+    if (!fn) return false;
+    if (s <= 0 || b <= 0) {
+        std::memset(m, 0, sizeof(*m));  // never dereferenced: no tile of this tensor is loaded
+        return true;
+    }
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)h, (cuuint64_t)s, (cuuint64_t)b};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)h * d * 2, (cuuint64_t)s * h * d * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_h, (cuuint32_t)box_s, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------------------------------
+// profiling hooks
+// ------------------------------------------------------------------------------------------
+const char* const kKernelNames[] = {"fwd", "decode", "combine", "bwd_pre", "bwd_main", "bwd_post"};
+enum KernelId { kFwd = 0, kDecode, kCombine, kBwdPre, kBwdMain, kBwdPost, kNumKernels };
+
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    cudaEvent_t ev[kNumKernels][2] = {};
+    bool recorded[kNumKernels] = {};
+};
+Profiler& prof() {
+    static Profiler p;
+    return p;
+}
+
+template <class F>
+cudaError_t timed(KernelId id, cudaStream_t st, F&& launch) {
+    Profiler& P = prof();
+    bool on;
+    {
+        std::lock_guard<std::mutex> g(P.mu);
+        on = P.on;
+    }
+    if (!on) return launch();
+    cudaEventRecord(P.ev[id][0], st);
+    cudaError_t e = launch();
+    cudaEventRecord(P.ev[id][1], st);
+    std::lock_guard<std::mutex> g(P.mu);
+    P.recorded[id] = (e == cudaSuccess);
+    return e;
+}
+
+// ------------------------------------------------------------------------------------------
+// argument normalisation
+// ------------------------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-visible total token counts of a packed call are not known without reading the
+// offsets; the caller passes them as s_q / s_kv (T_q, T_k).
+fa_status normalise(const fa_params* in, Problem& p) {
+    if (!in) return FA_ERR_INVALID_ARG;
+    const fa_params& a = *in;
+    if (a.B < 0 || a.s_q < 0 || a.s_kv < 0 || a.h_q <= 0 || a.h_kv <= 0 || a.d <= 0) return FA_ERR_INVALID_ARG;
+    if (a.h_q % a.h_kv != 0) return FA_ERR_INVALID_ARG;
+    if ((a.cu_seqlens_q == nullptr) != (a.cu_seqlens_k == nullptr)) return FA_ERR_INVALID_ARG;
+    if (a.window_left < -1 || a.window_right < -1) return FA_ERR_INVALID_ARG;
+    if (a.d % 8 != 0 || a.d > 256) return FA_ERR_UNSUPPORTED;
+    std::memset(&p, 0, sizeof(p));
+    p.B = a.B;
+    p.s_q = a.s_q;
+    p.s_kv = a.s_kv;
+    p.h_q = a.h_q;
+    p.h_kv = a.h_kv;
+    p.d = a.d;
+    p.G = a.h_q / a.h_kv;
+    if (p.G > 128) return FA_ERR_UNSUPPORTED;
+    p.P = 128 / p.G;
+    p.scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / std::sqrt((float)a.d);
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.causal = a.causal ? 1 : 0;
+    p.left = a.window_left;
+    p.right = a.window_right;
+    if (p.causal) p.right = 0;  // intersection of the causal mask with any right window
+    p.sinks = a.sinks;
+    p.cu_q = a.cu_seqlens_q;
+    p.cu_k = a.cu_seqlens_k;
+    if (p.cu_q) {
+        p.T_q = a.s_q;
+        p.T_k = a.s_kv;
+    }
+    return FA_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// forward plan
+// ------------------------------------------------------------------------------------------
+enum class FwdPath { kEmpty, kTensor, kDecode };
+
+constexpr int kDecodeRowsMax = 16;  // query rows per key/value head served by the decode kernel
+constexpr int kDecodeKeys = 64;     // keys per decode tile
+constexpr size_t kStatusBytes = 256;
+
+struct FwdPlan {
+    FwdPath path = FwdPath::kEmpty;
+    int n_blocks = 0, n_splits = 1, split_tiles = 0;
+    size_t part_rows = 0;  // rows of the split partials
+    size_t ws_bytes = kStatusBytes;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Chooses the number of KV splits that minimises (waves) x (tiles per split), with a
+// small charge per split for the partial results written and read back.
+int choose_splits(long ctas, int tiles, int slots, double part_cost_per_split) {
+    int best = 1;
+    double best_cost = 1e300;
+    for (int s = 1; s <= 64 && s <= tiles; ++s) {
+        const int per = (tiles + s - 1) / s;
+        const long waves = (ctas * s + slots - 1) / slots;
+        const double cost = (double)waves * per * (1.0 + (s > 1 ? part_cost_per_split * s : 0.0));
+        if (cost < best_cost * 0.98) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
+    pl = FwdPlan();
+    const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
+    if (p.B == 0 || rows_total == 0) return FA_OK;  // nothing to compute
+    const bool dense = p.cu_q == nullptr;
+    const int R = p.s_q * p.G;  // query rows per key/value head (dense)
+    if (dense && R <= kDecodeRowsMax && (p.d == 64 || p.d == 128 || p.d == 256)) {
+        pl.path = FwdPath::kDecode;
+        const int tiles = (p.s_kv + kDecodeKeys - 1) / kDecodeKeys;
+        const long units = (long)p.B * p.h_kv;
+        const int slots = sm_count() * 2;
+        // partials: R rows x (d + 1) floats per split, written and read, against the
+        // unit's 2 * s_kv * d bf16 of keys and values
+        const double part = p.s_kv > 0 ? (double)R * (p.d + 1) * 8.0 / ((double)p.s_kv * p.d * 4.0) : 1.0;
+        pl.n_splits = tiles > 0 ? choose_splits(units, tiles, slots, part) : 1;
+        pl.split_tiles = tiles > 0 ? (tiles + pl.n_splits - 1) / pl.n_splits : 0;
+        pl.n_splits = pl.split_tiles > 0 ? (tiles + pl.split_tiles - 1) / pl.split_tiles : 1;
+        pl.part_rows = (size_t)p.B * p.h_q * p.s_q;
+        pl.ws_bytes = kStatusBytes + align256(pl.part_rows * pl.n_splits * p.d * 4) +
+                      align256(pl.part_rows * pl.n_splits * 4);
+        return FA_OK;
+    }
+    if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
+    pl.path = FwdPath::kTensor;
+    if (dense) {
+        pl.n_blocks = (p.s_q + 2 * p.P - 1) / (2 * p.P);
+        const int tiles = (p.s_kv + kTileRows - 1) / kTileRows;
+        const long ctas = (long)pl.n_blocks * p.h_kv * p.B;
+        pl.n_splits = 1;
+        if (!(flags & FA_FLAG_NO_SPLIT) && !p.causal && p.left < 0 && p.right < 0 && tiles >= 8 &&
+            ctas < 4L * sm_count()) {
+            const double part = (double)(2 * 128) * (p.d + 1) * 8.0 / ((double)p.s_kv * p.d * 4.0);
+            pl.n_splits = choose_splits(ctas, tiles, sm_count(), part);
+        } else if (!(flags & FA_FLAG_NO_SPLIT) && tiles >= 8 && ctas < 4L * sm_count() && p.s_q * 4 <= p.s_kv) {
+            // masked decode-like shapes: every query block sees (almost) every key
+            const double part = (double)(2 * 128) * (p.d + 1) * 8.0 / ((double)p.s_kv * p.d * 4.0);
+            pl.n_splits = choose_splits(ctas, tiles, sm_count(), part);
+        }
+        if (pl.n_splits > 1) {
+            pl.split_tiles = (tiles + pl.n_splits - 1) / pl.n_splits;
+            pl.n_splits = (tiles + pl.split_tiles - 1) / pl.split_tiles;
+        }
+        if (pl.n_splits > 1) {
+            pl.part_rows = (size_t)p.B * p.h_q * p.s_q;
+            pl.ws_bytes = kStatusBytes + align256(pl.part_rows * pl.n_splits * p.d * 4) +
+                          align256(pl.part_rows * pl.n_splits * 4);
+        }
+    } else {
+        pl.n_blocks = p.T_q / (2 * p.P) + p.B;
+    }
+    return FA_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// backward plan
+// ------------------------------------------------------------------------------------------
+struct BwdPlan {
+    bool empty = true;
+    int n_qtiles = 0, n_kvblocks = 0;
+    size_t off_delta = 0, off_lse2 = 0, off_dq = 0;
+    size_t ws_bytes = kStatusBytes;
+};
+
+fa_status plan_bwd(const Problem& p, BwdPlan& pl) {
+    pl = BwdPlan();
+    if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
+    const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
+    const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
+    if (p.B == 0 || (rows_total == 0 && keys_total == 0)) return FA_OK;
+    pl.empty = false;
+    if (p.cu_q) {
+        pl.n_qtiles = p.T_q / p.P + p.B;
+        pl.n_kvblocks = p.T_k / kTileRows + p.B;
+    } else {
+        pl.n_qtiles = p.B * ((p.s_q + p.P - 1) / p.P);
+        pl.n_kvblocks = (p.s_kv + kTileRows - 1) / kTileRows;
+    }
+    const size_t stat = (size_t)p.h_kv * pl.n_qtiles * 128 * 4;
+    pl.off_delta = kStatusBytes;
+    pl.off_lse2 = pl.off_delta + align256(stat);
+    pl.off_dq = pl.off_lse2 + align256(stat);
+    pl.ws_bytes = pl.off_dq + align256((size_t)p.h_kv * pl.n_qtiles * 128 * p.d * 4);
+    return FA_OK;
+}
+
+fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+__global__ void validate_cu_kernel(const int32_t* cu_q, const int32_t* cu_k, int n, int Tq, int Tk, int* status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i > n) return;
+    bool bad = false;
+    if (i == 0) bad = cu_q[0] != 0 || cu_k[0] != 0;
+    if (i == n) bad = bad || cu_q[n] != Tq || cu_k[n] != Tk;
+    if (i < n) bad = bad || cu_q[i + 1] < cu_q[i] || cu_k[i + 1] < cu_k[i];
+    if (bad) atomicCAS(status, 0, 6);
+}
+
+fa_status maybe_validate(const Problem& p, unsigned flags, int* status, cudaStream_t st) {
+    if (!(flags & FA_FLAG_VALIDATE_CU) || !p.cu_q) return FA_OK;
+    validate_cu_kernel<<<(p.B + 1 + 255) / 256, 256, 0, st>>>(p.cu_q, p.cu_k, p.B, p.T_q, p.T_k, status);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_version(void) { return "fa_gb300 0.1 (sm_103a, tcgen05)"; }
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARG: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported problem";
+        case FA_ERR_WORKSPACE: return "workspace too small";
+        case FA_ERR_CUDA: return "CUDA error";
+        case FA_ERR_TIMEOUT: return "kernel pipeline timed out";
+        case FA_ERR_DEVICE_CHECK: return "device-side argument check failed";
+    }
+    return "unknown status";
+}
+
+size_t fa_fwd_workspace_size(const fa_params* in) {
+    Problem p;
+    if (normalise(in, p) != FA_OK) return 0;
+    FwdPlan pl;
+    if (plan_fwd(p, in->flags, pl) != FA_OK) return 0;
+    return pl.ws_bytes;
+}
+
+size_t fa_bwd_workspace_size(const fa_params* in) {
+    Problem p;
+    if (normalise(in, p) != FA_OK) return 0;
+    BwdPlan pl;
+    if (plan_bwd(p, pl) != FA_OK) return 0;
+    return pl.ws_bytes;
+}
+
+fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* v, void* o, float* lse,
+                 void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
+    Problem p;
+    fa_status rc = normalise(in, p);
+    if (rc != FA_OK) return rc;
+    FwdPlan pl;
+    if ((rc = plan_fwd(p, in->flags, pl)) != FA_OK) return rc;
+    if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+    if (ws_bytes < pl.ws_bytes) return FA_ERR_WORKSPACE;
+    const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
+    const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
+    if (rows_total > 0 && (!q || !o || !aligned16(q) || !aligned16(o))) return FA_ERR_INVALID_ARG;
+    if (keys_total > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int* status = reinterpret_cast<int*>(workspace);
+    if ((rc = cuda_status(cudaMemsetAsync(status, 0, sizeof(int), st))) != FA_OK) return rc;
+    if ((rc = maybe_validate(p, in->flags, status, st)) != FA_OK) return rc;
+    if (pl.path == FwdPath::kEmpty) return FA_OK;
+
+    const int tokens_q = p.cu_q ? p.T_q : p.s_q;
+    const int tokens_k = p.cu_q ? p.T_k : p.s_kv;
+    const int bdim = p.cu_q ? 1 : p.B;
+    CUtensorMap tk, tv;
+    if (!encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, pl.path == FwdPath::kDecode ? 64 : 128) ||
+        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, pl.path == FwdPath::kDecode ? 64 : 128))
+        return FA_ERR_CUDA;
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    float* o_part = reinterpret_cast<float*>(ws + kStatusBytes);
+    float* lse_part = reinterpret_cast<float*>(ws + kStatusBytes + align256(pl.part_rows * pl.n_splits * p.d * 4));
+
+    if (pl.path == FwdPath::kDecode) {
+        DecodeArgs a{};
+        a.p = p;
+        a.q = reinterpret_cast<const __nv_bfloat16*>(q);
+        a.n_splits = pl.n_splits;
+        a.split_keys = pl.split_tiles * kDecodeKeys;
+        a.o_part = o_part;
+        a.lse_part = lse_part;
+        a.status = status;
+        cudaError_t e = timed(kDecode, st, [&] { return launch_decode(a, tk, tv, st); });
+        if (e != cudaSuccess) return FA_ERR_CUDA;
+        CombineArgs c{};
+        c.p = p;
+        c.n_splits = pl.n_splits;
+        c.o_part = o_part;
+        c.lse_part = lse_part;
+        c.o = reinterpret_cast<__nv_bfloat16*>(o);
+        c.lse = lse;
+        e = timed(kCombine, st, [&] { return launch_combine(c, st); });
+        return cuda_status(e);
+    }
+
+    CUtensorMap tq;
+    if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P)) return FA_ERR_CUDA;
+    FwdArgs a{};
+    a.p = p;
+    a.n_blocks = pl.n_blocks;
+    a.n_splits = pl.n_splits;
+    a.split_tiles = pl.split_tiles;
+    a.o = reinterpret_cast<__nv_bfloat16*>(o);
+    a.lse = lse;
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    a.status = status;
+    cudaError_t e = timed(kFwd, st, [&] { return launch_fwd(a, tq, tk, tv, st); });
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (pl.n_splits > 1) {
+        CombineArgs c{};
+        c.p = p;
+        c.n_splits = pl.n_splits;
+        c.o_part = o_part;
+        c.lse_part = lse_part;
+        c.o = reinterpret_cast<__nv_bfloat16*>(o);
+        c.lse = lse;
+        e = timed(kCombine, st, [&] { return launch_combine(c, st); });
+    }
+    return cuda_status(e);
+}
+
+fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, float* dsinks, void* workspace, size_t ws_bytes,
+                 struct CUstream_st* stream) {
+    Problem p;
+    fa_status rc = normalise(in, p);
+    if (rc != FA_OK) return rc;
+    BwdPlan pl;
+    if ((rc = plan_bwd(p, pl)) != FA_OK) return rc;
+    if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+    if (ws_bytes < pl.ws_bytes) return FA_ERR_WORKSPACE;
+    if (p.sinks && !dsinks) return FA_ERR_INVALID_ARG;
+    const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
+    const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
+    if (rows_total > 0 && (!q || !o || !lse || !dout || !dq || !aligned16(q) || !aligned16(o) ||
+                           !aligned16(dout) || !aligned16(dq)))
+        return FA_ERR_INVALID_ARG;
+    if (keys_total > 0 && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) ||
+                           !aligned16(dv)))
+        return FA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int* status = reinterpret_cast<int*>(workspace);
+    if ((rc = cuda_status(cudaMemsetAsync(status, 0, sizeof(int), st))) != FA_OK) return rc;
+    if (p.sinks && (rc = cuda_status(cudaMemsetAsync(dsinks, 0, sizeof(float) * p.h_q, st))) != FA_OK) return rc;
+    if ((rc = maybe_validate(p, in->flags, status, st)) != FA_OK) return rc;
+    if (pl.empty) return FA_OK;
+
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    BwdArgs a{};
+    a.p = p;
+    a.n_qtiles = pl.n_qtiles;
+    a.n_kvblocks = pl.n_kvblocks;
+    a.o = reinterpret_cast<const __nv_bfloat16*>(o);
+    a.lse = lse;
+    a.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
+    a.delta_t = reinterpret_cast<float*>(ws + pl.off_delta);
+    a.lse2_t = reinterpret_cast<float*>(ws + pl.off_lse2);
+    a.dq_acc = reinterpret_cast<float*>(ws + pl.off_dq);
+    a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
+    a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
+    a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+    a.dsinks = p.sinks ? dsinks : nullptr;
+    a.status = status;
+
+    const int tokens_q = p.cu_q ? p.T_q : p.s_q;
+    const int tokens_k = p.cu_q ? p.T_k : p.s_kv;
+    const int bdim = p.cu_q ? 1 : p.B;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P) ||
+        !encode_bhsd(&tdo, dout, p.d, p.h_q, tokens_q, bdim, p.G, p.P) ||
+        !encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, 128) ||
+        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, 128))
+        return FA_ERR_CUDA;
+    cudaError_t e = timed(kBwdPre, st, [&] { return launch_bwd_pre(a, st); });
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    e = timed(kBwdMain, st, [&] { return launch_bwd_main(a, tq, tk, tv, tdo, st); });
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    e = timed(kBwdPost, st, [&] { return launch_bwd_post(a, st); });
+    return cuda_status(e);
+}
+
+fa_status fa_read_device_status(const void* workspace, struct CUstream_st* stream) {
+    if (!workspace) return FA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (v == FA_ERR_TIMEOUT || v == FA_ERR_DEVICE_CHECK) return (fa_status)v;
+    return v == 0 ? FA_OK : FA_ERR_DEVICE_CHECK;
+}
+
+fa_status fa_profile_enable(int on) {
+    Profiler& P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    if (on && !P.ev[0][0]) {
+        for (int i = 0; i < kNumKernels; ++i)
+            for (int j = 0; j < 2; ++j)
+                if (cudaEventCreate(&P.ev[i][j]) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    P.on = on != 0;
+    for (int i = 0; i < kNumKernels; ++i) P.recorded[i] = false;
+    return FA_OK;
+}
+
+fa_status fa_profile_read(const char* kernel, float* ms) {
+    if (!kernel || !ms) return FA_ERR_INVALID_ARG;
+    Profiler& P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    for (int i = 0; i < kNumKernels; ++i) {
+        if (std::strcmp(kernel, kKernelNames[i]) != 0) continue;
+        if (!P.recorded[i]) return FA_ERR_INVALID_ARG;
+        if (cudaEventSynchronize(P.ev[i][1]) != cudaSuccess) return FA_ERR_CUDA;
+        return cudaEventElapsedTime(ms, P.ev[i][0], P.ev[i][1]) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
+    return FA_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

@@ -1,0 +1,550 @@
+// Backward attention on the 5th-generation tensor cores, sm_103a.
+//
+// The derivation is the one of the "Flash Attention Tutorial" README (GitHub search
+// results page, section 6 "Flash Attention Backward Pass", "Key derivations"), with the
+// softmax scale kept where the chain rule puts it:
+//   P = exp(scale Q K^T - LSE)         recomputed from the saved per-row LSE
+//   dV = P^T dO
+//   D_i = rowsum(dO_i * O_i)           (preprocess kernel)
+//   dS = P * (dO V^T - D)
+//   dQ = scale dS K,   dK = scale dS^T Q
+// The tiled loop is the tutorial's: the outer loop runs over key/value tiles (one CTA
+// each, dK and dV accumulated on chip), the inner loop over the query tiles that can see
+// the key tile, with dQ summed across key tiles.  Here the inner loop runs over packed
+// query tiles that hold all G query heads of the key/value head, so the grouped-query
+// reduction of dK and dV happens in the fp32 TMEM accumulators (fa4-jax PyPI page,
+// Restrictions: GQA backward accumulates dK/dV in fp32).  dQ is accumulated in an fp32
+// workspace with atomic adds and converted by the postprocess kernel.
+//
+// Main-kernel warp roles (384 threads):
+//   warp 0      TMA producer: K and V once, then Q_i and dO_i through a two-stage ring
+//   warp 1      MMA issuer: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q,
+//               dQ_i = dS K, all into TMEM
+//   warp 2      owns the TMEM allocation
+//   warps 4-11  two groups of 128: thread = key row; group c takes query columns
+//               [64c, 64c+64): P^T = exp2(S^T * c - LSE2), dS^T = P^T (dP^T - D) into
+//               shared memory; then thread = query row for the dQ tile, columns split in
+//               halves between the groups, reduced into the workspace.
+#include "common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreadsBwd = 384;
+constexpr int kRows = 128;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int KCH = D / 64;
+    static constexpr int TILE = 128 * D * 2;     // Q / K / V / dO tile bytes
+    static constexpr int CHUNK = 128 * 128;      // one [128 rows][64 cols] chunk
+    static constexpr int TMEM_COLS = 512;
+    // TMEM columns
+    static constexpr uint32_t C_S = 0;           // S^T (fp32); P^T (bf16) in [0, 32) and [64, 96)
+    static constexpr uint32_t C_DP = 128;        // dP^T
+    static constexpr uint32_t C_DV = 256;
+    static constexpr uint32_t C_DK = 256 + D;
+    static constexpr uint32_t C_DQ = (D == 128) ? 128 : 384;  // dQ_i (rows = query rows)
+    static constexpr bool DQ_OVER_DP = (D == 128);             // dQ_i reuses the dP^T columns
+};
+
+template <int D>
+struct __align__(1024) BwdSmem {
+    uint8_t k[BwdCfg<D>::TILE];
+    uint8_t v[BwdCfg<D>::TILE];
+    uint8_t q[2][BwdCfg<D>::TILE];
+    uint8_t dO[2][BwdCfg<D>::TILE];
+    uint8_t dst[2][128 * 128];   // dS^T: [key row][query col], two 64-column chunks
+    uint64_t kv_full;
+    uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+    uint64_t s_full, dp_full, p_full, ds_full, ds_free, dq_full, dq_free, dkv_full;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// First tiled-layout index of the query tiles of sequence `seq` (see the workspace
+// layout in the planner): dense = seq * ceil(s_q / P), packed = cu_q[seq] / P + seq.
+__device__ __forceinline__ int qtile_base(const Problem& p, int seq) {
+    if (p.cu_q) return p.cu_q[seq] / p.P + seq;
+    return seq * cdiv(p.s_q, p.P);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsBwd, 1)
+    bwd_main_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    BwdSmem<D>& s = *reinterpret_cast<BwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Problem& p = a.p;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.y;
+
+    int seq, blk;
+    if (p.cu_q) {
+        blk = blockIdx.x;
+        seq = owner_sequence(p.cu_k, p.B, blk, kRows);
+        blk -= p.cu_k[seq] / kRows + seq;
+    } else {
+        seq = blockIdx.z;
+        blk = blockIdx.x;
+    }
+    const SeqView sv = seq_view(p, seq);
+    const int j0 = blk * kRows;
+    if (j0 >= sv.nk) return;  // idle packed-batch block
+    // an earlier CTA of this launch gave up: do not start new work
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
+    const int j1 = min(j0 + kRows, sv.nk) - 1;
+    const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
+    // query positions whose band reaches [j0, j1]
+    int i_lo = 0, i_hi = sv.nq - 1;
+    if (p.right >= 0) i_lo = max(i_lo, j0 - band.off - p.right);
+    if (p.left >= 0) i_hi = min(i_hi, j1 - band.off + p.left);
+    const int qt0 = (i_hi >= i_lo) ? i_lo / p.P : 0;
+    const int qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
+    const int nsteps = qt1 - qt0;
+    const int tbase = qtile_base(p, seq);
+
+    Abort ab{&s.abort_flag, a.status};
+    if (tid == 0) {
+        s.abort_flag = 0;
+        mbar_init(&s.kv_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.q_full[i], 1);
+            mbar_init(&s.q_empty[i], 1);
+            mbar_init(&s.do_full[i], 1);
+            mbar_init(&s.do_empty[i], 1);
+        }
+        mbar_init(&s.s_full, 1);
+        mbar_init(&s.dp_full, 1);
+        mbar_init(&s.p_full, 256);
+        mbar_init(&s.ds_full, 256);
+        mbar_init(&s.ds_free, 1);
+        mbar_init(&s.dq_full, 1);
+        mbar_init(&s.dq_free, 256);
+        mbar_init(&s.dkv_full, 1);
+        fence_mbar_init();
+    }
+    if (p.P * p.G < 128) {
+        // rows past P*G of a query tile are never written by TMA: zero them once
+        for (int st = 0; st < 2; ++st)
+            for (int c = 0; c < C::KCH; ++c)
+                for (int x = p.P * p.G * 128 + tid * 16; x < 128 * 128; x += kThreadsBwd * 16) {
+                    *reinterpret_cast<uint4*>(&s.q[st][c * C::CHUNK + x]) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(&s.dO[st][c * C::CHUNK + x]) = make_uint4(0, 0, 0, 0);
+                }
+        fence_proxy_async_smem();
+    }
+    if (warp == 2) {
+        tmem_alloc(&s.tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0 && nsteps > 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            tma_prefetch_desc(&tmdo);
+            mbar_expect_tx(&s.kv_full, 2 * C::TILE);
+            for (int c = 0; c < C::KCH; ++c) {
+                tma_load_4d(s.k + c * C::CHUNK, &tmk, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
+                tma_load_4d(s.v + c * C::CHUNK, &tmv, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
+            }
+            const uint32_t qbytes = (uint32_t)(p.P * p.G) * 128u * C::KCH;
+            int q_issued = 0, do_issued = 0;
+            for (int it = 0; it < nsteps; ++it) {
+                const int st = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                const int row = sv.q0 + (qt0 + it) * p.P;
+                if (!mbar_wait(&s.q_empty[st], ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.q_full[st], qbytes);
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_4d(s.q[st] + c * C::CHUNK, &tmq, &s.q_full[st], c * 64, g * p.G, row, sv.tma_b);
+                ++q_issued;
+                if (!mbar_wait(&s.do_empty[st], ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.do_full[st], qbytes);
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_4d(s.dO[st] + c * C::CHUNK, &tmdo, &s.do_full[st], c * 64, g * p.G, row, sv.tma_b);
+                ++do_issued;
+            }
+            for (int back = 1; back <= 2; ++back) {
+                if (q_issued - back >= 0) mbar_wait_quiet(&s.q_full[(q_issued - back) & 1], ((q_issued - back) >> 1) & 1);
+                if (do_issued - back >= 0)
+                    mbar_wait_quiet(&s.do_full[(do_issued - back) & 1], ((do_issued - back) >> 1) & 1);
+            }
+            mbar_wait_quiet(&s.kv_full, 0);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0 && nsteps > 0) {
+            constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: K-major both
+            constexpr uint32_t id_dv = idesc_bf16(128, D, false, true);    // A from TMEM, B MN-major
+            constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);    // A K-major, B MN-major
+            constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);     // A MN-major, B MN-major
+            const uint32_t ka = smem_u32(s.k), va = smem_u32(s.v);
+            bool ok = mbar_wait(&s.kv_full, 0, ab);
+            tc_fence_after();
+            for (int it = 0; ok && it < nsteps; ++it) {
+                const int st = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                const uint32_t par = it & 1;
+                const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
+                // S^T = K Q_i^T
+                if (!(ok = mbar_wait(&s.q_full[st], ph, ab))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+                    mma_ss(tmem + C::C_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_s, kk > 0);
+                }
+                tc_commit(&s.s_full);
+                // dP^T = V dO_i^T (its columns held dQ_{i-1} when D == 128)
+                if (!(ok = mbar_wait(&s.do_full[st], ph, ab))) break;
+                if (C::DQ_OVER_DP && it > 0) {
+                    if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+                    mma_ss(tmem + C::C_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), id_s, kk > 0);
+                }
+                tc_commit(&s.dp_full);
+                // dV += P^T dO_i
+                if (!(ok = mbar_wait(&s.p_full, par, ab))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // query pairs of group kk/4 sit at columns 64*(kk/4) + 8*(kk%4)
+                    mma_ts(tmem + C::C_DV, tmem + C::C_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                           sdesc_sw128(da + kk * 2048, C::CHUNK, 1024), id_dv, (it > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&s.do_empty[st]);
+                // dK += dS^T Q_i ;  dQ_i = dS K
+                if (!(ok = mbar_wait(&s.ds_full, par, ab))) break;
+                if (!C::DQ_OVER_DP && it > 0) {
+                    if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(s.dst[0]);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                    mma_ss(tmem + C::C_DK, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, C::CHUNK, 1024),
+                           id_dk, (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(&s.q_empty[st]);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + C::C_DQ, sdesc_sw128(sa + kk * 2048, 128 * 128, 1024),
+                           sdesc_sw128(ka + kk * 2048, C::CHUNK, 1024), id_dq, kk > 0);
+                tc_commit(&s.dq_full);
+                tc_commit(&s.ds_free);
+            }
+            tc_commit(&s.dkv_full);
+            mbar_wait_quiet(&s.dkv_full, 0);
+        }
+    } else if (warp >= 4) {
+        // ================= compute groups =================
+        const int cg = (warp - 4) >> 2;            // column group
+        const int wq = warp & 3;
+        const int jr = (wq << 5) | lane;           // key row of this thread (TMEM lane)
+        const uint32_t lane_base = (uint32_t)(wq << 5) << 16;
+        const int j = j0 + jr;
+        const float c = p.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < nsteps; ++it) {
+            const uint32_t par = it & 1;
+            const int t = qt0 + it;                 // query tile within the sequence
+            const int s0 = t * p.P;                 // its first query position
+            const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;  // tiled row base
+            const float* lse2 = a.lse2_t + trow + 64 * cg;
+            const float* dlt = a.delta_t + trow + 64 * cg;
+            // edge test: does the band cut this (query tile, key tile) pair?
+            const int iq_first = s0, iq_last = min(s0 + p.P, sv.nq) - 1;
+            const bool interior = j0 >= band.lo(iq_last) && j0 + kRows - 1 <= band.hi(iq_first);
+            // ---- P^T ----
+            {
+                const bool w = mbar_wait(&s.s_full, par, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            tc_fence_after();
+            float pf[64];
+            {
+                uint32_t sr[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + C::C_S + 64 * cg, sr);
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(lse2 + cc);
+                    pf[cc + 0] = ex2(fmaf(__uint_as_float(sr[cc + 0]), c, -l4.x));
+                    pf[cc + 1] = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -l4.y));
+                    pf[cc + 2] = ex2(fmaf(__uint_as_float(sr[cc + 2]), c, -l4.z));
+                    pf[cc + 3] = ex2(fmaf(__uint_as_float(sr[cc + 3]), c, -l4.w));
+                }
+                if (!interior) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc) {
+                        const int qr = 64 * cg + cc;
+                        const int iq = s0 + qr / p.G;
+                        if (j > band.hi(iq) || j < band.lo(iq)) pf[cc] = 0.f;
+                    }
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 2) pk[cc / 2] = pack_bf16(pf[cc], pf[cc + 1]);
+                // P^T of query columns [64cg, 64cg+64) goes over the first half of the S^T
+                // columns this group has just read (the other group never touches them)
+                tmem_st_32x32b_x32(tmem + lane_base + C::C_S + 64 * cg, pk);
+            }
+            tc_fence_before();
+            mbar_arrive(&s.p_full);
+            // ---- dS^T = P^T (dP^T - D) -> shared memory ----
+            {
+                const bool w = mbar_wait(&s.dp_full, par, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            if (it > 0) {
+                const bool w = mbar_wait(&s.ds_free, par ^ 1, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            tc_fence_after();
+            {
+                uint8_t* drow = s.dst[cg] + jr * 128;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t dr[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DP + 64 * cg + 32 * hf, dr);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {  // 16-byte units of 8 columns
+                        const int cb = 32 * hf + 8 * u;
+                        const float4 d0 = *reinterpret_cast<const float4*>(dlt + cb);
+                        const float4 d1 = *reinterpret_cast<const float4*>(dlt + cb + 4);
+                        uint4 w;
+                        w.x = pack_bf16(pf[cb + 0] * (__uint_as_float(dr[8 * u + 0]) - d0.x),
+                                        pf[cb + 1] * (__uint_as_float(dr[8 * u + 1]) - d0.y));
+                        w.y = pack_bf16(pf[cb + 2] * (__uint_as_float(dr[8 * u + 2]) - d0.z),
+                                        pf[cb + 3] * (__uint_as_float(dr[8 * u + 3]) - d0.w));
+                        w.z = pack_bf16(pf[cb + 4] * (__uint_as_float(dr[8 * u + 4]) - d1.x),
+                                        pf[cb + 5] * (__uint_as_float(dr[8 * u + 5]) - d1.y));
+                        w.w = pack_bf16(pf[cb + 6] * (__uint_as_float(dr[8 * u + 6]) - d1.z),
+                                        pf[cb + 7] * (__uint_as_float(dr[8 * u + 7]) - d1.w));
+                        const int unit = (cb >> 3) ^ (jr & 7);
+                        *reinterpret_cast<uint4*>(drow + unit * 16) = w;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&s.ds_full);
+            // ---- dQ_i: thread = query row; reduce into the fp32 workspace ----
+            {
+                const bool w = mbar_wait(&s.dq_full, par, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            tc_fence_after();
+            {
+                const int qr = jr;  // TMEM lane = query row of the tile
+                float* acc = a.dq_acc + (trow + qr) * D + (D / 2) * cg;
+#pragma unroll
+                for (int cb = 0; cb < D / 2; cb += 32) {
+                    uint32_t qv[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg + cb, qv);
+#pragma unroll
+                    for (int t4 = 0; t4 < 8; ++t4)
+                        atomicAdd(reinterpret_cast<float4*>(acc + cb) + t4,
+                                  make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
+                                              __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&s.dq_free);
+        }
+        // ---- epilogue: dK, dV for this key tile ----
+        if (nsteps > 0 && ok) {
+            const bool w = mbar_wait(&s.dkv_full, 0, ab);
+            ok = __all_sync(0xffffffffu, w);
+            tc_fence_after();
+        }
+        const bool row_ok = j <= j1;
+        const long krow = key_row(p, sv, j);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            __nv_bfloat16* dst = (which == 0 ? a.dv : a.dk) + (krow * p.h_kv + g) * D + (D / 2) * cg;
+            const float mul = which == 0 ? 1.f : p.scale;
+            const uint32_t col = (which == 0 ? C::C_DV : C::C_DK) + (D / 2) * cg;
+#pragma unroll
+            for (int cb = 0; cb < D / 2; cb += 32) {
+                uint32_t v[32];
+                if (nsteps > 0 && ok) {
+                    tmem_ld_32x32b_x32(tmem + lane_base + col + cb, v);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) v[t] = 0u;
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(v[8 * t + 0]) * mul, __uint_as_float(v[8 * t + 1]) * mul);
+                        w.y = pack_bf16(__uint_as_float(v[8 * t + 2]) * mul, __uint_as_float(v[8 * t + 3]) * mul);
+                        w.z = pack_bf16(__uint_as_float(v[8 * t + 4]) * mul, __uint_as_float(v[8 * t + 5]) * mul);
+                        w.w = pack_bf16(__uint_as_float(v[8 * t + 6]) * mul, __uint_as_float(v[8 * t + 7]) * mul);
+                        reinterpret_cast<uint4*>(dst + cb)[t] = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// preprocess: one CTA (128 threads) per (tiled query tile, key/value head)
+// ------------------------------------------------------------------------------------------
+// Decodes a tiled query-tile index into (sequence, tile within it); false for an idle tile.
+__device__ __forceinline__ bool decode_qtile(const Problem& p, int idx, int& seq, int& t) {
+    if (p.cu_q) {
+        seq = owner_sequence(p.cu_q, p.B, idx, p.P);
+        t = idx - (p.cu_q[seq] / p.P + seq);
+        return t * p.P < p.cu_q[seq + 1] - p.cu_q[seq];
+    }
+    const int per = cdiv(p.s_q, p.P);
+    seq = idx / per;
+    t = idx % per;
+    return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
+    const Problem& p = a.p;
+    const int idx = blockIdx.x, g = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int seq, t;
+    const bool live = decode_qtile(p, idx, seq, t);
+    const long trow = ((long)g * a.n_qtiles + idx) * 128;
+    if (!live) {
+        a.lse2_t[trow + threadIdx.x] = INFINITY;
+        a.delta_t[trow + threadIdx.x] = 0.f;
+        return;
+    }
+    const SeqView sv = seq_view(p, seq);
+    __shared__ float sink_part[128];  // per query head of this tile (at most G <= 128 heads)
+    if (p.sinks) {
+        sink_part[threadIdx.x] = 0.f;
+        __syncthreads();
+    }
+    for (int rr = 0; rr < 32; ++rr) {
+        const int r = warp * 32 + rr;
+        const int i = t * p.P + r / p.G;
+        const int h = g * p.G + r % p.G;
+        const bool valid = r < p.P * p.G && i < sv.nq;
+        float dsum = 0.f, l2 = INFINITY;
+        if (valid) {
+            const long tok = token_row(p, sv, i);
+            const __nv_bfloat16* orow = a.o + (tok * p.h_q + h) * D;
+            const __nv_bfloat16* drow = a.dout + (tok * p.h_q + h) * D;
+            for (int c = lane * 2; c < D; c += 64) {
+                const uint32_t ov = *reinterpret_cast<const uint32_t*>(orow + c);
+                const uint32_t dv = *reinterpret_cast<const uint32_t*>(drow + c);
+                dsum = fmaf(bf16_lo(ov), bf16_lo(dv), dsum);
+                dsum = fmaf(bf16_hi(ov), bf16_hi(dv), dsum);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+            const float lse = a.lse[lse_index(p, sv, i, h)];
+            l2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+            if (p.sinks && lane == 0 && lse > -INFINITY) {
+                // d(sum O.dO)/d(sink_h) = - exp(sink_h - LSE_i) * D_i
+                atomicAdd(&sink_part[r % p.G], -__expf(p.sinks[h] - lse) * dsum);
+            }
+        }
+        if (lane == 0) {
+            a.delta_t[trow + r] = valid ? dsum : 0.f;
+            a.lse2_t[trow + r] = l2;
+        }
+    }
+    if (p.sinks) {
+        __syncthreads();
+        if ((int)threadIdx.x < p.G) atomicAdd(a.dsinks + g * p.G + threadIdx.x, sink_part[threadIdx.x]);
+    }
+    // zero this tile's dQ accumulator rows
+    float4* acc = reinterpret_cast<float4*>(a.dq_acc + trow * D);
+    for (int x = threadIdx.x; x < 128 * D / 4; x += 128) acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// postprocess: dQ = scale * acc -> bf16 rows
+template <int D>
+__global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
+    const Problem& p = a.p;
+    const int idx = blockIdx.x, g = blockIdx.y;
+    int seq, t;
+    if (!decode_qtile(p, idx, seq, t)) return;
+    const SeqView sv = seq_view(p, seq);
+    const long trow = ((long)g * a.n_qtiles + idx) * 128;
+    constexpr int V = 8;  // columns per thread step
+    for (int x = threadIdx.x; x < 128 * D / V; x += 128) {
+        const int r = x / (D / V), cb = (x % (D / V)) * V;
+        const int i = t * p.P + r / p.G;
+        const int h = g * p.G + r % p.G;
+        if (r >= p.P * p.G || i >= sv.nq) continue;
+        const float4 u0 = *reinterpret_cast<const float4*>(a.dq_acc + (trow + r) * D + cb);
+        const float4 u1 = *reinterpret_cast<const float4*>(a.dq_acc + (trow + r) * D + cb + 4);
+        const float sc = p.scale;
+        uint4 w;
+        w.x = pack_bf16(u0.x * sc, u0.y * sc);
+        w.y = pack_bf16(u0.z * sc, u0.w * sc);
+        w.z = pack_bf16(u1.x * sc, u1.y * sc);
+        w.w = pack_bf16(u1.z * sc, u1.w * sc);
+        *reinterpret_cast<uint4*>(a.dq + (token_row(p, sv, i) * p.h_q + h) * D + cb) = w;
+    }
+}
+
+}  // namespace
+
+template <int D>
+static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, cudaStream_t st) {
+    const size_t smem = sizeof(BwdSmem<D>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.n_kvblocks, a.p.h_kv, a.p.cu_q ? 1 : a.p.B);
+    bwd_main_kernel<D><<<grid, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, cudaStream_t st) {
+    switch (a.p.d) {
+        case 64: return launch_main_d<64>(a, tq, tk, tv, tdo, st);
+        case 128: return launch_main_d<128>(a, tq, tk, tv, tdo, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st) {
+    dim3 grid(a.n_qtiles, a.p.h_kv);
+    if (a.n_qtiles == 0) return cudaSuccess;
+    if (a.p.d == 64) bwd_pre_kernel<64><<<grid, 128, 0, st>>>(a);
+    else bwd_pre_kernel<128><<<grid, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t st) {
+    dim3 grid(a.n_qtiles, a.p.h_kv);
+    if (a.n_qtiles == 0) return cudaSuccess;
+    if (a.p.d == 64) bwd_post_kernel<64><<<grid, 128, 0, st>>>(a);
+    else bwd_post_kernel<128><<<grid, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,93 @@
+// Device-side helpers shared by the attention kernels: mask bands, packed-row
+// bookkeeping and the packed-batch block numbering.
+#pragma once
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+// Allowed key interval [lo(i), hi(i)] of query position i in a sequence of nq queries
+// and nk keys, bottom-right aligned (off = nk - nq).  A causal call arrives here with
+// right = 0, so the causal mask is the right edge of the window.
+struct Band {
+    int off, left, right, nk;
+    __device__ __forceinline__ int lo(int i) const { return left >= 0 ? max(0, i + off - left) : 0; }
+    __device__ __forceinline__ int hi(int i) const {
+        return right >= 0 ? min(nk - 1, i + off + right) : nk - 1;
+    }
+};
+
+// Range [t0, t1) of `bn`-key tiles that intersect the band of query positions
+// [i0, i1] (inclusive); empty (t0 == t1) when no key is allowed.
+__device__ __forceinline__ void kv_tile_range(const Band& bd, int i0, int i1, int bn, int& t0, int& t1) {
+    int jlo = bd.lo(i0);
+    int jhi = bd.hi(i1);
+    if (bd.nk <= 0 || jhi < jlo || i1 < i0) {
+        t0 = t1 = 0;
+        return;
+    }
+    t0 = jlo / bn;
+    t1 = jhi / bn + 1;
+}
+
+// Packed-batch block numbering: sequence s owns blocks starting at cu[s] / bs + s, so a
+// sequence of n tokens has at least ceil(n / bs) blocks and an empty one costs a single
+// idle block.  Returns the sequence that owns block g (binary search over the offsets).
+__device__ __forceinline__ int owner_sequence(const int32_t* cu, int nseq, int g, int bs) {
+    int lo = 0, hi = nseq - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] / bs + mid <= g)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Global view of one sequence's rows.
+struct SeqView {
+    int b;        // batch index (dense) or sequence index (packed)
+    int q0, nq;   // first token row of the sequence and its query count
+    int k0, nk;   // first key row and key count
+    int tma_b;    // 4th TMA coordinate: batch index (dense) or 0 (packed)
+};
+
+__device__ __forceinline__ SeqView seq_view(const Problem& p, int b) {
+    SeqView v;
+    v.b = b;
+    if (p.cu_q) {
+        v.q0 = p.cu_q[b];
+        v.nq = p.cu_q[b + 1] - v.q0;
+        v.k0 = p.cu_k[b];
+        v.nk = p.cu_k[b + 1] - v.k0;
+        v.tma_b = 0;
+    } else {
+        v.q0 = 0;
+        v.nq = p.s_q;
+        v.k0 = 0;
+        v.nk = p.s_kv;
+        v.tma_b = b;
+    }
+    return v;
+}
+
+// Index of (sequence b, local row i, head h) in the LSE output.
+__device__ __forceinline__ long lse_index(const Problem& p, const SeqView& sv, int i, int h) {
+    if (p.cu_q) return (long)h * p.T_q + sv.q0 + i;
+    return ((long)sv.b * p.h_q + h) * p.s_q + i;
+}
+
+// Token row (global) of local row i.
+__device__ __forceinline__ long token_row(const Problem& p, const SeqView& sv, int i) {
+    return p.cu_q ? (long)sv.q0 + i : (long)sv.b * p.s_q + i;
+}
+
+__device__ __forceinline__ long key_row(const Problem& p, const SeqView& sv, int j) {
+    return p.cu_q ? (long)sv.k0 + j : (long)sv.b * p.s_kv + j;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+}  // namespace fa

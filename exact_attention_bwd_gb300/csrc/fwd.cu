@@ -1,0 +1,471 @@
+// Forward attention on the 5th-generation tensor cores (tcgen05 + TMEM), sm_103a.
+//
+// One CTA owns two 128-row query tiles of one key/value head.  A tile's rows are
+// "packed": the G query heads that share the key/value head are interleaved, row
+// r = (position s0 + r / G, head g*G + r % G), so one pass over K/V serves all of them
+// (grouped-query heads; vllm-project/flash-attention README, flash_attn_func docstring).
+//
+// Warp roles (384 threads):
+//   warp 0       TMA producer: Q tiles once, then K and V tiles through a STAGES-deep ring
+//   warp 1       MMA issuer (one thread): S_k = Q_k K^T into TMEM, O_k += P_k V with P_k
+//                read back from TMEM
+//   warp 2       owns the TMEM allocation
+//   warps 4..7   softmax of tile 0, warps 8..11 softmax of tile 1: each thread owns one
+//                row (one TMEM lane); exp2-based online softmax with lazy rescaling
+//
+// The online softmax follows the recurrence of the "Flash Attention Tutorial" README
+// (GitHub search results page, sections 3 to 5): a running max m and running sum l per
+// row, with the accumulated output rescaled when the max moves.  Here the output stays
+// un-normalised in TMEM and is divided by l once at the end, and the running max is only
+// moved when it grows by more than 2^8 (the stale max keeps every exponential below 256,
+// and the final division uses the same max, so the result is unchanged).
+//
+// Key tiles that lie wholly outside a tile's causal / sliding-window band are skipped
+// (fa4-jax PyPI page, "Native two-sided sliding windows"); only tiles that cut the band
+// edge evaluate the mask per element.
+#include "common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreadsFwd = 384;
+constexpr int BN = 128;  // keys per KV tile
+
+template <int D>
+struct FwdCfg {
+    static constexpr int KCH = D / 64;                  // 64-column chunks of a row
+    static constexpr int TILE_BYTES = 128 * D * 2;      // one Q / K / V tile (128 rows)
+    static constexpr int CHUNK_BYTES = 128 * 128;       // one [128 rows][64 cols] chunk
+    static constexpr int STAGES = (D == 64) ? 4 : 2;
+    static constexpr int TMEM_COLS = 512;
+    // TMEM columns: S_k at 128k, O_k at 256 + 128k
+};
+
+template <int D>
+struct __align__(1024) FwdSmem {
+    uint8_t q[2][FwdCfg<D>::TILE_BYTES];
+    uint8_t k[FwdCfg<D>::STAGES][FwdCfg<D>::TILE_BYTES];
+    uint8_t v[FwdCfg<D>::STAGES][FwdCfg<D>::TILE_BYTES];
+    uint64_t q_full;
+    uint64_t k_full[FwdCfg<D>::STAGES], k_empty[FwdCfg<D>::STAGES];
+    uint64_t v_full[FwdCfg<D>::STAGES], v_empty[FwdCfg<D>::STAGES];
+    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ int split_idx(const FwdArgs& a, int bx) { return bx % a.n_splits; }
+
+struct TileInfo {
+    int s0;       // first query position of the tile
+    int t0, t1;   // KV tile range [t0, t1)
+    bool active;  // the tile holds at least one valid query row
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsFwd, 1)
+    fwd_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+               const __grid_constant__ CUtensorMap tmv) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Problem& p = a.p;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    // ---------------- work unit ----------------
+    const int g = blockIdx.y;  // key/value head
+    int seq, blk, split = 0;
+    if (p.cu_q) {
+        const int bs = 2 * p.P;
+        blk = blockIdx.x;
+        seq = owner_sequence(p.cu_q, p.B, blk, bs);
+        blk -= p.cu_q[seq] / bs + seq;
+    } else {
+        seq = blockIdx.z;
+        int x = blockIdx.x;
+        split = x % a.n_splits;
+        x /= a.n_splits;
+        blk = a.n_blocks - 1 - x;  // heaviest (latest) query blocks first
+    }
+    const SeqView sv = seq_view(p, seq);
+    const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
+    TileInfo ti[2];
+    int u0 = 0x7fffffff, u1 = 0;  // union KV range
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        ti[k].s0 = (2 * blk + k) * p.P;
+        ti[k].active = ti[k].s0 < sv.nq;
+        int i1 = min(ti[k].s0 + p.P, sv.nq) - 1;
+        if (ti[k].active) {
+            kv_tile_range(band, ti[k].s0, i1, BN, ti[k].t0, ti[k].t1);
+            if (a.n_splits > 1) {
+                ti[k].t0 = max(ti[k].t0, split * a.split_tiles);
+                ti[k].t1 = min(ti[k].t1, (split + 1) * a.split_tiles);
+                if (ti[k].t1 < ti[k].t0) ti[k].t1 = ti[k].t0;
+            }
+        } else {
+            ti[k].t0 = ti[k].t1 = 0;
+        }
+        if (ti[k].t1 > ti[k].t0) {
+            u0 = min(u0, ti[k].t0);
+            u1 = max(u1, ti[k].t1);
+        }
+    }
+    if (u1 == 0) u0 = 0;
+    if (blk * 2 * p.P >= sv.nq) return;  // idle packed-batch block (uniform for the CTA)
+    // an earlier CTA of this launch gave up: do not start new work
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
+
+    // ---------------- setup ----------------
+    Abort ab{&s.abort_flag, a.status};
+    if (tid == 0) {
+        s.abort_flag = 0;
+        mbar_init(&s.q_full, 1);
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&s.k_full[i], 1);
+            mbar_init(&s.k_empty[i], 1);
+            mbar_init(&s.v_full[i], 1);
+            mbar_init(&s.v_empty[i], 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&s.s_full[k], 1);
+            mbar_init(&s.p_full[k], 128);
+            mbar_init(&s.o_full[k], 1);
+        }
+        mbar_init(&s.drain, 1);
+        fence_mbar_init();
+    }
+    if (p.P * p.G < 128) {
+        // rows past P*G of a Q tile are never written by TMA: zero them once
+        for (int k = 0; k < 2; ++k)
+            for (int c = 0; c < C::KCH; ++c)
+                for (int x = p.P * p.G * 128 + tid * 16; x < 128 * 128; x += kThreadsFwd * 16)
+                    *reinterpret_cast<uint4*>(&s.q[k][c * C::CHUNK_BYTES + x]) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == 2) {
+        tmem_alloc(&s.tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0 && u1 > u0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            const uint32_t qbox = (uint32_t)(p.P * p.G) * 128u;  // bytes of one 64-col Q box
+            uint32_t qbytes = 0;
+            for (int k = 0; k < 2; ++k)
+                if (ti[k].t1 > ti[k].t0) qbytes += qbox * C::KCH;
+            mbar_expect_tx(&s.q_full, qbytes);
+            for (int k = 0; k < 2; ++k) {
+                if (ti[k].t1 <= ti[k].t0) continue;
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_4d(&s.q[k][c * C::CHUNK_BYTES], &tmq, &s.q_full, c * 64, g * p.G, sv.q0 + ti[k].s0,
+                                sv.tma_b);
+            }
+            int it = 0, k_issued = 0, v_issued = 0;
+            for (int j = u0; j < u1; ++j, ++it) {
+                const int st = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1;
+                if (!mbar_wait(&s.k_empty[st], ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.k_full[st], C::TILE_BYTES);
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, g, sv.k0 + j * BN,
+                                sv.tma_b);
+                ++k_issued;
+                if (!mbar_wait(&s.v_empty[st], ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.v_full[st], C::TILE_BYTES);
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, g, sv.k0 + j * BN,
+                                sv.tma_b);
+                ++v_issued;
+            }
+            // wait for every copy still in flight before the CTA may exit
+            for (int back = 1; back <= C::STAGES; ++back) {
+                if (k_issued - back >= 0) {
+                    const int i2 = k_issued - back;
+                    mbar_wait_quiet(&s.k_full[i2 % C::STAGES], (i2 / C::STAGES) & 1);
+                }
+                if (v_issued - back >= 0) {
+                    const int i2 = v_issued - back;
+                    mbar_wait_quiet(&s.v_full[i2 % C::STAGES], (i2 / C::STAGES) & 1);
+                }
+            }
+            mbar_wait_quiet(&s.q_full, 0);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0 && u1 > u0) {
+            constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
+            constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+            bool ok = mbar_wait(&s.q_full, 0, ab);
+            tc_fence_after();
+            uint32_t pcount[2] = {0, 0};
+            auto issue_s = [&](int k, int st) {
+                const uint32_t qa = smem_u32(s.q[k]), ka = smem_u32(s.k[st]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                    mma_ss(tmem + 128 * k, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
+                           kk > 0);
+                }
+                tc_commit(&s.s_full[k]);
+            };
+            int it = 0;
+            if (ok) {
+                // prologue: S_k for the first KV tile
+                ok = mbar_wait(&s.k_full[0], 0, ab);
+                if (ok) {
+                    tc_fence_after();
+                    for (int k = 0; k < 2; ++k)
+                        if (u0 >= ti[k].t0 && u0 < ti[k].t1) issue_s(k, 0);
+                    tc_commit(&s.k_empty[0]);
+                }
+            }
+            for (int j = u0; ok && j < u1; ++j, ++it) {
+                const int st = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1;
+                const int st1 = (it + 1) % C::STAGES;
+                const uint32_t ph1 = ((it + 1) / C::STAGES) & 1;
+                bool k_next_ready = false;
+                if (!(ok = mbar_wait(&s.v_full[st], ph, ab))) break;
+                tc_fence_after();
+                for (int k = 0; k < 2 && ok; ++k) {
+                    if (j >= ti[k].t0 && j < ti[k].t1) {
+                        if (!(ok = mbar_wait(&s.p_full[k], pcount[k] & 1, ab))) break;
+                        ++pcount[k];
+                        tc_fence_after();
+                        const uint32_t va = smem_u32(s.v[st]);
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            mma_ts(tmem + 256 + 128 * k, tmem + 128 * k + kk * 8,
+                                   sdesc_sw128(va + kk * 2048, C::CHUNK_BYTES, 1024), idO,
+                                   (j > ti[k].t0 || kk > 0) ? 1u : 0u);
+                        if (j == ti[k].t1 - 1) tc_commit(&s.o_full[k]);
+                    }
+                    if (j + 1 < u1 && j + 1 >= ti[k].t0 && j + 1 < ti[k].t1) {
+                        if (!k_next_ready) {
+                            if (!(ok = mbar_wait(&s.k_full[st1], ph1, ab))) break;
+                            tc_fence_after();
+                            k_next_ready = true;
+                        }
+                        issue_s(k, st1);
+                    }
+                }
+                tc_commit(&s.v_empty[st]);
+                if (k_next_ready) tc_commit(&s.k_empty[st1]);
+                else if (j + 1 < u1 && ok) {
+                    // the next K tile feeds no S of this CTA (cannot happen for a contiguous
+                    // union of two bands, kept for safety): release it once it lands
+                    if ((ok = mbar_wait(&s.k_full[st1], ph1, ab))) tc_commit(&s.k_empty[st1]);
+                }
+            }
+            // let every issued MMA finish before the CTA tears down
+            tc_commit(&s.drain);
+            mbar_wait_quiet(&s.drain, 0);
+        }
+    } else if (warp >= 4) {
+        // ================= softmax: one thread per row =================
+        const int k = (warp - 4) >> 2;           // query tile
+        const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+        const uint32_t tS = tmem + lane_base + 128 * k;
+        const uint32_t tO = tmem + lane_base + 256 + 128 * k;
+        const int i = ti[k].s0 + r / p.G;        // query position
+        const int h = g * p.G + r % p.G;         // query head
+        const bool row_valid = ti[k].active && (r < p.P * p.G) && i < sv.nq;
+        const int jlo = row_valid ? band.lo(i) : 1;
+        const int jhi = row_valid ? band.hi(i) : 0;
+        const float c = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        uint32_t scount = 0;
+        bool ok = true;
+        for (int j = ti[k].t0; j < ti[k].t1; ++j) {
+            const bool w = mbar_wait(&s.s_full[k], scount & 1, ab);
+            if (!__all_sync(0xffffffffu, w)) {
+                ok = false;
+                break;
+            }
+            ++scount;
+            tc_fence_after();
+            // pass 1: row max over the tile (two 64-column halves)
+            const int j0 = j * BN;
+            const bool edge = (j0 < jlo || j0 + BN - 1 > jhi);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t sr[64];
+                tmem_ld_32x32b_x64(tS + 64 * hf, sr);
+                if (edge) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc) {
+                        const int jj = j0 + 64 * hf + cc;
+                        if (jj >= jlo && jj <= jhi) mx = fmaxf(mx, __uint_as_float(sr[cc]));
+                    }
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc) mx = fmaxf(mx, __uint_as_float(sr[cc]));
+                }
+            }
+            const float m_new = fmaxf(m_used, mx * c);
+            float alpha = 1.f;
+            bool rescale = false;
+            if (m_used == -INFINITY) {
+                m_used = m_new;  // nothing accumulated yet (O is exactly 0)
+            } else if (m_new > m_used + 8.f) {
+                alpha = ex2(m_used - m_new);
+                m_used = m_new;
+                l *= alpha;
+                rescale = true;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O_k row *= alpha (warp-wide TMEM access; alpha = 1 on the other lanes)
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 32) {
+                    uint32_t orr[32];
+                    tmem_ld_32x32b_x32(tO + cb, orr);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) orr[t] = __float_as_uint(__uint_as_float(orr[t]) * alpha);
+                    tmem_st_32x32b_x32(tO + cb, orr);
+                }
+            }
+            // pass 2: P = exp2(S*c - m) as bf16 pairs, written over the S columns already read
+            const float base = (m_used == -INFINITY) ? 0.f : m_used;
+            float sum = 0.f;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t sr[64];
+                tmem_ld_32x32b_x64(tS + 64 * hf, sr);
+                if (edge) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc) {
+                        const int jj = j0 + 64 * hf + cc;
+                        if (jj < jlo || jj > jhi) sr[cc] = __float_as_uint(-INFINITY);
+                    }
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 2) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[cc]), c, -base));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -base));
+                    sum += p0 + p1;
+                    pk[cc / 2] = pack_bf16(p0, p1);
+                }
+                tmem_st_32x32b_x32(tS + 32 * hf, pk);
+            }
+            l += sum;
+            tc_fence_before();
+            mbar_arrive(&s.p_full[k]);
+        }
+        // ---------------- epilogue ----------------
+        const bool has_o = ti[k].t1 > ti[k].t0;  // uniform over the warp group
+        if (has_o && ok) {
+            const bool w = mbar_wait(&s.o_full[k], 0, ab);
+            ok = __all_sync(0xffffffffu, w);
+            tc_fence_after();
+        }
+        const bool split_mode = a.n_splits > 1;
+        float oscale = 0.f, lse = -INFINITY;
+        if (!split_mode && p.sinks && row_valid) {
+            const float s2 = p.sinks[h] * kLog2e;
+            const float mf = fmaxf(m_used, s2);
+            const float wgt = (m_used == -INFINITY) ? 0.f : ex2(m_used - mf);
+            const float lt = l * wgt + ex2(s2 - mf);
+            oscale = wgt / lt;
+            lse = (mf + log2f(lt)) * kLn2;
+        } else if (l > 0.f) {
+            oscale = 1.f / l;
+            lse = (m_used + log2f(l)) * kLn2;
+        }
+        const long nrows = (long)p.B * p.h_q * p.s_q;
+        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;  // split-mode row (dense only)
+        if (row_valid) {
+            if (!split_mode) {
+                if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
+            } else {
+                a.lse_part[(long)split_idx(a, blockIdx.x) * nrows + prow] = lse;
+            }
+        }
+        if (has_o && ok) {
+            // warp-collective TMEM reads; only valid rows store
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t orr[32];
+                tmem_ld_32x32b_x32(tO + cb, orr);
+                if (!row_valid) continue;
+                if (!split_mode) {
+                    __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        uint4 wv;
+                        wv.x = pack_bf16(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
+                        wv.y = pack_bf16(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
+                        wv.z = pack_bf16(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
+                        wv.w = pack_bf16(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
+                        reinterpret_cast<uint4*>(orow)[t] = wv;
+                    }
+                } else {
+                    float* op = a.o_part + ((long)split_idx(a, blockIdx.x) * nrows + prow) * D + cb;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        reinterpret_cast<float4*>(op)[t] = make_float4(
+                            __uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
+                            __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
+                }
+            }
+        } else if (row_valid) {
+            if (!split_mode) {
+                __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
+#pragma unroll
+                for (int t = 0; t < D / 8; ++t) reinterpret_cast<uint4*>(orow)[t] = make_uint4(0, 0, 0, 0);
+            } else {
+                float* op = a.o_part + ((long)split_idx(a, blockIdx.x) * nrows + prow) * D;
+#pragma unroll
+                for (int t = 0; t < D / 4; ++t) reinterpret_cast<float4*>(op)[t] = make_float4(0, 0, 0, 0);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+template <int D>
+static cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t st) {
+    const size_t smem = sizeof(FwdSmem<D>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid;
+    if (a.p.cu_q)
+        grid = dim3(a.n_blocks, a.p.h_kv, 1);
+    else
+        grid = dim3(a.n_blocks * a.n_splits, a.p.h_kv, a.p.B);
+    fwd_kernel<D><<<grid, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       cudaStream_t st) {
+    switch (a.p.d) {
+        case 64: return launch_fwd_d<64>(a, tq, tk, tv, st);
+        case 128: return launch_fwd_d<128>(a, tq, tk, tv, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa

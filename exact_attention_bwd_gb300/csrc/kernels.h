@@ -1,0 +1,97 @@
+// Launch-argument structures shared by the host planner (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Problem description after host-side normalisation.
+struct Problem {
+    int B, s_q, s_kv, h_q, h_kv, d;
+    int G;             // h_q / h_kv
+    int P;             // query positions per 128-row tile: floor(128 / G)
+    float scale;       // softmax scale
+    float scale_log2;  // softmax scale * log2(e)
+    int causal;
+    int left, right;   // -1 = unbounded side; a causal call has right = 0
+    const float* sinks;       // [h_q] fp32 or null
+    const int32_t* cu_q;      // [B+1] or null (dense)
+    const int32_t* cu_k;
+    int T_q, T_k;             // packed token counts (varlen)
+};
+
+// ------------------------------------------------------------------------------------------
+// forward (tensor-core path)
+// ------------------------------------------------------------------------------------------
+struct FwdArgs {
+    Problem p;
+    int n_blocks;      // CTA work units along grid.x (before splitting)
+    int n_splits;      // KV splits (1 = write final outputs)
+    int split_tiles;   // KV tiles per split
+    __nv_bfloat16* o;  // [tokens, h_q, d]
+    float* lse;        // [B, h_q, s_q] or [h_q, T_q]; may be null
+    float* o_part;     // split mode: [n_splits, rows, d] fp32
+    float* lse_part;   // split mode: [n_splits, rows] fp32 (natural log, no sink)
+    int* status;
+};
+
+// ------------------------------------------------------------------------------------------
+// decode (CUDA-core path for few query rows per key/value head)
+// ------------------------------------------------------------------------------------------
+struct DecodeArgs {
+    Problem p;
+    const __nv_bfloat16* q;
+    int n_splits;
+    int split_keys;    // keys per split (a multiple of the key tile)
+    float* o_part;     // [n_splits, rows, d]
+    float* lse_part;   // [n_splits, rows]
+    int* status;
+};
+
+struct CombineArgs {
+    Problem p;
+    int n_splits;
+    const float* o_part;
+    const float* lse_part;
+    __nv_bfloat16* o;
+    float* lse;
+};
+
+// ------------------------------------------------------------------------------------------
+// backward
+// ------------------------------------------------------------------------------------------
+struct BwdArgs {
+    Problem p;
+    int n_qtiles;          // q tiles per (key/value head) in the tiled layouts below
+    int n_kvblocks;        // grid.x of the main kernel
+    const __nv_bfloat16* o;
+    const float* lse;
+    const __nv_bfloat16* dout;
+    float* delta_t;        // [h_kv, n_qtiles, 128]  rowsum(dO * O)
+    float* lse2_t;         // [h_kv, n_qtiles, 128]  LSE * log2(e) (+inf for empty rows)
+    float* dq_acc;         // [h_kv, n_qtiles, 128, d] fp32
+    __nv_bfloat16* dq;     // [tokens, h_q, d]
+    __nv_bfloat16* dk;     // [tokens_k, h_kv, d]
+    __nv_bfloat16* dv;
+    float* dsinks;         // [h_q] or null
+    int* status;
+};
+
+// host-side launchers (defined next to each kernel)
+cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t st);
+cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t st);
+
+// Number of 16-byte-aligned KV tiles etc. shared by planner and kernels.
+constexpr int kTileRows = 128;
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace fa

@@ -173,3 +173,15 @@ def make(w: dict) -> dict:
     out["sinks"] = normal_f32(seed_of(wid, var, SINKS), (h_q,)) if w.get("sinks") else None
     out.setdefault("scale", 1.0 / math.sqrt(d))
     return out
+
+
+def normal_bf16_torch(seed: int, shape, device):
+    """i.i.d. N(0, 1) bf16 tensor drawn on `device` by torch's seeded Philox generator.
+
+    For inputs too large to draw on the host in reasonable time (the long key/value
+    caches); slices are copied back to the host for the oracle.
+    """
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)

@@ -1,0 +1,144 @@
+/*
+ * fa.h — C ABI of libfa_gb300.so: exact softmax attention, forward and backward,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (the plain definition; the kernels reach it with an online
+ * softmax that never materialises the S x S matrix):
+ *
+ *   O_i   = sum_j P_ij v_j,   P_ij = exp(scale * q_i.k_j - LSE_i) over the allowed keys j
+ *   LSE_i = log( sum_j exp(scale * q_i.k_j) [+ exp(sink_h)] )
+ *
+ * following the "Flash Attention Tutorial" README (GitHub search results page for
+ * "flash attention implementation notes"), sections 1-5 for the forward and
+ * section 6 "Key derivations" for the backward (dV = P^T dO; D_i = dO_i.O_i;
+ * dS_ij = P_ij (dO_i.v_j - D_i); dQ = scale dS K; dK = scale dS^T Q — the scale
+ * is kept in dQ and dK, which that tutorial's listing omits).
+ *
+ * Masks are bottom-right aligned when s_q != s_kv (vllm-project/flash-attention
+ * README, flash_attn_func and flash_attn_with_kvcache docstrings, changelog 2.1):
+ * with off = s_kv - s_q of the sequence, query i keeps key j iff
+ *   causal      : j <= i + off
+ *   window_left  >= 0 : j >= i + off - window_left
+ *   window_right >= 0 : j <= i + off + window_right      (inclusive; -1 = unbounded)
+ * A causal call with a window keeps the intersection.  A row with no allowed key
+ * gets O = 0 and LSE = -inf (LSE = sink_h when the head has a sink).
+ *
+ * Grouped-query heads: h_kv divides h_q and query head h reads key/value head
+ * h / (h_q / h_kv) (same README, flash_attn_func docstring: 6 query heads on 2
+ * key/value heads map 0,1,2 -> 0 and 3,4,5 -> 1).
+ *
+ * Sinks: one fp32 logit per query head joins every row's softmax denominator and
+ * carries no value (dew-flash-attn PyPI page, the sinks paragraph).  The returned
+ * LSE includes the sink; fa_bwd returns the sink gradient
+ *   dsink_h = - sum_rows exp(sink_h - LSE_i) D_i.
+ *
+ * Packed batches (dew-flash-attn PyPI page, "Packed sequences"; fa4-jax PyPI page,
+ * "Varlen semantics"): with cu_seqlens_q / cu_seqlens_k given, tensors are
+ * [T, H, D], sequence b owns rows cu[b] .. cu[b+1]-1, masks apply per sequence,
+ * attention never crosses sequences, zero-length sequences are legal, and the
+ * LSE is laid out [h_q, T_q].  The offsets are read on the device and are not
+ * checked unless FA_FLAG_VALIDATE_CU is set (tokens they do not cover get
+ * unspecified outputs, as on the pages).
+ *
+ * Conventions common to every call:
+ *  - Layouts: dense tensors are contiguous [B, S, H, D] bf16; packed ones [T, H, D].
+ *    LSE is fp32 [B, h_q, s_q] (dense) or [h_q, T_q] (packed), natural log.
+ *  - Ownership: every pointer is caller-owned device memory (except the params
+ *    struct itself, read on the host during the call).  The library allocates no
+ *    device memory; scratch lives in the caller's workspace, sized by the
+ *    fa_*_workspace_size functions.  Base pointers of q, k, v, o, dout, dq, dk, dv
+ *    and the workspace must be 16-byte aligned.
+ *  - Streams: work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronising.
+ *  - Errors: arguments are checked on the host before anything is launched; a
+ *    violation returns a code and launches nothing.  No C++ exception crosses this
+ *    ABI and no kernel traps: a kernel whose pipeline stalls gives up after a time
+ *    limit and records FA_ERR_TIMEOUT in the workspace status word, which
+ *    fa_read_device_status reports.
+ *  - Supported: bf16; head dim d in {64, 128} for both passes, plus d = 256 for
+ *    forward calls with at most 16 query rows per key/value head (decode shapes);
+ *    h_q / h_kv <= 128.  Anything else returns FA_ERR_UNSUPPORTED.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* a null, misaligned or inconsistent argument */
+    FA_ERR_UNSUPPORTED = 2,  /* a valid problem this build does not implement */
+    FA_ERR_WORKSPACE = 3,    /* workspace smaller than fa_*_workspace_size */
+    FA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    FA_ERR_TIMEOUT = 5,      /* a kernel pipeline stalled and gave up (device status) */
+    FA_ERR_DEVICE_CHECK = 6  /* a device-side argument check failed (device status) */
+} fa_status;
+
+/* Flags */
+#define FA_FLAG_VALIDATE_CU 1u  /* check cu_seqlens on the device; result in the status word */
+#define FA_FLAG_NO_SPLIT 2u     /* forward: never split the key range across CTAs */
+
+typedef struct fa_params {
+    int B;            /* batch (dense) or number of sequences (packed) */
+    int s_q, s_kv;    /* sequence lengths (dense); total tokens T_q, T_k (packed) */
+    int h_q, h_kv;    /* query heads, key/value heads (h_kv divides h_q) */
+    int d;            /* head dimension */
+    float softmax_scale;  /* <= 0 selects 1 / sqrt(d) */
+    int causal;           /* nonzero: bottom-right aligned causal mask */
+    int window_left, window_right;  /* -1 = unbounded side */
+    const float *sinks;             /* device fp32 [h_q], or NULL */
+    const int32_t *cu_seqlens_q;    /* device int32 [B+1], or NULL for dense tensors */
+    const int32_t *cu_seqlens_k;    /* device int32 [B+1]; required iff cu_seqlens_q */
+    int max_seqlen_q, max_seqlen_k; /* optional hints (0 = unknown); never needed */
+    unsigned flags;                 /* FA_FLAG_* */
+} fa_params;
+
+/* Bytes of workspace fa_fwd / fa_bwd need for these parameters (>= 256: the first
+ * 256 bytes hold the device status word).  Returns 0 when the parameters are
+ * invalid or unsupported. */
+size_t fa_fwd_workspace_size(const fa_params *p);
+size_t fa_bwd_workspace_size(const fa_params *p);
+
+/* Forward.  q: [.., h_q, d]; k, v: [.., h_kv, d]; o: layout of q (written);
+ * lse: fp32 (written; may be NULL when not wanted). */
+fa_status fa_fwd(const fa_params *p, const void *q, const void *k, const void *v, void *o, float *lse,
+                 void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
+
+/* Backward of L = sum(O * dout).  o and lse must be what fa_fwd returned for the
+ * same inputs.  dq: layout of q; dk, dv: layout of k (all written, bf16).
+ * dsinks: fp32 [h_q], written when p->sinks is given (must then be non-NULL). */
+fa_status fa_bwd(const fa_params *p, const void *q, const void *k, const void *v, const void *o,
+                 const float *lse, const void *dout, void *dq, void *dk, void *dv, float *dsinks,
+                 void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
+
+/* Synchronises `stream` and returns the status word the kernels of the last call
+ * on this workspace left (FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK), or
+ * FA_ERR_CUDA if the stream itself reports an error. */
+fa_status fa_read_device_status(const void *workspace, struct CUstream_st *stream);
+
+/* Static text for a status code. */
+const char *fa_status_string(fa_status s);
+
+/* Per-kernel timing: when enabled, every launch the library makes is bracketed by
+ * CUDA events on its stream.  fa_profile_read synchronises on the last launch of
+ * the named kernel ("fwd", "decode", "combine", "bwd_pre", "bwd_main", "bwd_post")
+ * and writes its duration in milliseconds; returns FA_ERR_INVALID_ARG for an
+ * unknown name or a kernel not launched since profiling was enabled. */
+fa_status fa_profile_enable(int on);
+fa_status fa_profile_read(const char *kernel, float *ms);
+
+/* Library version string. */
+const char *fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,130 @@
+"""The C ABI on a host without a GPU: exports, argument checks and workspace sizing.
+
+Every call here fails its host-side checks before anything is launched (the pointers
+are never dereferenced), or only asks for a workspace size.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from exact_attention_bwd_gb300 import binding as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    lib = fa.load()
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} is declared in include/fa.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (fa_\w+)", out))
+    assert set(names) <= exported
+    assert set(names) == set(fa.EXPORTS)
+
+
+def test_status_strings():
+    for code in range(7):
+        assert fa.fa_status_string(code) and fa.fa_status_string(code) != "unknown status"
+    assert fa.fa_status_string(99) == "unknown status"
+
+
+def params(**kw):
+    p = fa.FaParams()
+    base = dict(B=1, s_q=256, s_kv=256, h_q=4, h_kv=2, d=128, softmax_scale=0.0, causal=0, window_left=-1,
+                window_right=-1, sinks=None, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=0, max_seqlen_k=0,
+                flags=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+FAKE = ctypes.c_void_p(0x100000)     # 16-byte aligned, never dereferenced
+MISAL = ctypes.c_void_p(0x100008)
+
+
+def call_fwd(p, q=FAKE, k=FAKE, v=FAKE, o=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    return fa.fa_fwd(p, q, k, v, o, None, ws, ws_bytes, None)
+
+
+def call_bwd(p, dsinks=FAKE, ws=FAKE, ws_bytes=1 << 30, q=FAKE):
+    return fa.fa_bwd(p, q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dsinks, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h_q=6, h_kv=4), fa.FA_ERR_INVALID_ARG),          # h_kv must divide h_q
+    (dict(B=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(h_q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(window_left=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(cu_seqlens_q=0x2000), fa.FA_ERR_INVALID_ARG),     # cu_q without cu_k
+    (dict(d=100), fa.FA_ERR_UNSUPPORTED),                    # not a multiple of 8
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),                    # d=256 only for decode shapes
+    (dict(h_q=256, h_kv=1, s_q=1), fa.FA_ERR_UNSUPPORTED),   # group of 256 heads
+])
+def test_forward_rejects(kw, code):
+    assert call_fwd(params(**kw)) == code
+
+
+def test_forward_pointer_checks():
+    p = params()
+    assert call_fwd(p, q=None) == fa.FA_ERR_INVALID_ARG
+    assert call_fwd(p, o=MISAL) == fa.FA_ERR_INVALID_ARG
+    assert call_fwd(p, ws=None) == fa.FA_ERR_INVALID_ARG
+    assert call_fwd(p, ws=MISAL) == fa.FA_ERR_INVALID_ARG
+
+
+def test_workspace_too_small():
+    p = params(s_q=1, s_kv=4096, h_q=8, h_kv=2, causal=1)   # decode shape: needs split partials
+    need = fa.fa_fwd_workspace_size(p)
+    assert need > 256
+    assert call_fwd(p, ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+    pb = params()
+    needb = fa.fa_bwd_workspace_size(pb)
+    assert call_bwd(pb, ws_bytes=needb - 1) == fa.FA_ERR_WORKSPACE
+
+
+def test_backward_rejects():
+    assert call_bwd(params(sinks=0x3000), dsinks=None) == fa.FA_ERR_INVALID_ARG
+    assert call_bwd(params(d=256)) == fa.FA_ERR_UNSUPPORTED
+    assert call_bwd(params(h_q=3, h_kv=2)) == fa.FA_ERR_INVALID_ARG
+    assert call_bwd(params(), q=MISAL) == fa.FA_ERR_INVALID_ARG
+
+
+def test_workspace_sizes():
+    # dense prefill forward needs only the status word
+    assert fa.fa_fwd_workspace_size(params()) == 256
+    # backward: status + tiled D and LSE (h_kv x tiles x 128 fp32 each) + dQ accumulator
+    p = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=64)
+    G, P = 2, 64
+    tiles = 2 * -(-300 // P)
+    stat = 2 * tiles * 128 * 4
+    align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert fa.fa_bwd_workspace_size(p) == 256 + 2 * align(stat) + align(2 * tiles * 128 * 64 * 4)
+    # invalid parameters report 0
+    assert fa.fa_fwd_workspace_size(params(h_q=5, h_kv=2)) == 0
+    assert fa.fa_bwd_workspace_size(params(d=96)) == 0
+
+
+def test_empty_problem_needs_no_launch_until_status():
+    # B = 0: only the status-word reset would run; sizes still defined
+    assert fa.fa_fwd_workspace_size(params(B=0)) == 256
+    assert fa.fa_bwd_workspace_size(params(B=0)) == 256
+
+
+def test_profile_read_unknown_kernel():
+    rc, _ = fa.fa_profile_read("nope")
+    assert rc == fa.FA_ERR_INVALID_ARG

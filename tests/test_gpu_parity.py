@@ -1,0 +1,120 @@
+"""GPU parity: the CUDA library against the fp64 oracle, element by element.
+
+Sizes are small enough for the oracle to finish in seconds yet span several 128-row
+tiles with a ragged tail, and cover the masks, grouped-query heads (including a group
+size that does not divide 128), sinks, packed batches with empty sequences, s_q != s_kv
+in both directions, and decode shapes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from exact_attention_bwd_gb300 import inputs
+from gpu_helpers import check, check_lse, f64, oracle_args, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def make_case(wid, variant, *, B=1, s_q=128, s_kv=None, h_q=2, h_kv=None, d=64, causal=False, window=(-1, -1),
+              sinks=False, lengths=None, lengths_k=None):
+    w = dict(wid=wid, variant=variant, B=B, s_q=s_q, s_kv=s_kv if s_kv is not None else s_q, h_q=h_q,
+             h_kv=h_kv or h_q, d=d, causal=causal, window=window, sinks=sinks, varlen=lengths is not None)
+    if lengths is not None:
+        w["lengths"] = lengths
+        if lengths_k is not None:
+            w["lengths_k"] = lengths_k
+        w["B"] = len(lengths)
+    return inputs.make(w)
+
+
+def compare(w, bwd=True, flags=0):
+    got = run_gpu(w, bwd=bwd, flags=flags)
+    q, k, v, do = f64(w, "q"), f64(w, "k"), f64(w, "v"), f64(w, "dout")
+    kw = oracle_args(w)
+    o, lse, _ = oracle.fwd(q, k, v, **kw)
+    check("O", got["o"], o)
+    check_lse("LSE", got["lse"], lse)
+    if bwd:
+        dq, dk, dv, ds = oracle.bwd(q, k, v, do, **kw)
+        check("dQ", got["dq"], dq)
+        check("dK", got["dk"], dk)
+        check("dV", got["dv"], dv)
+        if ds is not None:
+            scale = max(1.0, float(np.abs(ds).max()))
+            err = float(np.abs(got["dsinks"] - ds).max())
+            assert err <= 2e-2 * scale, f"dsink max-abs {err:.3e} (scale {scale:.2f})"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_workload(causal):
+    """B=1, s=128, h=2, d=64, scale 1/8 — the tiny forward+backward workload."""
+    compare(inputs.make(inputs.workload("tiny_causal" if causal else "tiny")))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_multi_tile(d, causal):
+    compare(make_case(100, 10 * d + causal, B=2, s_q=300, h_q=4, d=d, causal=causal))
+
+
+@pytest.mark.parametrize("s_q,s_kv", [(200, 333), (333, 200), (1, 300), (257, 1)])
+def test_bottom_right_alignment(s_q, s_kv):
+    compare(make_case(101, s_q % 97, B=2, s_q=s_q, s_kv=s_kv, h_q=2, d=64, causal=True))
+
+
+@pytest.mark.parametrize("window,causal", [((127, 0), True), ((128, 128), False), ((5, 40), False),
+                                           ((0, 0), False), ((-1, 3), False), ((300, -1), False)])
+def test_gqa_windows_sinks(window, causal):
+    compare(make_case(102, window[0] % 50 + 3, B=1, s_q=700, h_q=16, h_kv=2, d=64, causal=causal, window=window,
+                      sinks=True))
+
+
+@pytest.mark.parametrize("h_q,h_kv,d", [(6, 2, 64), (6, 2, 128), (8, 1, 128), (5, 5, 64)])
+def test_group_sizes(h_q, h_kv, d):
+    compare(make_case(103, h_q + 10 * h_kv, B=2, s_q=250, h_q=h_q, h_kv=h_kv, d=d, causal=True, sinks=True))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_packed_batch(d):
+    # the pages' offsets [0, 17, 300, 428] plus empty and one-token sequences
+    lengths = [17, 283, 128, 0, 1, 0, 300, 129]
+    compare(make_case(104, d, h_q=4, h_kv=2, d=d, causal=True, lengths=lengths))
+
+
+def test_packed_batch_different_q_k_packing():
+    compare(make_case(105, 0, h_q=4, h_kv=4, d=64, causal=True, lengths=[1, 5, 0, 130, 64, 3],
+                      lengths_k=[300, 5, 17, 200, 0, 1], sinks=True))
+
+
+def test_packed_batch_window():
+    compare(make_case(105, 1, h_q=8, h_kv=2, d=128, causal=False, window=(50, 20),
+                      lengths=[400, 3, 0, 250], sinks=True))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("s_q", [1, 4])
+def test_decode_shapes(d, s_q):
+    """Few query rows per key/value head against a long cache (CUDA-core split path)."""
+    compare(make_case(106, d + s_q, B=2, s_q=s_q, s_kv=3000, h_q=8, h_kv=2, d=d, causal=True), bwd=False)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_chunked_prefill_split(d):
+    """s_q = 64 against a long cache: the tensor-core path with the key range split."""
+    compare(make_case(107, d, B=1, s_q=64, s_kv=4100, h_q=8, h_kv=2, d=d, causal=True), bwd=False)
+
+
+def test_no_split_flag_matches():
+    from exact_attention_bwd_gb300 import binding as fa
+    w = make_case(107, 3, B=1, s_q=64, s_kv=2100, h_q=8, h_kv=2, d=128, causal=True)
+    a = run_gpu(w, bwd=False)
+    b = run_gpu(w, bwd=False, flags=fa.FA_FLAG_NO_SPLIT)
+    check("O split vs unsplit", a["o"], b["o"], max_abs=1e-2, mean_abs=1e-3)
+
+
+def test_empty_key_sequences_give_zero_and_neg_inf():
+    w = make_case(108, 0, h_q=2, d=64, causal=False, lengths=[5, 3], lengths_k=[0, 4])
+    got = run_gpu(w, bwd=True)
+    assert np.all(got["o"][:5] == 0)
+    assert np.all(np.isneginf(got["lse"][:, :5]))
+    assert np.all(got["dq"][:5] == 0)
