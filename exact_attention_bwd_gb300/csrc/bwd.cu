@@ -55,6 +55,7 @@ struct __align__(1024) BwdSmem {
     uint8_t q[2][BwdCfg<D>::TILE];
     uint8_t dO[2][BwdCfg<D>::TILE];
     uint8_t dst[2][128 * 128];   // dS^T: [key row][query col], two 64-column chunks
+    float stat[2][2][128];       // per Q stage: LSE * log2(e) and D of the tile's 128 rows
     uint64_t kv_full;
     uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
     uint64_t s_full, dp_full, p_full, ds_full, ds_free, dq_full, dq_free, dkv_full;
@@ -74,8 +75,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     bwd_main_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
     using C = BwdCfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    BwdSmem<D>& s = *reinterpret_cast<BwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the layout needs 1024-byte alignment (128-byte swizzle atoms) and fills the whole
+    // 227 KB, so there is no room to realign by hand: refuse to run if the window is not
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0 && a.status) atomicCAS(a.status, 0, kStatusDeviceCheck);
+        return;
+    }
+    BwdSmem<D>& s = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.y;
@@ -156,7 +163,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 tma_load_4d(s.k + c * C::CHUNK, &tmk, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
                 tma_load_4d(s.v + c * C::CHUNK, &tmv, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
             }
-            const uint32_t qbytes = (uint32_t)(p.P * p.G) * 128u * C::KCH;
+            const uint32_t tile_bytes = (uint32_t)(p.P * p.G) * 128u * C::KCH;  // one Q or dO tile
+            const uint32_t qbytes = tile_bytes + 2 * 128 * 4;                       // Q plus LSE2, D rows
             int q_issued = 0, do_issued = 0;
             for (int it = 0; it < nsteps; ++it) {
                 const int st = it & 1;
@@ -166,9 +174,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 mbar_expect_tx(&s.q_full[st], qbytes);
                 for (int c = 0; c < C::KCH; ++c)
                     tma_load_4d(s.q[st] + c * C::CHUNK, &tmq, &s.q_full[st], c * 64, g * p.G, row, sv.tma_b);
+                {
+                    const long trow = ((long)g * a.n_qtiles + tbase + qt0 + it) * 128;
+                    bulk_load(s.stat[st][0], a.lse2_t + trow, 512, &s.q_full[st]);
+                    bulk_load(s.stat[st][1], a.delta_t + trow, 512, &s.q_full[st]);
+                }
                 ++q_issued;
                 if (!mbar_wait(&s.do_empty[st], ph ^ 1, ab)) break;
-                mbar_expect_tx(&s.do_full[st], qbytes);
+                mbar_expect_tx(&s.do_full[st], tile_bytes);
                 for (int c = 0; c < C::KCH; ++c)
                     tma_load_4d(s.dO[st] + c * C::CHUNK, &tmdo, &s.do_full[st], c * 64, g * p.G, row, sv.tma_b);
                 ++do_issued;
@@ -262,14 +275,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             const int t = qt0 + it;                 // query tile within the sequence
             const int s0 = t * p.P;                 // its first query position
             const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;  // tiled row base
-            const float* lse2 = a.lse2_t + trow + 64 * cg;
-            const float* dlt = a.delta_t + trow + 64 * cg;
+            const int st = it & 1;
+            const float* lse2 = s.stat[st][0] + 64 * cg;
+            const float* dlt = s.stat[st][1] + 64 * cg;
             // edge test: does the band cut this (query tile, key tile) pair?
             const int iq_first = s0, iq_last = min(s0 + p.P, sv.nq) - 1;
             const bool interior = j0 >= band.lo(iq_last) && j0 + kRows - 1 <= band.hi(iq_first);
             // ---- P^T ----
             {
-                const bool w = mbar_wait(&s.s_full, par, ab);
+                // the stage's LSE / D rows landed with Q_i (already complete by the time S^T is)
+                bool w = mbar_wait(&s.q_full[st], (it >> 1) & 1, ab);
+                w = w && mbar_wait(&s.s_full, par, ab);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             tc_fence_after();
@@ -349,19 +365,20 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             {
                 const int qr = jr;  // TMEM lane = query row of the tile
                 float* acc = a.dq_acc + (trow + qr) * D + (D / 2) * cg;
+                uint32_t qv[D / 2];
+                if constexpr (D == 128)
+                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
+                else
+                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
+                // the columns are free as soon as they are in registers
+                tc_fence_before();
+                mbar_arrive(&s.dq_free);
 #pragma unroll
-                for (int cb = 0; cb < D / 2; cb += 32) {
-                    uint32_t qv[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg + cb, qv);
-#pragma unroll
-                    for (int t4 = 0; t4 < 8; ++t4)
-                        atomicAdd(reinterpret_cast<float4*>(acc + cb) + t4,
-                                  make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
-                                              __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
-                }
+                for (int t4 = 0; t4 < D / 8; ++t4)
+                    atomicAdd(reinterpret_cast<float4*>(acc) + t4,
+                              make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
+                                          __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
             }
-            tc_fence_before();
-            mbar_arrive(&s.dq_free);
         }
         // ---- epilogue: dK, dV for this key tile ----
         if (nsteps > 0 && ok) {
@@ -514,7 +531,7 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
 template <int D>
 static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, cudaStream_t st) {
-    const size_t smem = sizeof(BwdSmem<D>) + 1024;
+    const size_t smem = sizeof(BwdSmem<D>);
     cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.n_kvblocks, a.p.h_kv, a.p.cu_q ? 1 : a.p.B);

@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(kThreadsDec) decode_kernel(const DecodeArgs a,
     const int t_begin = j_begin / BK;
     const int n_tiles = j_end > j_begin ? (j_end - 1) / BK + 1 - t_begin : 0;
 
+    // an earlier CTA of this launch gave up: do not start new work
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     Abort ab{&s.abort_flag, a.status};
     if (tid == 0) {
         s.abort_flag = 0;
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kThreadsDec) decode_kernel(const DecodeArgs a,
     for (int r = 0; r < RMAX; ++r) acc[r][0] = acc[r][1] = 0.f;
 
     int issued = min(C::STAGES, n_tiles);
+    int consumed = 0;  // tiles whose copies have landed and been waited for
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
         const int st = t % C::STAGES;
@@ -117,6 +120,7 @@ __global__ void __launch_bounds__(kThreadsDec) decode_kernel(const DecodeArgs a,
             ok = false;
             break;
         }
+        consumed = t + 1;
         const int j0 = (t_begin + t) * BK;
         // ---- scores: thread = (key, row group) ----
         {
@@ -219,9 +223,10 @@ __global__ void __launch_bounds__(kThreadsDec) decode_kernel(const DecodeArgs a,
             ++issued;
         }
     }
-    // drain copies that are still in flight (abort path)
+    // abort path: wait for the copies issued but never waited for (at most STAGES of
+    // them, each the latest phase of its stage) before the shared memory goes away
     if (tid == 0) {
-        for (int t = 0; t < issued; ++t) mbar_wait_quiet(&s.full[t % C::STAGES], (t / C::STAGES) & 1);
+        for (int t = consumed; t < issued; ++t) mbar_wait_quiet(&s.full[t % C::STAGES], (t / C::STAGES) & 1);
     }
     __syncthreads();
 

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&s.s_full[k], 1);
-            mbar_init(&s.p_full[k], 128);
+            mbar_init(&s.p_full[k], 4);  // one arrive per softmax warp
             mbar_init(&s.o_full[k], 1);
         }
         mbar_init(&s.drain, 1);
@@ -153,7 +153,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-
+    // registers: 384 x 168 at launch; the producer/MMA group hands part of its share to
+    // the two softmax groups (128 x 72 + 256 x 216 = 64512).  The change is made at the
+    // top of each warp group's branch so the register allocator sees it on every path.
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && u1 > u0) {
@@ -272,7 +276,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tc_commit(&s.drain);
             mbar_wait_quiet(&s.drain, 0);
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
         // ================= softmax: one thread per row =================
         const int k = (warp - 4) >> 2;           // query tile
         const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
@@ -296,26 +302,23 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             }
             ++scount;
             tc_fence_after();
-            // pass 1: row max over the tile (two 64-column halves)
+            // one TMEM read of the whole S row (128 fp32 columns)
             const int j0 = j * BN;
             const bool edge = (j0 < jlo || j0 + BN - 1 > jhi);
-            float mx = -INFINITY;
+            uint32_t sr[128];
+            tmem_ld_32x32b_x128(tS, sr);
+            if (edge) {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t sr[64];
-                tmem_ld_32x32b_x64(tS + 64 * hf, sr);
-                if (edge) {
-#pragma unroll
-                    for (int cc = 0; cc < 64; ++cc) {
-                        const int jj = j0 + 64 * hf + cc;
-                        if (jj >= jlo && jj <= jhi) mx = fmaxf(mx, __uint_as_float(sr[cc]));
-                    }
-                } else {
-#pragma unroll
-                    for (int cc = 0; cc < 64; ++cc) mx = fmaxf(mx, __uint_as_float(sr[cc]));
-                }
+                for (int cc = 0; cc < BN; ++cc)
+                    if (j0 + cc < jlo || j0 + cc > jhi) sr[cc] = __float_as_uint(-INFINITY);
             }
-            const float m_new = fmaxf(m_used, mx * c);
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < BN; cc += 2) {
+                mx0 = fmaxf(mx0, __uint_as_float(sr[cc]));
+                mx1 = fmaxf(mx1, __uint_as_float(sr[cc + 1]));
+            }
+            const float m_new = fmaxf(m_used, fmaxf(mx0, mx1) * c);
             float alpha = 1.f;
             bool rescale = false;
             if (m_used == -INFINITY) {
@@ -337,33 +340,23 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     tmem_st_32x32b_x32(tO + cb, orr);
                 }
             }
-            // pass 2: P = exp2(S*c - m) as bf16 pairs, written over the S columns already read
+            // P = exp2(S*c - m) as bf16 pairs, packed in place (slot cc/2 is already consumed)
             const float base = (m_used == -INFINITY) ? 0.f : m_used;
-            float sum = 0.f;
+            float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t sr[64];
-                tmem_ld_32x32b_x64(tS + 64 * hf, sr);
-                if (edge) {
-#pragma unroll
-                    for (int cc = 0; cc < 64; ++cc) {
-                        const int jj = j0 + 64 * hf + cc;
-                        if (jj < jlo || jj > jhi) sr[cc] = __float_as_uint(-INFINITY);
-                    }
-                }
-                uint32_t pk[32];
-#pragma unroll
-                for (int cc = 0; cc < 64; cc += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[cc]), c, -base));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -base));
-                    sum += p0 + p1;
-                    pk[cc / 2] = pack_bf16(p0, p1);
-                }
-                tmem_st_32x32b_x32(tS + 32 * hf, pk);
+            for (int cc = 0; cc < BN; cc += 2) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[cc]), c, -base));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -base));
+                sum0 += p0;
+                sum1 += p1;
+                sr[cc / 2] = pack_bf16(p0, p1);
             }
+            const float sum = sum0 + sum1;
+            tmem_st_32x32b_x64(tS, sr);
             l += sum;
             tc_fence_before();
-            mbar_arrive(&s.p_full[k]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.p_full[k]);
         }
         // ---------------- epilogue ----------------
         const bool has_o = ti[k].t1 > ti[k].t0;  // uniform over the warp group

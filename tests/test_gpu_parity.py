@@ -27,18 +27,38 @@ def make_case(wid, variant, *, B=1, s_q=128, s_kv=None, h_q=2, h_kv=None, d=64, 
     return inputs.make(w)
 
 
-def compare(w, bwd=True, flags=0):
+def compare(w, bwd=True, flags=0, fa_rule=()):
+    """Element-wise parity with the oracle.  Outputs named in `fa_rule` are judged by the
+    pages' secondary rule instead: max error at most twice that of the bf16-operand
+    emulation (tests/bf16_emulation.py) — for shapes where bf16 rounding of the GEMM
+    operands alone exceeds the absolute bound."""
     got = run_gpu(w, bwd=bwd, flags=flags)
     q, k, v, do = f64(w, "q"), f64(w, "k"), f64(w, "v"), f64(w, "dout")
     kw = oracle_args(w)
     o, lse, _ = oracle.fwd(q, k, v, **kw)
-    check("O", got["o"], o)
+    emul = None
+    if fa_rule:
+        import bf16_emulation
+        f32 = lambda x: x.astype(np.float32)  # noqa: E731
+        emul = bf16_emulation.fwd_bwd(f32(q), f32(k), f32(v), f32(do), scale=w["scale"], causal=w["causal"],
+                                      window=w["window"], sinks=kw["sinks"])
+
+    def judge(name, key, ref):
+        if key in fa_rule:
+            e_gpu = float(np.abs(got[key] - ref).max())
+            e_emu = float(np.abs(emul[key] - ref).max())
+            assert e_gpu <= 2.0 * e_emu + 1e-4, f"{name}: max error {e_gpu:.3e} > 2 x bf16 emulation {e_emu:.3e}"
+            assert float(np.abs(got[key] - ref).mean()) <= 2e-3
+        else:
+            check(name, got[key], ref)
+
+    judge("O", "o", o)
     check_lse("LSE", got["lse"], lse)
     if bwd:
         dq, dk, dv, ds = oracle.bwd(q, k, v, do, **kw)
-        check("dQ", got["dq"], dq)
-        check("dK", got["dk"], dk)
-        check("dV", got["dv"], dv)
+        judge("dQ", "dq", dq)
+        judge("dK", "dk", dk)
+        judge("dV", "dv", dv)
         if ds is not None:
             scale = max(1.0, float(np.abs(ds).max()))
             err = float(np.abs(got["dsinks"] - ds).max())
@@ -65,8 +85,11 @@ def test_bottom_right_alignment(s_q, s_kv):
 @pytest.mark.parametrize("window,causal", [((127, 0), True), ((128, 128), False), ((5, 40), False),
                                            ((0, 0), False), ((-1, 3), False), ((300, -1), False)])
 def test_gqa_windows_sinks(window, causal):
+    # window (0, 0): one key per row, so dK is a short sum of large, cancelling dS q terms
+    # and the bf16 rounding of dS alone reaches the absolute bound; judged by the FA rule
+    fa_rule = ("dk", "dq") if window == (0, 0) else ()
     compare(make_case(102, window[0] % 50 + 3, B=1, s_q=700, h_q=16, h_kv=2, d=64, causal=causal, window=window,
-                      sinks=True))
+                      sinks=True), fa_rule=fa_rule)
 
 
 @pytest.mark.parametrize("h_q,h_kv,d", [(6, 2, 64), (6, 2, 128), (8, 1, 128), (5, 5, 64)])
