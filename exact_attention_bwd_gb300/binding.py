@@ -27,7 +27,9 @@ FA_FLAG_VALIDATE_CU = 1
 FA_FLAG_NO_SPLIT = 2
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_read_device_status",
-           "fa_status_string", "fa_profile_enable", "fa_profile_read", "fa_version")
+           "fa_status_string", "fa_profile_enable", "fa_profile_read", "fa_version", "fa_fwd_noalloc")
+
+FA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class FaParams(ctypes.Structure):
@@ -85,6 +87,8 @@ def load(build_if_missing: bool = True):
         lib.fa_profile_enable.restype = ctypes.c_int
         lib.fa_profile_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_float)]
         lib.fa_profile_read.restype = ctypes.c_int
+        lib.fa_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp]
+        lib.fa_fwd_noalloc.restype = ctypes.c_int
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ctypes.c_char_p
         _lib = lib
@@ -97,6 +101,11 @@ def load(build_if_missing: bool = True):
 
 def fa_fwd(params: FaParams, q, k, v, o, lse, workspace, workspace_bytes, stream) -> int:
     return load().fa_fwd(ctypes.byref(params), q, k, v, o, lse, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_noalloc(params: FaParams, q, k, v, o, lse, stream) -> int:
+    """fa_fwd on the library's built-in scratch array: for callers that cannot allocate."""
+    return load().fa_fwd_noalloc(ctypes.byref(params), q, k, v, o, lse, stream)
 
 
 def fa_bwd(params: FaParams, q, k, v, o, lse, dout, dq, dk, dv, dsinks, workspace, workspace_bytes,

@@ -134,6 +134,23 @@ const char *fa_status_string(fa_status s);
 fa_status fa_profile_enable(int on);
 fa_status fa_profile_read(const char *kernel, float *ms);
 
+/* Forward without a caller workspace, for callers that cannot allocate device memory
+ * (a host framework that owns every allocation, or a loop that must not enter the CUDA
+ * allocator).  No passage on the pages has a counterpart: it is fa_fwd run on a scratch
+ * array of FA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library, which every GPU
+ * that loads the library holds until the process exits.  Arguments, layouts and results
+ * are those of fa_fwd.  Allocates nothing.  Returns FA_ERR_WORKSPACE, launching nothing,
+ * when the problem needs more scratch than the array holds (fa_fwd_workspace_size(p)
+ * larger than FA_NOALLOC_SCRATCH_BYTES); FA_ERR_CUDA if the array's address cannot be
+ * had.  The first call on each device looks the array's address up, so make it before
+ * any stream capture.  All calls share the array and it keeps the last call's contents:
+ * each call resets what must start at zero, but calls that overlap on the GPU race on
+ * it, so serialise them (one stream, or events between streams).  The kernels' status
+ * word also lives in the array and is not readable through this ABI. */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+fa_status fa_fwd_noalloc(const fa_params *p, const void *q, const void *k, const void *v, void *o, float *lse,
+                         struct CUstream_st *stream);
+
 /* Library version string. */
 const char *fa_version(void);
 
