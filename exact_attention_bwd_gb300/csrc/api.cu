@@ -196,11 +196,15 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
                       align256(pl.part_rows * pl.n_splits * 4);
         return FA_OK;
     }
-    if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
+    if (p.d != 64 && p.d != 128 && p.d != 256) return FA_ERR_UNSUPPORTED;
     pl.path = FwdPath::kTensor;
+    // d <= 128: two 128-row query tiles and 128-key tiles per CTA; d = 256: one query
+    // tile and 64-key tiles (the 256-column accumulator fills half the tensor memory)
+    const int rows_per_cta = (p.d == 256 ? 1 : 2) * p.P;
+    const int kv_tile = p.d == 256 ? 64 : kTileRows;
     if (dense) {
-        pl.n_blocks = (p.s_q + 2 * p.P - 1) / (2 * p.P);
-        const int tiles = (p.s_kv + kTileRows - 1) / kTileRows;
+        pl.n_blocks = (p.s_q + rows_per_cta - 1) / rows_per_cta;
+        const int tiles = (p.s_kv + kv_tile - 1) / kv_tile;
         const long ctas = (long)pl.n_blocks * p.h_kv * p.B;
         pl.n_splits = 1;
         if (!(flags & FA_FLAG_NO_SPLIT) && !p.causal && p.left < 0 && p.right < 0 && tiles >= 8 &&
@@ -222,7 +226,7 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
                           align256(pl.part_rows * pl.n_splits * 4);
         }
     } else {
-        pl.n_blocks = p.T_q / (2 * p.P) + p.B;
+        pl.n_blocks = p.T_q / rows_per_cta + p.B;
     }
     return FA_OK;
 }
@@ -338,8 +342,9 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     const int tokens_k = p.cu_q ? p.T_k : p.s_kv;
     const int bdim = p.cu_q ? 1 : p.B;
     CUtensorMap tk, tv;
-    if (!encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, pl.path == FwdPath::kDecode ? 64 : 128) ||
-        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, pl.path == FwdPath::kDecode ? 64 : 128))
+    const int kv_box = (pl.path == FwdPath::kDecode || p.d == 256) ? 64 : 128;
+    if (!encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, kv_box) ||
+        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, kv_box))
         return FA_ERR_CUDA;
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     float* o_part = reinterpret_cast<float*>(ws + kStatusBytes);

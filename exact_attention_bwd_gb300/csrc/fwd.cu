@@ -457,6 +457,7 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMa
     switch (a.p.d) {
         case 64: return launch_fwd_d<64>(a, tq, tk, tv, st);
         case 128: return launch_fwd_d<128>(a, tq, tk, tv, st);
+        case 256: return launch_fwd256(a, tq, tk, tv, st);
         default: return cudaErrorInvalidValue;
     }
 }

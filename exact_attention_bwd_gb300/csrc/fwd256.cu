@@ -1,0 +1,350 @@
+// Forward attention for head dimension 256 on the tcgen05 tensor cores.
+//
+// The accumulator of one 128-row query tile is 256 TMEM columns wide, so a CTA holds a
+// single query tile: O in columns [256, 512) and two 64-column S buffers in [0, 128).
+// Keys and values stream in 64-row tiles (32 KB each at d = 256) through a two-stage
+// ring.  The MMA thread runs one tile ahead: S(j+1) is computed while the softmax group
+// works on S(j), then O += P(j) V(j).  Rows are packed across the G query heads of the
+// key/value head exactly as in the d <= 128 kernel, and the online softmax is the same
+// (running max / running sum with lazy rescaling, "Flash Attention Tutorial" README,
+// sections 3 to 5); key tiles outside the causal / sliding-window band are skipped.
+#include "common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads256 = 256;
+constexpr int D = 256;
+constexpr int BN = 64;               // keys per KV tile
+constexpr int KCH = D / 64;          // 64-column chunks
+constexpr int Q_CHUNK = 128 * 128;   // [128 rows][64 cols] bf16
+constexpr int KV_CHUNK = BN * 128;   // [64 rows][64 cols] bf16
+constexpr int STAGES = 2;
+constexpr uint32_t C_S = 0;          // S buffer b at columns 64 b
+constexpr uint32_t C_O = 256;
+
+struct __align__(1024) Smem256 {
+    uint8_t q[KCH * Q_CHUNK];
+    uint8_t k[STAGES][KCH * KV_CHUNK];
+    uint8_t v[STAGES][KCH * KV_CHUNK];
+    uint64_t q_full;
+    uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+    uint64_t s_full[2], p_full[2], pv_done, o_full, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(kThreads256, 1)
+    fwd256_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem256& s = *reinterpret_cast<Smem256*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Problem& p = a.p;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---------------- work unit ----------------
+    const int g = blockIdx.y;
+    int seq, blk, split = 0;
+    if (p.cu_q) {
+        blk = blockIdx.x;
+        seq = owner_sequence(p.cu_q, p.B, blk, p.P);
+        blk -= p.cu_q[seq] / p.P + seq;
+    } else {
+        seq = blockIdx.z;
+        int x = blockIdx.x;
+        split = x % a.n_splits;
+        x /= a.n_splits;
+        blk = a.n_blocks - 1 - x;
+    }
+    const SeqView sv = seq_view(p, seq);
+    const int s0 = blk * p.P;
+    if (s0 >= sv.nq) return;  // idle packed-batch block
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
+    const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
+    int t0, t1;
+    kv_tile_range(band, s0, min(s0 + p.P, sv.nq) - 1, BN, t0, t1);
+    if (a.n_splits > 1) {
+        t0 = max(t0, split * a.split_tiles);
+        t1 = min(t1, (split + 1) * a.split_tiles);
+        if (t1 < t0) t1 = t0;
+    }
+    const int ntiles = t1 - t0;
+
+    Abort ab{&s.abort_flag, a.status};
+    if (tid == 0) {
+        s.abort_flag = 0;
+        mbar_init(&s.q_full, 1);
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&s.k_full[i], 1);
+            mbar_init(&s.k_empty[i], 1);
+            mbar_init(&s.v_full[i], 1);
+            mbar_init(&s.v_empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s.s_full[b], 1);
+            mbar_init(&s.p_full[b], 4);  // one arrive per softmax warp
+        }
+        mbar_init(&s.pv_done, 1);
+        mbar_init(&s.o_full, 1);
+        mbar_init(&s.drain, 1);
+        fence_mbar_init();
+    }
+    if (p.P * p.G < 128) {
+        for (int c = 0; c < KCH; ++c)
+            for (int x = p.P * p.G * 128 + tid * 16; x < 128 * 128; x += kThreads256 * 16)
+                *reinterpret_cast<uint4*>(&s.q[c * Q_CHUNK + x]) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == 2) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0 && ntiles > 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            mbar_expect_tx(&s.q_full, (uint32_t)(p.P * p.G) * 128u * KCH);
+            for (int c = 0; c < KCH; ++c)
+                tma_load_4d(&s.q[c * Q_CHUNK], &tmq, &s.q_full, c * 64, g * p.G, sv.q0 + s0, sv.tma_b);
+            int k_issued = 0, v_issued = 0;
+            for (int it = 0; it < ntiles; ++it) {
+                const int st = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                const int row = sv.k0 + (t0 + it) * BN;
+                if (!mbar_wait(&s.k_empty[st], ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.k_full[st], KCH * KV_CHUNK);
+                for (int c = 0; c < KCH; ++c)
+                    tma_load_4d(&s.k[st][c * KV_CHUNK], &tmk, &s.k_full[st], c * 64, g, row, sv.tma_b);
+                ++k_issued;
+                if (!mbar_wait(&s.v_empty[st], ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.v_full[st], KCH * KV_CHUNK);
+                for (int c = 0; c < KCH; ++c)
+                    tma_load_4d(&s.v[st][c * KV_CHUNK], &tmv, &s.v_full[st], c * 64, g, row, sv.tma_b);
+                ++v_issued;
+            }
+            for (int back = 1; back <= STAGES; ++back) {
+                if (k_issued - back >= 0)
+                    mbar_wait_quiet(&s.k_full[(k_issued - back) % STAGES], ((k_issued - back) / STAGES) & 1);
+                if (v_issued - back >= 0)
+                    mbar_wait_quiet(&s.v_full[(v_issued - back) % STAGES], ((v_issued - back) / STAGES) & 1);
+            }
+            mbar_wait_quiet(&s.q_full, 0);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
+            constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+            const uint32_t qa = smem_u32(s.q);
+            auto issue_s = [&](int it) {  // S(it) = Q K(it)^T into buffer it & 1
+                const int st = it % STAGES;
+                const uint32_t ka = smem_u32(s.k[st]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qoff = (kk >> 2) * Q_CHUNK + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * KV_CHUNK + (kk & 3) * 32;
+                    mma_ss(tmem + C_S + 64 * (it & 1), sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024),
+                           idS, kk > 0);
+                }
+                tc_commit(&s.s_full[it & 1]);
+                tc_commit(&s.k_empty[st]);
+            };
+            bool ok = mbar_wait(&s.q_full, 0, ab);
+            if (ok && (ok = mbar_wait(&s.k_full[0], 0, ab))) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            uint32_t pcount[2] = {0, 0};
+            for (int it = 0; ok && it < ntiles; ++it) {
+                if (it + 1 < ntiles) {
+                    const int st1 = (it + 1) % STAGES;
+                    if (!(ok = mbar_wait(&s.k_full[st1], ((it + 1) / STAGES) & 1, ab))) break;
+                    tc_fence_after();
+                    issue_s(it + 1);  // its buffer held P(it-1), read by PV(it-1) issued earlier
+                }
+                const int st = it % STAGES, b = it & 1;
+                if (!(ok = mbar_wait(&s.v_full[st], (it / STAGES) & 1, ab))) break;
+                if (!(ok = mbar_wait(&s.p_full[b], pcount[b] & 1, ab))) break;
+                ++pcount[b];
+                tc_fence_after();
+                const uint32_t va = smem_u32(s.v[st]);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + C_O, tmem + C_S + 64 * b + kk * 8, sdesc_sw128(va + kk * 2048, KV_CHUNK, 1024), idO,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&s.pv_done);
+                tc_commit(&s.v_empty[st]);
+                if (it == ntiles - 1) tc_commit(&s.o_full);  // single-phase: O is final
+            }
+            tc_commit(&s.drain);
+            mbar_wait_quiet(&s.drain, 0);
+        }
+    } else if (warp >= 4) {
+        // ================= softmax: one thread per row =================
+        const int r = ((warp & 3) << 5) | lane;
+        const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+        const uint32_t tO = tmem + lane_base + C_O;
+        const int i = s0 + r / p.G;
+        const int h = g * p.G + r % p.G;
+        const bool row_valid = (r < p.P * p.G) && i < sv.nq;
+        const int jlo = row_valid ? band.lo(i) : 1;
+        const int jhi = row_valid ? band.hi(i) : 0;
+        const float c = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        uint32_t scount[2] = {0, 0};
+        bool ok = true;
+        for (int it = 0; it < ntiles; ++it) {
+            const int b = it & 1;
+            {
+                const bool w = mbar_wait(&s.s_full[b], scount[b] & 1, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            ++scount[b];
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_base + C_S + 64 * b;
+            const int j0 = (t0 + it) * BN;
+            const bool edge = (j0 < jlo || j0 + BN - 1 > jhi);
+            uint32_t sr[64];
+            tmem_ld_32x32b_x64(tS, sr);
+            if (edge) {
+#pragma unroll
+                for (int cc = 0; cc < BN; ++cc)
+                    if (j0 + cc < jlo || j0 + cc > jhi) sr[cc] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < BN; ++cc) mx = fmaxf(mx, __uint_as_float(sr[cc]));
+            const float m_new = fmaxf(m_used, mx * c);
+            float alpha = 1.f;
+            bool rescale = false;
+            if (m_used == -INFINITY) {
+                m_used = m_new;
+            } else if (m_new > m_used + 8.f) {
+                alpha = ex2(m_used - m_new);
+                m_used = m_new;
+                l *= alpha;
+                rescale = true;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O must hold PV(it-1) before it is rescaled
+                const bool w = mbar_wait(&s.pv_done, (it - 1) & 1, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 32) {
+                    uint32_t orr[32];
+                    tmem_ld_32x32b_x32(tO + cb, orr);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) orr[t] = __float_as_uint(__uint_as_float(orr[t]) * alpha);
+                    tmem_st_32x32b_x32(tO + cb, orr);
+                }
+            }
+            const float base = (m_used == -INFINITY) ? 0.f : m_used;
+            float sum = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < BN; cc += 2) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[cc]), c, -base));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -base));
+                sum += p0 + p1;
+                sr[cc / 2] = pack_bf16(p0, p1);
+            }
+            l += sum;
+            tmem_st_32x32b_x32(tS, sr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.p_full[b]);
+        }
+        // ---------------- epilogue ----------------
+        const bool has_o = ntiles > 0;
+        if (has_o && ok) {
+            // pv_done can lag two phases behind here (S(last) was issued before
+            // PV(last-1)), which a parity wait cannot tell apart: use the one-shot barrier
+            const bool w = mbar_wait(&s.o_full, 0, ab);
+            ok = __all_sync(0xffffffffu, w);
+            tc_fence_after();
+        }
+        const bool split_mode = a.n_splits > 1;
+        float oscale = 0.f, lse = -INFINITY;
+        if (!split_mode && p.sinks && row_valid) {
+            const float s2 = p.sinks[h] * kLog2e;
+            const float mf = fmaxf(m_used, s2);
+            const float wgt = (m_used == -INFINITY) ? 0.f : ex2(m_used - mf);
+            const float lt = l * wgt + ex2(s2 - mf);
+            oscale = wgt / lt;
+            lse = (mf + log2f(lt)) * kLn2;
+        } else if (l > 0.f) {
+            oscale = 1.f / l;
+            lse = (m_used + log2f(l)) * kLn2;
+        }
+        const long nrows = (long)p.B * p.h_q * p.s_q;
+        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;
+        if (row_valid) {
+            if (!split_mode) {
+                if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
+            } else {
+                a.lse_part[(long)split * nrows + prow] = lse;
+            }
+        }
+        for (int cb = 0; cb < D; cb += 32) {
+            uint32_t orr[32];
+            if (has_o && ok) {
+                tmem_ld_32x32b_x32(tO + cb, orr);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) orr[t] = 0u;
+            }
+            if (!row_valid) continue;
+            if (!split_mode) {
+                __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    uint4 wv;
+                    wv.x = pack_bf16(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
+                    wv.y = pack_bf16(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
+                    wv.z = pack_bf16(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
+                    wv.w = pack_bf16(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
+                    reinterpret_cast<uint4*>(orow)[t] = wv;
+                }
+            } else {
+                float* op = a.o_part + ((long)split * nrows + prow) * D + cb;
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    reinterpret_cast<float4*>(op)[t] =
+                        make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
+                                    __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          cudaStream_t st) {
+    const size_t smem = sizeof(Smem256) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid;
+    if (a.p.cu_q)
+        grid = dim3(a.n_blocks, a.p.h_kv, 1);
+    else
+        grid = dim3(a.n_blocks * a.n_splits, a.p.h_kv, a.p.B);
+    fwd256_kernel<<<grid, kThreads256, smem, st>>>(a, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -82,6 +82,8 @@ struct BwdArgs {
 // host-side launchers (defined next to each kernel)
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t st);
+cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st);

@@ -55,9 +55,8 @@
  *    ABI and no kernel traps: a kernel whose pipeline stalls gives up after a time
  *    limit and records FA_ERR_TIMEOUT in the workspace status word, which
  *    fa_read_device_status reports.
- *  - Supported: bf16; head dim d in {64, 128} for both passes, plus d = 256 for
- *    forward calls with at most 16 query rows per key/value head (decode shapes);
- *    h_q / h_kv <= 128.  Anything else returns FA_ERR_UNSUPPORTED.
+ *  - Supported: bf16; head dim d in {64, 128, 256} for the forward, {64, 128} for
+ *    the backward; h_q / h_kv <= 128.  Anything else returns FA_ERR_UNSUPPORTED.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H

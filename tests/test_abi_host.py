@@ -72,11 +72,17 @@ def call_bwd(p, dsinks=FAKE, ws=FAKE, ws_bytes=1 << 30, q=FAKE):
     (dict(d=100), fa.FA_ERR_UNSUPPORTED),                    # not a multiple of 8
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(d=512), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),                    # d=256 only for decode shapes
     (dict(h_q=256, h_kv=1, s_q=1), fa.FA_ERR_UNSUPPORTED),   # group of 256 heads
 ])
 def test_forward_rejects(kw, code):
     assert call_fwd(params(**kw)) == code
+
+
+def test_d256_forward_is_planned():
+    # d = 256 forward is supported: it passes the problem checks and stops at the
+    # (deliberately too small) workspace, before anything is launched
+    assert fa.fa_fwd_workspace_size(params(d=256)) == 256
+    assert call_fwd(params(d=256), ws_bytes=16) == fa.FA_ERR_WORKSPACE
 
 
 def test_forward_pointer_checks():
