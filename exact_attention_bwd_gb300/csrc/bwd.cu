@@ -44,8 +44,9 @@ struct BwdCfg {
     static constexpr uint32_t C_DP = 128;        // dP^T
     static constexpr uint32_t C_DV = 256;
     static constexpr uint32_t C_DK = 256 + D;
-    static constexpr uint32_t C_DQ = (D == 128) ? 128 : 384;  // dQ_i (rows = query rows)
+    static constexpr uint32_t C_DQ = (D == 128) ? 128 : 384;  // dQ^T_i (lanes = d, columns = query rows)
     static constexpr bool DQ_OVER_DP = (D == 128);             // dQ_i reuses the dP^T columns
+    static constexpr bool DQ_T = (D == 128);                   // dQ computed transposed (lanes = d)
 };
 
 template <int D>
@@ -199,25 +200,33 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: K-major both
             constexpr uint32_t id_dv = idesc_bf16(128, D, false, true);    // A from TMEM, B MN-major
             constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);    // A K-major, B MN-major
-            constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);     // A MN-major, B MN-major
+            // dQ^T (M = d, N = query rows) when d = 128; dQ (M = query rows, N = d) when d = 64,
+            // whose 64-row accumulator would need the M = 64 lane layout
+            constexpr uint32_t id_dq = C::DQ_T ? idesc_bf16(128, 128, true, true) : idesc_bf16(128, D, true, true);
             const uint32_t ka = smem_u32(s.k), va = smem_u32(s.v);
             bool ok = mbar_wait(&s.kv_full, 0, ab);
             tc_fence_after();
-            for (int it = 0; ok && it < nsteps; ++it) {
-                const int st = it & 1;
-                const uint32_t ph = (it >> 1) & 1;
-                const uint32_t par = it & 1;
-                const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
-                // S^T = K Q_i^T
-                if (!(ok = mbar_wait(&s.q_full[st], ph, ab))) break;
-                tc_fence_after();
+            auto issue_st = [&](int it) {  // S^T_it = K Q_it^T into the S^T columns
+                const uint32_t qa = smem_u32(s.q[it & 1]);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
                     mma_ss(tmem + C::C_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_s, kk > 0);
                 }
                 tc_commit(&s.s_full);
-                // dP^T = V dO_i^T (its columns held dQ_{i-1} when D == 128)
+            };
+            // issue order per step i:  dP^T_i, dV_i, S^T_{i+1}, dK_i, dQ^T_i  (S^T_0 first)
+            // S^T_{i+1} goes before dK_i / dQ^T_i so that the next step's P^T overlaps them
+            if (ok && (ok = mbar_wait(&s.q_full[0], 0, ab))) {
+                tc_fence_after();
+                issue_st(0);
+            }
+            for (int it = 0; ok && it < nsteps; ++it) {
+                const int st = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                const uint32_t par = it & 1;
+                const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
+                // dP^T = V dO_i^T (its columns held dQ^T_{i-1} when D == 128)
                 if (!(ok = mbar_wait(&s.do_full[st], ph, ab))) break;
                 if (C::DQ_OVER_DP && it > 0) {
                     if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
@@ -237,7 +246,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     mma_ts(tmem + C::C_DV, tmem + C::C_S + (kk >> 2) * 64 + (kk & 3) * 8,
                            sdesc_sw128(da + kk * 2048, C::CHUNK, 1024), id_dv, (it > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(&s.do_empty[st]);
-                // dK += dS^T Q_i ;  dQ_i = dS K
+                // S^T_{i+1}: its columns held P^T_i, read by dV_i issued just above
+                if (it + 1 < nsteps) {
+                    if (!(ok = mbar_wait(&s.q_full[st ^ 1], ((it + 1) >> 1) & 1, ab))) break;
+                    tc_fence_after();
+                    issue_st(it + 1);
+                }
+                // dK += dS^T Q_i ;  dQ^T_i = K^T dS^T
                 if (!(ok = mbar_wait(&s.ds_full, par, ab))) break;
                 if (!C::DQ_OVER_DP && it > 0) {
                     if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
@@ -251,10 +266,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                            id_dk, (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&s.q_empty[st]);
+                if constexpr (C::DQ_T) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + C::C_DQ, sdesc_sw128(sa + kk * 2048, 128 * 128, 1024),
-                           sdesc_sw128(ka + kk * 2048, C::CHUNK, 1024), id_dq, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: A = K tile (MN-major), B = dS^T (MN-major)
+                        mma_ss(tmem + C::C_DQ, sdesc_sw128(ka + kk * 2048, C::CHUNK, 1024),
+                               sdesc_sw128(sa + kk * 2048, 128 * 128, 1024), id_dq, kk > 0);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dQ = dS K: A = dS (MN-major), B = K tile (MN-major)
+                        mma_ss(tmem + C::C_DQ, sdesc_sw128(sa + kk * 2048, 128 * 128, 1024),
+                               sdesc_sw128(ka + kk * 2048, C::CHUNK, 1024), id_dq, kk > 0);
+                }
                 tc_commit(&s.dq_full);
                 tc_commit(&s.ds_free);
             }
@@ -356,23 +378,30 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.ds_full);
-            // ---- dQ_i: thread = query row; reduce into the fp32 workspace ----
+            // ---- dQ^T_i: thread = column d of dQ (TMEM lane), 64 query rows per group ----
             {
                 const bool w = mbar_wait(&s.dq_full, par, ab);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             tc_fence_after();
-            {
-                const int qr = jr;  // TMEM lane = query row of the tile
-                float* acc = a.dq_acc + (trow + qr) * D + (D / 2) * cg;
-                uint32_t qv[D / 2];
-                if constexpr (D == 128)
-                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
-                else
-                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
+            if constexpr (C::DQ_T) {
+                uint32_t qv[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ + 64 * cg, qv);
                 // the columns are free as soon as they are in registers
                 tc_fence_before();
                 mbar_arrive(&s.dq_free);
+                // rows 64cg .. 64cg+63 of the tile, column jr: for each row the 32 lanes of a
+                // warp add to 32 consecutive floats, one 128-byte line
+                float* acc = a.dq_acc + (trow + 64 * cg) * D + jr;
+#pragma unroll
+                for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qv[r]));
+            } else {
+                const int qr = jr;  // TMEM lane = query row of the tile
+                uint32_t qv[D / 2];
+                tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
+                tc_fence_before();
+                mbar_arrive(&s.dq_free);
+                float* acc = a.dq_acc + (trow + qr) * D + (D / 2) * cg;
 #pragma unroll
                 for (int t4 = 0; t4 < D / 8; ++t4)
                     atomicAdd(reinterpret_cast<float4*>(acc) + t4,
