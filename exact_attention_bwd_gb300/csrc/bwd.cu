@@ -30,7 +30,7 @@
 namespace fa {
 namespace {
 
-constexpr int kThreadsBwd = 384;
+constexpr int kThreadsBwd = 512;
 constexpr int kRows = 128;
 
 template <int D>
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         mbar_init(&s.ds_full, 256);
         mbar_init(&s.ds_free, 1);
         mbar_init(&s.dq_full, 1);
-        mbar_init(&s.dq_free, 256);
+        mbar_init(&s.dq_free, C::DQ_T ? 128 : 256);
         mbar_init(&s.dkv_full, 1);
         fence_mbar_init();
     }
@@ -152,6 +152,39 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
 
+    // registers: 512 x 128 at launch, redistributed per warp group (the change is made at
+    // the top of each group's branch): producer/MMA 64, the two compute groups 160, the
+    // dQ group 128 (128*64 + 256*160 + 128*128 = 65536)
+    if (warp >= 12) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 128;\n" ::: "memory");
+        // ================= dQ group: drains dQ^T_i and reduces it into the workspace =================
+        if constexpr (C::DQ_T) {
+            const int dcol = ((warp & 3) << 5) | lane;  // TMEM lane = column d of dQ
+            const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+            for (int it = 0; it < nsteps; ++it) {
+                const int t = qt0 + it;
+                const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
+                {
+                    const bool w = mbar_wait(&s.dq_full, it & 1, ab);
+                    if (!__all_sync(0xffffffffu, w)) break;
+                }
+                tc_fence_after();
+                uint32_t qa[64], qb[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ, qa);
+                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ + 64, qb);
+                // the columns are free as soon as they are in registers
+                tc_fence_before();
+                mbar_arrive(&s.dq_free);
+                // for each query row the 32 lanes of a warp add to 32 consecutive floats
+                float* acc = a.dq_acc + trow * D + dcol;
+#pragma unroll
+                for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qa[r]));
+#pragma unroll
+                for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
+            }
+        }
+    } else if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && nsteps > 0) {
@@ -283,7 +316,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             tc_commit(&s.dkv_full);
             mbar_wait_quiet(&s.dkv_full, 0);
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 160;\n" ::: "memory");
         // ================= compute groups =================
         const int cg = (warp - 4) >> 2;            // column group
         const int wq = warp & 3;
@@ -378,24 +413,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.ds_full);
-            // ---- dQ^T_i: thread = column d of dQ (TMEM lane), 64 query rows per group ----
-            {
-                const bool w = mbar_wait(&s.dq_full, par, ab);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            }
-            tc_fence_after();
-            if constexpr (C::DQ_T) {
-                uint32_t qv[64];
-                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ + 64 * cg, qv);
-                // the columns are free as soon as they are in registers
-                tc_fence_before();
-                mbar_arrive(&s.dq_free);
-                // rows 64cg .. 64cg+63 of the tile, column jr: for each row the 32 lanes of a
-                // warp add to 32 consecutive floats, one 128-byte line
-                float* acc = a.dq_acc + (trow + 64 * cg) * D + jr;
-#pragma unroll
-                for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qv[r]));
-            } else {
+            // ---- dQ_i (d = 64 only; for d = 128 the dQ warp group drains it) ----
+            if constexpr (!C::DQ_T) {
+                {
+                    const bool w = mbar_wait(&s.dq_full, par, ab);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                }
+                tc_fence_after();
                 const int qr = jr;  // TMEM lane = query row of the tile
                 uint32_t qv[D / 2];
                 tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
