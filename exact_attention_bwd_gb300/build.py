@@ -21,6 +21,8 @@ SOURCES = ["api.cu", "fwd.cu", "fwd256.cu", "bwd.cu", "decode.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 f"-I{INCLUDE}"]
+# extra nvcc flags for tuning builds (e.g. -DFA_FWD_EXP_POLY_PAIRS=2); empty by default
+EXTRA = os.environ.get("FA_NVCC_EXTRA", "").split()
 
 
 def nvcc() -> str:
@@ -52,7 +54,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def one(src):
         obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [cc] + FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [cc] + FLAGS + EXTRA + (["-Xptxas", "-v"] if verbose else []) + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")

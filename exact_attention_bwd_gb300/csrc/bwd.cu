@@ -86,16 +86,22 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     BwdSmem<D>& s = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.y;
-
-    int seq, blk;
-    if (p.cu_q) {
-        blk = blockIdx.x;
-        seq = owner_sequence(p.cu_k, p.B, blk, kRows);
-        blk -= p.cu_k[seq] / kRows + seq;
-    } else {
-        seq = blockIdx.z;
-        blk = blockIdx.x;
+    // 1-D grid: key/value head (and batch) fastest, key block slowest, so the key blocks
+    // that see the most query tiles under a causal mask (the first ones) start first
+    int g, seq, blk;
+    {
+        const int idx = blockIdx.x;
+        if (p.cu_q) {
+            g = idx % p.h_kv;
+            blk = idx / p.h_kv;
+            seq = owner_sequence(p.cu_k, p.B, blk, kRows);
+            blk -= p.cu_k[seq] / kRows + seq;
+        } else {
+            const int hb = p.h_kv * p.B;
+            g = (idx % hb) % p.h_kv;
+            seq = (idx % hb) / p.h_kv;
+            blk = idx / hb;
+        }
     }
     const SeqView sv = seq_view(p, seq);
     const int j0 = blk * kRows;
@@ -587,8 +593,8 @@ static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const 
     const size_t smem = sizeof(BwdSmem<D>);
     cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.n_kvblocks, a.p.h_kv, a.p.cu_q ? 1 : a.p.B);
-    bwd_main_kernel<D><<<grid, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
+    const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
+    bwd_main_kernel<D><<<(unsigned)n, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
     return cudaGetLastError();
 }
 

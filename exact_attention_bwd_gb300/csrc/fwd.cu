@@ -30,6 +30,11 @@ namespace {
 
 constexpr int kThreadsFwd = 384;
 constexpr int BN = 128;  // keys per KV tile
+#ifndef FA_FWD_EXP_POLY_PAIRS
+#define FA_FWD_EXP_POLY_PAIRS 0
+#endif
+// of every 4 column pairs of an unmasked tile, this many take the polynomial exp2
+constexpr int kExpPolyPairs = FA_FWD_EXP_POLY_PAIRS;
 
 template <int D>
 struct FwdCfg {
@@ -55,8 +60,6 @@ struct __align__(1024) FwdSmem {
     int abort_flag;
 };
 
-__device__ __forceinline__ int split_idx(const FwdArgs& a, int bx) { return bx % a.n_splits; }
-
 struct TileInfo {
     int s0;       // first query position of the tile
     int t0, t1;   // KV tile range [t0, t1)
@@ -75,19 +78,25 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     const int warp = tid >> 5, lane = tid & 31;
 
     // ---------------- work unit ----------------
-    const int g = blockIdx.y;  // key/value head
-    int seq, blk, split = 0;
-    if (p.cu_q) {
-        const int bs = 2 * p.P;
-        blk = blockIdx.x;
-        seq = owner_sequence(p.cu_q, p.B, blk, bs);
-        blk -= p.cu_q[seq] / bs + seq;
-    } else {
-        seq = blockIdx.z;
-        int x = blockIdx.x;
-        split = x % a.n_splits;
-        x /= a.n_splits;
-        blk = a.n_blocks - 1 - x;  // heaviest (latest) query blocks first
+    // 1-D grid, heaviest work first: the key/value head (and batch) vary fastest, the
+    // query block slowest, latest (longest causal band) blocks first
+    int g, seq, blk, split = 0;
+    {
+        const int idx = blockIdx.x;
+        if (p.cu_q) {
+            g = idx % p.h_kv;
+            const int bs = 2 * p.P;
+            blk = idx / p.h_kv;
+            seq = owner_sequence(p.cu_q, p.B, blk, bs);
+            blk -= p.cu_q[seq] / bs + seq;
+        } else {
+            const int hb = p.h_kv * p.B;
+            g = (idx % hb) % p.h_kv;
+            seq = (idx % hb) / p.h_kv;
+            const int x = idx / hb;
+            split = x % a.n_splits;
+            blk = a.n_blocks - 1 - x / a.n_splits;
+        }
     }
     const SeqView sv = seq_view(p, seq);
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
@@ -213,13 +222,15 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             bool ok = mbar_wait(&s.q_full, 0, ab);
             tc_fence_after();
             uint32_t pcount[2] = {0, 0};
+            // a descriptor's start-address field is addr >> 4 in its low bits, so stepping
+            // through a tile is a plain add to a base descriptor (no carry: addr < 256 KB)
             auto issue_s = [&](int k, int st) {
-                const uint32_t qa = smem_u32(s.q[k]), ka = smem_u32(s.k[st]);
+                const uint64_t qd = sdesc_sw128(smem_u32(s.q[k]), 16, 1024);
+                const uint64_t kd = sdesc_sw128(smem_u32(s.k[st]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + 128 * k, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
-                           kk > 0);
+                    const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + 128 * k, qd + off, kd + off, idS, kk > 0);
                 }
                 tc_commit(&s.s_full[k]);
             };
@@ -247,11 +258,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         if (!(ok = mbar_wait(&s.p_full[k], pcount[k] & 1, ab))) break;
                         ++pcount[k];
                         tc_fence_after();
-                        const uint32_t va = smem_u32(s.v[st]);
+                        const uint64_t vd = sdesc_sw128(smem_u32(s.v[st]), C::CHUNK_BYTES, 1024);
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_ts(tmem + 256 + 128 * k, tmem + 128 * k + kk * 8,
-                                   sdesc_sw128(va + kk * 2048, C::CHUNK_BYTES, 1024), idO,
+                            mma_ts(tmem + 256 + 128 * k, tmem + 128 * k + kk * 8, vd + (kk * 2048 >> 4), idO,
                                    (j > ti[k].t0 || kk > 0) ? 1u : 0u);
                         if (j == ti[k].t1 - 1) tc_commit(&s.o_full[k]);
                     }
@@ -314,9 +324,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             }
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int cc = 0; cc < BN; cc += 2) {
-                mx0 = fmaxf(mx0, __uint_as_float(sr[cc]));
-                mx1 = fmaxf(mx1, __uint_as_float(sr[cc + 1]));
+            for (int cc = 0; cc < BN; cc += 4) {
+                mx0 = max3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
+                mx1 = max3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
             }
             const float m_new = fmaxf(m_used, fmaxf(mx0, mx1) * c);
             float alpha = 1.f;
@@ -340,18 +350,28 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     tmem_st_32x32b_x32(tO + cb, orr);
                 }
             }
-            // P = exp2(S*c - m) as bf16 pairs, packed in place (slot cc/2 is already consumed)
+            // P = exp2(S*c - m) as bf16 pairs, packed in place (slot cc/2 is already consumed).
+            // On tiles without masked entries a fraction of the exponentials runs on the FMA
+            // pipe (exp2_poly2) to share the load with the MUFU unit.
             const float base = (m_used == -INFINITY) ? 0.f : m_used;
-            float sum0 = 0.f, sum1 = 0.f;
+            const bool poly_ok = !__any_sync(0xffffffffu, edge);
+            const float2 c2 = make_float2(c, c), nb2 = make_float2(-base, -base);
+            float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int cc = 0; cc < BN; cc += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[cc]), c, -base));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -base));
-                sum0 += p0;
-                sum1 += p1;
-                sr[cc / 2] = pack_bf16(p0, p1);
+                float2 xv = __ffma2_rn(make_float2(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), c2, nb2);
+                float2 pv;
+                if (kExpPolyPairs > 0 && ((cc >> 1) & 3) < kExpPolyPairs && poly_ok) {
+                    xv.x = fmaxf(xv.x, -125.f);
+                    xv.y = fmaxf(xv.y, -125.f);
+                    pv = exp2_poly2(xv);
+                } else {
+                    pv = make_float2(ex2(xv.x), ex2(xv.y));
+                }
+                sum2 = __fadd2_rn(sum2, pv);
+                sr[cc / 2] = pack_bf16(pv.x, pv.y);
             }
-            const float sum = sum0 + sum1;
+            const float sum = sum2.x + sum2.y;
             tmem_st_32x32b_x64(tS, sr);
             l += sum;
             tc_fence_before();
@@ -384,7 +404,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             if (!split_mode) {
                 if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
             } else {
-                a.lse_part[(long)split_idx(a, blockIdx.x) * nrows + prow] = lse;
+                a.lse_part[(long)split * nrows + prow] = lse;
             }
         }
         if (has_o && ok) {
@@ -406,7 +426,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         reinterpret_cast<uint4*>(orow)[t] = wv;
                     }
                 } else {
-                    float* op = a.o_part + ((long)split_idx(a, blockIdx.x) * nrows + prow) * D + cb;
+                    float* op = a.o_part + ((long)split * nrows + prow) * D + cb;
 #pragma unroll
                     for (int t = 0; t < 8; ++t)
                         reinterpret_cast<float4*>(op)[t] = make_float4(
@@ -420,7 +440,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
                 for (int t = 0; t < D / 8; ++t) reinterpret_cast<uint4*>(orow)[t] = make_uint4(0, 0, 0, 0);
             } else {
-                float* op = a.o_part + ((long)split_idx(a, blockIdx.x) * nrows + prow) * D;
+                float* op = a.o_part + ((long)split * nrows + prow) * D;
 #pragma unroll
                 for (int t = 0; t < D / 4; ++t) reinterpret_cast<float4*>(op)[t] = make_float4(0, 0, 0, 0);
             }
@@ -443,12 +463,8 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const C
     const size_t smem = sizeof(FwdSmem<D>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid;
-    if (a.p.cu_q)
-        grid = dim3(a.n_blocks, a.p.h_kv, 1);
-    else
-        grid = dim3(a.n_blocks * a.n_splits, a.p.h_kv, a.p.B);
-    fwd_kernel<D><<<grid, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
+    const long n = a.p.cu_q ? (long)a.n_blocks * a.p.h_kv : (long)a.n_blocks * a.n_splits * a.p.h_kv * a.p.B;
+    fwd_kernel<D><<<(unsigned)n, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
 }
 

@@ -43,18 +43,23 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---------------- work unit ----------------
-    const int g = blockIdx.y;
-    int seq, blk, split = 0;
-    if (p.cu_q) {
-        blk = blockIdx.x;
-        seq = owner_sequence(p.cu_q, p.B, blk, p.P);
-        blk -= p.cu_q[seq] / p.P + seq;
-    } else {
-        seq = blockIdx.z;
-        int x = blockIdx.x;
-        split = x % a.n_splits;
-        x /= a.n_splits;
-        blk = a.n_blocks - 1 - x;
+    // 1-D grid, heaviest work first (see the d <= 128 kernel)
+    int g, seq, blk, split = 0;
+    {
+        const int idx = blockIdx.x;
+        if (p.cu_q) {
+            g = idx % p.h_kv;
+            blk = idx / p.h_kv;
+            seq = owner_sequence(p.cu_q, p.B, blk, p.P);
+            blk -= p.cu_q[seq] / p.P + seq;
+        } else {
+            const int hb = p.h_kv * p.B;
+            g = (idx % hb) % p.h_kv;
+            seq = (idx % hb) / p.h_kv;
+            const int x = idx / hb;
+            split = x % a.n_splits;
+            blk = a.n_blocks - 1 - x / a.n_splits;
+        }
     }
     const SeqView sv = seq_view(p, seq);
     const int s0 = blk * p.P;
@@ -338,12 +343,8 @@ cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtenso
     const size_t smem = sizeof(Smem256) + 1024;
     cudaError_t e = cudaFuncSetAttribute(fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid;
-    if (a.p.cu_q)
-        grid = dim3(a.n_blocks, a.p.h_kv, 1);
-    else
-        grid = dim3(a.n_blocks * a.n_splits, a.p.h_kv, a.p.B);
-    fwd256_kernel<<<grid, kThreads256, smem, st>>>(a, tq, tk, tv);
+    const long n = a.p.cu_q ? (long)a.n_blocks * a.p.h_kv : (long)a.n_blocks * a.n_splits * a.p.h_kv * a.p.B;
+    fwd256_kernel<<<(unsigned)n, kThreads256, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
 }
 

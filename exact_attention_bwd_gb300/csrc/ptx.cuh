@@ -272,6 +272,32 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// 2^x on the FMA pipe, for x in [-125, 128): Cody-Waite style reduction x = n + f with
+// n = round(x) (by adding 1.5 * 2^23, which leaves n in the low mantissa bits) and
+// f in [-1/2, 1/2], then a degree-3 polynomial for 2^f whose coefficients are a minimax
+// (Remez) fit of relative error on [-1/2, 1/2] (max relative error 7.5e-5), and the
+// exponent n added to the result's exponent field.  Two values at a time with the
+// packed fp32 instructions.  Callers clamp x below at -125 so the exponent stays normal.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    const float2 magic = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
+    const float2 t = __fadd2_rn(x, magic);
+    const float2 n = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
+    const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
+    float2 p = __ffma2_rn(make_float2(0.0551716685f, 0.0551716685f), f,
+                          make_float2(0.2426111251f, 0.2426111251f));
+    p = __ffma2_rn(p, f, make_float2(0.6932609677f, 0.6932609677f));
+    p = __ffma2_rn(p, f, make_float2(0.9999280572f, 0.9999280572f));
+    // low bits of t hold n (two's complement): shifting them into the exponent field adds n
+    const uint32_t ex = __float_as_uint(t.x) << 23, ey = __float_as_uint(t.y) << 23;
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + ex), __uint_as_float(__float_as_uint(p.y) + ey));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
