@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     return ap.parse_args()
 
 
@@ -252,6 +253,9 @@ def run_ours(args):
         "step_ms": {"median": statistics.median(times), "mean": statistics.mean(times),
                     "std": statistics.pstdev(times), "min": min(times), "max": max(times)},
     }
+    if not args.no_decode:
+        line["decode"] = {n: measure_decode(dev, n) for n in
+                          ("decode_d128_sq1", "decode_d128_sq64", "decode_d256_sq1", "decode_d256_sq64")}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = oracle_sample(w)
     if rank == 0:
@@ -259,6 +263,56 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------------------
+# decode / chunked prefill against a long cache: HBM-bound, reported as GB/s
+# ----------------------------------------------------------------------------------------------
+
+def measure_decode(dev, name, steps=10, warmup=3):
+    """Forward of one decode workload: algorithmic bytes (K and V read once, Q read, O and
+    LSE written) per launch over the CUDA-event time of the whole forward (split kernel +
+    combine), L2 flushed between launches; per-kernel times from the library's hooks."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    w = inputs.workload(name)
+    B, s_q, s_kv, h_q, h_kv, d = w["B"], w["s_q"], w["s_kv"], w["h_q"], w["h_kv"], w["d"]
+    sd = lambda t: inputs.seed_of(w["wid"], w["variant"], t)  # noqa: E731
+    q = inputs.normal_bf16_torch(sd(inputs.Q), (B, s_q, h_q, d), dev)
+    k = inputs.normal_bf16_torch(sd(inputs.K), (B, s_kv, h_kv, d), dev)
+    v = inputs.normal_bf16_torch(sd(inputs.V), (B, s_kv, h_kv, d), dev)
+    kw = dict(causal=True, softmax_scale=1.0 / math.sqrt(d))
+    o, lse, ws = fa.forward(q, k, v, **kw)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(warmup):
+        fa.forward(q, k, v, **kw, out=o, lse=lse, workspace=ws)
+    fa.fa_profile_enable(True)
+    times, kern = [], {}
+    for _ in range(steps):
+        flush.zero_()
+        e0.record(stream)
+        fa.forward(q, k, v, **kw, out=o, lse=lse, workspace=ws)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+        for n in ("fwd", "decode", "combine"):
+            rc, ms = fa.fa_profile_read(n)
+            if rc == 0:
+                kern.setdefault(n, []).append(ms)
+    fa.fa_profile_enable(False)
+    torch.cuda.synchronize()
+    nbytes = 2 * (2 * B * s_kv * h_kv * d) + 2 * (2 * B * s_q * h_q * d) + 4 * B * h_q * s_q
+    ms = statistics.mean(times)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    pk = peaks()
+    flops = metrics.fwd_flops(dict(w, varlen=False))
+    del q, k, v, o, lse, ws
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "GB_per_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm"], 4),
+            "hbm_peak": pk["hbm"], "TFLOPS": round(flops / (ms * 1e-3) / 1e12, 1), "algorithmic_bytes": nbytes,
+            "kernel_ms": {n: round(statistics.mean(x), 4) for n, x in kern.items()}}
 
 
 # ----------------------------------------------------------------------------------------------

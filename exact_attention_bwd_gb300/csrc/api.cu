@@ -144,7 +144,6 @@ fa_status normalise(const fa_params* in, Problem& p) {
 // ------------------------------------------------------------------------------------------
 enum class FwdPath { kEmpty, kTensor, kDecode };
 
-constexpr int kDecodeRowsMax = 16;  // query rows per key/value head served by the decode kernel
 constexpr int kDecodeKeys = 64;     // keys per decode tile
 constexpr size_t kStatusBytes = 256;
 
@@ -180,11 +179,11 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
     if (p.B == 0 || rows_total == 0) return FA_OK;  // nothing to compute
     const bool dense = p.cu_q == nullptr;
     const int R = p.s_q * p.G;  // query rows per key/value head (dense)
-    if (dense && R <= kDecodeRowsMax && (p.d == 64 || p.d == 128 || p.d == 256)) {
+    if (dense && (p.d == 64 || p.d == 128 || p.d == 256) && R <= decode_rows_max(p.d)) {
         pl.path = FwdPath::kDecode;
         const int tiles = (p.s_kv + kDecodeKeys - 1) / kDecodeKeys;
         const long units = (long)p.B * p.h_kv;
-        const int slots = sm_count() * 2;
+        const int slots = sm_count() * decode_ctas_per_sm(p.d, R);
         // partials: R rows x (d + 1) floats per split, written and read, against the
         // unit's 2 * s_kv * d bf16 of keys and values
         const double part = p.s_kv > 0 ? (double)R * (p.d + 1) * 8.0 / ((double)p.s_kv * p.d * 4.0) : 1.0;

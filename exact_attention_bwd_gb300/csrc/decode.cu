@@ -1,6 +1,6 @@
 // Decode-shaped forward (few query rows per key/value head) and the split-KV combine.
 //
-// With s_q * (h_q / h_kv) <= 16 query rows per key/value head the work is a stream over
+// With s_q * (h_q / h_kv) <= 8 query rows per key/value head (4 at d = 256) the work is a stream over
 // the key/value cache: about 2 multiply-adds per byte read, far below what the tensor
 // cores would need, so this path runs on the CUDA cores and is sized to keep HBM busy.
 // The cache of one (batch, key/value head) is split across CTAs, each CTA writes a
@@ -12,29 +12,29 @@
 namespace fa {
 namespace {
 
-constexpr int kThreadsDec = 256;
-constexpr int BK = 64;        // keys per tile
-constexpr int RMAX = 16;      // query rows per CTA
+constexpr int kComputeWarps = 8;
+constexpr int kThreadsDec = 32 * (kComputeWarps + 1);  // + one producer warp
+constexpr int BK = 64;                                 // keys per tile
+constexpr int KPW = BK / kComputeWarps;                // keys per warp per tile (8)
 
-template <int D>
+template <int D, int RG>
 struct DecCfg {
     static constexpr int KCH = D / 64;
     static constexpr int CHUNK = BK * 128;             // [64 rows][64 cols] bf16, swizzled
     static constexpr int TILE = BK * D * 2;            // one K (or V) tile
-    static constexpr int STAGES = (D == 256) ? 3 : 4;
-    static constexpr int DP = D / 2;                   // column pairs
-    static constexpr int KG = kThreadsDec / DP;        // key groups in the P.V phase
+    static constexpr int EPL = D / 32;                 // head-dim elements per lane
+    static constexpr int R = 4 * RG;                   // query rows held (padded)
+    // two CTAs per SM where the stages fit in half the shared memory
+    static constexpr int STAGES = (D == 256) ? 3 : (D == 128 ? 3 : 6);
+    static constexpr int MIN_BLOCKS = (D == 256 || RG > 1) ? 1 : 2;
 };
 
-template <int D>
+template <int D, int RG>
 struct __align__(1024) DecSmem {
-    uint8_t k[DecCfg<D>::STAGES][DecCfg<D>::TILE];
-    uint8_t v[DecCfg<D>::STAGES][DecCfg<D>::TILE];
-    float q[RMAX][D];        // query rows pre-multiplied by scale * log2(e)
-    float sc[RMAX][BK];      // scores, then probabilities
-    float alpha[RMAX];
-    float m[RMAX], l[RMAX];
-    uint64_t full[DecCfg<D>::STAGES];
+    uint8_t k[DecCfg<D, RG>::STAGES][DecCfg<D, RG>::TILE];
+    uint8_t v[DecCfg<D, RG>::STAGES][DecCfg<D, RG>::TILE];
+    float mw[kComputeWarps][4 * RG], lw[kComputeWarps][4 * RG];
+    uint64_t full[DecCfg<D, RG>::STAGES], empty[DecCfg<D, RG>::STAGES];
     int abort_flag;
 };
 
@@ -44,212 +44,244 @@ __device__ __forceinline__ int sw128(int row, int col) {
     return row * 128 + ((((col >> 3) ^ row) & 7) << 4) + ((col & 7) << 1);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreadsDec) decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
-                                                             const __grid_constant__ CUtensorMap tmv) {
-    using C = DecCfg<D>;
+// EPL consecutive bf16 values of row `row` starting at column `col` of a swizzled tile,
+// widened to fp32 (EPL = 2, 4 or 8: one 4-, 8- or 16-byte load that stays in a unit).
+template <int EPL, int CHUNK>
+__device__ __forceinline__ void load_row_slice(const uint8_t* tile, int row, int col, float* out) {
+    const uint8_t* src = tile + (col >> 6) * CHUNK + sw128(row, col & 63);
+    if constexpr (EPL == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+        out[0] = bf16_lo(w);
+        out[1] = bf16_hi(w);
+    } else if constexpr (EPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(src);
+        out[0] = bf16_lo(w.x); out[1] = bf16_hi(w.x); out[2] = bf16_lo(w.y); out[3] = bf16_hi(w.y);
+    } else {
+        const uint4 w = *reinterpret_cast<const uint4*>(src);
+        out[0] = bf16_lo(w.x); out[1] = bf16_hi(w.x); out[2] = bf16_lo(w.y); out[3] = bf16_hi(w.y);
+        out[4] = bf16_lo(w.z); out[5] = bf16_hi(w.z); out[6] = bf16_lo(w.w); out[7] = bf16_hi(w.w);
+    }
+}
+
+// Each compute warp streams its own 8 keys of every 64-key tile and keeps a private online
+// softmax (running max m, running sum l, un-normalised output) for every query row; lane
+// L holds head-dim elements [EPL L, EPL L + EPL).  Per tile and group of 4 rows, the 32
+// (key, row) dot products are formed by a reduce-scatter across the lanes, so lane L ends
+// with item L = 4 * key + row.  The warps' states are merged by their log-sum-exp at the
+// end and the CTA writes the partial (O, LSE) of its key range.
+template <int D, int RG>
+__global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
+    decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    using C = DecCfg<D, RG>;
+    constexpr int EPL = C::EPL;
     extern __shared__ uint8_t smem_raw[];
-    DecSmem<D>& s = *reinterpret_cast<DecSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    DecSmem<D, RG>& s =
+        *reinterpret_cast<DecSmem<D, RG>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x % a.n_splits;
+    const int unit = blockIdx.x / a.n_splits;
+    const int g = unit % p.h_kv, b = unit / p.h_kv;
     const int R = p.s_q * p.G;
     const Band band{p.s_kv - p.s_q, p.left, p.right, p.s_kv};
 
-    // key range of this split, clipped to the union of the rows' bands
     int j_begin = split * a.split_keys, j_end = min(p.s_kv, (split + 1) * a.split_keys);
-    {
-        const int lo = band.lo(0), hi = band.hi(p.s_q - 1);
-        j_begin = max(j_begin, lo);
-        j_end = min(j_end, hi + 1);
-    }
+    j_begin = max(j_begin, band.lo(0));
+    j_end = min(j_end, band.hi(p.s_q - 1) + 1);
     const int t_begin = j_begin / BK;
     const int n_tiles = j_end > j_begin ? (j_end - 1) / BK + 1 - t_begin : 0;
 
-    // an earlier CTA of this launch gave up: do not start new work
     if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     Abort ab{&s.abort_flag, a.status};
     if (tid == 0) {
         s.abort_flag = 0;
-        for (int i = 0; i < C::STAGES; ++i) mbar_init(&s.full[i], 1);
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], kComputeWarps);
+        }
         fence_mbar_init();
     }
-    for (int x = tid; x < RMAX * D; x += kThreadsDec) {
-        const int r = x / D, c = x % D;
-        float val = 0.f;
-        if (r < R) {
-            const int i = r / p.G, h = g * p.G + r % p.G;
-            val = __bfloat162float(a.q[(((long)b * p.s_q + i) * p.h_q + h) * D + c]) * p.scale_log2;
-        }
-        s.q[r][c] = val;
-    }
-    if (tid < RMAX) {
-        s.m[tid] = -INFINITY;
-        s.l[tid] = 0.f;
-    }
     __syncthreads();
 
-    auto issue = [&](int t) {  // tile t (relative) into stage t % STAGES
-        const int st = t % C::STAGES;
-        const int j0 = (t_begin + t) * BK;
-        mbar_expect_tx(&s.full[st], 2 * C::TILE);
-        for (int c = 0; c < C::KCH; ++c) {
-            tma_load_4d(&s.k[st][c * C::CHUNK], &tmk, &s.full[st], c * 64, g, j0, b);
-            tma_load_4d(&s.v[st][c * C::CHUNK], &tmv, &s.full[st], c * 64, g, j0, b);
-        }
-    };
-    if (tid == 0) {
-        tma_prefetch_desc(&tmk);
-        tma_prefetch_desc(&tmv);
-        for (int t = 0; t < C::STAGES && t < n_tiles; ++t) issue(t);
+    // per-lane state of a compute warp: un-normalised output, running max and sum per row
+    float acc[C::R][EPL], m[C::R], l[C::R];
+#pragma unroll
+    for (int r = 0; r < C::R; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[r][e] = 0.f;
     }
 
-    // P.V accumulators: column pair dp, key group kg, all rows
-    const int dp = tid % C::DP, kg = tid / C::DP;
-    float acc[RMAX][2];
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) acc[r][0] = acc[r][1] = 0.f;
-
-    int issued = min(C::STAGES, n_tiles);
-    int consumed = 0;  // tiles whose copies have landed and been waited for
-    bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-        const int st = t % C::STAGES;
-        const bool w = mbar_wait(&s.full[st], (t / C::STAGES) & 1, ab);
-        if (!__syncthreads_and(w)) {
-            ok = false;
-            break;
+    if (warp == kComputeWarps) {
+        // ================= producer =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            int issued = 0;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % C::STAGES;
+                if (!mbar_wait(&s.empty[st], ((t / C::STAGES) & 1) ^ 1, ab)) break;
+                const int j0 = (t_begin + t) * BK;
+                mbar_expect_tx(&s.full[st], 2 * C::TILE);
+                for (int c = 0; c < C::KCH; ++c) {
+                    tma_load_4d(&s.k[st][c * C::CHUNK], &tmk, &s.full[st], c * 64, g, j0, b);
+                    tma_load_4d(&s.v[st][c * C::CHUNK], &tmv, &s.full[st], c * 64, g, j0, b);
+                }
+                ++issued;
+            }
+            // wait for the copies still in flight (the latest phase of each used stage)
+            for (int back = 1; back <= C::STAGES && back <= issued; ++back) {
+                const int t = issued - back;
+                mbar_wait_quiet(&s.full[t % C::STAGES], (t / C::STAGES) & 1);
+            }
         }
-        consumed = t + 1;
-        const int j0 = (t_begin + t) * BK;
-        // ---- scores: thread = (key, row group) ----
-        {
-            const int jj = tid & (BK - 1);
-            const int rg = tid / BK;  // 0..3
-            const uint8_t* kb = s.k[st];
-            float dots[RMAX / 4];
+    } else {
+        // ================= compute warps =================
+        const int e0 = EPL * lane;
+        float q[C::R][EPL];
 #pragma unroll
-            for (int u = 0; u < RMAX / 4; ++u) dots[u] = 0.f;
-#pragma unroll 4
-            for (int c8 = 0; c8 < D; c8 += 8) {
-                const uint4 kv = *reinterpret_cast<const uint4*>(kb + (c8 >> 6) * C::CHUNK + sw128(jj, c8 & 63));
-                const float k0 = bf16_lo(kv.x), k1 = bf16_hi(kv.x), k2 = bf16_lo(kv.y), k3 = bf16_hi(kv.y);
-                const float k4 = bf16_lo(kv.z), k5 = bf16_hi(kv.z), k6 = bf16_lo(kv.w), k7 = bf16_hi(kv.w);
+        for (int r = 0; r < C::R; ++r) {
 #pragma unroll
-                for (int u = 0; u < RMAX / 4; ++u) {
-                    const int r = rg + 4 * u;
-                    if (r < R) {
-                        const float4 qa = *reinterpret_cast<const float4*>(&s.q[r][c8]);
-                        const float4 qb = *reinterpret_cast<const float4*>(&s.q[r][c8 + 4]);
-                        float d0 = dots[u];
-                        d0 = fmaf(qa.x, k0, d0);
-                        d0 = fmaf(qa.y, k1, d0);
-                        d0 = fmaf(qa.z, k2, d0);
-                        d0 = fmaf(qa.w, k3, d0);
-                        d0 = fmaf(qb.x, k4, d0);
-                        d0 = fmaf(qb.y, k5, d0);
-                        d0 = fmaf(qb.z, k6, d0);
-                        d0 = fmaf(qb.w, k7, d0);
-                        dots[u] = d0;
+            for (int e = 0; e < EPL; ++e) {
+                float val = 0.f;
+                if (r < R) {
+                    const int i = r / p.G, h = g * p.G + r % p.G;
+                    val = __bfloat162float(a.q[(((long)b * p.s_q + i) * p.h_q + h) * D + e0 + e]) * p.scale_log2;
+                }
+                q[r][e] = val;
+            }
+        }
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % C::STAGES;
+            {
+                const bool w = mbar_wait(&s.full[st], (t / C::STAGES) & 1, ab);
+                if (!__all_sync(0xffffffffu, w)) break;
+            }
+            const int jw = (t_begin + t) * BK + KPW * warp;  // first key of this warp
+            float kv[KPW][EPL];
+#pragma unroll
+            for (int k = 0; k < KPW; ++k) load_row_slice<EPL, C::CHUNK>(s.k[st], KPW * warp + k, e0, kv[k]);
+            const int kk = lane >> 2, rr = lane & 3;   // item of this lane after the reduction
+            const int j = jw + kk;
+#pragma unroll
+            for (int rg = 0; rg < RG; ++rg) {
+                // 32 partial dot products: item 4k + rr
+                float v32[32];
+#pragma unroll
+                for (int k = 0; k < KPW; ++k)
+#pragma unroll
+                    for (int r4 = 0; r4 < 4; ++r4) {
+                        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < EPL; e += 2)
+                            acc2 = __ffma2_rn(make_float2(q[4 * rg + r4][e], q[4 * rg + r4][e + 1]),
+                                              make_float2(kv[k][e], kv[k][e + 1]), acc2);
+                        v32[4 * k + r4] = acc2.x + acc2.y;
+                    }
+                // reduce-scatter: lane L ends with the full sum of item L
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+                    for (int i = 0; i < o; ++i) {
+                        const bool up = (lane & o) != 0;
+                        const float send = up ? v32[i] : v32[i + o];
+                        const float keep = up ? v32[i + o] : v32[i];
+                        v32[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                     }
                 }
-            }
-            const int j = j0 + jj;
-#pragma unroll
-            for (int u = 0; u < RMAX / 4; ++u) {
-                const int r = rg + 4 * u;
-                if (r < R) {
+                const int r = 4 * rg + rr;
+                float sc = v32[0];
+                {
                     const int i = r / p.G;
-                    const bool keep = j >= j_begin && j < j_end && j >= band.lo(i) && j <= band.hi(i);
-                    s.sc[r][jj] = keep ? dots[u] : -INFINITY;
+                    const bool keep = r < R && j >= j_begin && j < j_end && j >= band.lo(i) && j <= band.hi(i);
+                    if (!keep) sc = -INFINITY;
                 }
-            }
-        }
-        __syncthreads();
-        // ---- online softmax: warp w owns rows w and w + 8 ----
-        for (int r = warp; r < R; r += kThreadsDec / 32) {
-            const float x0 = s.sc[r][lane], x1 = s.sc[r][lane + 32];
-            float mx = fmaxf(x0, x1);
+                // per-row max and sum over the warp's 8 keys (lanes with equal lane % 4)
+                float mt = sc;
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                const float m_old = (rr == 0) ? m[4 * rg] : (rr == 1) ? m[4 * rg + 1] : (rr == 2) ? m[4 * rg + 2] : m[4 * rg + 3];
+                const float m_new = fmaxf(m_old, mt);
+                const float base = (m_new == -INFINITY) ? 0.f : m_new;
+                const float pr = ex2(sc - base);
+                const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - base);
+                float ps = pr;
+                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+                // every lane takes the new state of the group's 4 rows from lanes 0..3
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float m_old = s.m[r];
-            const float m_new = fmaxf(m_old, mx);
-            const float base = (m_new == -INFINITY) ? 0.f : m_new;
-            const float p0 = ex2(x0 - base), p1 = ex2(x1 - base);
-            float sum = p0 + p1;
+                for (int r4 = 0; r4 < 4; ++r4) {
+                    const float al = __shfl_sync(0xffffffffu, alpha, r4);
+                    m[4 * rg + r4] = __shfl_sync(0xffffffffu, m_new, r4);
+                    l[4 * rg + r4] = l[4 * rg + r4] * al + __shfl_sync(0xffffffffu, ps, r4);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            s.sc[r][lane] = p0;
-            s.sc[r][lane + 32] = p1;
-            __syncwarp();
-            if (lane == 0) {
-                const float al = (m_old == -INFINITY) ? 0.f : ex2(m_old - base);
-                s.alpha[r] = al;
-                s.l[r] = s.l[r] * al + sum;
-                s.m[r] = m_new;
-            }
-        }
-        __syncthreads();
-        // ---- O += P V: thread = (column pair, key group) ----
-        {
-#pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                if (r < R) {
-                    const float al = s.alpha[r];
-                    acc[r][0] *= al;
-                    acc[r][1] *= al;
+                    for (int e = 0; e < EPL; ++e) acc[4 * rg + r4][e] *= al;
                 }
-            }
-            const uint8_t* vb = s.v[st];
-            const int c = 2 * dp;
-            constexpr int KPG = BK / C::KG;  // keys per group
-            for (int kk = 0; kk < KPG; ++kk) {
-                const int jj = kg * KPG + kk;
-                const uint32_t vv = *reinterpret_cast<const uint32_t*>(vb + (c >> 6) * C::CHUNK + sw128(jj, c & 63));
-                const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
+                // O += P V over the warp's 8 keys
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    if (r < R) {
-                        const float pr = s.sc[r][jj];
-                        acc[r][0] = fmaf(pr, v0, acc[r][0]);
-                        acc[r][1] = fmaf(pr, v1, acc[r][1]);
+                for (int k = 0; k < KPW; ++k) {
+                    float vv[EPL];
+                    load_row_slice<EPL, C::CHUNK>(s.v[st], KPW * warp + k, e0, vv);
+#pragma unroll
+                    for (int r4 = 0; r4 < 4; ++r4) {
+                        const float pk = __shfl_sync(0xffffffffu, pr, 4 * k + r4);
+#pragma unroll
+                        for (int e = 0; e < EPL; e += 2) {
+                            const float2 o2 = __ffma2_rn(make_float2(pk, pk), make_float2(vv[e], vv[e + 1]),
+                                                         make_float2(acc[4 * rg + r4][e], acc[4 * rg + r4][e + 1]));
+                            acc[4 * rg + r4][e] = o2.x;
+                            acc[4 * rg + r4][e + 1] = o2.y;
+                        }
                     }
                 }
             }
-        }
-        __syncthreads();  // stage st and the scores are free again
-        if (tid == 0 && issued < n_tiles) {
-            issue(issued);
-            ++issued;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.empty[st]);
         }
     }
-    // abort path: wait for the copies issued but never waited for (at most STAGES of
-    // them, each the latest phase of its stage) before the shared memory goes away
-    if (tid == 0) {
-        for (int t = consumed; t < issued; ++t) mbar_wait_quiet(&s.full[t % C::STAGES], (t / C::STAGES) & 1);
-    }
+    // every tile is consumed and the producer has drained: the stages become the merge buffer
     __syncthreads();
-
-    // ---- reduce the key groups and write the partial (O / l, LSE) ----
-    float* red = reinterpret_cast<float*>(s.k[0]);  // [KG][RMAX][D] floats, fits in the K stages
+    float* red = reinterpret_cast<float*>(s.k[0]);  // [warp][row][D], spans the K and V stages
+    if (warp < kComputeWarps) {
+        const int e0 = EPL * lane;
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-        if (r < R) {
-            red[(kg * RMAX + r) * D + 2 * dp] = acc[r][0];
-            red[(kg * RMAX + r) * D + 2 * dp + 1] = acc[r][1];
+        for (int r = 0; r < C::R; ++r)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) red[(warp * C::R + r) * D + e0 + e] = acc[r][e];
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < C::R; ++r) {
+                s.mw[warp][r] = m[r];
+                s.lw[warp][r] = l[r];
+            }
         }
     }
     __syncthreads();
+    // merge the warps' states by their running max, write the CTA's partial (O / l, LSE)
     const long nrows = (long)p.B * p.h_q * p.s_q;
     for (int x = tid; x < R * D; x += kThreadsDec) {
         const int r = x / D, c = x % D;
-        float sum = 0.f;
-        for (int q = 0; q < C::KG; ++q) sum += red[(q * RMAX + r) * D + c];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, s.mw[w][r]);
+        float L = 0.f, O = 0.f;
+        if (M > -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kComputeWarps; ++w) {
+                const float mw = s.mw[w][r];
+                if (mw == -INFINITY) continue;
+                const float sc = ex2(mw - M);
+                L += s.lw[w][r] * sc;
+                O += red[(w * C::R + r) * D + c] * sc;
+            }
+        }
         const int i = r / p.G, h = g * p.G + r % p.G;
         const long row = ((long)b * p.h_q + h) * p.s_q + i;
-        const float l = s.l[r];
-        a.o_part[((long)split * nrows + row) * D + c] = (l > 0.f && ok) ? sum / l : 0.f;
-        if (c == 0) a.lse_part[(long)split * nrows + row] = (l > 0.f && ok) ? (s.m[r] + log2f(l)) * kLn2 : -INFINITY;
+        a.o_part[((long)split * nrows + row) * D + c] = L > 0.f ? O / L : 0.f;
+        if (c == 0) a.lse_part[(long)split * nrows + row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
 }
 
@@ -302,14 +334,24 @@ __global__ void combine_kernel(const CombineArgs a) {
 
 }  // namespace
 
+template <int D, int RG>
+static cudaError_t launch_decode_dr(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+    const size_t smem = sizeof(DecSmem<D, RG>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long n = (long)a.n_splits * a.p.h_kv * a.p.B;
+    decode_kernel<D, RG><<<(unsigned)n, kThreadsDec, smem, st>>>(a, tk, tv);
+    return cudaGetLastError();
+}
+
 template <int D>
 static cudaError_t launch_decode_d(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-    const size_t smem = sizeof(DecSmem<D>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid(a.n_splits, a.p.h_kv, a.p.B);
-    decode_kernel<D><<<grid, kThreadsDec, smem, st>>>(a, tk, tv);
-    return cudaGetLastError();
+    const int R = a.p.s_q * a.p.G;
+    if (R <= 4) return launch_decode_dr<D, 1>(a, tk, tv, st);
+    if constexpr (D != 256) {
+        if (R <= 8) return launch_decode_dr<D, 2>(a, tk, tv, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
@@ -320,6 +362,11 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
         default: return cudaErrorInvalidValue;
     }
 }
+
+// The per-lane state (query rows and output accumulators) grows with the rows; past these
+// counts the registers spill, and the tensor-core path takes the problem instead.
+int decode_rows_max(int d) { return d == 256 ? 4 : 8; }
+int decode_ctas_per_sm(int d, int rows) { return (d == 256 || rows > 4) ? 1 : 2; }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
     const long nrows = (long)a.p.B * a.p.h_q * a.p.s_q;

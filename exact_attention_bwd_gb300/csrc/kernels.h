@@ -86,6 +86,8 @@ cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtenso
                           cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+int decode_rows_max(int d);                // query rows per key/value head the decode kernel takes
+int decode_ctas_per_sm(int d, int rows);   // its CTAs resident per SM
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t st);

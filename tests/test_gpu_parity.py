@@ -117,10 +117,17 @@ def test_packed_batch_window():
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
-@pytest.mark.parametrize("s_q", [1, 4])
+@pytest.mark.parametrize("s_q", [1, 2, 4])
 def test_decode_shapes(d, s_q):
-    """Few query rows per key/value head against a long cache (CUDA-core split path)."""
+    """Few query rows per key/value head against a long cache: 4 or 8 rows per key/value
+    head take the CUDA-core split path, 16 rows the tensor-core path."""
     compare(make_case(106, d + s_q, B=2, s_q=s_q, s_kv=3000, h_q=8, h_kv=2, d=d, causal=True), bwd=False)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_window_and_sinks(d):
+    compare(make_case(106, 7 * d, B=3, s_q=2, s_kv=1500, h_q=8, h_kv=4, d=d, causal=False, window=(300, 0),
+                      sinks=True), bwd=False)
 
 
 @pytest.mark.parametrize("d", [64, 128])

@@ -62,7 +62,9 @@ def test_noalloc_matches_workspace_forward_twice(first, second):
 def test_noalloc_rejects_problems_beyond_its_scratch():
     from exact_attention_bwd_gb300 import binding as fa
     p = fa.FaParams()
-    p.B, p.s_q, p.s_kv, p.h_q, p.h_kv, p.d = 1024, 4, 65536, 32, 8, 128
+    # a decode-shaped problem (8 query rows per key/value head) whose split partials alone
+    # need 4096 * 32 * 2 rows * 128 floats = 128 MiB
+    p.B, p.s_q, p.s_kv, p.h_q, p.h_kv, p.d = 4096, 2, 1024, 32, 8, 128
     p.causal, p.window_left, p.window_right = 1, -1, -1
     assert fa.fa_fwd_workspace_size(p) > fa.FA_NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(0x100000)
