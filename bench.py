@@ -37,7 +37,7 @@ UNIT = "TFLOP/s"
 WORKLOAD = "sweep_s8192_causal"
 # dram__bytes_read.sum + dram__bytes_write.sum of one bwd_main launch, from the ncu
 # capture summarised in profiles/ (None until a capture of the current kernel exists)
-BWD_MAIN_DRAM_BYTES = None
+BWD_MAIN_DRAM_BYTES = 2920055000  # profiles/fwd_bwd_main_s8192_causal_ncu.md
 
 
 def parse():
@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", default=None, help="time one decode workload and exit")
+    ap.add_argument("--decode-batch", type=int, default=None, help="batch override for --decode-only")
     return ap.parse_args()
 
 
@@ -269,13 +271,13 @@ def run_ours(args):
 # decode / chunked prefill against a long cache: HBM-bound, reported as GB/s
 # ----------------------------------------------------------------------------------------------
 
-def measure_decode(dev, name, steps=10, warmup=3):
+def measure_decode(dev, name, steps=10, warmup=3, batch=None):
     """Forward of one decode workload: algorithmic bytes (K and V read once, Q read, O and
     LSE written) per launch over the CUDA-event time of the whole forward (split kernel +
     combine), L2 flushed between launches; per-kernel times from the library's hooks."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
-    w = inputs.workload(name)
+    w = inputs.workload(name) if batch is None else inputs.workload(name, B=batch)
     B, s_q, s_kv, h_q, h_kv, d = w["B"], w["s_q"], w["s_kv"], w["h_q"], w["h_kv"], w["d"]
     sd = lambda t: inputs.seed_of(w["wid"], w["variant"], t)  # noqa: E731
     q = inputs.normal_bf16_torch(sd(inputs.Q), (B, s_q, h_q, d), dev)
@@ -370,6 +372,13 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.decode_only:
+        import torch
+        torch.cuda.set_device(0)
+        r = measure_decode(torch.device("cuda", 0), args.decode_only, steps=args.steps, warmup=args.warmup,
+                           batch=args.decode_batch)
+        print(json.dumps({"workload": args.decode_only, "batch": args.decode_batch, **r}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
