@@ -126,6 +126,19 @@ class ClockSampler:
 # the GPU arm
 # ----------------------------------------------------------------------------------------------
 
+def aggregate(total_ms_local, flops_per_step, steps, world, device=None):
+    """Whole-job throughput of N replicas: the timed region ends when the slowest rank
+    does, so the step time is the maximum over ranks and the value counts every rank's
+    work.  Returns (max total ms, TFLOP/s).  Backend-agnostic (nccl on GPUs, gloo on CPU)."""
+    total = float(total_ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    return total, world * flops_per_step * steps / (total * 1e-3) / 1e12
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -184,13 +197,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     fa.fa_profile_enable(False)
     clocks = clk.summary()
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = aggregate(sum(times), fl_fwd + fl_bwd, args.steps, world, dev)
     ms_step = total_ms / args.steps
-    value = world * (fl_fwd + fl_bwd) * args.steps / (total_ms * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs in, results out, through the same public API ----
     e2e = None
@@ -216,12 +224,8 @@ def run_ours(args):
             ev1.synchronize()
             if it >= args.warmup:
                 e2e_ms.append(ev0.elapsed_time(ev1))
-        tot = sum(e2e_ms)
-        if world > 1:
-            t = torch.tensor([tot], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            tot = float(t.item())
-        e2e = {"value": world * (fl_fwd + fl_bwd) * len(e2e_ms) / (tot * 1e-3) / 1e12, "unit": UNIT,
+        tot, e2e_value = aggregate(sum(e2e_ms), fl_fwd + fl_bwd, len(e2e_ms), world, dev)
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": tot / len(e2e_ms)}
 
     pk = peaks()
