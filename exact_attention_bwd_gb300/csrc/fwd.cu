@@ -163,10 +163,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     // registers: 384 x 168 at launch; the producer/MMA group hands part of its share to
-    // the two softmax groups (128 x 72 + 256 x 216 = 64512).  The change is made at the
+    // the two softmax groups (128 x 88 + 256 x 208 = 64512).  The change is made at the
     // top of each warp group's branch so the register allocator sees it on every path.
     if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && u1 > u0) {
@@ -216,70 +216,107 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
+        // Everything the issue path touches lives in registers (no per-tile arrays indexed
+        // at run time), so consecutive MMAs go out back to back.
         if (lane == 0 && u1 > u0) {
             constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
             constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-            bool ok = mbar_wait(&s.q_full, 0, ab);
-            tc_fence_after();
-            uint32_t pcount[2] = {0, 0};
+            constexpr uint32_t kStageStep = (uint32_t)C::TILE_BYTES >> 4;  // descriptor units per stage
+            const int ta0 = ti[0].t0, ta1 = ti[0].t1, tb0 = ti[1].t0, tb1 = ti[1].t1;
             // a descriptor's start-address field is addr >> 4 in its low bits, so stepping
             // through a tile is a plain add to a base descriptor (no carry: addr < 256 KB)
-            auto issue_s = [&](int k, int st) {
-                const uint64_t qd = sdesc_sw128(smem_u32(s.q[k]), 16, 1024);
-                const uint64_t kd = sdesc_sw128(smem_u32(s.k[st]), 16, 1024);
+            const uint64_t qd0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
+            const uint64_t qd1 = sdesc_sw128(smem_u32(s.q[1]), 16, 1024);
+            const uint64_t kd_base = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
+            const uint64_t vd_base = sdesc_sw128(smem_u32(s.v[0]), C::CHUNK_BYTES, 1024);
+            auto issue_s = [&](uint64_t qd, uint32_t scol, uint64_t kd) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + 128 * k, qd + off, kd + off, idS, kk > 0);
+                    mma_ss(tmem + scol, qd + off, kd + off, idS, kk > 0);
                 }
-                tc_commit(&s.s_full[k]);
             };
-            int it = 0;
-            if (ok) {
+            auto issue_pv = [&](uint32_t ocol, uint32_t pcol, uint64_t vd, uint32_t acc0) {
+                mma_ts(tmem + ocol, tmem + pcol, vd, idO, acc0);
+#pragma unroll
+                for (int kk = 1; kk < BN / 16; ++kk)
+                    mma_ts(tmem + ocol, tmem + pcol + kk * 8, vd + (kk * 2048 >> 4), idO, 1u);
+            };
+            uint32_t pc0 = 0, pc1 = 0;
+            bool ok = mbar_wait(&s.q_full, 0, ab);
+            tc_fence_after();
+            if (ok && (ok = mbar_wait(&s.k_full[0], 0, ab))) {
                 // prologue: S_k for the first KV tile
-                ok = mbar_wait(&s.k_full[0], 0, ab);
-                if (ok) {
-                    tc_fence_after();
-                    for (int k = 0; k < 2; ++k)
-                        if (u0 >= ti[k].t0 && u0 < ti[k].t1) issue_s(k, 0);
-                    tc_commit(&s.k_empty[0]);
+                tc_fence_after();
+                if (u0 >= ta0 && u0 < ta1) {
+                    issue_s(qd0, 0, kd_base);
+                    tc_commit(&s.s_full[0]);
                 }
+                if (u0 >= tb0 && u0 < tb1) {
+                    issue_s(qd1, 128, kd_base);
+                    tc_commit(&s.s_full[1]);
+                }
+                tc_commit(&s.k_empty[0]);
             }
+            int it = 0;
             for (int j = u0; ok && j < u1; ++j, ++it) {
                 const int st = it % C::STAGES;
                 const uint32_t ph = (it / C::STAGES) & 1;
                 const int st1 = (it + 1) % C::STAGES;
                 const uint32_t ph1 = ((it + 1) / C::STAGES) & 1;
-                bool k_next_ready = false;
-                if (!(ok = mbar_wait(&s.v_full[st], ph, ab))) break;
+                const uint64_t vd = vd_base + (uint64_t)(st * kStageStep);
+                const uint64_t kd1 = kd_base + (uint64_t)(st1 * kStageStep);
+                const bool next = j + 1 < u1;
+                bool k_ready = false;
+                ok = mbar_wait(&s.v_full[st], ph, ab);
                 tc_fence_after();
-                for (int k = 0; k < 2 && ok; ++k) {
-                    if (j >= ti[k].t0 && j < ti[k].t1) {
-                        if (!(ok = mbar_wait(&s.p_full[k], pcount[k] & 1, ab))) break;
-                        ++pcount[k];
-                        tc_fence_after();
-                        const uint64_t vd = sdesc_sw128(smem_u32(s.v[st]), C::CHUNK_BYTES, 1024);
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_ts(tmem + 256 + 128 * k, tmem + 128 * k + kk * 8, vd + (kk * 2048 >> 4), idO,
-                                   (j > ti[k].t0 || kk > 0) ? 1u : 0u);
-                        if (j == ti[k].t1 - 1) tc_commit(&s.o_full[k]);
-                    }
-                    if (j + 1 < u1 && j + 1 >= ti[k].t0 && j + 1 < ti[k].t1) {
-                        if (!k_next_ready) {
-                            if (!(ok = mbar_wait(&s.k_full[st1], ph1, ab))) break;
-                            tc_fence_after();
-                            k_next_ready = true;
-                        }
-                        issue_s(k, st1);
+                // tile 0: O_0 += P_0 V_j, then S_0 for the next key tile
+                if (ok && j >= ta0 && j < ta1) {
+                    ok = mbar_wait(&s.p_full[0], pc0 & 1, ab);
+                    ++pc0;
+                    tc_fence_after();
+                    if (ok) {
+                        issue_pv(256, 0, vd, j > ta0 ? 1u : 0u);
+                        if (j == ta1 - 1) tc_commit(&s.o_full[0]);
                     }
                 }
+                if (ok && next && j + 1 >= ta0 && j + 1 < ta1) {
+                    ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                    tc_fence_after();
+                    k_ready = true;
+                    if (ok) {
+                        issue_s(qd0, 0, kd1);
+                        tc_commit(&s.s_full[0]);
+                    }
+                }
+                // tile 1
+                if (ok && j >= tb0 && j < tb1) {
+                    ok = mbar_wait(&s.p_full[1], pc1 & 1, ab);
+                    ++pc1;
+                    tc_fence_after();
+                    if (ok) {
+                        issue_pv(384, 128, vd, j > tb0 ? 1u : 0u);
+                        if (j == tb1 - 1) tc_commit(&s.o_full[1]);
+                    }
+                }
+                if (ok && next && j + 1 >= tb0 && j + 1 < tb1) {
+                    if (!k_ready) {
+                        ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                        tc_fence_after();
+                        k_ready = true;
+                    }
+                    if (ok) {
+                        issue_s(qd1, 128, kd1);
+                        tc_commit(&s.s_full[1]);
+                    }
+                }
+                if (!ok) break;
                 tc_commit(&s.v_empty[st]);
-                if (k_next_ready) tc_commit(&s.k_empty[st1]);
-                else if (j + 1 < u1 && ok) {
-                    // the next K tile feeds no S of this CTA (cannot happen for a contiguous
-                    // union of two bands, kept for safety): release it once it lands
-                    if ((ok = mbar_wait(&s.k_full[st1], ph1, ab))) tc_commit(&s.k_empty[st1]);
+                if (next) {
+                    // the next K tile always feeds an S of this CTA (the union of two bands is
+                    // contiguous); wait for it here if neither tile did
+                    if (!k_ready) ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                    if (ok) tc_commit(&s.k_empty[st1]);
                 }
             }
             // let every issued MMA finish before the CTA tears down
@@ -288,23 +325,28 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
     }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
         // ================= softmax: one thread per row =================
         const int k = (warp - 4) >> 2;           // query tile
         const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
         const uint32_t tS = tmem + lane_base + 128 * k;
         const uint32_t tO = tmem + lane_base + 256 + 128 * k;
-        const int i = ti[k].s0 + r / p.G;        // query position
+        // this group's tile, copied out of ti[] by selection (no run-time array index)
+        const int my_s0 = k ? ti[1].s0 : ti[0].s0;
+        const int my_t0 = k ? ti[1].t0 : ti[0].t0;
+        const int my_t1 = k ? ti[1].t1 : ti[0].t1;
+        const bool my_active = k ? ti[1].active : ti[0].active;
+        const int i = my_s0 + r / p.G;          // query position
         const int h = g * p.G + r % p.G;         // query head
-        const bool row_valid = ti[k].active && (r < p.P * p.G) && i < sv.nq;
+        const bool row_valid = my_active && (r < p.P * p.G) && i < sv.nq;
         const int jlo = row_valid ? band.lo(i) : 1;
         const int jhi = row_valid ? band.hi(i) : 0;
         const float c = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         uint32_t scount = 0;
         bool ok = true;
-        for (int j = ti[k].t0; j < ti[k].t1; ++j) {
+        for (int j = my_t0; j < my_t1; ++j) {
             const bool w = mbar_wait(&s.s_full[k], scount & 1, ab);
             if (!__all_sync(0xffffffffu, w)) {
                 ok = false;
@@ -379,7 +421,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             if (lane == 0) mbar_arrive(&s.p_full[k]);
         }
         // ---------------- epilogue ----------------
-        const bool has_o = ti[k].t1 > ti[k].t0;  // uniform over the warp group
+        const bool has_o = my_t1 > my_t0;  // uniform over the warp group
         if (has_o && ok) {
             const bool w = mbar_wait(&s.o_full[k], 0, ab);
             ok = __all_sync(0xffffffffu, w);
