@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other prefill workloads")
     ap.add_argument("--decode-only", default=None, help="time one decode workload and exit")
     ap.add_argument("--decode-batch", type=int, default=None, help="batch override for --decode-only")
     return ap.parse_args()
@@ -262,6 +263,8 @@ def run_ours(args):
     if not args.no_decode:
         line["decode"] = {n: measure_decode(dev, n) for n in
                           ("decode_d128_sq1", "decode_d128_sq64", "decode_d256_sq1", "decode_d256_sq64")}
+    if not args.no_sweep:
+        line["workloads"] = {n: measure_workload(dev, n) for n in SWEEP + OTHER}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = oracle_sample(w)
     if rank == 0:
@@ -269,6 +272,67 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------------------
+# every other workload: forward and forward+backward TFLOPS (context beside the headline)
+# ----------------------------------------------------------------------------------------------
+
+def measure_workload(dev, name, steps=5, warmup=2):
+    """fwd and fwd+bwd of one prefill workload with seeded on-device inputs (the same recipe
+    seeds, drawn by torch's generator); L2 flushed before every timed step."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    w = inputs.workload(name)
+    sd = lambda t: inputs.seed_of(w["wid"], w.get("variant", 0), t)  # noqa: E731
+    if w.get("varlen"):
+        lengths = inputs.varlen_lengths(sd(inputs.LENGTHS), n=w["B"], total=w["T"])
+        cu = inputs.cu_seqlens(lengths)
+        wf = dict(w, cu_q=cu, cu_k=cu)
+        qs, ks = (w["T"], w["h_q"], w["d"]), (w["T"], w["h_kv"], w["d"])
+        cu_d = torch.from_numpy(cu).to(dev)
+    else:
+        wf = dict(w)
+        qs, ks = (w["B"], w["s_q"], w["h_q"], w["d"]), (w["B"], w["s_kv"], w["h_kv"], w["d"])
+        cu_d = None
+    q = inputs.normal_bf16_torch(sd(inputs.Q), qs, dev)
+    k = inputs.normal_bf16_torch(sd(inputs.K), ks, dev)
+    v = inputs.normal_bf16_torch(sd(inputs.V), ks, dev)
+    do = inputs.normal_bf16_torch(sd(inputs.DO), qs, dev)
+    sinks = None
+    if w.get("sinks"):
+        g = torch.Generator(device=dev)
+        g.manual_seed(sd(inputs.SINKS))
+        sinks = torch.randn(w["h_q"], generator=g, device=dev, dtype=torch.float32)
+    kw = dict(causal=w["causal"], window=w["window"], softmax_scale=1.0 / math.sqrt(w["d"]), sinks=sinks,
+              cu_q=cu_d, cu_k=cu_d)
+    o, lse, wsf = fa.forward(q, k, v, **kw)
+    dq, dk, dv, ds, wsb = fa.backward(q, k, v, o, lse, do, **kw)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    tf, tb = [], []
+    for it in range(warmup + steps):
+        flush.zero_()
+        e0.record(stream)
+        fa.forward(q, k, v, **kw, out=o, lse=lse, workspace=wsf)
+        e1.record(stream)
+        fa.backward(q, k, v, o, lse, do, **kw, workspace=wsb, grads=(dq, dk, dv, ds))
+        e2.record(stream)
+        e2.synchronize()
+        if it >= warmup:
+            tf.append(e0.elapsed_time(e1))
+            tb.append(e1.elapsed_time(e2))
+    ff = metrics.fwd_flops(wf)
+    mf, mb = statistics.mean(tf), statistics.mean(tb)
+    del q, k, v, do, o, lse, wsf, dq, dk, dv, wsb
+    torch.cuda.empty_cache()
+    return {"fwd_ms": round(mf, 4), "bwd_ms": round(mb, 4), "fwd_TFLOPS": round(ff / (mf * 1e-3) / 1e12, 1),
+            "fwd_bwd_TFLOPS": round(3.5 * ff / ((mf + mb) * 1e-3) / 1e12, 1)}
+
+
+SWEEP = [f"sweep_s{s}{c}" for s in (512, 1024, 2048, 4096, 8192, 16384) for c in ("", "_causal")]
+OTHER = ["gqa_window_causal", "gqa_window_2sided", "varlen"]
 
 
 # ----------------------------------------------------------------------------------------------
