@@ -150,6 +150,7 @@ constexpr size_t kStatusBytes = 256;
 struct FwdPlan {
     FwdPath path = FwdPath::kEmpty;
     int n_blocks = 0, n_splits = 1, split_tiles = 0;
+    int unit_major = 0;
     size_t part_rows = 0;  // rows of the split partials
     size_t ws_bytes = kStatusBytes;
 };
@@ -219,6 +220,9 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
             pl.split_tiles = (tiles + pl.n_splits - 1) / pl.n_splits;
             pl.n_splits = (tiles + pl.split_tiles - 1) / pl.split_tiles;
         }
+        // few queries against a long key range: every query block does about the same work,
+        // so launch the blocks of one (batch, kv head) together and let them share K/V in L2
+        pl.unit_major = (p.s_q * 4 <= p.s_kv) ? 1 : 0;
         if (pl.n_splits > 1) {
             pl.part_rows = (size_t)p.B * p.h_q * p.s_q;
             pl.ws_bytes = kStatusBytes + align256(pl.part_rows * pl.n_splits * p.d * 4) +
@@ -378,6 +382,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.n_blocks = pl.n_blocks;
     a.n_splits = pl.n_splits;
     a.split_tiles = pl.split_tiles;
+    a.unit_major = pl.unit_major;
     a.o = reinterpret_cast<__nv_bfloat16*>(o);
     a.lse = lse;
     a.o_part = o_part;

@@ -91,9 +91,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             blk -= p.cu_q[seq] / bs + seq;
         } else {
             const int hb = p.h_kv * p.B;
-            g = (idx % hb) % p.h_kv;
-            seq = (idx % hb) / p.h_kv;
-            const int x = idx / hb;
+            const int per_unit = a.n_blocks * a.n_splits;
+            const int unit = a.unit_major ? idx / per_unit : idx % hb;
+            const int x = a.unit_major ? idx % per_unit : idx / hb;
+            g = unit % p.h_kv;
+            seq = unit / p.h_kv;
             split = x % a.n_splits;
             blk = a.n_blocks - 1 - x / a.n_splits;
         }

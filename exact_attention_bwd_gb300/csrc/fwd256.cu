@@ -54,9 +54,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
             blk -= p.cu_q[seq] / p.P + seq;
         } else {
             const int hb = p.h_kv * p.B;
-            g = (idx % hb) % p.h_kv;
-            seq = (idx % hb) / p.h_kv;
-            const int x = idx / hb;
+            const int per_unit = a.n_blocks * a.n_splits;
+            const int unit = a.unit_major ? idx / per_unit : idx % hb;
+            const int x = a.unit_major ? idx % per_unit : idx / hb;
+            g = unit % p.h_kv;
+            seq = unit / p.h_kv;
             split = x % a.n_splits;
             blk = a.n_blocks - 1 - x / a.n_splits;
         }
@@ -147,16 +149,20 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
             constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-            const uint32_t qa = smem_u32(s.q);
+            // descriptors: base values plus (byte offset >> 4) in the start-address field
+            const uint64_t qd = sdesc_sw128(smem_u32(s.q), 16, 1024);
+            const uint64_t kd0 = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
+            const uint64_t vd0 = sdesc_sw128(smem_u32(s.v[0]), KV_CHUNK, 1024);
+            constexpr uint32_t kStage = (KCH * KV_CHUNK) >> 4;
             auto issue_s = [&](int it) {  // S(it) = Q K(it)^T into buffer it & 1
                 const int st = it % STAGES;
-                const uint32_t ka = smem_u32(s.k[st]);
+                const uint64_t kd = kd0 + (uint64_t)(st * kStage);
+                const uint32_t scol = C_S + 64 * (it & 1);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qoff = (kk >> 2) * Q_CHUNK + (kk & 3) * 32;
-                    const uint32_t koff = (kk >> 2) * KV_CHUNK + (kk & 3) * 32;
-                    mma_ss(tmem + C_S + 64 * (it & 1), sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024),
-                           idS, kk > 0);
+                    const uint32_t qoff = ((kk >> 2) * Q_CHUNK + (kk & 3) * 32) >> 4;
+                    const uint32_t koff = ((kk >> 2) * KV_CHUNK + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + scol, qd + qoff, kd + koff, idS, kk > 0);
                 }
                 tc_commit(&s.s_full[it & 1]);
                 tc_commit(&s.k_empty[st]);
@@ -166,7 +172,6 @@ __global__ void __launch_bounds__(kThreads256, 1)
                 tc_fence_after();
                 issue_s(0);
             }
-            uint32_t pcount[2] = {0, 0};
             for (int it = 0; ok && it < ntiles; ++it) {
                 if (it + 1 < ntiles) {
                     const int st1 = (it + 1) % STAGES;
@@ -176,14 +181,14 @@ __global__ void __launch_bounds__(kThreads256, 1)
                 }
                 const int st = it % STAGES, b = it & 1;
                 if (!(ok = mbar_wait(&s.v_full[st], (it / STAGES) & 1, ab))) break;
-                if (!(ok = mbar_wait(&s.p_full[b], pcount[b] & 1, ab))) break;
-                ++pcount[b];
+                // buffer b is used at iterations b, b + 2, ...: this is its (it >> 1)-th phase
+                if (!(ok = mbar_wait(&s.p_full[b], (it >> 1) & 1, ab))) break;
                 tc_fence_after();
-                const uint32_t va = smem_u32(s.v[st]);
+                const uint64_t vd = vd0 + (uint64_t)(st * kStage);
+                mma_ts(tmem + C_O, tmem + C_S + 64 * b, vd, idO, it > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + C_O, tmem + C_S + 64 * b + kk * 8, sdesc_sw128(va + kk * 2048, KV_CHUNK, 1024), idO,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 1; kk < BN / 16; ++kk)
+                    mma_ts(tmem + C_O, tmem + C_S + 64 * b + kk * 8, vd + (kk * 2048 >> 4), idO, 1u);
                 tc_commit(&s.pv_done);
                 tc_commit(&s.v_empty[st]);
                 if (it == ntiles - 1) tc_commit(&s.o_full);  // single-phase: O is final
@@ -203,15 +208,13 @@ __global__ void __launch_bounds__(kThreads256, 1)
         const int jhi = row_valid ? band.hi(i) : 0;
         const float c = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
-        uint32_t scount[2] = {0, 0};
         bool ok = true;
         for (int it = 0; it < ntiles; ++it) {
             const int b = it & 1;
             {
-                const bool w = mbar_wait(&s.s_full[b], scount[b] & 1, ab);
+                const bool w = mbar_wait(&s.s_full[b], (it >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
-            ++scount[b];
             tc_fence_after();
             const uint32_t tS = tmem + lane_base + C_S + 64 * b;
             const int j0 = (t0 + it) * BN;

@@ -30,6 +30,8 @@ struct FwdArgs {
     int n_blocks;      // CTA work units along grid.x (before splitting)
     int n_splits;      // KV splits (1 = write final outputs)
     int split_tiles;   // KV tiles per split
+    int unit_major;    // grid order: blocks of one (batch, kv head) adjacent (decode-like
+                       // shapes, so they share K/V through L2) instead of heaviest first
     __nv_bfloat16* o;  // [tokens, h_q, d]
     float* lse;        // [B, h_q, s_q] or [h_q, T_q]; may be null
     float* o_part;     // split mode: [n_splits, rows, d] fp32
