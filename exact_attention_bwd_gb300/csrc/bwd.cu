@@ -245,13 +245,16 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             const uint32_t ka = smem_u32(s.k), va = smem_u32(s.v);
             bool ok = mbar_wait(&s.kv_full, 0, ab);
             tc_fence_after();
+            // each GEMM goes out as one MMA burst (ptx.cuh): base descriptors only, the step
+            // offsets are immediates inside the asm block
+            const uint64_t kd_k = sdesc_sw128(ka, 16, 1024), vd_k = sdesc_sw128(va, 16, 1024);
+            const uint64_t kd_mn = sdesc_sw128(ka, C::CHUNK, 1024);
+            const uint32_t sa = smem_u32(s.dst[0]);
+            const uint64_t sd_k = sdesc_sw128(sa, 16, 1024), sd_mn = sdesc_sw128(sa, 128 * 128, 1024);
             auto issue_st = [&](int it) {  // S^T_it = K Q_it^T into the S^T columns
-                const uint32_t qa = smem_u32(s.q[it & 1]);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-                    mma_ss(tmem + C::C_S, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), id_s, kk > 0);
-                }
+                const uint64_t qd = sdesc_sw128(smem_u32(s.q[it & 1]), 16, 1024);
+                if constexpr (D == 128) mma_ss_kk16_x8(tmem + C::C_S, kd_k, qd, id_s, 0u);
+                else mma_ss_kk16_x4(tmem + C::C_S, kd_k, qd, id_s, 0u);
                 tc_commit(&s.s_full);
             };
             // issue order per step i:  dP^T_i, dV_i, S^T_{i+1}, dK_i, dQ^T_i  (S^T_0 first)
@@ -271,19 +274,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-                    mma_ss(tmem + C::C_DP, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), id_s, kk > 0);
-                }
+                if constexpr (D == 128) mma_ss_kk16_x8(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
+                else mma_ss_kk16_x4(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
                 tc_commit(&s.dp_full);
-                // dV += P^T dO_i
+                // dV += P^T dO_i (query pairs of group c sit at columns 64c + 8k, k < 4)
                 if (!(ok = mbar_wait(&s.p_full, par, ab))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // query pairs of group kk/4 sit at columns 64*(kk/4) + 8*(kk%4)
-                    mma_ts(tmem + C::C_DV, tmem + C::C_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                           sdesc_sw128(da + kk * 2048, C::CHUNK, 1024), id_dv, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_ts_p_mn_x8(tmem + C::C_DV, tmem + C::C_S, sdesc_sw128(da, C::CHUNK, 1024), id_dv, it > 0 ? 1u : 0u);
                 tc_commit(&s.do_empty[st]);
                 // S^T_{i+1}: its columns held P^T_i, read by dV_i issued just above
                 if (it + 1 < nsteps) {
@@ -297,25 +294,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
                 }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(s.dst[0]);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-                    mma_ss(tmem + C::C_DK, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, C::CHUNK, 1024),
-                           id_dk, (it > 0 || kk > 0) ? 1u : 0u);
-                }
+                mma_ss_kmn16_x8(tmem + C::C_DK, sd_k, sdesc_sw128(qa, C::CHUNK, 1024), id_dk, it > 0 ? 1u : 0u);
                 tc_commit(&s.q_empty[st]);
-                if constexpr (C::DQ_T) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: A = K tile (MN-major), B = dS^T (MN-major)
-                        mma_ss(tmem + C::C_DQ, sdesc_sw128(ka + kk * 2048, C::CHUNK, 1024),
-                               sdesc_sw128(sa + kk * 2048, 128 * 128, 1024), id_dq, kk > 0);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // dQ = dS K: A = dS (MN-major), B = K tile (MN-major)
-                        mma_ss(tmem + C::C_DQ, sdesc_sw128(sa + kk * 2048, 128 * 128, 1024),
-                               sdesc_sw128(ka + kk * 2048, C::CHUNK, 1024), id_dq, kk > 0);
-                }
+                if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: A = K tile (MN-major), B = dS^T (MN-major)
+                    mma_ss_mnmn_x8(tmem + C::C_DQ, kd_mn, sd_mn, id_dq, 0u);
+                else                    // dQ = dS K: A = dS (MN-major), B = K tile (MN-major)
+                    mma_ss_mnmn_x8(tmem + C::C_DQ, sd_mn, kd_mn, id_dq, 0u);
                 tc_commit(&s.dq_full);
                 tc_commit(&s.ds_free);
             }

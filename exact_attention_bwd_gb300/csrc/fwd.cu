@@ -232,17 +232,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             const uint64_t kd_base = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
             const uint64_t vd_base = sdesc_sw128(smem_u32(s.v[0]), C::CHUNK_BYTES, 1024);
             auto issue_s = [&](uint64_t qd, uint32_t scol, uint64_t kd) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + scol, qd + off, kd + off, idS, kk > 0);
-                }
+                if constexpr (D == 128) mma_ss_kk16_x8(tmem + scol, qd, kd, idS, 0u);
+                else mma_ss_kk16_x4(tmem + scol, qd, kd, idS, 0u);
             };
             auto issue_pv = [&](uint32_t ocol, uint32_t pcol, uint64_t vd, uint32_t acc0) {
-                mma_ts(tmem + ocol, tmem + pcol, vd, idO, acc0);
-#pragma unroll
-                for (int kk = 1; kk < BN / 16; ++kk)
-                    mma_ts(tmem + ocol, tmem + pcol + kk * 8, vd + (kk * 2048 >> 4), idO, 1u);
+                mma_ts_lin_mn_x8(tmem + ocol, tmem + pcol, vd, idO, acc0);
             };
             uint32_t pc0 = 0, pc1 = 0;
             bool ok = mbar_wait(&s.q_full, 0, ab);

@@ -157,13 +157,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
             auto issue_s = [&](int it) {  // S(it) = Q K(it)^T into buffer it & 1
                 const int st = it % STAGES;
                 const uint64_t kd = kd0 + (uint64_t)(st * kStage);
-                const uint32_t scol = C_S + 64 * (it & 1);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qoff = ((kk >> 2) * Q_CHUNK + (kk & 3) * 32) >> 4;
-                    const uint32_t koff = ((kk >> 2) * KV_CHUNK + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + scol, qd + qoff, kd + koff, idS, kk > 0);
-                }
+                mma_ss_k16k8_x16(tmem + C_S + 64 * (it & 1), qd, kd, idS, 0u);
                 tc_commit(&s.s_full[it & 1]);
                 tc_commit(&s.k_empty[st]);
             };
@@ -185,10 +179,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
                 if (!(ok = mbar_wait(&s.p_full[b], (it >> 1) & 1, ab))) break;
                 tc_fence_after();
                 const uint64_t vd = vd0 + (uint64_t)(st * kStage);
-                mma_ts(tmem + C_O, tmem + C_S + 64 * b, vd, idO, it > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 1; kk < BN / 16; ++kk)
-                    mma_ts(tmem + C_O, tmem + C_S + 64 * b + kk * 8, vd + (kk * 2048 >> 4), idO, 1u);
+                mma_ts_lin_mn_x4(tmem + C_O, tmem + C_S + 64 * b, vd, idO, it > 0 ? 1u : 0u);
                 tc_commit(&s.pv_done);
                 tc_commit(&s.v_empty[st]);
                 if (it == ntiles - 1) tc_commit(&s.o_full);  // single-phase: O is final

@@ -185,6 +185,263 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// ------------------------------------------------------------------------------------------
+// MMA bursts: one GEMM (its K-steps) issued from a single asm block.  Each takes the base
+// descriptor of every operand and adds the per-step offsets (in 16-byte descriptor units,
+// fixed by the tile layout) as immediates, so the issuing thread runs no dependent
+// instructions between the MMAs.  The first MMA accumulates iff acc0 != 0, the rest always.
+// Step patterns: K-major in 128-byte-swizzled [rows][64] chunks of 16 KB (or 8 KB):
+// +32 B per step, next chunk every 4 steps; MN-major: +16 rows (2 KB) per step.
+// ------------------------------------------------------------------------------------------
+
+// A, B K-major, 16 KB chunks, 8 steps (K = 128)
+__device__ __forceinline__ void mma_ss_kk16_x8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 2; mov.b64 da, {ta, %4}; add.u32 tb, %5, 2; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 4; mov.b64 da, {ta, %4}; add.u32 tb, %5, 4; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 6; mov.b64 da, {ta, %4}; add.u32 tb, %5, 6; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1024; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1024; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1026; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1026; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1028; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1028; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1030; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1030; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A, B K-major, 16 KB chunks, 4 steps (K = 64)
+__device__ __forceinline__ void mma_ss_kk16_x4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 2; mov.b64 da, {ta, %4}; add.u32 tb, %5, 2; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 4; mov.b64 da, {ta, %4}; add.u32 tb, %5, 4; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 6; mov.b64 da, {ta, %4}; add.u32 tb, %5, 6; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A K-major (16 KB chunks), B MN-major, 8 steps
+__device__ __forceinline__ void mma_ss_kmn16_x8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 2; mov.b64 da, {ta, %4}; add.u32 tb, %5, 128; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 4; mov.b64 da, {ta, %4}; add.u32 tb, %5, 256; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 6; mov.b64 da, {ta, %4}; add.u32 tb, %5, 384; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1024; mov.b64 da, {ta, %4}; add.u32 tb, %5, 512; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1026; mov.b64 da, {ta, %4}; add.u32 tb, %5, 640; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1028; mov.b64 da, {ta, %4}; add.u32 tb, %5, 768; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1030; mov.b64 da, {ta, %4}; add.u32 tb, %5, 896; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A, B MN-major, 8 steps
+__device__ __forceinline__ void mma_ss_mnmn_x8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 128; mov.b64 da, {ta, %4}; add.u32 tb, %5, 128; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 256; mov.b64 da, {ta, %4}; add.u32 tb, %5, 256; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 384; mov.b64 da, {ta, %4}; add.u32 tb, %5, 384; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 512; mov.b64 da, {ta, %4}; add.u32 tb, %5, 512; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 640; mov.b64 da, {ta, %4}; add.u32 tb, %5, 640; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 768; mov.b64 da, {ta, %4}; add.u32 tb, %5, 768; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 896; mov.b64 da, {ta, %4}; add.u32 tb, %5, 896; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A K-major 16 KB chunks, B K-major 8 KB chunks, 16 steps (K = 256)
+__device__ __forceinline__ void mma_ss_k16k8_x16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 2; mov.b64 da, {ta, %4}; add.u32 tb, %5, 2; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 4; mov.b64 da, {ta, %4}; add.u32 tb, %5, 4; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 6; mov.b64 da, {ta, %4}; add.u32 tb, %5, 6; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1024; mov.b64 da, {ta, %4}; add.u32 tb, %5, 512; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1026; mov.b64 da, {ta, %4}; add.u32 tb, %5, 514; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1028; mov.b64 da, {ta, %4}; add.u32 tb, %5, 516; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1030; mov.b64 da, {ta, %4}; add.u32 tb, %5, 518; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2048; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1024; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2050; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1026; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2052; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1028; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2054; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1030; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 3072; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1536; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 3074; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1538; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 3076; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1540; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 3078; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1542; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A from TMEM at columns a + 8 k, B MN-major, 8 steps
+__device__ __forceinline__ void mma_ts_lin_mn_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; add.u32 tb, %4, 0; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p0;\n"
+        "add.u32 ta, %3, 8; add.u32 tb, %4, 128; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 16; add.u32 tb, %4, 256; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 24; add.u32 tb, %4, 384; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 32; add.u32 tb, %4, 512; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 40; add.u32 tb, %4, 640; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 48; add.u32 tb, %4, 768; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 56; add.u32 tb, %4, 896; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(a_tmem), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A from TMEM at columns a + 8 k, B MN-major, 4 steps
+__device__ __forceinline__ void mma_ts_lin_mn_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; add.u32 tb, %4, 0; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p0;\n"
+        "add.u32 ta, %3, 8; add.u32 tb, %4, 128; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 16; add.u32 tb, %4, 256; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 24; add.u32 tb, %4, 384; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(a_tmem), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A from TMEM at columns a + 64 (k / 4) + 8 (k % 4), B MN-major, 8 steps
+__device__ __forceinline__ void mma_ts_p_mn_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; add.u32 tb, %4, 0; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p0;\n"
+        "add.u32 ta, %3, 8; add.u32 tb, %4, 128; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 16; add.u32 tb, %4, 256; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 24; add.u32 tb, %4, 384; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 64; add.u32 tb, %4, 512; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 72; add.u32 tb, %4, 640; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 80; add.u32 tb, %4, 768; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 88; add.u32 tb, %4, 896; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(a_tmem), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
 // a_mn / b_mn: operand stored MN-major (true) or K-major (false).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
