@@ -145,6 +145,7 @@ fa_status normalise(const fa_params* in, Problem& p) {
 enum class FwdPath { kEmpty, kTensor, kDecode };
 
 constexpr int kDecodeKeys = 64;     // keys per decode tile
+constexpr double kBandBytes = 64.0 * (1 << 20);  // L2 share for one band of backward units
 constexpr size_t kStatusBytes = 256;
 
 struct FwdPlan {
@@ -239,7 +240,7 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
 // ------------------------------------------------------------------------------------------
 struct BwdPlan {
     bool empty = true;
-    int n_qtiles = 0, n_kvblocks = 0;
+    int n_qtiles = 0, n_kvblocks = 0, n_bands = 1;
     size_t off_delta = 0, off_lse2 = 0, off_dq = 0;
     size_t ws_bytes = kStatusBytes;
 };
@@ -257,6 +258,15 @@ fa_status plan_bwd(const Problem& p, BwdPlan& pl) {
     } else {
         pl.n_qtiles = p.B * ((p.s_q + p.P - 1) / p.P);
         pl.n_kvblocks = (p.s_kv + kTileRows - 1) / kTileRows;
+        // a (batch, key/value head) unit's CTAs all read its Q and dO tiles and add into its
+        // dQ accumulator rows (bf16 Q + dO, fp32 accumulator: 8 bytes per row and column);
+        // take as many units at a time as keep that within half the L2, in bands of
+        // near-equal size (a small last band would start its heaviest blocks last)
+        const double unit_bytes = (double)p.s_q * p.G * p.d * 8.0;
+        const int hb = p.h_kv * p.B;
+        int u = unit_bytes > 0 ? (int)(kBandBytes / unit_bytes) : hb;
+        u = u < 1 ? 1 : (u > hb ? hb : u);
+        pl.n_bands = (hb + u - 1) / u;
     }
     const size_t stat = (size_t)p.h_kv * pl.n_qtiles * 128 * 4;
     pl.off_delta = kStatusBytes;
@@ -434,6 +444,7 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.p = p;
     a.n_qtiles = pl.n_qtiles;
     a.n_kvblocks = pl.n_kvblocks;
+    a.n_bands = pl.n_bands;
     a.o = reinterpret_cast<const __nv_bfloat16*>(o);
     a.lse = lse;
     a.dout = reinterpret_cast<const __nv_bfloat16*>(dout);

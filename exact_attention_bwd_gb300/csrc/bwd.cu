@@ -86,8 +86,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     BwdSmem<D>& s = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // 1-D grid: key/value head (and batch) fastest, key block slowest, so the key blocks
-    // that see the most query tiles under a causal mask (the first ones) start first
+    // 1-D grid.  Dense: the (batch, key/value head) units are split into n_bands bands of
+    // near-equal size (the first hb % n_bands bands one unit larger); inside a band the unit
+    // varies fastest and the key block slowest, so the key blocks that see the most query
+    // tiles under a causal mask (the first ones) start first, while the query tiles, dO
+    // tiles and dQ accumulator rows that a band's CTAs share stay in L2.
     int g, seq, blk;
     {
         const int idx = blockIdx.x;
@@ -98,9 +101,25 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             blk -= p.cu_k[seq] / kRows + seq;
         } else {
             const int hb = p.h_kv * p.B;
-            g = (idx % hb) % p.h_kv;
-            seq = (idx % hb) / p.h_kv;
-            blk = idx / hb;
+            const int base = hb / a.n_bands, big = hb % a.n_bands;  // band sizes base + 1 (first big), base
+            const int big_ctas = big * (base + 1) * a.n_kvblocks;
+            int ub, unit0, r;
+            if (idx < big_ctas) {
+                ub = base + 1;
+                const int band = idx / (ub * a.n_kvblocks);
+                r = idx - band * ub * a.n_kvblocks;
+                unit0 = band * ub;
+            } else {
+                ub = base;
+                const int x = idx - big_ctas;
+                const int band = x / (ub * a.n_kvblocks);
+                r = x - band * ub * a.n_kvblocks;
+                unit0 = big * (base + 1) + band * ub;
+            }
+            const int unit = unit0 + r % ub;
+            g = unit % p.h_kv;
+            seq = unit / p.h_kv;
+            blk = r / ub;
         }
     }
     const SeqView sv = seq_view(p, seq);
@@ -257,8 +276,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 else mma_ss_kk16_x4(tmem + C::C_S, kd_k, qd, id_s, 0u);
                 tc_commit(&s.s_full);
             };
-            // issue order per step i:  dP^T_i, dV_i, S^T_{i+1}, dK_i, dQ^T_i  (S^T_0 first)
-            // S^T_{i+1} goes before dK_i / dQ^T_i so that the next step's P^T overlaps them
+            // issue order per step i:  dP^T_i, dV_i, S^T_{i+1}, dQ^T_i, dK_i  (S^T_0 first)
+            // S^T_{i+1} goes before dQ^T_i / dK_i so that the next step's P^T overlaps them
             if (ok && (ok = mbar_wait(&s.q_full[0], 0, ab))) {
                 tc_fence_after();
                 issue_st(0);
@@ -288,19 +307,20 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     tc_fence_after();
                     issue_st(it + 1);
                 }
-                // dK += dS^T Q_i ;  dQ^T_i = K^T dS^T
+                // dQ^T_i = K^T dS^T, then dK += dS^T Q_i: dQ goes first so that its drain by the
+                // dQ warps (which frees the dP^T columns for the next step) overlaps dK
                 if (!(ok = mbar_wait(&s.ds_full, par, ab))) break;
                 if (!C::DQ_OVER_DP && it > 0) {
                     if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
                 }
                 tc_fence_after();
-                mma_ss_kmn16_x8(tmem + C::C_DK, sd_k, sdesc_sw128(qa, C::CHUNK, 1024), id_dk, it > 0 ? 1u : 0u);
-                tc_commit(&s.q_empty[st]);
                 if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: A = K tile (MN-major), B = dS^T (MN-major)
                     mma_ss_mnmn_x8(tmem + C::C_DQ, kd_mn, sd_mn, id_dq, 0u);
                 else                    // dQ = dS K: A = dS (MN-major), B = K tile (MN-major)
                     mma_ss_mnmn_x8(tmem + C::C_DQ, sd_mn, kd_mn, id_dq, 0u);
                 tc_commit(&s.dq_full);
+                mma_ss_kmn16_x8(tmem + C::C_DK, sd_k, sdesc_sw128(qa, C::CHUNK, 1024), id_dk, it > 0 ? 1u : 0u);
+                tc_commit(&s.q_empty[st]);
                 tc_commit(&s.ds_free);
             }
             tc_commit(&s.dkv_full);

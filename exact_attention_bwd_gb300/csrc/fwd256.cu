@@ -1,13 +1,17 @@
 // Forward attention for head dimension 256 on the tcgen05 tensor cores.
 //
 // The accumulator of one 128-row query tile is 256 TMEM columns wide, so a CTA holds a
-// single query tile: O in columns [256, 512) and two 64-column S buffers in [0, 128).
-// Keys and values stream in 64-row tiles (32 KB each at d = 256) through a two-stage
-// ring.  The MMA thread runs one tile ahead: S(j+1) is computed while the softmax group
-// works on S(j), then O += P(j) V(j).  Rows are packed across the G query heads of the
-// key/value head exactly as in the d <= 128 kernel, and the online softmax is the same
-// (running max / running sum with lazy rescaling, "Flash Attention Tutorial" README,
-// sections 3 to 5); key tiles outside the causal / sliding-window band are skipped.
+// single query tile.  Tensor memory: O in columns [0, 256), two 64-column S buffers in
+// [256, 384), and the Q tile itself in [384, 512) (bf16 pairs, one row per lane), so
+// S = Q K^T takes its A operand from tensor memory and reads only K from shared memory.
+// Q arrives by TMA in the first 64 KB ring slot; the softmax warps copy their rows into
+// tensor memory, after which that slot joins the key/value ring as its third stage.
+// Keys and values stream in 64-row tiles (32 KB each at d = 256).  The MMA thread runs one
+// tile ahead: S(j+1) is computed while the softmax group works on S(j), then
+// O += P(j) V(j).  Rows are packed across the G query heads of the key/value head exactly
+// as in the d <= 128 kernel, and the online softmax is the same (running max / running
+// sum with lazy rescaling, "Flash Attention Tutorial" README, sections 3 to 5); key tiles
+// outside the causal / sliding-window band are skipped.
 #include "common.cuh"
 
 namespace fa {
@@ -19,15 +23,22 @@ constexpr int BN = 64;               // keys per KV tile
 constexpr int KCH = D / 64;          // 64-column chunks
 constexpr int Q_CHUNK = 128 * 128;   // [128 rows][64 cols] bf16
 constexpr int KV_CHUNK = BN * 128;   // [64 rows][64 cols] bf16
-constexpr int STAGES = 2;
-constexpr uint32_t C_S = 0;          // S buffer b at columns 64 b
-constexpr uint32_t C_O = 256;
+constexpr int KV_BYTES = KCH * KV_CHUNK;  // one K or V tile (32 KB)
+constexpr int STAGES = 3;            // ring slots of K + V (64 KB each); slot 0 first holds Q
+constexpr int SLOT_BYTES = 2 * KV_BYTES;
+static_assert(KCH * Q_CHUNK == SLOT_BYTES, "the Q tile fills one ring slot");
+constexpr uint32_t C_O = 0;
+constexpr uint32_t C_S = 256;        // S buffer b at columns 256 + 64 b
+constexpr uint32_t C_Q = 384;        // Q: column c holds elements 2c, 2c+1 of the row
+
+// ring slot and use count of KV tile `it`: tiles 0 and 1 take slots 1 and 2, tile 2 the
+// slot Q came in, and so on round the ring
+__device__ __forceinline__ int slot_of(int it) { return (it + 1) % STAGES; }
+__device__ __forceinline__ uint32_t use_parity(int it) { return (uint32_t)(it / STAGES) & 1u; }
 
 struct __align__(1024) Smem256 {
-    uint8_t q[KCH * Q_CHUNK];
-    uint8_t k[STAGES][KCH * KV_CHUNK];
-    uint8_t v[STAGES][KCH * KV_CHUNK];
-    uint64_t q_full;
+    uint8_t ring[STAGES][SLOT_BYTES];  // K at 0, V at KV_BYTES
+    uint64_t q_full, q_tmem;
     uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
     uint64_t s_full[2], p_full[2], pv_done, o_full, drain;
     uint32_t tmem_base;
@@ -81,6 +92,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     if (tid == 0) {
         s.abort_flag = 0;
         mbar_init(&s.q_full, 1);
+        mbar_init(&s.q_tmem, 4);  // one arrive per softmax warp once its Q rows are in TMEM
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.k_empty[i], 1);
@@ -99,7 +111,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     if (p.P * p.G < 128) {
         for (int c = 0; c < KCH; ++c)
             for (int x = p.P * p.G * 128 + tid * 16; x < 128 * 128; x += kThreads256 * 16)
-                *reinterpret_cast<uint4*>(&s.q[c * Q_CHUNK + x]) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(&s.ring[0][c * Q_CHUNK + x]) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 2) {
@@ -119,67 +131,67 @@ __global__ void __launch_bounds__(kThreads256, 1)
             tma_prefetch_desc(&tmv);
             mbar_expect_tx(&s.q_full, (uint32_t)(p.P * p.G) * 128u * KCH);
             for (int c = 0; c < KCH; ++c)
-                tma_load_4d(&s.q[c * Q_CHUNK], &tmq, &s.q_full, c * 64, g * p.G, sv.q0 + s0, sv.tma_b);
+                tma_load_4d(&s.ring[0][c * Q_CHUNK], &tmq, &s.q_full, c * 64, g * p.G, sv.q0 + s0, sv.tma_b);
             int k_issued = 0, v_issued = 0;
             for (int it = 0; it < ntiles; ++it) {
-                const int st = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1;
+                const int st = slot_of(it);
+                const uint32_t ph = use_parity(it);
                 const int row = sv.k0 + (t0 + it) * BN;
+                // slot 0 is free for keys once the softmax warps have copied Q out of it
+                if (it == STAGES - 1 && !mbar_wait(&s.q_tmem, 0, ab)) break;
                 if (!mbar_wait(&s.k_empty[st], ph ^ 1, ab)) break;
-                mbar_expect_tx(&s.k_full[st], KCH * KV_CHUNK);
+                mbar_expect_tx(&s.k_full[st], KV_BYTES);
                 for (int c = 0; c < KCH; ++c)
-                    tma_load_4d(&s.k[st][c * KV_CHUNK], &tmk, &s.k_full[st], c * 64, g, row, sv.tma_b);
+                    tma_load_4d(&s.ring[st][c * KV_CHUNK], &tmk, &s.k_full[st], c * 64, g, row, sv.tma_b);
                 ++k_issued;
                 if (!mbar_wait(&s.v_empty[st], ph ^ 1, ab)) break;
-                mbar_expect_tx(&s.v_full[st], KCH * KV_CHUNK);
+                mbar_expect_tx(&s.v_full[st], KV_BYTES);
                 for (int c = 0; c < KCH; ++c)
-                    tma_load_4d(&s.v[st][c * KV_CHUNK], &tmv, &s.v_full[st], c * 64, g, row, sv.tma_b);
+                    tma_load_4d(&s.ring[st][KV_BYTES + c * KV_CHUNK], &tmv, &s.v_full[st], c * 64, g, row,
+                                sv.tma_b);
                 ++v_issued;
             }
+            // wait for every copy still in flight before the CTA may exit
             for (int back = 1; back <= STAGES; ++back) {
                 if (k_issued - back >= 0)
-                    mbar_wait_quiet(&s.k_full[(k_issued - back) % STAGES], ((k_issued - back) / STAGES) & 1);
+                    mbar_wait_quiet(&s.k_full[slot_of(k_issued - back)], use_parity(k_issued - back));
                 if (v_issued - back >= 0)
-                    mbar_wait_quiet(&s.v_full[(v_issued - back) % STAGES], ((v_issued - back) / STAGES) & 1);
+                    mbar_wait_quiet(&s.v_full[slot_of(v_issued - back)], use_parity(v_issued - back));
             }
             mbar_wait_quiet(&s.q_full, 0);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
-            constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+            constexpr uint32_t idS = idesc_bf16(128, BN, false, false);  // A = Q from TMEM, B = K K-major
+            constexpr uint32_t idO = idesc_bf16(128, D, false, true);    // A = P from TMEM, B = V MN-major
             // descriptors: base values plus (byte offset >> 4) in the start-address field
-            const uint64_t qd = sdesc_sw128(smem_u32(s.q), 16, 1024);
-            const uint64_t kd0 = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
-            const uint64_t vd0 = sdesc_sw128(smem_u32(s.v[0]), KV_CHUNK, 1024);
-            constexpr uint32_t kStage = (KCH * KV_CHUNK) >> 4;
+            const uint64_t kd0 = sdesc_sw128(smem_u32(s.ring[0]), 16, 1024);
+            const uint64_t vd0 = sdesc_sw128(smem_u32(s.ring[0] + KV_BYTES), KV_CHUNK, 1024);
+            constexpr uint32_t kSlot = SLOT_BYTES >> 4;
             auto issue_s = [&](int it) {  // S(it) = Q K(it)^T into buffer it & 1
-                const int st = it % STAGES;
-                const uint64_t kd = kd0 + (uint64_t)(st * kStage);
-                mma_ss_k16k8_x16(tmem + C_S + 64 * (it & 1), qd, kd, idS, 0u);
+                const int st = slot_of(it);
+                mma_ts_lin_k8_x16(tmem + C_S + 64 * (it & 1), tmem + C_Q, kd0 + (uint64_t)(st * kSlot), idS, 0u);
                 tc_commit(&s.s_full[it & 1]);
                 tc_commit(&s.k_empty[st]);
             };
-            bool ok = mbar_wait(&s.q_full, 0, ab);
-            if (ok && (ok = mbar_wait(&s.k_full[0], 0, ab))) {
+            bool ok = mbar_wait(&s.q_tmem, 0, ab);
+            if (ok && (ok = mbar_wait(&s.k_full[slot_of(0)], 0, ab))) {
                 tc_fence_after();
                 issue_s(0);
             }
             for (int it = 0; ok && it < ntiles; ++it) {
                 if (it + 1 < ntiles) {
-                    const int st1 = (it + 1) % STAGES;
-                    if (!(ok = mbar_wait(&s.k_full[st1], ((it + 1) / STAGES) & 1, ab))) break;
+                    if (!(ok = mbar_wait(&s.k_full[slot_of(it + 1)], use_parity(it + 1), ab))) break;
                     tc_fence_after();
                     issue_s(it + 1);  // its buffer held P(it-1), read by PV(it-1) issued earlier
                 }
-                const int st = it % STAGES, b = it & 1;
-                if (!(ok = mbar_wait(&s.v_full[st], (it / STAGES) & 1, ab))) break;
+                const int st = slot_of(it), b = it & 1;
+                if (!(ok = mbar_wait(&s.v_full[st], use_parity(it), ab))) break;
                 // buffer b is used at iterations b, b + 2, ...: this is its (it >> 1)-th phase
                 if (!(ok = mbar_wait(&s.p_full[b], (it >> 1) & 1, ab))) break;
                 tc_fence_after();
-                const uint64_t vd = vd0 + (uint64_t)(st * kStage);
-                mma_ts_lin_mn_x4(tmem + C_O, tmem + C_S + 64 * b, vd, idO, it > 0 ? 1u : 0u);
+                mma_ts_lin_mn_x4(tmem + C_O, tmem + C_S + 64 * b, vd0 + (uint64_t)(st * kSlot), idO, it > 0 ? 1u : 0u);
                 tc_commit(&s.pv_done);
                 tc_commit(&s.v_empty[st]);
                 if (it == ntiles - 1) tc_commit(&s.o_full);  // single-phase: O is final
@@ -200,7 +212,34 @@ __global__ void __launch_bounds__(kThreads256, 1)
         const float c = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int it = 0; it < ntiles; ++it) {
+        if (ntiles > 0) {
+            // copy this thread's Q row (TMEM lane r) out of the swizzled TMA layout: 16-byte
+            // unit u of a [128][64] chunk row sits at position u ^ (r & 7)
+            {
+                const bool w = mbar_wait(&s.q_full, 0, ab);
+                if (!__all_sync(0xffffffffu, w)) ok = false;
+            }
+            if (ok) {
+#pragma unroll
+                for (int cch = 0; cch < KCH; ++cch) {
+                    const uint8_t* qrow = &s.ring[0][cch * Q_CHUNK + r * 128];
+                    uint32_t qr[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(qrow + ((u ^ (r & 7)) << 4));
+                        qr[4 * u + 0] = x.x;
+                        qr[4 * u + 1] = x.y;
+                        qr[4 * u + 2] = x.z;
+                        qr[4 * u + 3] = x.w;
+                    }
+                    tmem_st_32x32b_x32(tmem + lane_base + C_Q + 32 * cch, qr);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.q_tmem);
+            }
+        }
+        for (int it = 0; ok && it < ntiles; ++it) {
             const int b = it & 1;
             {
                 const bool w = mbar_wait(&s.s_full[b], (it >> 1) & 1, ab);

@@ -67,7 +67,10 @@ struct CombineArgs {
 struct BwdArgs {
     Problem p;
     int n_qtiles;          // q tiles per (key/value head) in the tiled layouts below
-    int n_kvblocks;        // grid.x of the main kernel
+    int n_kvblocks;        // key blocks per (batch, key/value head) unit (dense) or numbered blocks (packed)
+    int n_bands;           // dense grid order: the (batch, kv head) units form this many bands of
+                           // near-equal size, key block slowest within a band, so a band's
+                           // query-side data stays in L2
     const __nv_bfloat16* o;
     const float* lse;
     const __nv_bfloat16* dout;

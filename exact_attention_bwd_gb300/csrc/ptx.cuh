@@ -357,6 +357,54 @@ __device__ __forceinline__ void mma_ss_k16k8_x16(uint32_t d_tmem, uint64_t a, ui
         : "memory");
 }
 
+// A from TMEM at columns a + 8 k, B K-major in 8 KB chunks (+32 B per step, next chunk
+// every 4 steps), 16 steps (K = 256)
+__device__ __forceinline__ void mma_ts_lin_k8_x16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; add.u32 tb, %4, 0; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p0;\n"
+        "add.u32 ta, %3, 8; add.u32 tb, %4, 2; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 16; add.u32 tb, %4, 4; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 24; add.u32 tb, %4, 6; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 32; add.u32 tb, %4, 512; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 40; add.u32 tb, %4, 514; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 48; add.u32 tb, %4, 516; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 56; add.u32 tb, %4, 518; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 64; add.u32 tb, %4, 1024; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 72; add.u32 tb, %4, 1026; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 80; add.u32 tb, %4, 1028; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 88; add.u32 tb, %4, 1030; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 96; add.u32 tb, %4, 1536; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 104; add.u32 tb, %4, 1538; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 112; add.u32 tb, %4, 1540; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 120; add.u32 tb, %4, 1542; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(a_tmem), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
 // A from TMEM at columns a + 8 k, B MN-major, 8 steps
 __device__ __forceinline__ void mma_ts_lin_mn_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc0) {
     const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
