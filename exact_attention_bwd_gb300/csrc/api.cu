@@ -393,6 +393,11 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.n_splits = pl.n_splits;
     a.split_tiles = pl.split_tiles;
     a.unit_major = pl.unit_major;
+    {
+        const long items = p.cu_q ? (long)pl.n_blocks * p.h_kv : (long)pl.n_blocks * pl.n_splits * p.h_kv * p.B;
+        a.n_items = (int)items;
+        a.n_ctas = (int)(items < sm_count() ? items : sm_count());
+    }
     a.o = reinterpret_cast<__nv_bfloat16*>(o);
     a.lse = lse;
     a.o_part = o_part;

@@ -23,6 +23,15 @@
 // Key tiles that lie wholly outside a tile's causal / sliding-window band are skipped
 // (fa4-jax PyPI page, "Native two-sided sliding windows"); only tiles that cut the band
 // edge evaluate the mask per element.
+//
+// Scheduling is persistent: one CTA per SM walks the work items (a key/value head's two
+// query tiles, and a key range in split mode) in heaviest-first order with a grid stride;
+// a packed batch's items are found by binary search over its offsets (dew-flash-attn PyPI
+// page, "Packed sequences"), and idle items cost only their decode.  Barrier phases carry
+// over from item to item, so the next item's Q load and first S = Q K^T overlap the
+// previous item's epilogue; two barriers hand the shared resources over: q_empty (the
+// previous item's S MMAs, which read the Q tiles, have completed) and o_free[k] (the
+// epilogue has read O_k out of tensor memory before the next P V overwrites it).
 #include "common.cuh"
 
 namespace fa {
@@ -54,7 +63,8 @@ struct __align__(1024) FwdSmem {
     uint64_t q_full;
     uint64_t k_full[FwdCfg<D>::STAGES], k_empty[FwdCfg<D>::STAGES];
     uint64_t v_full[FwdCfg<D>::STAGES], v_empty[FwdCfg<D>::STAGES];
-    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t q_empty;
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -66,6 +76,68 @@ struct TileInfo {
     bool active;  // the tile holds at least one valid query row
 };
 
+// One work item: the two query tiles [2 blk P, 2 blk P + 2P) of key/value head g of a
+// sequence (and one key split in split mode), numbered heaviest first: the key/value head
+// (and batch) vary fastest, the query block slowest, latest (longest causal band) first.
+struct FwdItem {
+    SeqView sv;
+    Band band;
+    int g, split;
+    TileInfo ti[2];
+    int u0, u1;  // union key-tile range of the two tiles
+    bool live;   // false for an idle block of a packed batch
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
+    const Problem& p = a.p;
+    FwdItem w;
+    int seq, blk;
+    w.split = 0;
+    if (p.cu_q) {
+        w.g = idx % p.h_kv;
+        const int bs = 2 * p.P;
+        blk = idx / p.h_kv;
+        seq = owner_sequence(p.cu_q, p.B, blk, bs);
+        blk -= p.cu_q[seq] / bs + seq;
+    } else {
+        const int hb = p.h_kv * p.B;
+        const int per_unit = a.n_blocks * a.n_splits;
+        const int unit = a.unit_major ? idx / per_unit : idx % hb;
+        const int x = a.unit_major ? idx % per_unit : idx / hb;
+        w.g = unit % p.h_kv;
+        seq = unit / p.h_kv;
+        w.split = x % a.n_splits;
+        blk = a.n_blocks - 1 - x / a.n_splits;
+    }
+    w.sv = seq_view(p, seq);
+    w.band = Band{w.sv.nk - w.sv.nq, p.left, p.right, w.sv.nk};
+    w.u0 = 0x7fffffff;
+    w.u1 = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        w.ti[k].s0 = (2 * blk + k) * p.P;
+        w.ti[k].active = w.ti[k].s0 < w.sv.nq;
+        const int i1 = min(w.ti[k].s0 + p.P, w.sv.nq) - 1;
+        if (w.ti[k].active) {
+            kv_tile_range(w.band, w.ti[k].s0, i1, BN, w.ti[k].t0, w.ti[k].t1);
+            if (a.n_splits > 1) {
+                w.ti[k].t0 = max(w.ti[k].t0, w.split * a.split_tiles);
+                w.ti[k].t1 = min(w.ti[k].t1, (w.split + 1) * a.split_tiles);
+                if (w.ti[k].t1 < w.ti[k].t0) w.ti[k].t1 = w.ti[k].t0;
+            }
+        } else {
+            w.ti[k].t0 = w.ti[k].t1 = 0;
+        }
+        if (w.ti[k].t1 > w.ti[k].t0) {
+            w.u0 = min(w.u0, w.ti[k].t0);
+            w.u1 = max(w.u1, w.ti[k].t1);
+        }
+    }
+    if (w.u1 == 0) w.u0 = 0;
+    w.live = blk * 2 * p.P < w.sv.nq;
+    return w;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fwd_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -76,57 +148,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     const Problem& p = a.p;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-
-    // ---------------- work unit ----------------
-    // 1-D grid, heaviest work first: the key/value head (and batch) vary fastest, the
-    // query block slowest, latest (longest causal band) blocks first
-    int g, seq, blk, split = 0;
-    {
-        const int idx = blockIdx.x;
-        if (p.cu_q) {
-            g = idx % p.h_kv;
-            const int bs = 2 * p.P;
-            blk = idx / p.h_kv;
-            seq = owner_sequence(p.cu_q, p.B, blk, bs);
-            blk -= p.cu_q[seq] / bs + seq;
-        } else {
-            const int hb = p.h_kv * p.B;
-            const int per_unit = a.n_blocks * a.n_splits;
-            const int unit = a.unit_major ? idx / per_unit : idx % hb;
-            const int x = a.unit_major ? idx % per_unit : idx / hb;
-            g = unit % p.h_kv;
-            seq = unit / p.h_kv;
-            split = x % a.n_splits;
-            blk = a.n_blocks - 1 - x / a.n_splits;
-        }
-    }
-    const SeqView sv = seq_view(p, seq);
-    const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
-    TileInfo ti[2];
-    int u0 = 0x7fffffff, u1 = 0;  // union KV range
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        ti[k].s0 = (2 * blk + k) * p.P;
-        ti[k].active = ti[k].s0 < sv.nq;
-        int i1 = min(ti[k].s0 + p.P, sv.nq) - 1;
-        if (ti[k].active) {
-            kv_tile_range(band, ti[k].s0, i1, BN, ti[k].t0, ti[k].t1);
-            if (a.n_splits > 1) {
-                ti[k].t0 = max(ti[k].t0, split * a.split_tiles);
-                ti[k].t1 = min(ti[k].t1, (split + 1) * a.split_tiles);
-                if (ti[k].t1 < ti[k].t0) ti[k].t1 = ti[k].t0;
-            }
-        } else {
-            ti[k].t0 = ti[k].t1 = 0;
-        }
-        if (ti[k].t1 > ti[k].t0) {
-            u0 = min(u0, ti[k].t0);
-            u1 = max(u1, ti[k].t1);
-        }
-    }
-    if (u1 == 0) u0 = 0;
-    if (blk * 2 * p.P >= sv.nq) return;  // idle packed-batch block (uniform for the CTA)
-    // an earlier CTA of this launch gave up: do not start new work
+    // an earlier CTA of this launch gave up: do not start
     if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
 
     // ---------------- setup ----------------
@@ -144,7 +166,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             mbar_init(&s.s_full[k], 1);
             mbar_init(&s.p_full[k], 4);  // one arrive per softmax warp
             mbar_init(&s.o_full[k], 1);
+            mbar_init(&s.o_free[k], 4);  // one arrive per softmax warp
         }
+        mbar_init(&s.q_empty, 1);
         mbar_init(&s.drain, 1);
         fence_mbar_init();
     }
@@ -165,43 +189,51 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     // registers: 384 x 168 at launch; the producer/MMA group hands part of its share to
-    // the two softmax groups (128 x 88 + 256 x 208 = 64512).  The change is made at the
-    // top of each warp group's branch so the register allocator sees it on every path.
+    // the two softmax groups (128 x 88 + 256 x 208 = 64512).  The change is made
+    // at the top of each warp group's branch so the register allocator sees it on every path.
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
-        if (lane == 0 && u1 > u0) {
+        if (lane == 0) {
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
             const uint32_t qbox = (uint32_t)(p.P * p.G) * 128u;  // bytes of one 64-col Q box
-            uint32_t qbytes = 0;
-            for (int k = 0; k < 2; ++k)
-                if (ti[k].t1 > ti[k].t0) qbytes += qbox * C::KCH;
-            mbar_expect_tx(&s.q_full, qbytes);
-            for (int k = 0; k < 2; ++k) {
-                if (ti[k].t1 <= ti[k].t0) continue;
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_4d(&s.q[k][c * C::CHUNK_BYTES], &tmq, &s.q_full, c * 64, g * p.G, sv.q0 + ti[k].s0,
-                                sv.tma_b);
-            }
-            int it = 0, k_issued = 0, v_issued = 0;
-            for (int j = u0; j < u1; ++j, ++it) {
-                const int st = it % C::STAGES;
-                const uint32_t ph = (it / C::STAGES) & 1;
-                if (!mbar_wait(&s.k_empty[st], ph ^ 1, ab)) break;
-                mbar_expect_tx(&s.k_full[st], C::TILE_BYTES);
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, g, sv.k0 + j * BN,
-                                sv.tma_b);
-                ++k_issued;
-                if (!mbar_wait(&s.v_empty[st], ph ^ 1, ab)) break;
-                mbar_expect_tx(&s.v_full[st], C::TILE_BYTES);
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, g, sv.k0 + j * BN,
-                                sv.tma_b);
-                ++v_issued;
+            int gt = 0, n_q = 0, k_issued = 0, v_issued = 0;    // key tiles, Q loads, copies issued
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+                const FwdItem w = fwd_item(a, idx);
+                if (!w.live || w.u1 <= w.u0) continue;
+                // the previous item's Q tiles are free once its S MMAs have completed
+                if (n_q > 0 && !(ok = mbar_wait(&s.q_empty, (n_q - 1) & 1, ab))) break;
+                uint32_t qbytes = 0;
+                for (int k = 0; k < 2; ++k)
+                    if (w.ti[k].t1 > w.ti[k].t0) qbytes += qbox * C::KCH;
+                mbar_expect_tx(&s.q_full, qbytes);
+                for (int k = 0; k < 2; ++k) {
+                    if (w.ti[k].t1 <= w.ti[k].t0) continue;
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_4d(&s.q[k][c * C::CHUNK_BYTES], &tmq, &s.q_full, c * 64, w.g * p.G,
+                                    w.sv.q0 + w.ti[k].s0, w.sv.tma_b);
+                }
+                ++n_q;
+                for (int j = w.u0; j < w.u1; ++j, ++gt) {
+                    const int st = gt % C::STAGES;
+                    const uint32_t ph = (gt / C::STAGES) & 1;
+                    if (!(ok = mbar_wait(&s.k_empty[st], ph ^ 1, ab))) break;
+                    mbar_expect_tx(&s.k_full[st], C::TILE_BYTES);
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, w.g,
+                                    w.sv.k0 + j * BN, w.sv.tma_b);
+                    ++k_issued;
+                    if (!(ok = mbar_wait(&s.v_empty[st], ph ^ 1, ab))) break;
+                    mbar_expect_tx(&s.v_full[st], C::TILE_BYTES);
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, w.g,
+                                    w.sv.k0 + j * BN, w.sv.tma_b);
+                    ++v_issued;
+                }
             }
             // wait for every copy still in flight before the CTA may exit
             for (int back = 1; back <= C::STAGES; ++back) {
@@ -214,17 +246,16 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     mbar_wait_quiet(&s.v_full[i2 % C::STAGES], (i2 / C::STAGES) & 1);
                 }
             }
-            mbar_wait_quiet(&s.q_full, 0);
+            if (n_q > 0) mbar_wait_quiet(&s.q_full, (n_q - 1) & 1);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         // Everything the issue path touches lives in registers (no per-tile arrays indexed
         // at run time), so consecutive MMAs go out back to back.
-        if (lane == 0 && u1 > u0) {
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
             constexpr uint32_t idO = idesc_bf16(128, D, false, true);
             constexpr uint32_t kStageStep = (uint32_t)C::TILE_BYTES >> 4;  // descriptor units per stage
-            const int ta0 = ti[0].t0, ta1 = ti[0].t1, tb0 = ti[1].t0, tb1 = ti[1].t1;
             // a descriptor's start-address field is addr >> 4 in its low bits, so stepping
             // through a tile is a plain add to a base descriptor (no carry: addr < 256 KB)
             const uint64_t qd0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
@@ -238,82 +269,121 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             auto issue_pv = [&](uint32_t ocol, uint32_t pcol, uint64_t vd, uint32_t acc0) {
                 mma_ts_lin_mn_x8(tmem + ocol, tmem + pcol, vd, idO, acc0);
             };
-            uint32_t pc0 = 0, pc1 = 0;
-            bool ok = mbar_wait(&s.q_full, 0, ab);
-            tc_fence_after();
-            if (ok && (ok = mbar_wait(&s.k_full[0], 0, ab))) {
-                // prologue: S_k for the first KV tile
+            uint32_t pc0 = 0, pc1 = 0;  // P tiles consumed per query tile
+            uint32_t oc0 = 0, oc1 = 0;  // O tiles completed per query tile (o_full commits)
+            int gt = 0, n_q = 0;        // key tiles, items consumed
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+                // the item's key-tile ranges are all the issue loop needs
+                int ta0, ta1, tb0, tb1, u0, u1;
+                {
+                    const FwdItem w = fwd_item(a, idx);
+                    ta0 = w.ti[0].t0;
+                    ta1 = w.ti[0].t1;
+                    tb0 = w.ti[1].t0;
+                    tb1 = w.ti[1].t1;
+                    u0 = w.u0;
+                    u1 = w.u1;
+                    if (!w.live) u1 = u0;
+                }
+                if (u1 <= u0) continue;
+                ok = mbar_wait(&s.q_full, n_q & 1, ab);
+                ++n_q;
                 tc_fence_after();
-                if (u0 >= ta0 && u0 < ta1) {
-                    issue_s(qd0, 0, kd_base);
-                    tc_commit(&s.s_full[0]);
-                }
-                if (u0 >= tb0 && u0 < tb1) {
-                    issue_s(qd1, 128, kd_base);
-                    tc_commit(&s.s_full[1]);
-                }
-                tc_commit(&s.k_empty[0]);
-            }
-            int it = 0;
-            for (int j = u0; ok && j < u1; ++j, ++it) {
-                const int st = it % C::STAGES;
-                const uint32_t ph = (it / C::STAGES) & 1;
-                const int st1 = (it + 1) % C::STAGES;
-                const uint32_t ph1 = ((it + 1) / C::STAGES) & 1;
-                const uint64_t vd = vd_base + (uint64_t)(st * kStageStep);
-                const uint64_t kd1 = kd_base + (uint64_t)(st1 * kStageStep);
-                const bool next = j + 1 < u1;
-                bool k_ready = false;
-                ok = mbar_wait(&s.v_full[st], ph, ab);
-                tc_fence_after();
-                // tile 0: O_0 += P_0 V_j, then S_0 for the next key tile
-                if (ok && j >= ta0 && j < ta1) {
-                    ok = mbar_wait(&s.p_full[0], pc0 & 1, ab);
-                    ++pc0;
-                    tc_fence_after();
-                    if (ok) {
-                        issue_pv(256, 0, vd, j > ta0 ? 1u : 0u);
-                        if (j == ta1 - 1) tc_commit(&s.o_full[0]);
+                {
+                    const int st0 = gt % C::STAGES;
+                    if (ok && (ok = mbar_wait(&s.k_full[st0], (gt / C::STAGES) & 1, ab))) {
+                        // prologue: S_k for the first KV tile (the S columns held the previous
+                        // item's last P, read by P V MMAs issued earlier)
+                        tc_fence_after();
+                        const uint64_t kd0 = kd_base + (uint64_t)(st0 * kStageStep);
+                        if (u0 >= ta0 && u0 < ta1) {
+                            issue_s(qd0, 0, kd0);
+                            tc_commit(&s.s_full[0]);
+                        }
+                        if (u0 >= tb0 && u0 < tb1) {
+                            issue_s(qd1, 128, kd0);
+                            tc_commit(&s.s_full[1]);
+                        }
+                        tc_commit(&s.k_empty[st0]);
+                        if (u1 - u0 == 1) tc_commit(&s.q_empty);  // the item's last S
                     }
                 }
-                if (ok && next && j + 1 >= ta0 && j + 1 < ta1) {
-                    ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                int it = gt;
+                for (int j = u0; ok && j < u1; ++j, ++it) {
+                    const int st = it % C::STAGES;
+                    const uint32_t ph = (it / C::STAGES) & 1;
+                    const int st1 = (it + 1) % C::STAGES;
+                    const uint32_t ph1 = ((it + 1) / C::STAGES) & 1;
+                    const uint64_t vd = vd_base + (uint64_t)(st * kStageStep);
+                    const uint64_t kd1 = kd_base + (uint64_t)(st1 * kStageStep);
+                    const bool next = j + 1 < u1;
+                    bool k_ready = false;
+                    ok = mbar_wait(&s.v_full[st], ph, ab);
                     tc_fence_after();
-                    k_ready = true;
-                    if (ok) {
-                        issue_s(qd0, 0, kd1);
-                        tc_commit(&s.s_full[0]);
+                    // tile 0: O_0 += P_0 V_j, then S_0 for the next key tile
+                    if (ok && j >= ta0 && j < ta1) {
+                        ok = mbar_wait(&s.p_full[0], pc0 & 1, ab);
+                        ++pc0;
+                        // the first P V of the item overwrites O_0: the previous item's
+                        // epilogue must have read it
+                        if (ok && j == ta0 && oc0 > 0) ok = mbar_wait(&s.o_free[0], (oc0 - 1) & 1, ab);
+                        tc_fence_after();
+                        if (ok) {
+                            issue_pv(256, 0, vd, j > ta0 ? 1u : 0u);
+                            if (j == ta1 - 1) {
+                                tc_commit(&s.o_full[0]);
+                                ++oc0;
+                            }
+                        }
                     }
-                }
-                // tile 1
-                if (ok && j >= tb0 && j < tb1) {
-                    ok = mbar_wait(&s.p_full[1], pc1 & 1, ab);
-                    ++pc1;
-                    tc_fence_after();
-                    if (ok) {
-                        issue_pv(384, 128, vd, j > tb0 ? 1u : 0u);
-                        if (j == tb1 - 1) tc_commit(&s.o_full[1]);
-                    }
-                }
-                if (ok && next && j + 1 >= tb0 && j + 1 < tb1) {
-                    if (!k_ready) {
+                    if (ok && next && j + 1 >= ta0 && j + 1 < ta1) {
                         ok = mbar_wait(&s.k_full[st1], ph1, ab);
                         tc_fence_after();
                         k_ready = true;
+                        if (ok) {
+                            issue_s(qd0, 0, kd1);
+                            tc_commit(&s.s_full[0]);
+                        }
                     }
-                    if (ok) {
-                        issue_s(qd1, 128, kd1);
-                        tc_commit(&s.s_full[1]);
+                    // tile 1
+                    if (ok && j >= tb0 && j < tb1) {
+                        ok = mbar_wait(&s.p_full[1], pc1 & 1, ab);
+                        ++pc1;
+                        if (ok && j == tb0 && oc1 > 0) ok = mbar_wait(&s.o_free[1], (oc1 - 1) & 1, ab);
+                        tc_fence_after();
+                        if (ok) {
+                            issue_pv(384, 128, vd, j > tb0 ? 1u : 0u);
+                            if (j == tb1 - 1) {
+                                tc_commit(&s.o_full[1]);
+                                ++oc1;
+                            }
+                        }
+                    }
+                    if (ok && next && j + 1 >= tb0 && j + 1 < tb1) {
+                        if (!k_ready) {
+                            ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        if (ok) {
+                            issue_s(qd1, 128, kd1);
+                            tc_commit(&s.s_full[1]);
+                        }
+                    }
+                    if (!ok) break;
+                    // the last S of the item has been issued: the Q tiles are free when it
+                    // completes, so the next item's Q load overlaps this item's last P V
+                    if (j + 2 == u1) tc_commit(&s.q_empty);
+                    tc_commit(&s.v_empty[st]);
+                    if (next) {
+                        // the next K tile always feeds an S of this CTA (the union of two bands is
+                        // contiguous); wait for it here if neither tile did
+                        if (!k_ready) ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                        if (ok) tc_commit(&s.k_empty[st1]);
                     }
                 }
-                if (!ok) break;
-                tc_commit(&s.v_empty[st]);
-                if (next) {
-                    // the next K tile always feeds an S of this CTA (the union of two bands is
-                    // contiguous); wait for it here if neither tile did
-                    if (!k_ready) ok = mbar_wait(&s.k_full[st1], ph1, ab);
-                    if (ok) tc_commit(&s.k_empty[st1]);
-                }
+                gt += u1 - u0;
             }
             // let every issued MMA finish before the CTA tears down
             tc_commit(&s.drain);
@@ -328,20 +398,24 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
         const uint32_t tS = tmem + lane_base + 128 * k;
         const uint32_t tO = tmem + lane_base + 256 + 128 * k;
-        // this group's tile, copied out of ti[] by selection (no run-time array index)
-        const int my_s0 = k ? ti[1].s0 : ti[0].s0;
-        const int my_t0 = k ? ti[1].t0 : ti[0].t0;
-        const int my_t1 = k ? ti[1].t1 : ti[0].t1;
-        const bool my_active = k ? ti[1].active : ti[0].active;
-        const int i = my_s0 + r / p.G;          // query position
-        const int h = g * p.G + r % p.G;         // query head
-        const bool row_valid = my_active && (r < p.P * p.G) && i < sv.nq;
-        const int jlo = row_valid ? band.lo(i) : 1;
-        const int jhi = row_valid ? band.hi(i) : 0;
         const float c = p.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
-        uint32_t scount = 0;
+        uint32_t scount = 0, ocount = 0;  // S tiles and O tiles received (carried across items)
         bool ok = true;
+        for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+        // only the loop bounds and the row's key band stay live across the key loop; the
+        // epilogue decodes the item again (cheap) instead of holding it in registers
+        int my_t0, my_t1, jlo, jhi;
+        {
+            const FwdItem w = fwd_item(a, idx);
+            if (!w.live) continue;
+            my_t0 = k ? w.ti[1].t0 : w.ti[0].t0;
+            my_t1 = k ? w.ti[1].t1 : w.ti[0].t1;
+            const int i = (k ? w.ti[1].s0 : w.ti[0].s0) + r / p.G;
+            const bool rv = (k ? w.ti[1].active : w.ti[0].active) && (r < p.P * p.G) && i < w.sv.nq;
+            jlo = rv ? w.band.lo(i) : 1;
+            jhi = rv ? w.band.hi(i) : 0;
+        }
+        float m_used = -INFINITY, l = 0.f;
         for (int j = my_t0; j < my_t1; ++j) {
             const bool w = mbar_wait(&s.s_full[k], scount & 1, ab);
             if (!__all_sync(0xffffffffu, w)) {
@@ -417,10 +491,19 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             if (lane == 0) mbar_arrive(&s.p_full[k]);
         }
         // ---------------- epilogue ----------------
+        int idx2 = idx;
+        asm volatile("" : "+r"(idx2));  // a fresh decode, not the one held before the loop
+        const FwdItem w = fwd_item(a, idx2);
+        const SeqView& sv = w.sv;
+        const int g = w.g, split = w.split;
+        const int i = (k ? w.ti[1].s0 : w.ti[0].s0) + r / p.G;  // query position
+        const int h = g * p.G + r % p.G;                         // query head
+        const bool row_valid = (k ? w.ti[1].active : w.ti[0].active) && (r < p.P * p.G) && i < sv.nq;
         const bool has_o = my_t1 > my_t0;  // uniform over the warp group
         if (has_o && ok) {
-            const bool w = mbar_wait(&s.o_full[k], 0, ab);
-            ok = __all_sync(0xffffffffu, w);
+            const bool wt = mbar_wait(&s.o_full[k], ocount & 1, ab);
+            ++ocount;
+            ok = __all_sync(0xffffffffu, wt);
             tc_fence_after();
         }
         const bool split_mode = a.n_splits > 1;
@@ -472,6 +555,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                             __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
                 }
             }
+            // O_k is in registers and stored: the next item's P V may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.o_free[k]);
         } else if (row_valid) {
             if (!split_mode) {
                 __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
@@ -483,6 +570,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 for (int t = 0; t < D / 4; ++t) reinterpret_cast<float4*>(op)[t] = make_float4(0, 0, 0, 0);
             }
         }
+        }  // items
     }
 
     tc_fence_before();
@@ -501,8 +589,8 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const C
     const size_t smem = sizeof(FwdSmem<D>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long n = a.p.cu_q ? (long)a.n_blocks * a.p.h_kv : (long)a.n_blocks * a.n_splits * a.p.h_kv * a.p.B;
-    fwd_kernel<D><<<(unsigned)n, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
+    if (a.n_items <= 0 || a.n_ctas <= 0) return cudaSuccess;
+    fwd_kernel<D><<<(unsigned)a.n_ctas, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
 }
 

@@ -32,6 +32,8 @@ struct FwdArgs {
     int split_tiles;   // KV tiles per split
     int unit_major;    // grid order: blocks of one (batch, kv head) adjacent (decode-like
                        // shapes, so they share K/V through L2) instead of heaviest first
+    int n_items;       // work items (query blocks x kv heads [x batch x splits])
+    int n_ctas;        // persistent CTAs of the d <= 128 kernel (at most one per SM)
     __nv_bfloat16* o;  // [tokens, h_q, d]
     float* lse;        // [B, h_q, s_q] or [h_q, T_q]; may be null
     float* o_part;     // split mode: [n_splits, rows, d] fp32
