@@ -41,6 +41,8 @@ class FaParams(ctypes.Structure):
         ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
         ("sinks", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("max_seqlen_q", ctypes.c_int), ("max_seqlen_k", ctypes.c_int), ("flags", ctypes.c_uint),
+        ("seqused_k", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int),
+        ("max_blocks_per_seq", ctypes.c_int), ("num_pages", ctypes.c_int),
     ]
 
 
@@ -153,9 +155,18 @@ def _ptr(t):
 
 
 def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None,
-                cu_k=None, flags=0) -> FaParams:
-    """fa_params from tensor shapes: [B,S,H,D] dense or [T,H,D] packed (with cu_q / cu_k)."""
-    if cu_q is None:
+                cu_k=None, flags=0, seqused_k=None, block_table=None, s_kv=None) -> FaParams:
+    """fa_params from tensor shapes: [B,S,H,D] dense or [T,H,D] packed (with cu_q / cu_k).
+
+    With a block_table ([B, max_blocks_per_seq] int32), k is a page pool
+    [num_pages, page_size, h_kv, d] and s_kv (the logical cache length) must be given.
+    seqused_k: int32 [B] keys used per sequence, or None."""
+    if block_table is not None:
+        B, s_q, h_q, d = q.shape
+        num_pages, page_size, h_kv, _ = k.shape
+        if s_kv is None:
+            raise ValueError("a paged cache needs the logical cache length s_kv")
+    elif cu_q is None:
         B, s_q, h_q, d = q.shape
         _, s_kv, h_kv, _ = k.shape
     else:
@@ -172,6 +183,11 @@ def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sink
     p.cu_seqlens_k = None if cu_k is None else cu_k.data_ptr()
     p.max_seqlen_q = p.max_seqlen_k = 0
     p.flags = flags
+    p.seqused_k = None if seqused_k is None else seqused_k.data_ptr()
+    if block_table is not None:
+        p.block_table = block_table.data_ptr()
+        p.page_size, p.num_pages = int(page_size), int(num_pages)
+        p.max_blocks_per_seq = int(block_table.shape[1])
     return p
 
 
@@ -181,11 +197,11 @@ def _stream():
 
 
 def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None, cu_k=None,
-            flags=0, out=None, lse=None, workspace=None):
+            flags=0, out=None, lse=None, workspace=None, seqused_k=None, block_table=None, s_kv=None):
     """Runs fa_fwd on torch CUDA tensors; returns (o, lse, workspace)."""
     import torch
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
-                    cu_k=cu_k, flags=flags)
+                    cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv)
     nbytes = fa_fwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_fwd_workspace_size")

@@ -136,6 +136,17 @@ fa_status normalise(const fa_params* in, Problem& p) {
         p.T_q = a.s_q;
         p.T_k = a.s_kv;
     }
+    // KV-cache forms: a per-sequence used length, and a paged cache (dense q only)
+    p.seqused_k = a.seqused_k;
+    p.block_table = a.block_table;
+    if (a.block_table) {
+        if (p.cu_q) return FA_ERR_UNSUPPORTED;
+        if (a.page_size <= 0 || a.page_size % 128 != 0 || a.max_blocks_per_seq <= 0 || a.num_pages <= 0)
+            return FA_ERR_INVALID_ARG;
+        if ((long)a.max_blocks_per_seq * a.page_size < (long)a.s_kv) return FA_ERR_INVALID_ARG;
+        p.page_size = a.page_size;
+        p.max_blocks = a.max_blocks_per_seq;
+    }
     return FA_OK;
 }
 
@@ -248,6 +259,7 @@ struct BwdPlan {
 fa_status plan_bwd(const Problem& p, BwdPlan& pl) {
     pl = BwdPlan();
     if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
+    if (p.seqused_k || p.block_table) return FA_ERR_UNSUPPORTED;  // KV-cache forms: forward only
     const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
     const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
     if (p.B == 0 || (rows_total == 0 && keys_total == 0)) return FA_OK;
@@ -356,8 +368,12 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     const int bdim = p.cu_q ? 1 : p.B;
     CUtensorMap tk, tv;
     const int kv_box = (pl.path == FwdPath::kDecode || p.d == 256) ? 64 : 128;
-    if (!encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, kv_box) ||
-        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, kv_box))
+    // a paged cache is a [num_pages][page_size][h_kv][d] pool: the map's key and outer
+    // dimensions are the row within a page and the page
+    const int kv_rows = p.block_table ? p.page_size : tokens_k;
+    const int kv_outer = p.block_table ? in->num_pages : bdim;
+    if (!encode_bhsd(&tk, k, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box) ||
+        !encode_bhsd(&tv, v, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box))
         return FA_ERR_CUDA;
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     float* o_part = reinterpret_cast<float*>(ws + kStatusBytes);

@@ -69,7 +69,23 @@ __device__ __forceinline__ SeqView seq_view(const Problem& p, int b) {
         v.nk = p.s_kv;
         v.tma_b = b;
     }
+    // a cache slot filled only up to seqused_k[b]: the rest of the slot is invisible
+    if (p.seqused_k) v.nk = min(v.nk, max(0, p.seqused_k[b]));
     return v;
+}
+
+// Tensor-map coordinates of the key tile that starts at key j (a multiple of the tile
+// size) of sequence sv: the key row and the outer (batch or page) coordinate.  A paged
+// cache keeps key j in row j % page_size of page block_table[b][j / page_size]; page_size
+// is a multiple of every key tile, so a tile never straddles two pages.
+__device__ __forceinline__ void kv_tile_coord(const Problem& p, const SeqView& sv, int j, int& row, int& outer) {
+    if (p.block_table) {
+        outer = p.block_table[(long)sv.b * p.max_blocks + j / p.page_size];
+        row = j % p.page_size;
+    } else {
+        row = sv.k0 + j;
+        outer = sv.tma_b;
+    }
 }
 
 // Index of (sequence b, local row i, head h) in the LSE output.

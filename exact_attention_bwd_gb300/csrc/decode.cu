@@ -83,9 +83,10 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
     const int unit = blockIdx.x / a.n_splits;
     const int g = unit % p.h_kv, b = unit / p.h_kv;
     const int R = p.s_q * p.G;
-    const Band band{p.s_kv - p.s_q, p.left, p.right, p.s_kv};
+    const SeqView sv = seq_view(p, b);  // dense; nk < s_kv when the cache slot is partly filled
+    const Band band{sv.nk - p.s_q, p.left, p.right, sv.nk};
 
-    int j_begin = split * a.split_keys, j_end = min(p.s_kv, (split + 1) * a.split_keys);
+    int j_begin = split * a.split_keys, j_end = min(sv.nk, (split + 1) * a.split_keys);
     j_begin = max(j_begin, band.lo(0));
     j_end = min(j_end, band.hi(p.s_q - 1) + 1);
     const int t_begin = j_begin / BK;
@@ -122,11 +123,12 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % C::STAGES;
                 if (!mbar_wait(&s.empty[st], ((t / C::STAGES) & 1) ^ 1, ab)) break;
-                const int j0 = (t_begin + t) * BK;
+                int row, outer;
+                kv_tile_coord(p, sv, (t_begin + t) * BK, row, outer);
                 mbar_expect_tx(&s.full[st], 2 * C::TILE);
                 for (int c = 0; c < C::KCH; ++c) {
-                    tma_load_4d(&s.k[st][c * C::CHUNK], &tmk, &s.full[st], c * 64, g, j0, b);
-                    tma_load_4d(&s.v[st][c * C::CHUNK], &tmv, &s.full[st], c * 64, g, j0, b);
+                    tma_load_4d(&s.k[st][c * C::CHUNK], &tmk, &s.full[st], c * 64, g, row, outer);
+                    tma_load_4d(&s.v[st][c * C::CHUNK], &tmv, &s.full[st], c * 64, g, row, outer);
                 }
                 ++issued;
             }

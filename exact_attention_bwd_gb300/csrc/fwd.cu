@@ -221,17 +221,17 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 for (int j = w.u0; j < w.u1; ++j, ++gt) {
                     const int st = gt % C::STAGES;
                     const uint32_t ph = (gt / C::STAGES) & 1;
+                    int krow, kouter;
+                    kv_tile_coord(p, w.sv, j * BN, krow, kouter);
                     if (!(ok = mbar_wait(&s.k_empty[st], ph ^ 1, ab))) break;
                     mbar_expect_tx(&s.k_full[st], C::TILE_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
-                        tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, w.g,
-                                    w.sv.k0 + j * BN, w.sv.tma_b);
+                        tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, w.g, krow, kouter);
                     ++k_issued;
                     if (!(ok = mbar_wait(&s.v_empty[st], ph ^ 1, ab))) break;
                     mbar_expect_tx(&s.v_full[st], C::TILE_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
-                        tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, w.g,
-                                    w.sv.k0 + j * BN, w.sv.tma_b);
+                        tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, w.g, krow, kouter);
                     ++v_issued;
                 }
             }

@@ -136,19 +136,19 @@ __global__ void __launch_bounds__(kThreads256, 1)
             for (int it = 0; it < ntiles; ++it) {
                 const int st = slot_of(it);
                 const uint32_t ph = use_parity(it);
-                const int row = sv.k0 + (t0 + it) * BN;
+                int row, outer;
+                kv_tile_coord(p, sv, (t0 + it) * BN, row, outer);
                 // slot 0 is free for keys once the softmax warps have copied Q out of it
                 if (it == STAGES - 1 && !mbar_wait(&s.q_tmem, 0, ab)) break;
                 if (!mbar_wait(&s.k_empty[st], ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.k_full[st], KV_BYTES);
                 for (int c = 0; c < KCH; ++c)
-                    tma_load_4d(&s.ring[st][c * KV_CHUNK], &tmk, &s.k_full[st], c * 64, g, row, sv.tma_b);
+                    tma_load_4d(&s.ring[st][c * KV_CHUNK], &tmk, &s.k_full[st], c * 64, g, row, outer);
                 ++k_issued;
                 if (!mbar_wait(&s.v_empty[st], ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.v_full[st], KV_BYTES);
                 for (int c = 0; c < KCH; ++c)
-                    tma_load_4d(&s.ring[st][KV_BYTES + c * KV_CHUNK], &tmv, &s.v_full[st], c * 64, g, row,
-                                sv.tma_b);
+                    tma_load_4d(&s.ring[st][KV_BYTES + c * KV_CHUNK], &tmv, &s.v_full[st], c * 64, g, row, outer);
                 ++v_issued;
             }
             // wait for every copy still in flight before the CTA may exit

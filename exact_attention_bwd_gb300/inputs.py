@@ -185,3 +185,23 @@ def normal_bf16_torch(seed: int, shape, device):
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     return torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def page_table(seed: int, B: int, max_blocks: int, num_pages: int) -> np.ndarray:
+    """Block table of a paged key/value cache: int32 [B, max_blocks] page indices, a
+    seeded draw of distinct pages (a permutation of the pool, cut to B * max_blocks)."""
+    if num_pages < B * max_blocks:
+        raise ValueError("the pool has fewer pages than the table needs")
+    perm = rng(seed).permutation(num_pages)[: B * max_blocks]
+    return perm.reshape(B, max_blocks).astype(np.int32)
+
+
+def used_lengths(seed: int, B: int, s_kv: int) -> np.ndarray:
+    """Filled lengths of B cache slots of s_kv keys: int32 [B], uniform on [0, s_kv], with
+    the first slot full and (for B > 2) the second empty, so both ends are always covered."""
+    n = rng(seed).integers(0, s_kv + 1, size=B).astype(np.int32)
+    if B > 0:
+        n[0] = s_kv
+    if B > 2:
+        n[1] = 0
+    return n

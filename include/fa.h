@@ -57,6 +57,22 @@
  *    fa_read_device_status reports.
  *  - Supported: bf16; head dim d in {64, 128, 256} for the forward, {64, 128} for
  *    the backward; h_q / h_kv <= 128.  Anything else returns FA_ERR_UNSUPPORTED.
+ *
+ * KV-cache forms (forward only; fa_bwd returns FA_ERR_UNSUPPORTED when either is set):
+ *  - seqused_k (fa4-jax PyPI page, "Varlen semantics": optional seqused_k limits each
+ *    slot to its first seqused[b] tokens, the cache case where slots are larger than
+ *    what is filled): sequence b uses only its first seqused_k[b] keys of its slot (s_kv
+ *    for dense tensors, cu_seqlens_k[b+1] - cu_seqlens_k[b] for packed ones); the other
+ *    keys are invisible and the bottom-right alignment uses the used length.  Values are
+ *    clamped to [0, slot].
+ *  - block_table (vllm-project/flash-attention README, flash_attn_with_kvcache docstring:
+ *    a paged cache of shape (num_blocks, page_block_size, nheads_k, headdim) addressed
+ *    through block_table (batch_size, max_num_blocks_per_seq) int32): dense q only; k and
+ *    v are page pools [num_pages, page_size, h_kv, d] and key j of sequence b is row
+ *    j % page_size of page block_table[b * max_blocks_per_seq + j / page_size].  s_kv is
+ *    the logical cache length (at most max_blocks_per_seq * page_size); page_size must be
+ *    a positive multiple of 128 (the page's builds ask for 256).  Table entries are read
+ *    on the device and not checked.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -97,6 +113,12 @@ typedef struct fa_params {
     const int32_t *cu_seqlens_k;    /* device int32 [B+1]; required iff cu_seqlens_q */
     int max_seqlen_q, max_seqlen_k; /* optional hints (0 = unknown); never needed */
     unsigned flags;                 /* FA_FLAG_* */
+    /* KV-cache forms (forward only; see above).  Zero / NULL = not used. */
+    const int32_t *seqused_k;       /* device int32 [B], or NULL */
+    const int32_t *block_table;     /* device int32 [B * max_blocks_per_seq], or NULL */
+    int page_size;                  /* keys per page (block_table only) */
+    int max_blocks_per_seq;         /* row stride of block_table */
+    int num_pages;                  /* pages in each of the k and v pools */
 } fa_params;
 
 /* Bytes of workspace fa_fwd / fa_bwd need for these parameters (>= 256: the first

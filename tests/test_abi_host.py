@@ -134,3 +134,28 @@ def test_empty_problem_needs_no_launch_until_status():
 def test_profile_read_unknown_kernel():
     rc, _ = fa.fa_profile_read("nope")
     assert rc == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(page_size=100, max_blocks_per_seq=4, num_pages=8), fa.FA_ERR_INVALID_ARG),   # not a multiple of 128
+    (dict(page_size=0, max_blocks_per_seq=4, num_pages=8), fa.FA_ERR_INVALID_ARG),
+    (dict(page_size=128, max_blocks_per_seq=1, num_pages=8), fa.FA_ERR_INVALID_ARG),   # 128 < s_kv = 256
+    (dict(page_size=128, max_blocks_per_seq=2, num_pages=0), fa.FA_ERR_INVALID_ARG),
+    (dict(page_size=128, max_blocks_per_seq=2, num_pages=4, cu_seqlens_q=0x2000, cu_seqlens_k=0x2000),
+     fa.FA_ERR_UNSUPPORTED),                                                             # paged: dense q only
+])
+def test_paged_cache_rejects(kw, code):
+    assert call_fwd(params(block_table=0x4000, **kw)) == code
+
+
+def test_paged_cache_is_planned():
+    p = params(block_table=0x4000, page_size=128, max_blocks_per_seq=2, num_pages=4)
+    assert fa.fa_fwd_workspace_size(p) == 256
+    assert call_fwd(p, ws_bytes=16) == fa.FA_ERR_WORKSPACE
+
+
+def test_backward_rejects_cache_forms():
+    assert call_bwd(params(seqused_k=0x4000)) == fa.FA_ERR_UNSUPPORTED
+    assert call_bwd(params(block_table=0x4000, page_size=128, max_blocks_per_seq=2, num_pages=4)) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_workspace_size(params(seqused_k=0x4000)) == 0
