@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the other prefill workloads")
     ap.add_argument("--decode-only", default=None, help="time one decode workload and exit")
     ap.add_argument("--decode-batch", type=int, default=None, help="batch override for --decode-only")
+    ap.add_argument("--paged", action="store_true", help="--decode-only over a paged cache")
     return ap.parse_args()
 
 
@@ -263,6 +264,8 @@ def run_ours(args):
     if not args.no_decode:
         line["decode"] = {n: measure_decode(dev, n) for n in
                           ("decode_d128_sq1", "decode_d128_sq64", "decode_d256_sq1", "decode_d256_sq64")}
+        line["decode"].update({n + "_paged": measure_decode(dev, n, paged=True) for n in
+                               ("decode_d128_sq1", "decode_d256_sq1", "decode_d128_sq64")})
     if not args.no_sweep:
         line["workloads"] = {n: measure_workload(dev, n) for n in SWEEP + OTHER}
     if rank == 0 and not args.no_cpu:
@@ -339,19 +342,31 @@ OTHER = ["gqa_window_causal", "gqa_window_2sided", "varlen"]
 # decode / chunked prefill against a long cache: HBM-bound, reported as GB/s
 # ----------------------------------------------------------------------------------------------
 
-def measure_decode(dev, name, steps=10, warmup=3, batch=None):
+PAGE_SIZE = 256  # keys per page of the paged-cache decode measurement
+
+
+def measure_decode(dev, name, steps=10, warmup=3, batch=None, paged=False):
     """Forward of one decode workload: algorithmic bytes (K and V read once, Q read, O and
     LSE written) per launch over the CUDA-event time of the whole forward (split kernel +
-    combine), L2 flushed between launches; per-kernel times from the library's hooks."""
+    combine), L2 flushed between launches; per-kernel times from the library's hooks.
+    paged: the cache is a pool of 256-key pages in a seeded random order, addressed
+    through a block table (the table's reads are not counted as algorithmic bytes)."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
     w = inputs.workload(name) if batch is None else inputs.workload(name, B=batch)
     B, s_q, s_kv, h_q, h_kv, d = w["B"], w["s_q"], w["s_kv"], w["h_q"], w["h_kv"], w["d"]
     sd = lambda t: inputs.seed_of(w["wid"], w["variant"], t)  # noqa: E731
     q = inputs.normal_bf16_torch(sd(inputs.Q), (B, s_q, h_q, d), dev)
-    k = inputs.normal_bf16_torch(sd(inputs.K), (B, s_kv, h_kv, d), dev)
-    v = inputs.normal_bf16_torch(sd(inputs.V), (B, s_kv, h_kv, d), dev)
     kw = dict(causal=True, softmax_scale=1.0 / math.sqrt(d))
+    if paged:
+        max_blocks = -(-s_kv // PAGE_SIZE)
+        kshape = (B * max_blocks, PAGE_SIZE, h_kv, d)
+        table = inputs.page_table(sd(7), B, max_blocks, B * max_blocks)
+        kw.update(block_table=torch.from_numpy(table).to(dev), s_kv=s_kv)
+    else:
+        kshape = (B, s_kv, h_kv, d)
+    k = inputs.normal_bf16_torch(sd(inputs.K), kshape, dev)
+    v = inputs.normal_bf16_torch(sd(inputs.V), kshape, dev)
     o, lse, ws = fa.forward(q, k, v, **kw)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -444,8 +459,9 @@ def main():
         import torch
         torch.cuda.set_device(0)
         r = measure_decode(torch.device("cuda", 0), args.decode_only, steps=args.steps, warmup=args.warmup,
-                           batch=args.decode_batch)
-        print(json.dumps({"workload": args.decode_only, "batch": args.decode_batch, **r}), flush=True)
+                           batch=args.decode_batch, paged=args.paged)
+        print(json.dumps({"workload": args.decode_only, "batch": args.decode_batch, "paged": args.paged, **r}),
+              flush=True)
         return
     if args.impl == "reference":
         run_reference(args)
