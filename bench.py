@@ -268,6 +268,8 @@ def run_ours(args):
                                ("decode_d128_sq1", "decode_d256_sq1", "decode_d128_sq64")})
     if not args.no_sweep:
         line["workloads"] = {n: measure_workload(dev, n) for n in SWEEP + OTHER}
+        line["deterministic_bwd"] = {n: measure_workload(dev, n, bwd_flags=fa.FA_FLAG_DETERMINISTIC)
+                                     for n in ("sweep_s8192_causal", "sweep_s2048", "gqa_window_causal", "varlen")}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = oracle_sample(w)
     if rank == 0:
@@ -281,9 +283,10 @@ def run_ours(args):
 # every other workload: forward and forward+backward TFLOPS (context beside the headline)
 # ----------------------------------------------------------------------------------------------
 
-def measure_workload(dev, name, steps=5, warmup=2):
+def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0):
     """fwd and fwd+bwd of one prefill workload with seeded on-device inputs (the same recipe
-    seeds, drawn by torch's generator); L2 flushed before every timed step."""
+    seeds, drawn by torch's generator); L2 flushed before every timed step.  bwd_flags:
+    fa_params flags of the backward (FA_FLAG_DETERMINISTIC for the fixed-order dQ sums)."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
     w = inputs.workload(name)
@@ -310,7 +313,7 @@ def measure_workload(dev, name, steps=5, warmup=2):
     kw = dict(causal=w["causal"], window=w["window"], softmax_scale=1.0 / math.sqrt(w["d"]), sinks=sinks,
               cu_q=cu_d, cu_k=cu_d)
     o, lse, wsf = fa.forward(q, k, v, **kw)
-    dq, dk, dv, ds, wsb = fa.backward(q, k, v, o, lse, do, **kw)
+    dq, dk, dv, ds, wsb = fa.backward(q, k, v, o, lse, do, **kw, flags=bwd_flags)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -320,7 +323,7 @@ def measure_workload(dev, name, steps=5, warmup=2):
         e0.record(stream)
         fa.forward(q, k, v, **kw, out=o, lse=lse, workspace=wsf)
         e1.record(stream)
-        fa.backward(q, k, v, o, lse, do, **kw, workspace=wsb, grads=(dq, dk, dv, ds))
+        fa.backward(q, k, v, o, lse, do, **kw, workspace=wsb, grads=(dq, dk, dv, ds), flags=bwd_flags)
         e2.record(stream)
         e2.synchronize()
         if it >= warmup:

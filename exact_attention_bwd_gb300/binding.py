@@ -25,6 +25,7 @@ FA_ERR_DEVICE_CHECK = 6
 
 FA_FLAG_VALIDATE_CU = 1
 FA_FLAG_NO_SPLIT = 2
+FA_FLAG_DETERMINISTIC = 4
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_read_device_status",
            "fa_status_string", "fa_profile_enable", "fa_profile_read", "fa_version", "fa_fwd_noalloc")

@@ -252,11 +252,11 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
 struct BwdPlan {
     bool empty = true;
     int n_qtiles = 0, n_kvblocks = 0, n_bands = 1;
-    size_t off_delta = 0, off_lse2 = 0, off_dq = 0;
+    size_t off_delta = 0, off_lse2 = 0, off_dq = 0, off_sink = 0, off_count = 0;
     size_t ws_bytes = kStatusBytes;
 };
 
-fa_status plan_bwd(const Problem& p, BwdPlan& pl) {
+fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     pl = BwdPlan();
     if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
     if (p.seqused_k || p.block_table) return FA_ERR_UNSUPPORTED;  // KV-cache forms: forward only
@@ -285,6 +285,14 @@ fa_status plan_bwd(const Problem& p, BwdPlan& pl) {
     pl.off_lse2 = pl.off_delta + align256(stat);
     pl.off_dq = pl.off_lse2 + align256(stat);
     pl.ws_bytes = pl.off_dq + align256((size_t)p.h_kv * pl.n_qtiles * 128 * p.d * 4);
+    if (p.sinks) {  // per-row sink-gradient terms, summed per head in a fixed order
+        pl.off_sink = pl.ws_bytes;
+        pl.ws_bytes += align256(stat);
+    }
+    if (flags & FA_FLAG_DETERMINISTIC) {  // one counter per (key/value head, query tile)
+        pl.off_count = pl.ws_bytes;
+        pl.ws_bytes += align256((size_t)p.h_kv * pl.n_qtiles * 4);
+    }
     return FA_OK;
 }
 
@@ -340,7 +348,7 @@ size_t fa_bwd_workspace_size(const fa_params* in) {
     Problem p;
     if (normalise(in, p) != FA_OK) return 0;
     BwdPlan pl;
-    if (plan_bwd(p, pl) != FA_OK) return 0;
+    if (plan_bwd(p, in->flags, pl) != FA_OK) return 0;
     return pl.ws_bytes;
 }
 
@@ -441,7 +449,7 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     fa_status rc = normalise(in, p);
     if (rc != FA_OK) return rc;
     BwdPlan pl;
-    if ((rc = plan_bwd(p, pl)) != FA_OK) return rc;
+    if ((rc = plan_bwd(p, in->flags, pl)) != FA_OK) return rc;
     if (!workspace || !aligned16(workspace)) return FA_ERR_INVALID_ARG;
     if (ws_bytes < pl.ws_bytes) return FA_ERR_WORKSPACE;
     if (p.sinks && !dsinks) return FA_ERR_INVALID_ARG;
@@ -476,6 +484,8 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
     a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
     a.dsinks = p.sinks ? dsinks : nullptr;
+    a.sink_t = p.sinks ? reinterpret_cast<float*>(ws + pl.off_sink) : nullptr;
+    a.dq_count = (in->flags & FA_FLAG_DETERMINISTIC) ? reinterpret_cast<int*>(ws + pl.off_count) : nullptr;
     a.status = status;
 
     const int tokens_q = p.cu_q ? p.T_q : p.s_q;

@@ -71,7 +71,86 @@ __device__ __forceinline__ int qtile_base(const Problem& p, int seq) {
     return seq * cdiv(p.s_q, p.P);
 }
 
-template <int D>
+// Query tiles [qt0, qt1) whose positions have a band reaching key block `blk` of the
+// sequence (qt0 == qt1 when no query sees the block).  Over the blocks that some query
+// sees, both ends are non-decreasing in the block index.
+__device__ __forceinline__ void block_qtiles(const Problem& p, const SeqView& sv, const Band& band, int blk, int& qt0,
+                                             int& qt1) {
+    const int j0 = blk * kRows;
+    const int j1 = min(j0 + kRows, sv.nk) - 1;
+    int i_lo = 0, i_hi = sv.nq - 1;
+    if (p.right >= 0) i_lo = max(i_lo, j0 - band.off - p.right);
+    if (p.left >= 0) i_hi = min(i_hi, j1 - band.off + p.left);
+    qt0 = (i_hi >= i_lo) ? i_lo / p.P : 0;
+    qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
+}
+
+// Deterministic dQ order.  Every query tile receives the contributions of the key blocks
+// that see it in descending block order, each block's contribution complete before the
+// next one starts, so the fp32 sums are formed in the same order on every run.  A key
+// block's CTA walks its query tiles in ascending order; before adding into tile t it
+// waits until the tile's counter shows every later block's contribution (one count per
+// adding warp).  The launch puts a sequence's later blocks at lower CTA indices, so each
+// CTA waits only on CTAs dispatched before it (and, run after run, on ones that are a
+// step ahead of it: the later block reached tile t one query tile earlier).
+struct DqOrder {
+    int next = 0;  // next later key block to examine
+    int n = 0;     // later blocks seen so far whose query tiles start at or before the tile
+};
+
+// Number of later key blocks whose contributions precede this block's in query tile t;
+// t never decreases between calls (the cursor only moves forward).
+__device__ __forceinline__ int dq_predecessors(const Problem& p, const SeqView& sv, const Band& band, DqOrder& o,
+                                               int t) {
+    while (o.next * kRows < sv.nk) {
+        int a0, a1;
+        block_qtiles(p, sv, band, o.next, a0, a1);
+        if (a1 > a0) {
+            if (a0 > t) break;  // later blocks start later still; each earlier one reaches t
+            ++o.n;
+        }
+        ++o.next;
+    }
+    return o.n;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+// Lane 0 waits until the counter reaches `need`; the warp learns the outcome.  Bounded
+// like every other wait: false when the limit passes, the CTA gave up, or another CTA of
+// the launch recorded a failure (its contributions may never come).
+__device__ __forceinline__ bool dq_turn_wait(const int* cnt, int need, const Abort& ab) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0 && ld_acquire_gpu(cnt) < need) {
+        const unsigned long long t0 = globaltimer();
+        while (ld_acquire_gpu(cnt) < need) {
+            if (ab.raised() || (ab.status && *reinterpret_cast<volatile int*>(ab.status) != 0)) {
+                ab.raise(kStatusTimeout);
+                ok = false;
+                break;
+            }
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                ab.raise(kStatusTimeout);
+                ok = false;
+                break;
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// After a warp's reductions into a tile: make them visible, then count the warp in.
+__device__ __forceinline__ void dq_turn_done(int* cnt) {
+    __threadfence();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) atomicAdd(cnt, 1);
+}
+
+template <int D, bool DET>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
     bwd_main_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
@@ -94,9 +173,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     int g, seq, blk;
     {
         const int idx = blockIdx.x;
+        // deterministic order: a sequence's later key blocks first (lower CTA indices)
+        constexpr bool rev = DET;
         if (p.cu_q) {
             g = idx % p.h_kv;
             blk = idx / p.h_kv;
+            if (rev) blk = a.n_kvblocks - 1 - blk;
             seq = owner_sequence(p.cu_k, p.B, blk, kRows);
             blk -= p.cu_k[seq] / kRows + seq;
         } else {
@@ -120,6 +202,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             g = unit % p.h_kv;
             seq = unit / p.h_kv;
             blk = r / ub;
+            if (rev) blk = a.n_kvblocks - 1 - blk;
         }
     }
     const SeqView sv = seq_view(p, seq);
@@ -129,12 +212,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     const int j1 = min(j0 + kRows, sv.nk) - 1;
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
-    // query positions whose band reaches [j0, j1]
-    int i_lo = 0, i_hi = sv.nq - 1;
-    if (p.right >= 0) i_lo = max(i_lo, j0 - band.off - p.right);
-    if (p.left >= 0) i_hi = min(i_hi, j1 - band.off + p.left);
-    const int qt0 = (i_hi >= i_lo) ? i_lo / p.P : 0;
-    const int qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
+    int qt0, qt1;  // query tiles whose positions have a band reaching [j0, j1]
+    block_qtiles(p, sv, band, blk, qt0, qt1);
     const int nsteps = qt1 - qt0;
     const int tbase = qtile_base(p, seq);
 
@@ -186,9 +265,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         if constexpr (C::DQ_T) {
             const int dcol = ((warp & 3) << 5) | lane;  // TMEM lane = column d of dQ
             const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+            DqOrder order;
+            order.next = blk + 1;
             for (int it = 0; it < nsteps; ++it) {
                 const int t = qt0 + it;
                 const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
+                int need = 0;
+                if constexpr (DET) need = 4 * dq_predecessors(p, sv, band, order, t);
                 {
                     const bool w = mbar_wait(&s.dq_full, it & 1, ab);
                     if (!__all_sync(0xffffffffu, w)) break;
@@ -200,12 +283,15 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 // the columns are free as soon as they are in registers
                 tc_fence_before();
                 mbar_arrive(&s.dq_free);
+                int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
+                if (DET && !dq_turn_wait(cnt, need, ab)) break;
                 // for each query row the 32 lanes of a warp add to 32 consecutive floats
                 float* acc = a.dq_acc + trow * D + dcol;
 #pragma unroll
                 for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qa[r]));
 #pragma unroll
                 for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
+                if constexpr (DET) dq_turn_done(cnt);
             }
         }
     } else if (warp < 4) {
@@ -337,6 +423,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int j = j0 + jr;
         const float c = p.scale_log2;
         bool ok = true;
+        DqOrder order;
+        order.next = blk + 1;
         for (int it = 0; it < nsteps; ++it) {
             const uint32_t par = it & 1;
             const int t = qt0 + it;                 // query tile within the sequence
@@ -435,12 +523,18 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
                 tc_fence_before();
                 mbar_arrive(&s.dq_free);
+                int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
+                if (DET && !dq_turn_wait(cnt, 8 * dq_predecessors(p, sv, band, order, t), ab)) {
+                    ok = false;
+                    break;
+                }
                 float* acc = a.dq_acc + (trow + qr) * D + (D / 2) * cg;
 #pragma unroll
                 for (int t4 = 0; t4 < D / 8; ++t4)
                     atomicAdd(reinterpret_cast<float4*>(acc) + t4,
                               make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
                                           __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
+                if constexpr (DET) dq_turn_done(cnt);
             }
         }
         // ---- epilogue: dK, dV for this key tile ----
@@ -512,23 +606,20 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
     int seq, t;
     const bool live = decode_qtile(p, idx, seq, t);
     const long trow = ((long)g * a.n_qtiles + idx) * 128;
+    if (a.dq_count && threadIdx.x == 0) a.dq_count[(long)g * a.n_qtiles + idx] = 0;
     if (!live) {
         a.lse2_t[trow + threadIdx.x] = INFINITY;
         a.delta_t[trow + threadIdx.x] = 0.f;
+        if (a.sink_t) a.sink_t[trow + threadIdx.x] = 0.f;
         return;
     }
     const SeqView sv = seq_view(p, seq);
-    __shared__ float sink_part[128];  // per query head of this tile (at most G <= 128 heads)
-    if (p.sinks) {
-        sink_part[threadIdx.x] = 0.f;
-        __syncthreads();
-    }
     for (int rr = 0; rr < 32; ++rr) {
         const int r = warp * 32 + rr;
         const int i = t * p.P + r / p.G;
         const int h = g * p.G + r % p.G;
         const bool valid = r < p.P * p.G && i < sv.nq;
-        float dsum = 0.f, l2 = INFINITY;
+        float dsum = 0.f, l2 = INFINITY, sterm = 0.f;
         if (valid) {
             const long tok = token_row(p, sv, i);
             const __nv_bfloat16* orow = a.o + (tok * p.h_q + h) * D;
@@ -543,23 +634,41 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
             for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
             const float lse = a.lse[lse_index(p, sv, i, h)];
             l2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-            if (p.sinks && lane == 0 && lse > -INFINITY) {
-                // d(sum O.dO)/d(sink_h) = - exp(sink_h - LSE_i) * D_i
-                atomicAdd(&sink_part[r % p.G], -__expf(p.sinks[h] - lse) * dsum);
-            }
+            // d(sum O.dO)/d(sink_h) = - exp(sink_h - LSE_i) * D_i, summed per head later
+            if (p.sinks && lse > -INFINITY) sterm = -__expf(p.sinks[h] - lse) * dsum;
         }
         if (lane == 0) {
             a.delta_t[trow + r] = valid ? dsum : 0.f;
             a.lse2_t[trow + r] = l2;
+            if (a.sink_t) a.sink_t[trow + r] = sterm;
         }
-    }
-    if (p.sinks) {
-        __syncthreads();
-        if ((int)threadIdx.x < p.G) atomicAdd(a.dsinks + g * p.G + threadIdx.x, sink_part[threadIdx.x]);
     }
     // zero this tile's dQ accumulator rows
     float4* acc = reinterpret_cast<float4*>(a.dq_acc + trow * D);
     for (int x = threadIdx.x; x < 128 * D / 4; x += 128) acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Sink gradient of one query head (one CTA each): the sum of its rows' terms, over the
+// tiles of its key/value head, in a fixed order (strided per-thread sums, then a tree).
+__global__ void __launch_bounds__(256) bwd_dsink_kernel(const BwdArgs a) {
+    const Problem& p = a.p;
+    const int h = blockIdx.x, g = h / p.G, hh = h % p.G;
+    // head h holds rows hh + G k (k < P) of every tile of its key/value head
+    const long n = (long)a.n_qtiles * p.P;
+    float acc = 0.f;
+    for (long x = threadIdx.x; x < n; x += 256) {
+        const long tile = x / p.P;
+        const int k = (int)(x - tile * p.P);
+        acc += a.sink_t[((long)g * a.n_qtiles + tile) * 128 + hh + p.G * k];
+    }
+    __shared__ float part[256];
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) a.dsinks[h] = part[0];
 }
 
 // postprocess: dQ = scale * acc -> bf16 rows
@@ -591,22 +700,27 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
 
 }  // namespace
 
-template <int D>
+template <int D, bool DET>
 static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem<D>);
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_main_kernel<D, DET>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
-    bwd_main_kernel<D><<<(unsigned)n, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
+    bwd_main_kernel<D, DET><<<(unsigned)n, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, cudaStream_t st) {
     switch (a.p.d) {
-        case 64: return launch_main_d<64>(a, tq, tk, tv, tdo, st);
-        case 128: return launch_main_d<128>(a, tq, tk, tv, tdo, st);
+        case 64:
+            return a.dq_count ? launch_main_d<64, true>(a, tq, tk, tv, tdo, st)
+                              : launch_main_d<64, false>(a, tq, tk, tv, tdo, st);
+        case 128:
+            return a.dq_count ? launch_main_d<128, true>(a, tq, tk, tv, tdo, st)
+                              : launch_main_d<128, false>(a, tq, tk, tv, tdo, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -624,6 +738,7 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t st) {
     if (a.n_qtiles == 0) return cudaSuccess;
     if (a.p.d == 64) bwd_post_kernel<64><<<grid, 128, 0, st>>>(a);
     else bwd_post_kernel<128><<<grid, 128, 0, st>>>(a);
+    if (a.dsinks) bwd_dsink_kernel<<<a.p.h_q, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -86,6 +86,9 @@ struct BwdArgs {
     __nv_bfloat16* dk;     // [tokens_k, h_kv, d]
     __nv_bfloat16* dv;
     float* dsinks;         // [h_q] or null
+    float* sink_t;         // [h_kv, n_qtiles, 128]  per-row sink-gradient terms (with sinks)
+    int* dq_count;         // [h_kv, n_qtiles] dQ contributions landed per query tile, or null:
+                           // non-null = deterministic order (key blocks in descending order)
     int* status;
 };
 

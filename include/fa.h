@@ -99,6 +99,11 @@ typedef enum fa_status {
 /* Flags */
 #define FA_FLAG_VALIDATE_CU 1u  /* check cu_seqlens on the device; result in the status word */
 #define FA_FLAG_NO_SPLIT 2u     /* forward: never split the key range across CTAs */
+/* backward: bitwise-reproducible results.  dQ is summed over key blocks in a fixed order
+ * (descending key block) instead of in arrival order; the workspace grows by 4 bytes per
+ * (query tile, key/value head).  The deterministic backward option of the
+ * vllm-project/flash-attention README (changelog 2.4). */
+#define FA_FLAG_DETERMINISTIC 4u
 
 typedef struct fa_params {
     int B;            /* batch (dense) or number of sequences (packed) */

@@ -159,3 +159,14 @@ def test_backward_rejects_cache_forms():
     assert call_bwd(params(block_table=0x4000, page_size=128, max_blocks_per_seq=2, num_pages=4)) == \
         fa.FA_ERR_UNSUPPORTED
     assert fa.fa_bwd_workspace_size(params(seqused_k=0x4000)) == 0
+
+
+def test_deterministic_workspace():
+    # the deterministic backward adds one int32 counter per (key/value head, query tile)
+    p = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=64)
+    base = fa.fa_bwd_workspace_size(p)
+    tiles = 2 * -(-300 // 64)
+    pd = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=64, flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_bwd_workspace_size(pd) == base + (2 * tiles * 4 + 255) // 256 * 256
+    # the forward ignores the flag
+    assert fa.fa_fwd_workspace_size(pd) == fa.fa_fwd_workspace_size(p)
