@@ -421,6 +421,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         const long items = p.cu_q ? (long)pl.n_blocks * p.h_kv : (long)pl.n_blocks * pl.n_splits * p.h_kv * p.B;
         a.n_items = (int)items;
         a.n_ctas = (int)(items < sm_count() ? items : sm_count());
+        a.snake = (!p.cu_q && p.causal && !pl.unit_major) ? 1 : 0;
     }
     a.o = reinterpret_cast<__nv_bfloat16*>(o);
     a.lse = lse;

@@ -182,26 +182,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             seq = owner_sequence(p.cu_k, p.B, blk, kRows);
             blk -= p.cu_k[seq] / kRows + seq;
         } else {
-            const int hb = p.h_kv * p.B;
-            const int base = hb / a.n_bands, big = hb % a.n_bands;  // band sizes base + 1 (first big), base
-            const int big_ctas = big * (base + 1) * a.n_kvblocks;
-            int ub, unit0, r;
-            if (idx < big_ctas) {
-                ub = base + 1;
-                const int band = idx / (ub * a.n_kvblocks);
-                r = idx - band * ub * a.n_kvblocks;
-                unit0 = band * ub;
-            } else {
-                ub = base;
-                const int x = idx - big_ctas;
-                const int band = x / (ub * a.n_kvblocks);
-                r = x - band * ub * a.n_kvblocks;
-                unit0 = big * (base + 1) + band * ub;
-            }
-            const int unit = unit0 + r % ub;
+            int unit;
+            band_order(idx, p.h_kv * p.B, a.n_bands, a.n_kvblocks, unit, blk);
             g = unit % p.h_kv;
             seq = unit / p.h_kv;
-            blk = r / ub;
             if (rev) blk = a.n_kvblocks - 1 - blk;
         }
     }

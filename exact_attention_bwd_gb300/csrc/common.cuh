@@ -45,6 +45,31 @@ __device__ __forceinline__ int owner_sequence(const int32_t* cu, int nseq, int g
     return lo;
 }
 
+// Banded work order over hb (batch, key/value head) units of per_unit items each: the
+// units form n_bands bands of near-equal size (the first hb % n_bands bands one unit
+// larger), taken one after the other; inside a band the unit varies fastest, so the items
+// running at one time share few units' data in L2.  Gives the unit of item idx and the
+// item's index x within its unit.  n_bands = 1 is the plain unit-fastest order.
+__device__ __forceinline__ void band_order(int idx, int hb, int n_bands, int per_unit, int& unit, int& x) {
+    const int base = hb / n_bands, big = hb % n_bands;  // band sizes base + 1 (first big), base
+    const int big_items = big * (base + 1) * per_unit;
+    int ub, unit0, r;
+    if (idx < big_items) {
+        ub = base + 1;
+        const int band = idx / (ub * per_unit);
+        r = idx - band * ub * per_unit;
+        unit0 = band * ub;
+    } else {
+        ub = base;
+        const int y = idx - big_items;
+        const int band = y / (ub * per_unit);
+        r = y - band * ub * per_unit;
+        unit0 = big * (base + 1) + band * ub;
+    }
+    unit = unit0 + r % ub;
+    x = r / ub;
+}
+
 // Global view of one sequence's rows.
 struct SeqView {
     int b;        // batch index (dense) or sequence index (packed)

@@ -25,7 +25,8 @@
 // edge evaluate the mask per element.
 //
 // Scheduling is persistent: one CTA per SM walks the work items (a key/value head's two
-// query tiles, and a key range in split mode) in heaviest-first order with a grid stride;
+// query tiles, and a key range in split mode) in heaviest-first order with a grid stride
+// (alternating direction from round to round under a causal mask, see first_step);
 // a packed batch's items are found by binary search over its offsets (dew-flash-attn PyPI
 // page, "Packed sequences"), and idle items cost only their decode.  Barrier phases carry
 // over from item to item, so the next item's Q load and first S = Q K^T overlap the
@@ -138,6 +139,16 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
     return w;
 }
 
+// The persistent loop's items: a plain grid stride (idx = c, c + G, c + 2G, ...), or with
+// `snake` rounds that alternate direction across the grid (c, 2G - 1 - c, 2G + c, ...,
+// strides 2G - 1 - 2c and 1 + 2c in turn).  Under a causal mask the dense items come
+// heaviest first, so the CTA that takes the heaviest item of one round takes the lightest
+// of the next, which evens out the CTAs' totals that a plain stride leaves skewed toward
+// the low CTA indices.  The loop advances with step' = 2G - step.
+__device__ __forceinline__ int first_step(int snake) {
+    return snake ? 2 * ((int)gridDim.x - (int)blockIdx.x) - 1 : (int)gridDim.x;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fwd_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -202,7 +213,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             const uint32_t qbox = (uint32_t)(p.P * p.G) * 128u;  // bytes of one 64-col Q box
             int gt = 0, n_q = 0, k_issued = 0, v_issued = 0;    // key tiles, Q loads, copies issued
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+            for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
+             idx += step, step = 2 * (int)gridDim.x - step) {
                 const FwdItem w = fwd_item(a, idx);
                 if (!w.live || w.u1 <= w.u0) continue;
                 // the previous item's Q tiles are free once its S MMAs have completed
@@ -273,7 +285,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             uint32_t oc0 = 0, oc1 = 0;  // O tiles completed per query tile (o_full commits)
             int gt = 0, n_q = 0;        // key tiles, items consumed
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+            for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
+             idx += step, step = 2 * (int)gridDim.x - step) {
                 // the item's key-tile ranges are all the issue loop needs
                 int ta0, ta1, tb0, tb1, u0, u1;
                 {
@@ -401,7 +414,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const float c = p.scale_log2;
         uint32_t scount = 0, ocount = 0;  // S tiles and O tiles received (carried across items)
         bool ok = true;
-        for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+        for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
+             idx += step, step = 2 * (int)gridDim.x - step) {
         // only the loop bounds and the row's key band stay live across the key loop; the
         // epilogue decodes the item again (cheap) instead of holding it in registers
         int my_t0, my_t1, jlo, jhi;

@@ -37,6 +37,7 @@ struct FwdArgs {
                        // shapes, so they share K/V through L2) instead of heaviest first
     int n_items;       // work items (query blocks x kv heads [x batch x splits])
     int n_ctas;        // persistent CTAs of the d <= 128 kernel (at most one per SM)
+    int snake;         // their rounds alternate direction (items heaviest first: dense causal)
     __nv_bfloat16* o;  // [tokens, h_q, d]
     float* lse;        // [B, h_q, s_q] or [h_q, T_q]; may be null
     float* o_part;     // split mode: [n_splits, rows, d] fp32
