@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--decode-only", default=None, help="time one decode workload and exit")
     ap.add_argument("--decode-batch", type=int, default=None, help="batch override for --decode-only")
     ap.add_argument("--paged", action="store_true", help="--decode-only over a paged cache")
+    ap.add_argument("--fp8-only", default=None, help="time the e4m3 forward of one workload and exit")
     return ap.parse_args()
 
 
@@ -247,6 +248,8 @@ def run_ours(args):
         line["workloads"] = {n: measure_workload(dev, n) for n in SWEEP + OTHER}
         line["deterministic_bwd"] = {n: measure_workload(dev, n, bwd_flags=fa.FA_FLAG_DETERMINISTIC)
                                      for n in ("sweep_s8192_causal", "sweep_s2048", "gqa_window_causal", "varlen")}
+        line["e4m3_fwd"] = {n: measure_fp8(dev, n) for n in ("sweep_s8192_causal", "sweep_s8192", "sweep_s16384",
+                                                              "sweep_s2048", "decode_d128_sq64")}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = oracle_sample(w)
     if rank == 0:
@@ -383,6 +386,53 @@ def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0):
             "fwd_bwd_TFLOPS": round(3.5 * ff / ((mf + mb) * 1e-3) / 1e12, 1)}
 
 
+def measure_fp8(dev, name, steps=8, warmup=3):
+    """Forward with e4m3 inputs (same shapes; stored values N(0, 32^2) rounded to e4m3 with
+    per-(batch, kv head) descales): the whole fa_fwd call (V transpose + kernel) by CUDA
+    events, L2 flushed before every timed call; TFLOPS with the same FLOP convention."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    w = inputs.workload(name)
+    B, s_q, s_kv, h_q, h_kv, d = w["B"], w["s_q"], w["s_kv"], w["h_q"], w["h_kv"], w["d"]
+    sd = lambda t: inputs.seed_of(w["wid"], w["variant"], t)  # noqa: E731
+
+    def draw(seed, shape):
+        x = inputs.normal_bf16_torch(seed, shape, dev).float() * 32.0
+        return x.to(torch.float8_e4m3fn).view(torch.uint8)
+    q = draw(sd(inputs.Q), (B, s_q, h_q, d))
+    k = draw(sd(inputs.K), (B, s_kv, h_kv, d))
+    v = draw(sd(inputs.V), (B, s_kv, h_kv, d))
+    ds = tuple(torch.full((B * h_kv,), 1.0 / 32.0, dtype=torch.float32, device=dev) for _ in range(3))
+    kw = dict(causal=w["causal"], window=w["window"], softmax_scale=1.0 / math.sqrt(d), descale=ds)
+    o, lse, ws = fa.forward(q, k, v, **kw)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.fa_profile_enable(True)
+    ts, tk = [], []
+    for it in range(warmup + steps):
+        flush.zero_()
+        e0.record(stream)
+        fa.forward(q, k, v, **kw, out=o, lse=lse, workspace=ws)
+        e1.record(stream)
+        e1.synchronize()
+        if it >= warmup:
+            ts.append(e0.elapsed_time(e1))
+            rc, ms = fa.fa_profile_read("fwd")
+            if rc == 0:
+                tk.append(ms)
+    fa.fa_profile_enable(False)
+    if fa.device_status(ws) != 0:
+        raise RuntimeError("device status nonzero after the e4m3 forward")
+    ff = metrics.fwd_flops(dict(w, varlen=False))
+    mf = statistics.mean(ts)
+    del q, k, v, o, lse, ws
+    torch.cuda.empty_cache()
+    return {"fwd_ms": round(mf, 4), "fwd_TFLOPS": round(ff / (mf * 1e-3) / 1e12, 1),
+            "kernel_ms": round(statistics.mean(tk), 4) if tk else None,
+            "kernel_TFLOPS": round(ff / (statistics.mean(tk) * 1e-3) / 1e12, 1) if tk else None}
+
+
 SWEEP = [f"sweep_s{s}{c}" for s in (512, 1024, 2048, 4096, 8192, 16384) for c in ("", "_causal")]
 OTHER = ["gqa_window_causal", "gqa_window_2sided", "varlen"]
 
@@ -504,6 +554,12 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.fp8_only:
+        import torch
+        torch.cuda.set_device(0)
+        r = measure_fp8(torch.device("cuda", 0), args.fp8_only, steps=args.steps, warmup=args.warmup)
+        print(json.dumps({"workload": args.fp8_only, "dtype": "e4m3", **r}), flush=True)
+        return
     if args.decode_only:
         import torch
         torch.cuda.set_device(0)

@@ -26,6 +26,8 @@ FA_ERR_DEVICE_CHECK = 6
 FA_FLAG_VALIDATE_CU = 1
 FA_FLAG_NO_SPLIT = 2
 FA_FLAG_DETERMINISTIC = 4
+FA_DTYPE_BF16 = 0
+FA_DTYPE_E4M3 = 1
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_read_device_status",
            "fa_status_string", "fa_profile_enable", "fa_profile_read", "fa_version", "fa_fwd_noalloc")
@@ -44,6 +46,8 @@ class FaParams(ctypes.Structure):
         ("max_seqlen_q", ctypes.c_int), ("max_seqlen_k", ctypes.c_int), ("flags", ctypes.c_uint),
         ("seqused_k", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int),
         ("max_blocks_per_seq", ctypes.c_int), ("num_pages", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("q_descale", ctypes.c_void_p), ("k_descale", ctypes.c_void_p),
+        ("v_descale", ctypes.c_void_p),
     ]
 
 
@@ -156,7 +160,8 @@ def _ptr(t):
 
 
 def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None,
-                cu_k=None, flags=0, seqused_k=None, block_table=None, s_kv=None) -> FaParams:
+                cu_k=None, flags=0, seqused_k=None, block_table=None, s_kv=None, dtype=None, q_descale=None,
+                k_descale=None, v_descale=None) -> FaParams:
     """fa_params from tensor shapes: [B,S,H,D] dense or [T,H,D] packed (with cu_q / cu_k).
 
     With a block_table ([B, max_blocks_per_seq] int32), k is a page pool
@@ -185,6 +190,10 @@ def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sink
     p.max_seqlen_q = p.max_seqlen_k = 0
     p.flags = flags
     p.seqused_k = None if seqused_k is None else seqused_k.data_ptr()
+    p.dtype = FA_DTYPE_BF16 if dtype is None else int(dtype)
+    p.q_descale = None if q_descale is None else q_descale.data_ptr()
+    p.k_descale = None if k_descale is None else k_descale.data_ptr()
+    p.v_descale = None if v_descale is None else v_descale.data_ptr()
     if block_table is not None:
         p.block_table = block_table.data_ptr()
         p.page_size, p.num_pages = int(page_size), int(num_pages)
@@ -198,18 +207,25 @@ def _stream():
 
 
 def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None, cu_k=None,
-            flags=0, out=None, lse=None, workspace=None, seqused_k=None, block_table=None, s_kv=None):
-    """Runs fa_fwd on torch CUDA tensors; returns (o, lse, workspace)."""
+            flags=0, out=None, lse=None, workspace=None, seqused_k=None, block_table=None, s_kv=None,
+            descale=None):
+    """Runs fa_fwd on torch CUDA tensors; returns (o, lse, workspace).
+
+    uint8 q, k, v are e4m3 bytes (FA_DTYPE_E4M3); descale = (q, k, v) fp32 [B * h_kv]
+    factors or None (all 1).  The output is bf16 either way."""
     import torch
+    fp8 = q.dtype == torch.uint8
+    dq_, dk_, dv_ = descale if descale is not None else (None, None, None)
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
-                    cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv)
+                    cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv,
+                    dtype=FA_DTYPE_E4M3 if fp8 else FA_DTYPE_BF16, q_descale=dq_, k_descale=dk_, v_descale=dv_)
     nbytes = fa_fwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_fwd_workspace_size")
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     if lse is None:
         shape = (p.B, p.h_q, p.s_q) if cu_q is None else (p.h_q, p.s_q)
         lse = torch.empty(shape, dtype=torch.float32, device=q.device)

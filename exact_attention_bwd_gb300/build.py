@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libfa_gb300.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "fwd.cu", "fwd256.cu", "bwd.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd256.cu", "fwd_e4m3.cu", "bwd.cu", "decode.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 f"-I{INCLUDE}"]

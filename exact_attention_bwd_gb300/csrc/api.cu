@@ -64,6 +64,26 @@ bool encode_bhsd(CUtensorMap* m, const void* base, int d, int h, int s, int b, i
     return r == CUDA_SUCCESS;
 }
 
+// 4-D tensor map over one-byte (e4m3) elements, 128-byte swizzle.  dims innermost first;
+// strides in bytes for dims 1..3.  Out-of-range elements read as zero.
+bool encode_u8_4d(CUtensorMap* m, const void* base, const cuuint64_t dims[4], const cuuint64_t strides[3],
+                  const cuuint32_t box[4]) {
+    auto fn = encoder();
+    if (!fn) return false;
+    if (dims[2] == 0 || dims[3] == 0 || dims[0] == 0) {
+        std::memset(m, 0, sizeof(*m));  // never dereferenced: no tile of this tensor is loaded
+        return true;
+    }
+    cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+    cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+    cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), d, st, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------------------------------
 // profiling hooks
 // ------------------------------------------------------------------------------------------
@@ -113,6 +133,9 @@ fa_status normalise(const fa_params* in, Problem& p) {
     if ((a.cu_seqlens_q == nullptr) != (a.cu_seqlens_k == nullptr)) return FA_ERR_INVALID_ARG;
     if (a.window_left < -1 || a.window_right < -1) return FA_ERR_INVALID_ARG;
     if (a.d % 8 != 0 || a.d > 256) return FA_ERR_UNSUPPORTED;
+    if (a.dtype != FA_DTYPE_BF16 && a.dtype != FA_DTYPE_E4M3) return FA_ERR_INVALID_ARG;
+    // e4m3: dense d = 128 only
+    if (a.dtype == FA_DTYPE_E4M3 && (a.d != 128 || a.cu_seqlens_q || a.block_table)) return FA_ERR_UNSUPPORTED;
     std::memset(&p, 0, sizeof(p));
     p.B = a.B;
     p.s_q = a.s_q;
@@ -136,6 +159,7 @@ fa_status normalise(const fa_params* in, Problem& p) {
         p.T_q = a.s_q;
         p.T_k = a.s_kv;
     }
+    p.dtype = a.dtype;
     // KV-cache forms: a per-sequence used length, and a paged cache (dense q only)
     p.seqused_k = a.seqused_k;
     p.block_table = a.block_table;
@@ -164,6 +188,8 @@ struct FwdPlan {
     int n_blocks = 0, n_splits = 1, split_tiles = 0;
     int unit_major = 0;
     size_t part_rows = 0;  // rows of the split partials
+    int s_pad = 0;         // e4m3: keys per V^T row (s_kv rounded up to 16)
+    size_t off_vt = 0;     // e4m3: workspace offset of V^T
     size_t ws_bytes = kStatusBytes;
 };
 
@@ -192,7 +218,7 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
     if (p.B == 0 || rows_total == 0) return FA_OK;  // nothing to compute
     const bool dense = p.cu_q == nullptr;
     const int R = p.s_q * p.G;  // query rows per key/value head (dense)
-    if (dense && (p.d == 64 || p.d == 128 || p.d == 256) && R <= decode_rows_max(p.d)) {
+    if (dense && p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128 || p.d == 256) && R <= decode_rows_max(p.d)) {
         pl.path = FwdPath::kDecode;
         const int tiles = (p.s_kv + kDecodeKeys - 1) / kDecodeKeys;
         const long units = (long)p.B * p.h_kv;
@@ -243,6 +269,11 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
     } else {
         pl.n_blocks = p.T_q / rows_per_cta + p.B;
     }
+    if (p.dtype == FA_DTYPE_E4M3) {  // V^T [B][h_kv][d][s_pad] after the partials
+        pl.s_pad = (p.s_kv + 15) / 16 * 16;
+        pl.off_vt = pl.ws_bytes;
+        pl.ws_bytes += align256((size_t)p.B * p.h_kv * p.d * pl.s_pad);
+    }
     return FA_OK;
 }
 
@@ -260,6 +291,7 @@ fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     pl = BwdPlan();
     if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
     if (p.seqused_k || p.block_table) return FA_ERR_UNSUPPORTED;  // KV-cache forms: forward only
+    if (p.dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;      // e4m3: forward only
     const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
     const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
     if (p.B == 0 || (rows_total == 0 && keys_total == 0)) return FA_OK;
@@ -380,8 +412,8 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     // dimensions are the row within a page and the page
     const int kv_rows = p.block_table ? p.page_size : tokens_k;
     const int kv_outer = p.block_table ? in->num_pages : bdim;
-    if (!encode_bhsd(&tk, k, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box) ||
-        !encode_bhsd(&tv, v, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box))
+    if (p.dtype == FA_DTYPE_BF16 && (!encode_bhsd(&tk, k, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box) ||
+                                     !encode_bhsd(&tv, v, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box)))
         return FA_ERR_CUDA;
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     float* o_part = reinterpret_cast<float*>(ws + kStatusBytes);
@@ -409,9 +441,34 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         return cuda_status(e);
     }
 
-    CUtensorMap tq;
-    if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P)) return FA_ERR_CUDA;
     FwdArgs a{};
+    CUtensorMap tq;
+    if (p.dtype == FA_DTYPE_E4M3) {
+        // Q, K: [b][s][h][128] bytes; V^T: [b][h_kv][128][s_pad] bytes, built here from V
+        const cuuint64_t dq[4] = {128, (cuuint64_t)p.h_q, (cuuint64_t)p.s_q, (cuuint64_t)p.B};
+        const cuuint64_t sq[3] = {128, (cuuint64_t)p.h_q * 128, (cuuint64_t)p.s_q * p.h_q * 128};
+        const cuuint32_t bq[4] = {128, (cuuint32_t)p.G, (cuuint32_t)p.P, 1};
+        const cuuint64_t dk[4] = {128, (cuuint64_t)p.h_kv, (cuuint64_t)p.s_kv, (cuuint64_t)p.B};
+        const cuuint64_t sk[3] = {128, (cuuint64_t)p.h_kv * 128, (cuuint64_t)p.s_kv * p.h_kv * 128};
+        const cuuint32_t bk[4] = {128, 1, 128, 1};
+        uint8_t* vt = ws + pl.off_vt;
+        const cuuint64_t dv[4] = {(cuuint64_t)p.s_kv, 128, (cuuint64_t)p.h_kv, (cuuint64_t)p.B};
+        const cuuint64_t sv[3] = {(cuuint64_t)pl.s_pad, (cuuint64_t)pl.s_pad * 128, (cuuint64_t)pl.s_pad * 128 * p.h_kv};
+        const cuuint32_t bv[4] = {128, 128, 1, 1};
+        CUtensorMap tk8, tvt;
+        if (!encode_u8_4d(&tq, q, dq, sq, bq) || !encode_u8_4d(&tk8, k, dk, sk, bk) || !encode_u8_4d(&tvt, vt, dv, sv, bv))
+            return FA_ERR_CUDA;
+        cudaError_t e = launch_transpose_v_e4m3(reinterpret_cast<const uint8_t*>(v), vt, p.B, p.s_kv, p.h_kv, pl.s_pad,
+                                                st);
+        if (e != cudaSuccess) return FA_ERR_CUDA;
+        a.q_descale = in->q_descale;
+        a.k_descale = in->k_descale;
+        a.v_descale = in->v_descale;
+        tk = tk8;
+        tv = tvt;
+    } else if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P)) {
+        return FA_ERR_CUDA;
+    }
     a.p = p;
     a.n_blocks = pl.n_blocks;
     a.n_splits = pl.n_splits;
@@ -428,7 +485,9 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.status = status;
-    cudaError_t e = timed(kFwd, st, [&] { return launch_fwd(a, tq, tk, tv, st); });
+    cudaError_t e = timed(kFwd, st, [&] {
+        return p.dtype == FA_DTYPE_E4M3 ? launch_fwd_e4m3(a, tq, tk, tv, st) : launch_fwd(a, tq, tk, tv, st);
+    });
     if (e != cudaSuccess) return FA_ERR_CUDA;
     if (pl.n_splits > 1) {
         CombineArgs c{};

@@ -23,6 +23,7 @@ struct Problem {
     const int32_t* seqused_k; // [B] keys used per sequence, or null
     const int32_t* block_table;  // [B * max_blocks] pages of a paged K/V cache, or null
     int page_size, max_blocks;
+    int dtype;                // input element type (FA_DTYPE_*)
 };
 
 // ------------------------------------------------------------------------------------------
@@ -43,6 +44,11 @@ struct FwdArgs {
     float* o_part;     // split mode: [n_splits, rows, d] fp32
     float* lse_part;   // split mode: [n_splits, rows] fp32 (natural log, no sink)
     int* status;
+    // e4m3 inputs only: per (batch, kv head) factors that turn the stored values into the
+    // true ones (x = stored * descale), [B * h_kv] fp32 or null (= 1)
+    const float* q_descale;
+    const float* k_descale;
+    const float* v_descale;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -98,6 +104,11 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMa
                        cudaStream_t st);
 cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t st);
+cudaError_t launch_fwd_e4m3(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                            cudaStream_t st);
+// V [B, s_kv, h_kv, 128] e4m3 -> V^T [B, h_kv, 128, s_pad] (keys innermost, zero past s_kv)
+cudaError_t launch_transpose_v_e4m3(const uint8_t* v, uint8_t* vt, int B, int s_kv, int h_kv, int s_pad,
+                                    cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 int decode_rows_max(int d);                // query rows per key/value head the decode kernel takes

@@ -248,6 +248,30 @@ __device__ __forceinline__ void mma_ss_kk16_x4(uint32_t d_tmem, uint64_t a, uint
         : "memory");
 }
 
+// e4m3 operands (kind::f8f6f4), A and B K-major with 128-byte rows (one swizzle atom per
+// row: K = 128 one-byte elements), 4 steps of K = 32 (+32 B each)
+__device__ __forceinline__ void mma_f8_ss_k128(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 2; mov.b64 da, {ta, %4}; add.u32 tb, %5, 2; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 4; mov.b64 da, {ta, %4}; add.u32 tb, %5, 4; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 6; mov.b64 da, {ta, %4}; add.u32 tb, %5, 6; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
 // A K-major (16 KB chunks), B MN-major, 8 steps
 __device__ __forceinline__ void mma_ss_kmn16_x8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
     const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
@@ -502,6 +526,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// Instruction descriptor of kind::f8f6f4 with both operands e4m3 (format code 0), fp32
+// accumulator, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+    return (1u << 4)                          // D: f32
+           | (0u << 7)                        // A: e4m3
+           | (0u << 10)                       // B: e4m3
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.  The operand lives in 1024-byte
 // atoms of 8 rows x 128 bytes (the layout a TMA load with SWIZZLE_128B writes).
 //   K-major:  rows are M (or N) indices, 64 K-elements per row; `sbo` = bytes between
@@ -606,6 +640,15 @@ __device__ __forceinline__ float2 exp2_poly2(float2 x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four fp32 values to e4m3 (round to nearest even, saturating at +-448), a in the lowest
+// byte.  cvt...e4m3x2 puts its first source in the upper byte of the 16-bit result.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -205,3 +205,50 @@ def used_lengths(seed: int, B: int, s_kv: int) -> np.ndarray:
     if B > 2:
         n[1] = 0
     return n
+
+
+# ----------------------------------------------------------------------------------------------
+# e4m3 (fp8) inputs: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; largest finite
+# value 448, subnormal spacing 2^-9, no infinities (0x7F / 0xFF are NaN)
+# ----------------------------------------------------------------------------------------------
+
+def e4m3_bits(x) -> np.ndarray:
+    """Round to the nearest e4m3 value (ties to even), saturating at +-448; uint8 bit patterns."""
+    x = np.asarray(x, np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.clip(ex - 1, -6, 8)                 # binade of a (subnormals share the -6 spacing)
+    quantum = np.ldexp(1.0, e - 3)
+    m = np.minimum(np.round(a / quantum) * quantum, 448.0)   # np.round: ties to even
+    _, em = np.frexp(np.where(m > 0, m, 1.0))
+    em = em - 1
+    normal = m >= 2.0 ** -6
+    field = np.where(normal, em + 7, 0).astype(np.int64)
+    mant = np.where(normal, np.round((m / np.ldexp(1.0, em) - 1.0) * 8.0), np.round(m / 2.0 ** -9)).astype(np.int64)
+    bits = (field << 3) | mant
+    bits = np.where(m == 0, 0, bits)
+    sign = np.signbit(x)  # kept on values that round to zero (-0), as the hardware conversion does
+    return (bits | (sign.astype(np.int64) << 7)).astype(np.uint8)
+
+
+def e4m3_to_f64(bits) -> np.ndarray:
+    b = np.asarray(bits, np.uint8).astype(np.int64)
+    s = np.where(b & 0x80, -1.0, 1.0)
+    field = (b >> 3) & 0xF
+    mant = b & 0x7
+    val = np.where(field == 0, mant * 2.0 ** -9, (1.0 + mant / 8.0) * np.ldexp(1.0, field - 7))
+    val = np.where((b & 0x7F) == 0x7F, np.nan, val)
+    return s * val
+
+
+def normal_e4m3(seed: int, shape, spread: float = 32.0) -> np.ndarray:
+    """i.i.d. N(0, spread^2) draws rounded to e4m3 bit patterns (spread 32 keeps them well
+    inside the format's range while using its full precision)."""
+    return e4m3_bits(rng(seed).standard_normal(size=shape, dtype=np.float32).astype(np.float64) * spread)
+
+
+def descales(seed: int, B: int, h_kv: int, spread: float = 32.0) -> np.ndarray:
+    """Per-(batch, kv head) descale factors, fp32 [B * h_kv]: 1/spread times a seeded factor
+    in [0.5, 2], so the true inputs have unit-order magnitudes that differ across heads."""
+    f = np.exp2(rng(seed).uniform(-1.0, 1.0, size=B * h_kv))
+    return (f / spread).astype(np.float32)

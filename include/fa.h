@@ -73,6 +73,17 @@
  *    the logical cache length (at most max_blocks_per_seq * page_size); page_size must be
  *    a positive multiple of 128 (the page's builds ask for 256).  Table entries are read
  *    on the device and not checked.
+ *
+ * FP8 forward (vllm-project/flash-attention README, "FlashAttention-3 beta release":
+ * "FP8 forward"): with dtype = FA_DTYPE_E4M3, q, k and v hold e4m3 bytes (1 byte per
+ * element, same layouts) and the true inputs are q * q_descale[b * h_kv + g] (likewise k,
+ * v) for batch b and key/value head g; a NULL descale means 1.  S = Q K^T and O = P V run
+ * on the fp8 tensor cores with fp32 accumulation, P is rounded to e4m3 for the second
+ * product, o is written as bf16 and lse (fp32) is that of the descaled problem.  Dense
+ * tensors with d = 128 only (no cu_seqlens, no block_table; seqused_k, windows, causal and
+ * sinks are supported); anything else returns FA_ERR_UNSUPPORTED, and fa_bwd rejects the
+ * type.  The workspace also holds a transposed copy of v (h_kv * 128 bytes per key, keys
+ * padded to 16).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -95,6 +106,10 @@ typedef enum fa_status {
     FA_ERR_TIMEOUT = 5,      /* a kernel pipeline stalled and gave up (device status) */
     FA_ERR_DEVICE_CHECK = 6  /* a device-side argument check failed (device status) */
 } fa_status;
+
+/* Input element types */
+#define FA_DTYPE_BF16 0
+#define FA_DTYPE_E4M3 1
 
 /* Flags */
 #define FA_FLAG_VALIDATE_CU 1u  /* check cu_seqlens on the device; result in the status word */
@@ -124,6 +139,11 @@ typedef struct fa_params {
     int page_size;                  /* keys per page (block_table only) */
     int max_blocks_per_seq;         /* row stride of block_table */
     int num_pages;                  /* pages in each of the k and v pools */
+    /* Input element type (FA_DTYPE_*; 0 = bf16).  See the FP8 forward above. */
+    int dtype;
+    const float *q_descale;         /* FA_DTYPE_E4M3 only: device fp32 [B * h_kv] or NULL (= 1) */
+    const float *k_descale;
+    const float *v_descale;
 } fa_params;
 
 /* Bytes of workspace fa_fwd / fa_bwd need for these parameters (>= 256: the first

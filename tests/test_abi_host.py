@@ -170,3 +170,24 @@ def test_deterministic_workspace():
     assert fa.fa_bwd_workspace_size(pd) == base + (2 * tiles * 4 + 255) // 256 * 256
     # the forward ignores the flag
     assert fa.fa_fwd_workspace_size(pd) == fa.fa_fwd_workspace_size(p)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=fa.FA_DTYPE_E4M3, d=64), fa.FA_ERR_UNSUPPORTED),        # e4m3: d = 128 only
+    (dict(dtype=fa.FA_DTYPE_E4M3, d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=fa.FA_DTYPE_E4M3, cu_seqlens_q=0x2000, cu_seqlens_k=0x2000), fa.FA_ERR_UNSUPPORTED),  # dense only
+    (dict(dtype=fa.FA_DTYPE_E4M3, block_table=0x4000, page_size=128, max_blocks_per_seq=2, num_pages=4),
+     fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
+])
+def test_e4m3_forward_rejects(kw, code):
+    assert call_fwd(params(**kw)) == code
+
+
+def test_e4m3_workspace_and_backward():
+    # the forward's workspace holds V^T: B * h_kv * 128 bytes per key, keys padded to 16
+    p = params(dtype=fa.FA_DTYPE_E4M3, B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=128)
+    s_pad = -(-300 // 16) * 16
+    assert fa.fa_fwd_workspace_size(p) == 256 + (2 * 2 * 128 * s_pad + 255) // 256 * 256
+    assert call_fwd(p, ws_bytes=300) == fa.FA_ERR_WORKSPACE
+    assert call_bwd(p) == fa.FA_ERR_UNSUPPORTED
