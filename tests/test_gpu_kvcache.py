@@ -174,3 +174,34 @@ def test_paged_equals_dense():
     o_d, lse_d = gpu_of(dense)
     assert np.array_equal(o_p, o_d)
     assert np.array_equal(lse_p, lse_d)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_paged_decode_full_size(d):
+    """The decode workload's size (B=64, s_kv=32768, h_q=32, h_kv=8, s_q=1) as a paged cache of
+    256-key pages in seeded random order with partly filled slots: sampled sequences (the
+    first, the last and two more, all heads) against the oracle on their gathered pages."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    B, s_kv, h_q, h_kv, ps = 64, 32768, 32, 8, 256
+    dev = torch.device("cuda", 0)
+    sd = lambda t: inputs.seed_of(WID, 900 + d, t)  # noqa: E731
+    mb = s_kv // ps
+    table = inputs.page_table(sd(TABLE), B, mb, B * mb)
+    used = inputs.used_lengths(sd(USED), B, s_kv)
+    q = inputs.normal_bf16_torch(sd(inputs.Q), (B, 1, h_q, d), dev)
+    k = inputs.normal_bf16_torch(sd(inputs.K), (B * mb, ps, h_kv, d), dev)
+    v = inputs.normal_bf16_torch(sd(inputs.V), (B * mb, ps, h_kv, d), dev)
+    o, lse, ws = fa.forward(q, k, v, causal=True, softmax_scale=d ** -0.5, seqused_k=torch.from_numpy(used).to(dev),
+                            block_table=torch.from_numpy(table).to(dev), s_kv=s_kv)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK
+    for b in (0, 1, 37, B - 1):
+        n = int(used[b])
+        pages = torch.from_numpy(table[b, : -(-n // ps)].astype(np.int64)).to(dev)
+        kb = k.index_select(0, pages).reshape(-1, h_kv, d)[:n]
+        vb = v.index_select(0, pages).reshape(-1, h_kv, d)[:n]
+        tof64 = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+        ro, rl, _ = oracle.fwd(tof64(q[b:b + 1]), tof64(kb)[None], tof64(vb)[None], scale=d ** -0.5, causal=True)
+        check(f"O[{b}]", from_dev(o[b:b + 1]), ro)
+        check_lse(f"LSE[{b}]", lse[b:b + 1].cpu().numpy().astype(np.float64), rl)
