@@ -241,10 +241,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     const uint32_t tmem = s.tmem_base;
 
     // registers: 512 x 128 at launch, redistributed per warp group (the change is made at
-    // the top of each group's branch): producer/MMA 64, the two compute groups 160, the
-    // dQ group 128 (128*64 + 256*160 + 128*128 = 65536)
+    // the top of each group's branch): the two compute groups 160; d = 128: producer/MMA 48
+    // and the dQ group, which holds a whole 128-row dQ^T column in registers, 144
+    // (128*48 + 256*160 + 128*144 = 65536); d = 64 (no dQ group work): 64 and 128.  Splits
+    // that leave a group short make it spill, which costs more than the registers save.
     if (warp >= 12) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 128;\n" ::: "memory");
+        if constexpr (D == 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 144;\n" ::: "memory");
+        else asm volatile("setmaxnreg.dec.sync.aligned.u32 128;\n" ::: "memory");
         // ================= dQ group: drains dQ^T_i and reduces it into the workspace =================
         if constexpr (C::DQ_T) {
             const int dcol = ((warp & 3) << 5) | lane;  // TMEM lane = column d of dQ
@@ -279,7 +282,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             }
         }
     } else if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+    if constexpr (D == 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 48;\n" ::: "memory");
+    else asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && nsteps > 0) {

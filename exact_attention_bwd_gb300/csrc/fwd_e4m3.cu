@@ -136,9 +136,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     // registers: 384 x 168 at launch; the producer/MMA group hands part of its share to
-    // the softmax groups (128 x 88 + 256 x 208 = 64512)
+    // the softmax groups (128 x 56 + 256 x 224 = 64512)
     if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         }
     }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
         // ================= softmax: one thread per row =================
         const int k = (warp - 4) >> 2;           // query tile
         const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
