@@ -47,7 +47,7 @@ class FaParams(ctypes.Structure):
         ("seqused_k", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int),
         ("max_blocks_per_seq", ctypes.c_int), ("num_pages", ctypes.c_int),
         ("dtype", ctypes.c_int), ("q_descale", ctypes.c_void_p), ("k_descale", ctypes.c_void_p),
-        ("v_descale", ctypes.c_void_p),
+        ("v_descale", ctypes.c_void_p), ("seqused_q", ctypes.c_void_p),
     ]
 
 
@@ -161,12 +161,12 @@ def _ptr(t):
 
 def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None,
                 cu_k=None, flags=0, seqused_k=None, block_table=None, s_kv=None, dtype=None, q_descale=None,
-                k_descale=None, v_descale=None) -> FaParams:
+                k_descale=None, v_descale=None, seqused_q=None) -> FaParams:
     """fa_params from tensor shapes: [B,S,H,D] dense or [T,H,D] packed (with cu_q / cu_k).
 
     With a block_table ([B, max_blocks_per_seq] int32), k is a page pool
     [num_pages, page_size, h_kv, d] and s_kv (the logical cache length) must be given.
-    seqused_k: int32 [B] keys used per sequence, or None."""
+    seqused_q / seqused_k: int32 [B] queries / keys used per sequence, or None."""
     if block_table is not None:
         B, s_q, h_q, d = q.shape
         num_pages, page_size, h_kv, _ = k.shape
@@ -190,6 +190,7 @@ def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sink
     p.max_seqlen_q = p.max_seqlen_k = 0
     p.flags = flags
     p.seqused_k = None if seqused_k is None else seqused_k.data_ptr()
+    p.seqused_q = None if seqused_q is None else seqused_q.data_ptr()
     p.dtype = FA_DTYPE_BF16 if dtype is None else int(dtype)
     p.q_descale = None if q_descale is None else q_descale.data_ptr()
     p.k_descale = None if k_descale is None else k_descale.data_ptr()
@@ -208,7 +209,7 @@ def _stream():
 
 def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None, cu_k=None,
             flags=0, out=None, lse=None, workspace=None, seqused_k=None, block_table=None, s_kv=None,
-            descale=None):
+            descale=None, seqused_q=None):
     """Runs fa_fwd on torch CUDA tensors; returns (o, lse, workspace).
 
     uint8 q, k, v are e4m3 bytes (FA_DTYPE_E4M3); descale = (q, k, v) fp32 [B * h_kv]
@@ -218,7 +219,8 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
     dq_, dk_, dv_ = descale if descale is not None else (None, None, None)
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
                     cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv,
-                    dtype=FA_DTYPE_E4M3 if fp8 else FA_DTYPE_BF16, q_descale=dq_, k_descale=dk_, v_descale=dv_)
+                    dtype=FA_DTYPE_E4M3 if fp8 else FA_DTYPE_BF16, q_descale=dq_, k_descale=dk_, v_descale=dv_,
+                    seqused_q=seqused_q)
     nbytes = fa_fwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_fwd_workspace_size")
@@ -236,11 +238,11 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
 
 
 def backward(q, k, v, o, lse, dout, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None,
-             cu_q=None, cu_k=None, flags=0, workspace=None, grads=None):
+             cu_q=None, cu_k=None, flags=0, workspace=None, grads=None, seqused_q=None, seqused_k=None):
     """Runs fa_bwd on torch CUDA tensors; returns (dq, dk, dv, dsinks, workspace)."""
     import torch
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
-                    cu_k=cu_k, flags=flags)
+                    cu_k=cu_k, flags=flags, seqused_q=seqused_q, seqused_k=seqused_k)
     nbytes = fa_bwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_bwd_workspace_size")

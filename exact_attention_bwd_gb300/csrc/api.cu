@@ -161,6 +161,7 @@ fa_status normalise(const fa_params* in, Problem& p) {
     }
     p.dtype = a.dtype;
     // KV-cache forms: a per-sequence used length, and a paged cache (dense q only)
+    p.seqused_q = a.seqused_q;
     p.seqused_k = a.seqused_k;
     p.block_table = a.block_table;
     if (a.block_table) {
@@ -290,7 +291,7 @@ struct BwdPlan {
 fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     pl = BwdPlan();
     if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
-    if (p.seqused_k || p.block_table) return FA_ERR_UNSUPPORTED;  // KV-cache forms: forward only
+    if (p.block_table) return FA_ERR_UNSUPPORTED;  // paged caches: forward only
     if (p.dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;      // e4m3: forward only
     const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
     const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;

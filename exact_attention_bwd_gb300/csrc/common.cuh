@@ -94,7 +94,8 @@ __device__ __forceinline__ SeqView seq_view(const Problem& p, int b) {
         v.nk = p.s_kv;
         v.tma_b = b;
     }
-    // a cache slot filled only up to seqused_k[b]: the rest of the slot is invisible
+    // a slot filled only up to seqused_q[b] / seqused_k[b]: the rest of the slot takes no part
+    if (p.seqused_q) v.nq = min(v.nq, max(0, p.seqused_q[b]));
     if (p.seqused_k) v.nk = min(v.nk, max(0, p.seqused_k[b]));
     return v;
 }

@@ -83,12 +83,12 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
     const int unit = blockIdx.x / a.n_splits;
     const int g = unit % p.h_kv, b = unit / p.h_kv;
     const int R = p.s_q * p.G;
-    const SeqView sv = seq_view(p, b);  // dense; nk < s_kv when the cache slot is partly filled
-    const Band band{sv.nk - p.s_q, p.left, p.right, sv.nk};
+    const SeqView sv = seq_view(p, b);  // dense; nq, nk below s_q, s_kv when the slot is partly filled
+    const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
 
     int j_begin = split * a.split_keys, j_end = min(sv.nk, (split + 1) * a.split_keys);
     j_begin = max(j_begin, band.lo(0));
-    j_end = min(j_end, band.hi(p.s_q - 1) + 1);
+    j_end = sv.nq > 0 ? min(j_end, band.hi(sv.nq - 1) + 1) : 0;
     const int t_begin = j_begin / BK;
     const int n_tiles = j_end > j_begin ? (j_end - 1) / BK + 1 - t_begin : 0;
 

@@ -20,6 +20,7 @@ struct Problem {
     const int32_t* cu_q;      // [B+1] or null (dense)
     const int32_t* cu_k;
     int T_q, T_k;             // packed token counts (varlen)
+    const int32_t* seqused_q; // [B] queries used per sequence, or null
     const int32_t* seqused_k; // [B] keys used per sequence, or null
     const int32_t* block_table;  // [B * max_blocks] pages of a paged K/V cache, or null
     int page_size, max_blocks;

@@ -58,14 +58,17 @@
  *  - Supported: bf16; head dim d in {64, 128, 256} for the forward, {64, 128} for
  *    the backward; h_q / h_kv <= 128.  Anything else returns FA_ERR_UNSUPPORTED.
  *
- * KV-cache forms (forward only; fa_bwd returns FA_ERR_UNSUPPORTED when either is set):
- *  - seqused_k (fa4-jax PyPI page, "Varlen semantics": optional seqused_k limits each
- *    slot to its first seqused[b] tokens, the cache case where slots are larger than
- *    what is filled): sequence b uses only its first seqused_k[b] keys of its slot (s_kv
- *    for dense tensors, cu_seqlens_k[b+1] - cu_seqlens_k[b] for packed ones); the other
- *    keys are invisible and the bottom-right alignment uses the used length.  Values are
- *    clamped to [0, slot].
- *  - block_table (vllm-project/flash-attention README, flash_attn_with_kvcache docstring:
+ * Partly filled slots and paged caches:
+ *  - seqused_q / seqused_k (fa4-jax PyPI page, "Varlen semantics": optional seqused_q /
+ *    seqused_k limit each slot to its first seqused[b] tokens, the cache case where slots
+ *    are larger than what is filled): sequence b uses only its first seqused_q[b] queries
+ *    and seqused_k[b] keys of its slot (s_q / s_kv for dense tensors, the cu_seqlens
+ *    difference for packed ones); the bottom-right alignment uses the used lengths, unused
+ *    keys are invisible, and the outputs of unused query rows (O, LSE, dQ) and the dK, dV
+ *    rows of unused keys are not written (unspecified).  Values are clamped to [0, slot].
+ *    Forward and backward.
+ *  - block_table (forward only; fa_bwd returns FA_ERR_UNSUPPORTED; vllm-project/flash-attention
+ *    README, flash_attn_with_kvcache docstring ("Does not support backward pass"):
  *    a paged cache of shape (num_blocks, page_block_size, nheads_k, headdim) addressed
  *    through block_table (batch_size, max_num_blocks_per_seq) int32): dense q only; k and
  *    v are page pools [num_pages, page_size, h_kv, d] and key j of sequence b is row
@@ -133,7 +136,7 @@ typedef struct fa_params {
     const int32_t *cu_seqlens_k;    /* device int32 [B+1]; required iff cu_seqlens_q */
     int max_seqlen_q, max_seqlen_k; /* optional hints (0 = unknown); never needed */
     unsigned flags;                 /* FA_FLAG_* */
-    /* KV-cache forms (forward only; see above).  Zero / NULL = not used. */
+    /* Partly filled slots and paged caches (see above).  Zero / NULL = not used. */
     const int32_t *seqused_k;       /* device int32 [B], or NULL */
     const int32_t *block_table;     /* device int32 [B * max_blocks_per_seq], or NULL */
     int page_size;                  /* keys per page (block_table only) */
@@ -144,6 +147,7 @@ typedef struct fa_params {
     const float *q_descale;         /* FA_DTYPE_E4M3 only: device fp32 [B * h_kv] or NULL (= 1) */
     const float *k_descale;
     const float *v_descale;
+    const int32_t *seqused_q;       /* device int32 [B], or NULL (see partly filled slots) */
 } fa_params;
 
 /* Bytes of workspace fa_fwd / fa_bwd need for these parameters (>= 256: the first

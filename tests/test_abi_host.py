@@ -154,11 +154,14 @@ def test_paged_cache_is_planned():
     assert call_fwd(p, ws_bytes=16) == fa.FA_ERR_WORKSPACE
 
 
-def test_backward_rejects_cache_forms():
-    assert call_bwd(params(seqused_k=0x4000)) == fa.FA_ERR_UNSUPPORTED
+def test_backward_cache_forms():
+    # partly filled slots are supported by the backward, paged caches are not
+    assert fa.fa_bwd_workspace_size(params(seqused_k=0x4000, seqused_q=0x5000)) > 256
+    assert call_bwd(params(seqused_k=0x4000), ws_bytes=16) == fa.FA_ERR_WORKSPACE
     assert call_bwd(params(block_table=0x4000, page_size=128, max_blocks_per_seq=2, num_pages=4)) == \
         fa.FA_ERR_UNSUPPORTED
-    assert fa.fa_bwd_workspace_size(params(seqused_k=0x4000)) == 0
+    assert fa.fa_bwd_workspace_size(params(block_table=0x4000, page_size=128, max_blocks_per_seq=2,
+                                           num_pages=4)) == 0
 
 
 def test_deterministic_workspace():

@@ -205,3 +205,81 @@ def test_paged_decode_full_size(d):
         ro, rl, _ = oracle.fwd(tof64(q[b:b + 1]), tof64(kb)[None], tof64(vb)[None], scale=d ** -0.5, causal=True)
         check(f"O[{b}]", from_dev(o[b:b + 1]), ro)
         check_lse(f"LSE[{b}]", lse[b:b + 1].cpu().numpy().astype(np.float64), rl)
+
+
+def _packed_oracle(w, used_q, used_k, bwd):
+    """Oracle of a dense batch restricted to its first used_q[b] queries and used_k[b] keys:
+    the packed batch of those rows (P2 "Varlen semantics"); returns per-batch lists."""
+    B = w["B"]
+    cat = lambda x, n: np.concatenate([x[b, :n[b]] for b in range(B)])  # noqa: E731
+    q, k, v, do = (inputs.bf16_to_f64(w[t]) for t in ("q", "k", "v", "dout"))
+    cu_q, cu_k = inputs.cu_seqlens(used_q), inputs.cu_seqlens(used_k)
+    kw = dict(scale=w["scale"], causal=w["causal"], window=w["window"], cu_q=cu_q, cu_k=cu_k,
+              sinks=None if w["sinks"] is None else w["sinks"].astype(np.float64))
+    args = (cat(q, used_q), cat(k, used_k), cat(v, used_k))
+    o, lse, _ = oracle.fwd(*args, **kw)
+    out = dict(o=o, lse=lse, cu_q=cu_q, cu_k=cu_k)
+    if bwd:
+        out["dq"], out["dk"], out["dv"], out["ds"] = oracle.bwd(*args, cat(do, used_q), **kw)
+    return out
+
+
+@pytest.mark.parametrize("d,causal,window,sinks", [(64, True, (-1, -1), False), (128, True, (-1, -1), True),
+                                                   (128, False, (90, 40), True), (64, False, (-1, -1), False)])
+def test_seqused_q_and_k_forward_backward(d, causal, window, sinks):
+    """Partly filled query and key slots, forward and backward: used rows of O, LSE, dQ and
+    used keys of dK, dV against the oracle on the packed batch of the used rows."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    B, s_q, s_kv = 4, 300, 450
+    w = inputs.make(dict(wid=WID, variant=40 + d + int(causal) + 2 * int(sinks), B=B, s_q=s_q, s_kv=s_kv, h_q=8,
+                         h_kv=2, d=d, causal=causal, window=window, sinks=sinks, varlen=False))
+    used_q = inputs.used_lengths(inputs.seed_of(WID, 60 + d, USED), B, s_q)
+    used_k = inputs.used_lengths(inputs.seed_of(WID, 61 + d, USED), B, s_kv)
+    used_q[2], used_k[2] = 0, 17   # an empty query slot, and
+    used_q[3], used_k[3] = 250, 0  # queries against an empty key slot
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    tq, tk, tv, tdo = (to_dev(w[t]) for t in ("q", "k", "v", "dout"))
+    sk = None if w["sinks"] is None else dev(w["sinks"])
+    kw = dict(causal=causal, window=window, softmax_scale=w["scale"], sinks=sk, seqused_q=dev(used_q),
+              seqused_k=dev(used_k))
+    o, lse, ws = fa.forward(tq, tk, tv, **kw)
+    dq, dk, dv, ds, ws2 = fa.backward(tq, tk, tv, o, lse, tdo, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK and fa.device_status(ws2) == fa.FA_OK
+    ref = _packed_oracle(w, used_q, used_k, bwd=True)
+    o, lse, dq, dk, dv = from_dev(o), lse.cpu().numpy().astype(np.float64), from_dev(dq), from_dev(dk), from_dev(dv)
+    for b in range(B):
+        q0, q1 = ref["cu_q"][b], ref["cu_q"][b + 1]
+        k0, k1 = ref["cu_k"][b], ref["cu_k"][b + 1]
+        check(f"O[{b}]", o[b, :used_q[b]], ref["o"][q0:q1])
+        check_lse(f"LSE[{b}]", lse[b, :, :used_q[b]], ref["lse"][:, q0:q1])
+        check(f"dQ[{b}]", dq[b, :used_q[b]], ref["dq"][q0:q1])
+        check(f"dK[{b}]", dk[b, :used_k[b]], ref["dk"][k0:k1])
+        check(f"dV[{b}]", dv[b, :used_k[b]], ref["dv"][k0:k1])
+    if sinks:
+        err = float(np.abs(ds.cpu().numpy() - ref["ds"]).max())
+        assert err <= 2e-2 * max(1.0, float(np.abs(ref["ds"]).max()))
+
+
+def test_seqused_q_decode():
+    """Few query rows per key/value head (the CUDA-core decode kernel) with partly filled
+    query slots: the bottom-right alignment follows the used query count."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    B, s_q, s_kv = 4, 2, 2000
+    w = inputs.make(dict(wid=WID, variant=77, B=B, s_q=s_q, s_kv=s_kv, h_q=8, h_kv=2, d=128, causal=True,
+                         window=(-1, -1), sinks=False, varlen=False))
+    used_q = np.array([2, 1, 0, 2], np.int32)
+    used_k = np.array([2000, 1500, 900, 0], np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    o, lse, ws = fa.forward(to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"]), causal=True, softmax_scale=w["scale"],
+                            seqused_q=dev(used_q), seqused_k=dev(used_k))
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK
+    ref = _packed_oracle(w, used_q, used_k, bwd=False)
+    o, lse = from_dev(o), lse.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        q0, q1 = ref["cu_q"][b], ref["cu_q"][b + 1]
+        check(f"O[{b}]", o[b, :used_q[b]], ref["o"][q0:q1])
+        check_lse(f"LSE[{b}]", lse[b, :, :used_q[b]], ref["lse"][:, q0:q1])
