@@ -445,12 +445,18 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     pf[cc + 3] = ex2(fmaf(__uint_as_float(sr[cc + 3]), c, -l4.w));
                 }
                 if (!interior) {
+                    // the query positions whose band holds key j form one interval
+                    // [i_min, i_max] (lo and hi are monotone in the position); in this tile's
+                    // packed columns (column = G (i - s0) + head) it is the column range
+                    // [G (i_min - s0), G (i_max + 1 - s0)), taken relative to this group's
+                    // first column
+                    const int i_min = p.right >= 0 ? j - band.off - p.right : 0;
+                    const int i_max = j >= sv.nk ? i_min - 1 : (p.left >= 0 ? j - band.off + p.left : sv.nq - 1);
+                    const int c_lo = (i_min - s0) * p.G - 64 * cg;
+                    const int c_hi = (i_max + 1 - s0) * p.G - 64 * cg;
 #pragma unroll
-                    for (int cc = 0; cc < 64; ++cc) {
-                        const int qr = 64 * cg + cc;
-                        const int iq = s0 + qr / p.G;
-                        if (j > band.hi(iq) || j < band.lo(iq)) pf[cc] = 0.f;
-                    }
+                    for (int cc = 0; cc < 64; ++cc)
+                        if (cc < c_lo || cc >= c_hi) pf[cc] = 0.f;
                 }
                 uint32_t pk[32];
 #pragma unroll
