@@ -608,30 +608,42 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
         return;
     }
     const SeqView sv = seq_view(p, seq);
-    for (int rr = 0; rr < 32; ++rr) {
-        const int r = warp * 32 + rr;
+    // a warp takes its 32 rows RPI at a time: LPR lanes per row, 16 bytes (8 elements) of O
+    // and dO each, so every load instruction moves whole 128-byte lines
+    constexpr int LPR = D / 8, RPI = 32 / LPR;
+    const int sub = lane / LPR, ch = lane % LPR;
+#pragma unroll 4
+    for (int rr = 0; rr < 32; rr += RPI) {
+        const int r = warp * 32 + rr + sub;
         const int i = t * p.P + r / p.G;
         const int h = g * p.G + r % p.G;
         const bool valid = r < p.P * p.G && i < sv.nq;
-        float dsum = 0.f, l2 = INFINITY, sterm = 0.f;
+        float dsum = 0.f;
+        long tok = 0;
         if (valid) {
-            const long tok = token_row(p, sv, i);
-            const __nv_bfloat16* orow = a.o + (tok * p.h_q + h) * D;
-            const __nv_bfloat16* drow = a.dout + (tok * p.h_q + h) * D;
-            for (int c = lane * 2; c < D; c += 64) {
-                const uint32_t ov = *reinterpret_cast<const uint32_t*>(orow + c);
-                const uint32_t dv = *reinterpret_cast<const uint32_t*>(drow + c);
-                dsum = fmaf(bf16_lo(ov), bf16_lo(dv), dsum);
-                dsum = fmaf(bf16_hi(ov), bf16_hi(dv), dsum);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-            const float lse = a.lse[lse_index(p, sv, i, h)];
-            l2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-            // d(sum O.dO)/d(sink_h) = - exp(sink_h - LSE_i) * D_i, summed per head later
-            if (p.sinks && lse > -INFINITY) sterm = -__expf(p.sinks[h] - lse) * dsum;
+            tok = token_row(p, sv, i);
+            const uint4 ov = *reinterpret_cast<const uint4*>(a.o + (tok * p.h_q + h) * D + 8 * ch);
+            const uint4 dv = *reinterpret_cast<const uint4*>(a.dout + (tok * p.h_q + h) * D + 8 * ch);
+            dsum = fmaf(bf16_lo(ov.x), bf16_lo(dv.x), dsum);
+            dsum = fmaf(bf16_hi(ov.x), bf16_hi(dv.x), dsum);
+            dsum = fmaf(bf16_lo(ov.y), bf16_lo(dv.y), dsum);
+            dsum = fmaf(bf16_hi(ov.y), bf16_hi(dv.y), dsum);
+            dsum = fmaf(bf16_lo(ov.z), bf16_lo(dv.z), dsum);
+            dsum = fmaf(bf16_hi(ov.z), bf16_hi(dv.z), dsum);
+            dsum = fmaf(bf16_lo(ov.w), bf16_lo(dv.w), dsum);
+            dsum = fmaf(bf16_hi(ov.w), bf16_hi(dv.w), dsum);
         }
-        if (lane == 0) {
+        // sum over the row's LPR lanes (all lanes take part: rows differ in validity)
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+        if (ch == 0) {
+            float l2 = INFINITY, sterm = 0.f;
+            if (valid) {
+                const float lse = a.lse[lse_index(p, sv, i, h)];
+                l2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+                // d(sum O.dO)/d(sink_h) = - exp(sink_h - LSE_i) * D_i, summed per head later
+                if (p.sinks && lse > -INFINITY) sterm = -__expf(p.sinks[h] - lse) * dsum;
+            }
             a.delta_t[trow + r] = valid ? dsum : 0.f;
             a.lse2_t[trow + r] = l2;
             if (a.sink_t) a.sink_t[trow + r] = sterm;
