@@ -142,3 +142,16 @@ def test_fp8_full_size_sampled():
         ro, rl, emu = reference(sub)
         judge(o[b:b + 1, -rows:], ro, emu)
         check_lse("LSE", lse[b:b + 1, :, -rows:], rl)
+
+
+def test_fp8_cache_shape_sampled():
+    """The chunked-prefill cache shape in e4m3 (s_q=64 against s_kv=32768, h_q=32, h_kv=8,
+    causal; split keys with the LSE combine), batch entries 0 and 7 of 8 against the oracle."""
+    c = case(51, B=8, s_q=64, s_kv=32768, h_q=32, h_kv=8, causal=True)
+    o, lse = run_gpu(c)
+    for b in (0, 7):
+        sub = dict(c, B=1, q=c["q"][b:b + 1], k=c["k"][b:b + 1], v=c["v"][b:b + 1],
+                   descale=tuple(x.reshape(8, 8)[b:b + 1].ravel() for x in c["descale"]))
+        ro, rl, emu = reference(sub)
+        judge(o[b:b + 1], ro, emu)
+        check_lse("LSE", lse[b:b + 1], rl)
