@@ -216,6 +216,11 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
     factors or None (all 1).  The output is bf16 either way."""
     import torch
     fp8 = q.dtype == torch.uint8
+    want = torch.uint8 if fp8 else torch.bfloat16
+    if q.dtype != want or k.dtype != want or v.dtype != want:
+        raise TypeError(f"q, k, v must all be bfloat16 or all uint8 (e4m3 bytes); got {q.dtype}, {k.dtype}, {v.dtype}")
+    if descale is not None and not fp8:
+        raise TypeError("descale factors apply to e4m3 (uint8) inputs only")
     dq_, dk_, dv_ = descale if descale is not None else (None, None, None)
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
                     cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv,
@@ -241,6 +246,9 @@ def backward(q, k, v, o, lse, dout, *, causal=False, window=(-1, -1), softmax_sc
              cu_q=None, cu_k=None, flags=0, workspace=None, grads=None, seqused_q=None, seqused_k=None):
     """Runs fa_bwd on torch CUDA tensors; returns (dq, dk, dv, dsinks, workspace)."""
     import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"the backward takes bfloat16 tensors; {name} is {t.dtype}")
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
                     cu_k=cu_k, flags=flags, seqused_q=seqused_q, seqused_k=seqused_k)
     nbytes = fa_bwd_workspace_size(p)

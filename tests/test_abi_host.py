@@ -194,3 +194,15 @@ def test_e4m3_workspace_and_backward():
     assert fa.fa_fwd_workspace_size(p) == 256 + (2 * 2 * 128 * s_pad + 255) // 256 * 256
     assert call_fwd(p, ws_bytes=300) == fa.FA_ERR_WORKSPACE
     assert call_bwd(p) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_binding_checks_dtypes():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    k8 = torch.zeros(1, 8, 2, 128, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        fa.forward(q, k8, k8)              # mixed bf16 / e4m3
+    with pytest.raises(TypeError):
+        fa.forward(q, q, q, descale=(None, None, None))
+    with pytest.raises(TypeError):
+        fa.backward(k8, k8, k8, q, None, q)
