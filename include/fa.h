@@ -55,8 +55,11 @@
  *    ABI and no kernel traps: a kernel whose pipeline stalls gives up after a time
  *    limit and records FA_ERR_TIMEOUT in the workspace status word, which
  *    fa_read_device_status reports.
- *  - Supported: bf16; head dim d in {64, 128, 256} for the forward, {64, 128} for
- *    the backward; h_q / h_kv <= 128.  Anything else returns FA_ERR_UNSUPPORTED.
+ *  - Supported: bf16 (and e4m3 for the forward at d = 128, see below); head dim d in
+ *    {64, 128, 256} for the forward, {64, 128} for the backward; h_q / h_kv <= 128.
+ *    Anything else returns FA_ERR_UNSUPPORTED.
+ *  - Zero-initialise fa_params (memset or `= {0}`): every optional field then means
+ *    "not used".
  *
  * Partly filled slots and paged caches:
  *  - seqused_q / seqused_k (fa4-jax PyPI page, "Varlen semantics": optional seqused_q /
@@ -120,7 +123,10 @@ typedef enum fa_status {
 /* backward: bitwise-reproducible results.  dQ is summed over key blocks in a fixed order
  * (descending key block) instead of in arrival order; the workspace grows by 4 bytes per
  * (query tile, key/value head).  The deterministic backward option of the
- * vllm-project/flash-attention README (changelog 2.4). */
+ * vllm-project/flash-attention README (changelog 2.4).  A key block's CTA waits (bounded,
+ * like every wait: FA_ERR_TIMEOUT) for the later blocks' contributions, which the launch
+ * puts at lower CTA indices; slower than the default, markedly so without a causal mask.
+ * The sink gradient is summed in a fixed order with or without the flag. */
 #define FA_FLAG_DETERMINISTIC 4u
 
 typedef struct fa_params {
