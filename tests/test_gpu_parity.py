@@ -166,3 +166,19 @@ def test_d256_chunked_prefill_split():
 
 def test_d256_packed_forward():
     compare(make_case(110, 10, h_q=4, h_kv=4, d=256, causal=True, lengths=[17, 283, 0, 1, 129]), bwd=False)
+
+
+@pytest.mark.parametrize("h_q,h_kv,d,causal", [(128, 1, 64, True), (128, 2, 128, False), (32, 2, 128, True),
+                                               (24, 8, 64, False)])
+def test_large_groups(h_q, h_kv, d, causal):
+    """Group sizes up to the largest supported (128 query heads per key/value head: one
+    query position per 128-row tile) and ones that do not divide 128."""
+    compare(make_case(111, h_q + h_kv + d, B=1, s_q=70, s_kv=200, h_q=h_q, h_kv=h_kv, d=d, causal=causal,
+                      sinks=True))
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_decode_long_cache(d):
+    """One query row per head against a quarter-million-key cache (the split count caps at
+    64 splits, each spanning many key tiles)."""
+    compare(make_case(112, d, B=1, s_q=1, s_kv=262144, h_q=8, h_kv=2, d=d, causal=True), bwd=False)
