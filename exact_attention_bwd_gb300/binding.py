@@ -28,6 +28,7 @@ FA_FLAG_NO_SPLIT = 2
 FA_FLAG_DETERMINISTIC = 4
 FA_DTYPE_BF16 = 0
 FA_DTYPE_E4M3 = 1
+FA_DTYPE_F16 = 2
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_fwd_workspace_size", "fa_bwd_workspace_size", "fa_read_device_status",
            "fa_status_string", "fa_profile_enable", "fa_profile_read", "fa_version", "fa_fwd_noalloc")
@@ -202,6 +203,12 @@ def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sink
     return p
 
 
+def _type_code(t):
+    """FA_DTYPE_* code of a torch dtype, or None when the library does not take it."""
+    import torch
+    return {torch.bfloat16: FA_DTYPE_BF16, torch.float16: FA_DTYPE_F16, torch.uint8: FA_DTYPE_E4M3}.get(t)
+
+
 def _stream():
     import torch
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -212,19 +219,20 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
             descale=None, seqused_q=None):
     """Runs fa_fwd on torch CUDA tensors; returns (o, lse, workspace).
 
-    uint8 q, k, v are e4m3 bytes (FA_DTYPE_E4M3); descale = (q, k, v) fp32 [B * h_kv]
-    factors or None (all 1).  The output is bf16 either way."""
+    q, k, v are all bfloat16, all float16, or all uint8 = e4m3 bytes (FA_DTYPE_E4M3);
+    descale = (q, k, v) fp32 [B * h_kv] factors or None (all 1).  The output has the
+    inputs' type (bf16 for e4m3 inputs)."""
     import torch
     fp8 = q.dtype == torch.uint8
-    want = torch.uint8 if fp8 else torch.bfloat16
-    if q.dtype != want or k.dtype != want or v.dtype != want:
-        raise TypeError(f"q, k, v must all be bfloat16 or all uint8 (e4m3 bytes); got {q.dtype}, {k.dtype}, {v.dtype}")
+    if _type_code(q.dtype) is None or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must all be bfloat16, all float16 or all uint8 (e4m3 bytes); "
+                        f"got {q.dtype}, {k.dtype}, {v.dtype}")
     if descale is not None and not fp8:
         raise TypeError("descale factors apply to e4m3 (uint8) inputs only")
     dq_, dk_, dv_ = descale if descale is not None else (None, None, None)
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
                     cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv,
-                    dtype=FA_DTYPE_E4M3 if fp8 else FA_DTYPE_BF16, q_descale=dq_, k_descale=dk_, v_descale=dv_,
+                    dtype=_type_code(q.dtype), q_descale=dq_, k_descale=dk_, v_descale=dv_,
                     seqused_q=seqused_q)
     nbytes = fa_fwd_workspace_size(p)
     if nbytes == 0:
@@ -232,7 +240,7 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     if out is None:
-        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+        out = torch.empty(q.shape, dtype=torch.bfloat16 if fp8 else q.dtype, device=q.device)
     if lse is None:
         shape = (p.B, p.h_q, p.s_q) if cu_q is None else (p.h_q, p.s_q)
         lse = torch.empty(shape, dtype=torch.float32, device=q.device)
@@ -244,13 +252,20 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
 
 def backward(q, k, v, o, lse, dout, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None,
              cu_q=None, cu_k=None, flags=0, workspace=None, grads=None, seqused_q=None, seqused_k=None):
-    """Runs fa_bwd on torch CUDA tensors; returns (dq, dk, dv, dsinks, workspace)."""
+    """Runs fa_bwd on torch CUDA tensors; returns (dq, dk, dv, dsinks, workspace).
+
+    q, k, v, o, dout (and dq, dk, dv when given) are all bfloat16 or all float16."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
-        if t.dtype != torch.bfloat16:
-            raise TypeError(f"the backward takes bfloat16 tensors; {name} is {t.dtype}")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"the backward takes bfloat16 or float16 tensors; q is {q.dtype}")
+    named = [("k", k), ("v", v), ("o", o), ("dout", dout)]
+    if grads is not None:
+        named += [("dq", grads[0]), ("dk", grads[1]), ("dv", grads[2])]
+    for name, t in named:
+        if t.dtype != q.dtype:
+            raise TypeError(f"the backward's tensors must share q's type {q.dtype}; {name} is {t.dtype}")
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
-                    cu_k=cu_k, flags=flags, seqused_q=seqused_q, seqused_k=seqused_k)
+                    cu_k=cu_k, flags=flags, seqused_q=seqused_q, seqused_k=seqused_k, dtype=_type_code(q.dtype))
     nbytes = fa_bwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_bwd_workspace_size")

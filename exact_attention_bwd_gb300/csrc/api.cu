@@ -45,9 +45,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-// 4-D bf16 tensor map over [b][s][h][d] (innermost first: d, h, s, b) with a
-// (64, box_h, box_s, 1) box and 128-byte swizzle.  Out-of-range rows read as zero.
-bool encode_bhsd(CUtensorMap* m, const void* base, int d, int h, int s, int b, int box_h, int box_s) {
+// 4-D tensor map of 16-bit elements (fp16 if f16, else bf16) over [b][s][h][d] (innermost
+// first: d, h, s, b) with a (64, box_h, box_s, 1) box and 128-byte swizzle.  Out-of-range
+// rows read as zero.
+bool encode_bhsd(CUtensorMap* m, const void* base, int d, int h, int s, int b, int box_h, int box_s, bool f16) {
     auto fn = encoder();
     if (!fn) return false;
     if (s <= 0 || b <= 0) {
@@ -58,7 +59,7 @@ bool encode_bhsd(CUtensorMap* m, const void* base, int d, int h, int s, int b, i
     cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)h * d * 2, (cuuint64_t)s * h * d * 2};
     cuuint32_t box[4] = {64, (cuuint32_t)box_h, (cuuint32_t)box_s, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+    CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -133,7 +134,7 @@ fa_status normalise(const fa_params* in, Problem& p) {
     if ((a.cu_seqlens_q == nullptr) != (a.cu_seqlens_k == nullptr)) return FA_ERR_INVALID_ARG;
     if (a.window_left < -1 || a.window_right < -1) return FA_ERR_INVALID_ARG;
     if (a.d % 8 != 0 || a.d > 256) return FA_ERR_UNSUPPORTED;
-    if (a.dtype != FA_DTYPE_BF16 && a.dtype != FA_DTYPE_E4M3) return FA_ERR_INVALID_ARG;
+    if (a.dtype != FA_DTYPE_BF16 && a.dtype != FA_DTYPE_F16 && a.dtype != FA_DTYPE_E4M3) return FA_ERR_INVALID_ARG;
     // e4m3: dense d = 128 only
     if (a.dtype == FA_DTYPE_E4M3 && (a.d != 128 || a.cu_seqlens_q || a.block_table)) return FA_ERR_UNSUPPORTED;
     std::memset(&p, 0, sizeof(p));
@@ -219,13 +220,13 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
     if (p.B == 0 || rows_total == 0) return FA_OK;  // nothing to compute
     const bool dense = p.cu_q == nullptr;
     const int R = p.s_q * p.G;  // query rows per key/value head (dense)
-    if (dense && p.dtype == FA_DTYPE_BF16 && (p.d == 64 || p.d == 128 || p.d == 256) && R <= decode_rows_max(p.d)) {
+    if (dense && p.dtype != FA_DTYPE_E4M3 && (p.d == 64 || p.d == 128 || p.d == 256) && R <= decode_rows_max(p.d)) {
         pl.path = FwdPath::kDecode;
         const int tiles = (p.s_kv + kDecodeKeys - 1) / kDecodeKeys;
         const long units = (long)p.B * p.h_kv;
         const int slots = sm_count() * decode_ctas_per_sm(p.d, R);
         // partials: R rows x (d + 1) floats per split, written and read, against the
-        // unit's 2 * s_kv * d bf16 of keys and values
+        // unit's 2 * s_kv * d 16-bit elements of keys and values
         const double part = p.s_kv > 0 ? (double)R * (p.d + 1) * 8.0 / ((double)p.s_kv * p.d * 4.0) : 1.0;
         pl.n_splits = tiles > 0 ? choose_splits(units, tiles, slots, part) : 1;
         pl.split_tiles = tiles > 0 ? (tiles + pl.n_splits - 1) / pl.n_splits : 0;
@@ -292,7 +293,7 @@ fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     pl = BwdPlan();
     if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
     if (p.block_table) return FA_ERR_UNSUPPORTED;  // paged caches: forward only
-    if (p.dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;      // e4m3: forward only
+    if (p.dtype == FA_DTYPE_E4M3) return FA_ERR_UNSUPPORTED;      // e4m3: forward only
     const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
     const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
     if (p.B == 0 || (rows_total == 0 && keys_total == 0)) return FA_OK;
@@ -304,7 +305,7 @@ fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
         pl.n_qtiles = p.B * ((p.s_q + p.P - 1) / p.P);
         pl.n_kvblocks = (p.s_kv + kTileRows - 1) / kTileRows;
         // a (batch, key/value head) unit's CTAs all read its Q and dO tiles and add into its
-        // dQ accumulator rows (bf16 Q + dO, fp32 accumulator: 8 bytes per row and column);
+        // dQ accumulator rows (16-bit Q + dO, fp32 accumulator: 8 bytes per row and column);
         // take as many units at a time as keep that within half the L2, in bands of
         // near-equal size (a small last band would start its heaviest blocks last)
         const double unit_bytes = (double)p.s_q * p.G * p.d * 8.0;
@@ -413,8 +414,9 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     // dimensions are the row within a page and the page
     const int kv_rows = p.block_table ? p.page_size : tokens_k;
     const int kv_outer = p.block_table ? in->num_pages : bdim;
-    if (p.dtype == FA_DTYPE_BF16 && (!encode_bhsd(&tk, k, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box) ||
-                                     !encode_bhsd(&tv, v, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box)))
+    const bool f16 = p.dtype == FA_DTYPE_F16;
+    if (p.dtype != FA_DTYPE_E4M3 && (!encode_bhsd(&tk, k, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box, f16) ||
+                                     !encode_bhsd(&tv, v, p.d, p.h_kv, kv_rows, kv_outer, 1, kv_box, f16)))
         return FA_ERR_CUDA;
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     float* o_part = reinterpret_cast<float*>(ws + kStatusBytes);
@@ -423,7 +425,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     if (pl.path == FwdPath::kDecode) {
         DecodeArgs a{};
         a.p = p;
-        a.q = reinterpret_cast<const __nv_bfloat16*>(q);
+        a.q = reinterpret_cast<const uint16_t*>(q);
         a.n_splits = pl.n_splits;
         a.split_keys = pl.split_tiles * kDecodeKeys;
         a.o_part = o_part;
@@ -436,7 +438,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         c.n_splits = pl.n_splits;
         c.o_part = o_part;
         c.lse_part = lse_part;
-        c.o = reinterpret_cast<__nv_bfloat16*>(o);
+        c.o = reinterpret_cast<uint16_t*>(o);
         c.lse = lse;
         e = timed(kCombine, st, [&] { return launch_combine(c, st); });
         return cuda_status(e);
@@ -467,7 +469,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         a.v_descale = in->v_descale;
         tk = tk8;
         tv = tvt;
-    } else if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P)) {
+    } else if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16)) {
         return FA_ERR_CUDA;
     }
     a.p = p;
@@ -481,7 +483,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         a.n_ctas = (int)(items < sm_count() ? items : sm_count());
         a.snake = (!p.cu_q && p.causal && !pl.unit_major) ? 1 : 0;
     }
-    a.o = reinterpret_cast<__nv_bfloat16*>(o);
+    a.o = reinterpret_cast<uint16_t*>(o);
     a.lse = lse;
     a.o_part = o_part;
     a.lse_part = lse_part;
@@ -496,7 +498,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         c.n_splits = pl.n_splits;
         c.o_part = o_part;
         c.lse_part = lse_part;
-        c.o = reinterpret_cast<__nv_bfloat16*>(o);
+        c.o = reinterpret_cast<uint16_t*>(o);
         c.lse = lse;
         e = timed(kCombine, st, [&] { return launch_combine(c, st); });
     }
@@ -535,15 +537,15 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.n_qtiles = pl.n_qtiles;
     a.n_kvblocks = pl.n_kvblocks;
     a.n_bands = pl.n_bands;
-    a.o = reinterpret_cast<const __nv_bfloat16*>(o);
+    a.o = reinterpret_cast<const uint16_t*>(o);
     a.lse = lse;
-    a.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
+    a.dout = reinterpret_cast<const uint16_t*>(dout);
     a.delta_t = reinterpret_cast<float*>(ws + pl.off_delta);
     a.lse2_t = reinterpret_cast<float*>(ws + pl.off_lse2);
     a.dq_acc = reinterpret_cast<float*>(ws + pl.off_dq);
-    a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
-    a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
-    a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+    a.dq = reinterpret_cast<uint16_t*>(dq);
+    a.dk = reinterpret_cast<uint16_t*>(dk);
+    a.dv = reinterpret_cast<uint16_t*>(dv);
     a.dsinks = p.sinks ? dsinks : nullptr;
     a.sink_t = p.sinks ? reinterpret_cast<float*>(ws + pl.off_sink) : nullptr;
     a.dq_count = (in->flags & FA_FLAG_DETERMINISTIC) ? reinterpret_cast<int*>(ws + pl.off_count) : nullptr;
@@ -553,10 +555,11 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     const int tokens_k = p.cu_q ? p.T_k : p.s_kv;
     const int bdim = p.cu_q ? 1 : p.B;
     CUtensorMap tq, tk, tv, tdo;
-    if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P) ||
-        !encode_bhsd(&tdo, dout, p.d, p.h_q, tokens_q, bdim, p.G, p.P) ||
-        !encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, 128) ||
-        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, 128))
+    const bool f16 = p.dtype == FA_DTYPE_F16;
+    if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16) ||
+        !encode_bhsd(&tdo, dout, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16) ||
+        !encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, 128, f16) ||
+        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, 128, f16))
         return FA_ERR_CUDA;
     cudaError_t e = timed(kBwdPre, st, [&] { return launch_bwd_pre(a, st); });
     if (e != cudaSuccess) return FA_ERR_CUDA;

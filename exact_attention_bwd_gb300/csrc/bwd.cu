@@ -40,7 +40,7 @@ struct BwdCfg {
     static constexpr int CHUNK = 128 * 128;      // one [128 rows][64 cols] chunk
     static constexpr int TMEM_COLS = 512;
     // TMEM columns
-    static constexpr uint32_t C_S = 0;           // S^T (fp32); P^T (bf16) in [0, 32) and [64, 96)
+    static constexpr uint32_t C_S = 0;           // S^T (fp32); P^T (16-bit) in [0, 32) and [64, 96)
     static constexpr uint32_t C_DP = 128;        // dP^T
     static constexpr uint32_t C_DV = 256;
     static constexpr uint32_t C_DK = 256 + D;
@@ -150,7 +150,7 @@ __device__ __forceinline__ void dq_turn_done(int* cnt) {
     if ((threadIdx.x & 31) == 0) atomicAdd(cnt, 1);
 }
 
-template <int D, bool DET>
+template <int D, bool DET, bool F16>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
     bwd_main_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
@@ -329,12 +329,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0 && nsteps > 0) {
-            constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: K-major both
-            constexpr uint32_t id_dv = idesc_bf16(128, D, false, true);    // A from TMEM, B MN-major
-            constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);    // A K-major, B MN-major
+            constexpr uint32_t id_s = idesc_16(128, 128, false, false, F16);  // S^T, dP^T: K-major both
+            constexpr uint32_t id_dv = idesc_16(128, D, false, true, F16);    // A from TMEM, B MN-major
+            constexpr uint32_t id_dk = idesc_16(128, D, false, true, F16);    // A K-major, B MN-major
             // dQ^T (M = d, N = query rows) when d = 128; dQ (M = query rows, N = d) when d = 64,
             // whose 64-row accumulator would need the M = 64 lane layout
-            constexpr uint32_t id_dq = C::DQ_T ? idesc_bf16(128, 128, true, true) : idesc_bf16(128, D, true, true);
+            constexpr uint32_t id_dq = C::DQ_T ? idesc_16(128, 128, true, true, F16) : idesc_16(128, D, true, true, F16);
             const uint32_t ka = smem_u32(s.k), va = smem_u32(s.v);
             bool ok = mbar_wait(&s.kv_full, 0, ab);
             tc_fence_after();
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 }
                 uint32_t pk[32];
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 2) pk[cc / 2] = pack_bf16(pf[cc], pf[cc + 1]);
+                for (int cc = 0; cc < 64; cc += 2) pk[cc / 2] = pack16<F16>(pf[cc], pf[cc + 1]);
                 // P^T of query columns [64cg, 64cg+64) goes over the first half of the S^T
                 // columns this group has just read (the other group never touches them)
                 tmem_st_32x32b_x32(tmem + lane_base + C::C_S + 64 * cg, pk);
@@ -489,13 +489,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                         const float4 d0 = *reinterpret_cast<const float4*>(dlt + cb);
                         const float4 d1 = *reinterpret_cast<const float4*>(dlt + cb + 4);
                         uint4 w;
-                        w.x = pack_bf16(pf[cb + 0] * (__uint_as_float(dr[8 * u + 0]) - d0.x),
+                        w.x = pack16<F16>(pf[cb + 0] * (__uint_as_float(dr[8 * u + 0]) - d0.x),
                                         pf[cb + 1] * (__uint_as_float(dr[8 * u + 1]) - d0.y));
-                        w.y = pack_bf16(pf[cb + 2] * (__uint_as_float(dr[8 * u + 2]) - d0.z),
+                        w.y = pack16<F16>(pf[cb + 2] * (__uint_as_float(dr[8 * u + 2]) - d0.z),
                                         pf[cb + 3] * (__uint_as_float(dr[8 * u + 3]) - d0.w));
-                        w.z = pack_bf16(pf[cb + 4] * (__uint_as_float(dr[8 * u + 4]) - d1.x),
+                        w.z = pack16<F16>(pf[cb + 4] * (__uint_as_float(dr[8 * u + 4]) - d1.x),
                                         pf[cb + 5] * (__uint_as_float(dr[8 * u + 5]) - d1.y));
-                        w.w = pack_bf16(pf[cb + 6] * (__uint_as_float(dr[8 * u + 6]) - d1.z),
+                        w.w = pack16<F16>(pf[cb + 6] * (__uint_as_float(dr[8 * u + 6]) - d1.z),
                                         pf[cb + 7] * (__uint_as_float(dr[8 * u + 7]) - d1.w));
                         const int unit = (cb >> 3) ^ (jr & 7);
                         *reinterpret_cast<uint4*>(drow + unit * 16) = w;
@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const long krow = key_row(p, sv, j);
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
-            __nv_bfloat16* dst = (which == 0 ? a.dv : a.dk) + (krow * p.h_kv + g) * D + (D / 2) * cg;
+            uint16_t* dst = (which == 0 ? a.dv : a.dk) + (krow * p.h_kv + g) * D + (D / 2) * cg;
             const float mul = which == 0 ? 1.f : p.scale;
             const uint32_t col = (which == 0 ? C::C_DV : C::C_DK) + (D / 2) * cg;
 #pragma unroll
@@ -557,10 +557,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         uint4 w;
-                        w.x = pack_bf16(__uint_as_float(v[8 * t + 0]) * mul, __uint_as_float(v[8 * t + 1]) * mul);
-                        w.y = pack_bf16(__uint_as_float(v[8 * t + 2]) * mul, __uint_as_float(v[8 * t + 3]) * mul);
-                        w.z = pack_bf16(__uint_as_float(v[8 * t + 4]) * mul, __uint_as_float(v[8 * t + 5]) * mul);
-                        w.w = pack_bf16(__uint_as_float(v[8 * t + 6]) * mul, __uint_as_float(v[8 * t + 7]) * mul);
+                        w.x = pack16<F16>(__uint_as_float(v[8 * t + 0]) * mul, __uint_as_float(v[8 * t + 1]) * mul);
+                        w.y = pack16<F16>(__uint_as_float(v[8 * t + 2]) * mul, __uint_as_float(v[8 * t + 3]) * mul);
+                        w.z = pack16<F16>(__uint_as_float(v[8 * t + 4]) * mul, __uint_as_float(v[8 * t + 5]) * mul);
+                        w.w = pack16<F16>(__uint_as_float(v[8 * t + 6]) * mul, __uint_as_float(v[8 * t + 7]) * mul);
                         reinterpret_cast<uint4*>(dst + cb)[t] = w;
                     }
                 }
@@ -592,7 +592,7 @@ __device__ __forceinline__ bool decode_qtile(const Problem& p, int idx, int& seq
     return true;
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
     const Problem& p = a.p;
     const int idx = blockIdx.x, g = blockIdx.y;
@@ -624,14 +624,14 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
             tok = token_row(p, sv, i);
             const uint4 ov = *reinterpret_cast<const uint4*>(a.o + (tok * p.h_q + h) * D + 8 * ch);
             const uint4 dv = *reinterpret_cast<const uint4*>(a.dout + (tok * p.h_q + h) * D + 8 * ch);
-            dsum = fmaf(bf16_lo(ov.x), bf16_lo(dv.x), dsum);
-            dsum = fmaf(bf16_hi(ov.x), bf16_hi(dv.x), dsum);
-            dsum = fmaf(bf16_lo(ov.y), bf16_lo(dv.y), dsum);
-            dsum = fmaf(bf16_hi(ov.y), bf16_hi(dv.y), dsum);
-            dsum = fmaf(bf16_lo(ov.z), bf16_lo(dv.z), dsum);
-            dsum = fmaf(bf16_hi(ov.z), bf16_hi(dv.z), dsum);
-            dsum = fmaf(bf16_lo(ov.w), bf16_lo(dv.w), dsum);
-            dsum = fmaf(bf16_hi(ov.w), bf16_hi(dv.w), dsum);
+            dsum = fmaf(lo16<F16>(ov.x), lo16<F16>(dv.x), dsum);
+            dsum = fmaf(hi16<F16>(ov.x), hi16<F16>(dv.x), dsum);
+            dsum = fmaf(lo16<F16>(ov.y), lo16<F16>(dv.y), dsum);
+            dsum = fmaf(hi16<F16>(ov.y), hi16<F16>(dv.y), dsum);
+            dsum = fmaf(lo16<F16>(ov.z), lo16<F16>(dv.z), dsum);
+            dsum = fmaf(hi16<F16>(ov.z), hi16<F16>(dv.z), dsum);
+            dsum = fmaf(lo16<F16>(ov.w), lo16<F16>(dv.w), dsum);
+            dsum = fmaf(hi16<F16>(ov.w), hi16<F16>(dv.w), dsum);
         }
         // sum over the row's LPR lanes (all lanes take part: rows differ in validity)
 #pragma unroll
@@ -677,8 +677,8 @@ __global__ void __launch_bounds__(256) bwd_dsink_kernel(const BwdArgs a) {
     if (threadIdx.x == 0) a.dsinks[h] = part[0];
 }
 
-// postprocess: dQ = scale * acc -> bf16 rows
-template <int D>
+// postprocess: dQ = scale * acc -> rows of the inputs' 16-bit type
+template <int D, bool F16>
 __global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
     const Problem& p = a.p;
     const int idx = blockIdx.x, g = blockIdx.y;
@@ -696,10 +696,10 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
         const float4 u1 = *reinterpret_cast<const float4*>(a.dq_acc + (trow + r) * D + cb + 4);
         const float sc = p.scale;
         uint4 w;
-        w.x = pack_bf16(u0.x * sc, u0.y * sc);
-        w.y = pack_bf16(u0.z * sc, u0.w * sc);
-        w.z = pack_bf16(u1.x * sc, u1.y * sc);
-        w.w = pack_bf16(u1.z * sc, u1.w * sc);
+        w.x = pack16<F16>(u0.x * sc, u0.y * sc);
+        w.y = pack16<F16>(u0.z * sc, u0.w * sc);
+        w.z = pack16<F16>(u1.x * sc, u1.y * sc);
+        w.w = pack16<F16>(u1.z * sc, u1.w * sc);
         *reinterpret_cast<uint4*>(a.dq + (token_row(p, sv, i) * p.h_q + h) * D + cb) = w;
     }
 }
@@ -710,11 +710,11 @@ template <int D, bool DET>
 static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem<D>);
-    cudaError_t e =
-        cudaFuncSetAttribute(bwd_main_kernel<D, DET>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd_main_kernel<D, DET, true> : bwd_main_kernel<D, DET, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
-    bwd_main_kernel<D, DET><<<(unsigned)n, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
+    kernel<<<(unsigned)n, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
     return cudaGetLastError();
 }
 
@@ -734,16 +734,20 @@ cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUten
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st) {
     dim3 grid(a.n_qtiles, a.p.h_kv);
     if (a.n_qtiles == 0) return cudaSuccess;
-    if (a.p.d == 64) bwd_pre_kernel<64><<<grid, 128, 0, st>>>(a);
-    else bwd_pre_kernel<128><<<grid, 128, 0, st>>>(a);
+    const bool f16 = a.p.dtype == FA_DTYPE_F16;
+    auto kernel = a.p.d == 64 ? (f16 ? bwd_pre_kernel<64, true> : bwd_pre_kernel<64, false>)
+                              : (f16 ? bwd_pre_kernel<128, true> : bwd_pre_kernel<128, false>);
+    kernel<<<grid, 128, 0, st>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t st) {
     dim3 grid(a.n_qtiles, a.p.h_kv);
     if (a.n_qtiles == 0) return cudaSuccess;
-    if (a.p.d == 64) bwd_post_kernel<64><<<grid, 128, 0, st>>>(a);
-    else bwd_post_kernel<128><<<grid, 128, 0, st>>>(a);
+    const bool f16 = a.p.dtype == FA_DTYPE_F16;
+    auto kernel = a.p.d == 64 ? (f16 ? bwd_post_kernel<64, true> : bwd_post_kernel<64, false>)
+                              : (f16 ? bwd_post_kernel<128, true> : bwd_post_kernel<128, false>);
+    kernel<<<grid, 128, 0, st>>>(a);
     if (a.dsinks) bwd_dsink_kernel<<<a.p.h_q, 256, 0, st>>>(a);
     return cudaGetLastError();
 }

@@ -20,7 +20,7 @@ constexpr int KPW = BK / kComputeWarps;                // keys per warp per tile
 template <int D, int RG>
 struct DecCfg {
     static constexpr int KCH = D / 64;
-    static constexpr int CHUNK = BK * 128;             // [64 rows][64 cols] bf16, swizzled
+    static constexpr int CHUNK = BK * 128;             // [64 rows][64 cols] 16-bit, swizzled
     static constexpr int TILE = BK * D * 2;            // one K (or V) tile
     static constexpr int EPL = D / 32;                 // head-dim elements per lane
     static constexpr int R = 4 * RG;                   // query rows held (padded)
@@ -38,28 +38,29 @@ struct __align__(1024) DecSmem {
     int abort_flag;
 };
 
-// Byte offset of element (row, col) of a [rows][64] bf16 chunk written by a TMA load with
+// Byte offset of element (row, col) of a [rows][64] 16-bit chunk written by a TMA load with
 // 128-byte swizzle: the 16-byte unit index is XORed with row % 8.
 __device__ __forceinline__ int sw128(int row, int col) {
     return row * 128 + ((((col >> 3) ^ row) & 7) << 4) + ((col & 7) << 1);
 }
 
-// EPL consecutive bf16 values of row `row` starting at column `col` of a swizzled tile,
-// widened to fp32 (EPL = 2, 4 or 8: one 4-, 8- or 16-byte load that stays in a unit).
-template <int EPL, int CHUNK>
+// EPL consecutive 16-bit values (fp16 if F16, else bf16) of row `row` starting at column
+// `col` of a swizzled tile, widened to fp32 (EPL = 2, 4 or 8: one 4-, 8- or 16-byte load
+// that stays in a unit).
+template <int EPL, int CHUNK, bool F16>
 __device__ __forceinline__ void load_row_slice(const uint8_t* tile, int row, int col, float* out) {
     const uint8_t* src = tile + (col >> 6) * CHUNK + sw128(row, col & 63);
     if constexpr (EPL == 2) {
         const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
-        out[0] = bf16_lo(w);
-        out[1] = bf16_hi(w);
+        out[0] = lo16<F16>(w);
+        out[1] = hi16<F16>(w);
     } else if constexpr (EPL == 4) {
         const uint2 w = *reinterpret_cast<const uint2*>(src);
-        out[0] = bf16_lo(w.x); out[1] = bf16_hi(w.x); out[2] = bf16_lo(w.y); out[3] = bf16_hi(w.y);
+        out[0] = lo16<F16>(w.x); out[1] = hi16<F16>(w.x); out[2] = lo16<F16>(w.y); out[3] = hi16<F16>(w.y);
     } else {
         const uint4 w = *reinterpret_cast<const uint4*>(src);
-        out[0] = bf16_lo(w.x); out[1] = bf16_hi(w.x); out[2] = bf16_lo(w.y); out[3] = bf16_hi(w.y);
-        out[4] = bf16_lo(w.z); out[5] = bf16_hi(w.z); out[6] = bf16_lo(w.w); out[7] = bf16_hi(w.w);
+        out[0] = lo16<F16>(w.x); out[1] = hi16<F16>(w.x); out[2] = lo16<F16>(w.y); out[3] = hi16<F16>(w.y);
+        out[4] = lo16<F16>(w.z); out[5] = hi16<F16>(w.z); out[6] = lo16<F16>(w.w); out[7] = hi16<F16>(w.w);
     }
 }
 
@@ -69,7 +70,7 @@ __device__ __forceinline__ void load_row_slice(const uint8_t* tile, int row, int
 // (key, row) dot products are formed by a reduce-scatter across the lanes, so lane L ends
 // with item L = 4 * key + row.  The warps' states are merged by their log-sum-exp at the
 // end and the CTA writes the partial (O, LSE) of its key range.
-template <int D, int RG>
+template <int D, int RG, bool F16>
 __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
     decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using C = DecCfg<D, RG>;
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
                 float val = 0.f;
                 if (r < R) {
                     const int i = r / p.G, h = g * p.G + r % p.G;
-                    val = __bfloat162float(a.q[(((long)b * p.s_q + i) * p.h_q + h) * D + e0 + e]) * p.scale_log2;
+                    val = lo16<F16>(a.q[(((long)b * p.s_q + i) * p.h_q + h) * D + e0 + e]) * p.scale_log2;
                 }
                 q[r][e] = val;
             }
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
             const int jw = (t_begin + t) * BK + KPW * warp;  // first key of this warp
             float kv[KPW][EPL];
 #pragma unroll
-            for (int k = 0; k < KPW; ++k) load_row_slice<EPL, C::CHUNK>(s.k[st], KPW * warp + k, e0, kv[k]);
+            for (int k = 0; k < KPW; ++k) load_row_slice<EPL, C::CHUNK, F16>(s.k[st], KPW * warp + k, e0, kv[k]);
             const int kk = lane >> 2, rr = lane & 3;   // item of this lane after the reduction
             const int j = jw + kk;
 #pragma unroll
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
 #pragma unroll
                 for (int k = 0; k < KPW; ++k) {
                     float vv[EPL];
-                    load_row_slice<EPL, C::CHUNK>(s.v[st], KPW * warp + k, e0, vv);
+                    load_row_slice<EPL, C::CHUNK, F16>(s.v[st], KPW * warp + k, e0, vv);
 #pragma unroll
                     for (int r4 = 0; r4 < 4; ++r4) {
                         const float pk = __shfl_sync(0xffffffffu, pr, 4 * k + r4);
@@ -289,6 +290,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
 
 // One warp per output row: merge the splits' partials by their log-sum-exp and fold in
 // the sink, which joins the denominator exactly once.
+template <bool F16>
 __global__ void combine_kernel(const CombineArgs a) {
     const Problem& p = a.p;
     const long nrows = (long)p.B * p.h_q * p.s_q;
@@ -311,7 +313,7 @@ __global__ void combine_kernel(const CombineArgs a) {
     if (p.sinks) den += __expf(sink - m_all);
     const float lse = den > 0.f ? m_all + __logf(den) : -INFINITY;
     const int D = p.d;
-    __nv_bfloat16* out = a.o + (((long)b * p.s_q + i) * p.h_q + h) * D;
+    uint16_t* out = a.o + (((long)b * p.s_q + i) * p.h_q + h) * D;
     for (int c = lane * 4; c < D; c += 128) {
         float4 o = make_float4(0, 0, 0, 0);
         if (den_keys > 0.f) {
@@ -327,8 +329,8 @@ __global__ void combine_kernel(const CombineArgs a) {
             }
         }
         uint2 packed;
-        packed.x = pack_bf16(o.x, o.y);
-        packed.y = pack_bf16(o.z, o.w);
+        packed.x = pack16<F16>(o.x, o.y);
+        packed.y = pack16<F16>(o.z, o.w);
         *reinterpret_cast<uint2*>(out + c) = packed;
     }
     if (lane == 0 && a.lse) a.lse[((long)b * p.h_q + h) * p.s_q + i] = lse;
@@ -339,10 +341,11 @@ __global__ void combine_kernel(const CombineArgs a) {
 template <int D, int RG>
 static cudaError_t launch_decode_dr(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
     const size_t smem = sizeof(DecSmem<D, RG>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? decode_kernel<D, RG, true> : decode_kernel<D, RG, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = (long)a.n_splits * a.p.h_kv * a.p.B;
-    decode_kernel<D, RG><<<(unsigned)n, kThreadsDec, smem, st>>>(a, tk, tv);
+    kernel<<<(unsigned)n, kThreadsDec, smem, st>>>(a, tk, tv);
     return cudaGetLastError();
 }
 
@@ -374,7 +377,8 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
     const long nrows = (long)a.p.B * a.p.h_q * a.p.s_q;
     const int rows_per_block = 8;
     const long blocks = (nrows + rows_per_block - 1) / rows_per_block;
-    combine_kernel<<<(unsigned)blocks, rows_per_block * 32, 0, st>>>(a);
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? combine_kernel<true> : combine_kernel<false>;
+    kernel<<<(unsigned)blocks, rows_per_block * 32, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -70,7 +70,7 @@ struct __align__(1024) FwdSmem {
     int abort_flag;
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fwd_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv) {
@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         // Everything the issue path touches lives in registers (no per-tile arrays indexed
         // at run time), so consecutive MMAs go out back to back.
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
-            constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+            constexpr uint32_t idS = idesc_16(128, BN, false, false, F16);
+            constexpr uint32_t idO = idesc_16(128, D, false, true, F16);
             constexpr uint32_t kStageStep = (uint32_t)C::TILE_BYTES >> 4;  // descriptor units per stage
             // a descriptor's start-address field is addr >> 4 in its low bits, so stepping
             // through a tile is a plain add to a base descriptor (no carry: addr < 256 KB)
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     tmem_st_32x32b_x32(tO + cb, orr);
                 }
             }
-            // P = exp2(S*c - m) as bf16 pairs, packed in place (slot cc/2 is already consumed).
+            // P = exp2(S*c - m) as 16-bit pairs (the inputs' type), packed in place (slot cc/2 is already consumed).
             // On tiles without masked entries a fraction of the exponentials runs on the FMA
             // pipe (exp2_poly2) to share the load with the MUFU unit.
             const float base = (m_used == -INFINITY) ? 0.f : m_used;
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     pv = make_float2(ex2(xv.x), ex2(xv.y));
                 }
                 sum2 = __fadd2_rn(sum2, pv);
-                sr[cc / 2] = pack_bf16(pv.x, pv.y);
+                sr[cc / 2] = pack16<F16>(pv.x, pv.y);
             }
             const float sum = sum2.x + sum2.y;
             tmem_st_32x32b_x64(tS, sr);
@@ -471,14 +471,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 tmem_ld_32x32b_x32(tO + cb, orr);
                 if (!row_valid) continue;
                 if (!split_mode) {
-                    __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
+                    uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         uint4 wv;
-                        wv.x = pack_bf16(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
-                        wv.y = pack_bf16(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
-                        wv.z = pack_bf16(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
-                        wv.w = pack_bf16(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
+                        wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
+                        wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
+                        wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
+                        wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
                         reinterpret_cast<uint4*>(orow)[t] = wv;
                     }
                 } else {
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             if (lane == 0) mbar_arrive(&s.o_free[k]);
         } else if (row_valid) {
             if (!split_mode) {
-                __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
+                uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
 #pragma unroll
                 for (int t = 0; t < D / 8; ++t) reinterpret_cast<uint4*>(orow)[t] = make_uint4(0, 0, 0, 0);
             } else {
@@ -518,22 +518,23 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 
 }  // namespace
 
-template <int D>
+template <int D, bool F16>
 static cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t st) {
     const size_t smem = sizeof(FwdSmem<D>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (a.n_items <= 0 || a.n_ctas <= 0) return cudaSuccess;
-    fwd_kernel<D><<<(unsigned)a.n_ctas, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
+    fwd_kernel<D, F16><<<(unsigned)a.n_ctas, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t st) {
+    const bool f16 = a.p.dtype == FA_DTYPE_F16;
     switch (a.p.d) {
-        case 64: return launch_fwd_d<64>(a, tq, tk, tv, st);
-        case 128: return launch_fwd_d<128>(a, tq, tk, tv, st);
+        case 64: return f16 ? launch_fwd_d<64, true>(a, tq, tk, tv, st) : launch_fwd_d<64, false>(a, tq, tk, tv, st);
+        case 128: return f16 ? launch_fwd_d<128, true>(a, tq, tk, tv, st) : launch_fwd_d<128, false>(a, tq, tk, tv, st);
         case 256: return launch_fwd256(a, tq, tk, tv, st);
         default: return cudaErrorInvalidValue;
     }

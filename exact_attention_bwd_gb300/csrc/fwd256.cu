@@ -2,7 +2,7 @@
 //
 // The accumulator of one 128-row query tile is 256 TMEM columns wide, so a CTA holds a
 // single query tile.  Tensor memory: O in columns [0, 256), two 64-column S buffers in
-// [256, 384), and the Q tile itself in [384, 512) (bf16 pairs, one row per lane), so
+// [256, 384), and the Q tile itself in [384, 512) (16-bit pairs, one row per lane), so
 // S = Q K^T takes its A operand from tensor memory and reads only K from shared memory.
 // Q arrives by TMA in the first 64 KB ring slot; the softmax warps copy their rows into
 // tensor memory, after which that slot joins the key/value ring as its third stage.
@@ -21,8 +21,8 @@ constexpr int kThreads256 = 256;
 constexpr int D = 256;
 constexpr int BN = 64;               // keys per KV tile
 constexpr int KCH = D / 64;          // 64-column chunks
-constexpr int Q_CHUNK = 128 * 128;   // [128 rows][64 cols] bf16
-constexpr int KV_CHUNK = BN * 128;   // [64 rows][64 cols] bf16
+constexpr int Q_CHUNK = 128 * 128;   // [128 rows][64 cols] 16-bit
+constexpr int KV_CHUNK = BN * 128;   // [64 rows][64 cols] 16-bit
 constexpr int KV_BYTES = KCH * KV_CHUNK;  // one K or V tile (32 KB)
 constexpr int STAGES = 3;            // ring slots of K + V (64 KB each); slot 0 first holds Q
 constexpr int SLOT_BYTES = 2 * KV_BYTES;
@@ -45,6 +45,7 @@ struct __align__(1024) Smem256 {
     int abort_flag;
 };
 
+template <bool F16>
 __global__ void __launch_bounds__(kThreads256, 1)
     fwd256_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
@@ -163,8 +164,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idS = idesc_bf16(128, BN, false, false);  // A = Q from TMEM, B = K K-major
-            constexpr uint32_t idO = idesc_bf16(128, D, false, true);    // A = P from TMEM, B = V MN-major
+            constexpr uint32_t idS = idesc_16(128, BN, false, false, F16);  // A = Q from TMEM, B = K K-major
+            constexpr uint32_t idO = idesc_16(128, D, false, true, F16);    // A = P from TMEM, B = V MN-major
             // descriptors: base values plus (byte offset >> 4) in the start-address field
             const uint64_t kd0 = sdesc_sw128(smem_u32(s.ring[0]), 16, 1024);
             const uint64_t vd0 = sdesc_sw128(smem_u32(s.ring[0] + KV_BYTES), KV_CHUNK, 1024);
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
                 const float p0 = ex2(fmaf(__uint_as_float(sr[cc]), c, -base));
                 const float p1 = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -base));
                 sum += p0 + p1;
-                sr[cc / 2] = pack_bf16(p0, p1);
+                sr[cc / 2] = pack16<F16>(p0, p1);
             }
             l += sum;
             tmem_st_32x32b_x32(tS, sr);
@@ -340,14 +341,14 @@ __global__ void __launch_bounds__(kThreads256, 1)
             }
             if (!row_valid) continue;
             if (!split_mode) {
-                __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
+                uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     uint4 wv;
-                    wv.x = pack_bf16(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
-                    wv.y = pack_bf16(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
-                    wv.z = pack_bf16(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
-                    wv.w = pack_bf16(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
+                    wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
+                    wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
+                    wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
+                    wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
                     reinterpret_cast<uint4*>(orow)[t] = wv;
                 }
             } else {
@@ -374,10 +375,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
 cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t st) {
     const size_t smem = sizeof(Smem256) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? fwd256_kernel<true> : fwd256_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = a.p.cu_q ? (long)a.n_blocks * a.p.h_kv : (long)a.n_blocks * a.n_splits * a.p.h_kv * a.p.B;
-    fwd256_kernel<<<(unsigned)n, kThreads256, smem, st>>>(a, tq, tk, tv);
+    kernel<<<(unsigned)n, kThreads256, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
 }
 

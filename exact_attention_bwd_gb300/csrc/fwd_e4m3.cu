@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
                 tmem_ld_32x32b_x32(tO + cb, orr);
                 if (!row_valid) continue;
                 if (!split_mode) {
-                    __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
+                    uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         uint4 wv;
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
             if (lane == 0) mbar_arrive(&s.o_free[k]);
         } else if (row_valid) {
             if (!split_mode) {
-                __nv_bfloat16* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
+                uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
 #pragma unroll
                 for (int t = 0; t < D / 8; ++t) reinterpret_cast<uint4*>(orow)[t] = make_uint4(0, 0, 0, 0);
             } else {

@@ -3,7 +3,10 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include "fa.h"
 
 namespace fa {
 
@@ -40,7 +43,7 @@ struct FwdArgs {
     int n_items;       // work items (query blocks x kv heads [x batch x splits])
     int n_ctas;        // persistent CTAs of the d <= 128 kernel (at most one per SM)
     int snake;         // their rounds alternate direction (items heaviest first: dense causal)
-    __nv_bfloat16* o;  // [tokens, h_q, d]
+    uint16_t* o;       // [tokens, h_q, d] bf16, or fp16 for fp16 inputs
     float* lse;        // [B, h_q, s_q] or [h_q, T_q]; may be null
     float* o_part;     // split mode: [n_splits, rows, d] fp32
     float* lse_part;   // split mode: [n_splits, rows] fp32 (natural log, no sink)
@@ -57,7 +60,7 @@ struct FwdArgs {
 // ------------------------------------------------------------------------------------------
 struct DecodeArgs {
     Problem p;
-    const __nv_bfloat16* q;
+    const uint16_t* q;  // [B, s_q, h_q, d] bf16 or fp16 (as the inputs)
     int n_splits;
     int split_keys;    // keys per split (a multiple of the key tile)
     float* o_part;     // [n_splits, rows, d]
@@ -70,7 +73,7 @@ struct CombineArgs {
     int n_splits;
     const float* o_part;
     const float* lse_part;
-    __nv_bfloat16* o;
+    uint16_t* o;       // bf16 or fp16 (as the inputs)
     float* lse;
 };
 
@@ -84,15 +87,16 @@ struct BwdArgs {
     int n_bands;           // dense grid order: the (batch, kv head) units form this many bands of
                            // near-equal size, key block slowest within a band, so a band's
                            // query-side data stays in L2
-    const __nv_bfloat16* o;
+    // 16-bit tensors hold bf16 or fp16 (Problem::dtype) like the inputs
+    const uint16_t* o;
     const float* lse;
-    const __nv_bfloat16* dout;
+    const uint16_t* dout;
     float* delta_t;        // [h_kv, n_qtiles, 128]  rowsum(dO * O)
     float* lse2_t;         // [h_kv, n_qtiles, 128]  LSE * log2(e) (+inf for empty rows)
     float* dq_acc;         // [h_kv, n_qtiles, 128, d] fp32
-    __nv_bfloat16* dq;     // [tokens, h_q, d]
-    __nv_bfloat16* dk;     // [tokens_k, h_kv, d]
-    __nv_bfloat16* dv;
+    uint16_t* dq;          // [tokens, h_q, d]
+    uint16_t* dk;          // [tokens_k, h_kv, d]
+    uint16_t* dv;
     float* dsinks;         // [h_q] or null
     float* sink_t;         // [h_kv, n_qtiles, 128]  per-row sink-gradient terms (with sinks)
     int* dq_count;         // [h_kv, n_qtiles] dQ contributions landed per query tile, or null:

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace fa {
 
@@ -514,17 +515,24 @@ __device__ __forceinline__ void mma_ts_p_mn_x8(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
-// a_mn / b_mn: operand stored MN-major (true) or K-major (false).
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor of kind::f16 with fp16 (f16 = true) or bf16 A and B (always the
+// same type) and an fp32 accumulator.  a_mn / b_mn: operand stored MN-major (true) or
+// K-major (false).
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn, bool b_mn, bool f16) {
     return (1u << 4)                          // D: f32
-           | (1u << 7)                        // A: bf16
-           | (1u << 10)                       // B: bf16
+           | ((f16 ? 0u : 1u) << 7)           // A: f16 (0) or bf16 (1)
+           | ((f16 ? 0u : 1u) << 10)          // B: the same type as A
            | ((a_mn ? 1u : 0u) << 15)         // A major
            | ((b_mn ? 1u : 0u) << 16)         // B major
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_16(M, N, a_mn, b_mn, false);
+}
+static_assert(idesc_16(128, 128, true, false, true) == (idesc_bf16(128, 128, true, false) & ~((1u << 7) | (1u << 10))),
+              "the fp16 descriptor differs from the bf16 one in the two operand-type fields only");
 
 // Instruction descriptor of kind::f8f6f4 with both operands e4m3 (format code 0), fp32
 // accumulator, both operands K-major.
@@ -653,5 +661,27 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// The 16-bit element type of a kernel instantiation: fp16 (F16) or bf16.  Two values to
+// one 32-bit word (lo in the low half, round to nearest even), and the halves back to fp32.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+    if constexpr (F16) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        return pack_bf16(lo, hi);
+    }
+}
+template <bool F16>
+__device__ __forceinline__ float lo16(uint32_t w) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+    else return bf16_lo(w);
+}
+template <bool F16>
+__device__ __forceinline__ float hi16(uint32_t w) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    else return bf16_hi(w);
+}
 
 }  // namespace fa

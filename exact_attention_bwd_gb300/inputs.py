@@ -1,7 +1,7 @@
 """Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
 
 This module holds none of the attention arithmetic: it draws random numbers,
-rounds them to bf16 bit patterns and builds packed-sequence offsets.  The same
+rounds them to bf16 (or fp16, e4m3) bit patterns and builds packed-sequence offsets.  The same
 bits are uploaded to the GPU and widened to fp64 for the oracle, so both sides
 see identical inputs.
 
@@ -47,6 +47,17 @@ def bf16_to_f64(bits) -> np.ndarray:
 def normal_bf16(seed: int, shape) -> np.ndarray:
     """i.i.d. N(0, 1) draws in fp32, rounded to bf16 bit patterns."""
     return bf16_bits(rng(seed).standard_normal(size=shape, dtype=np.float32))
+
+
+def f16_bits(x) -> np.ndarray:
+    """Round fp32 values to IEEE binary16 (round to nearest, ties to even; overflow to inf);
+    returns uint16 bit patterns.  numpy's float32 -> float16 cast rounds this way."""
+    with np.errstate(over="ignore"):  # overflow to inf is the format's rule
+        return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_to_f64(bits) -> np.ndarray:
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 
 
 def normal_f32(seed: int, shape) -> np.ndarray:
@@ -143,10 +154,11 @@ WORKLOADS = {
 
 
 def make(w: dict) -> dict:
-    """Draw the bf16 bit patterns (uint16) and side inputs of workload ``w``.
+    """Draw the 16-bit bit patterns (uint16) and side inputs of workload ``w``.
 
     Returns q, k, v, dout (uint16, [B,S,H,D] or packed [T,H,D]), sinks (fp32 or
-    None), cu_q / cu_k (int32 or None), and the sizes.
+    None), cu_q / cu_k (int32 or None), and the sizes.  The N(0, 1) draws are rounded
+    to bf16, or to fp16 when w["dtype"] == "f16" (the same fp32 draws either way).
     """
     wid, var = w["wid"], w.get("variant", 0)
     h_q, h_kv, d = w["h_q"], w["h_kv"], w["d"]
@@ -166,10 +178,12 @@ def make(w: dict) -> dict:
         qshape = (w["B"], w["s_q"], h_q, d)
         kshape = (w["B"], w["s_kv"], h_kv, d)
         out.update(cu_q=None, cu_k=None)
-    out["q"] = normal_bf16(seed_of(wid, var, Q), qshape)
-    out["k"] = normal_bf16(seed_of(wid, var, K), kshape)
-    out["v"] = normal_bf16(seed_of(wid, var, V), kshape)
-    out["dout"] = normal_bf16(seed_of(wid, var, DO), qshape)
+    rnd = f16_bits if w.get("dtype") == "f16" else bf16_bits
+    out["dtype"] = w.get("dtype", "bf16")
+    out["q"] = rnd(normal_f32(seed_of(wid, var, Q), qshape))
+    out["k"] = rnd(normal_f32(seed_of(wid, var, K), kshape))
+    out["v"] = rnd(normal_f32(seed_of(wid, var, V), kshape))
+    out["dout"] = rnd(normal_f32(seed_of(wid, var, DO), qshape))
     out["sinks"] = normal_f32(seed_of(wid, var, SINKS), (h_q,)) if w.get("sinks") else None
     out.setdefault("scale", 1.0 / math.sqrt(d))
     return out

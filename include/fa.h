@@ -41,7 +41,7 @@
  * unspecified outputs, as on the pages).
  *
  * Conventions common to every call:
- *  - Layouts: dense tensors are contiguous [B, S, H, D] bf16; packed ones [T, H, D].
+ *  - Layouts: dense tensors are contiguous [B, S, H, D] (bf16 or fp16); packed ones [T, H, D].
  *    LSE is fp32 [B, h_q, s_q] (dense) or [h_q, T_q] (packed), natural log.
  *  - Ownership: every pointer is caller-owned device memory (except the params
  *    struct itself, read on the host during the call).  The library allocates no
@@ -55,7 +55,7 @@
  *    ABI and no kernel traps: a kernel whose pipeline stalls gives up after a time
  *    limit and records FA_ERR_TIMEOUT in the workspace status word, which
  *    fa_read_device_status reports.
- *  - Supported: bf16 (and e4m3 for the forward at d = 128, see below); head dim d in
+ *  - Supported: bf16 and fp16 (and e4m3 for the forward at d = 128, see below); head dim d in
  *    {64, 128, 256} for the forward, {64, 128} for the backward; h_q / h_kv <= 128.
  *    Anything else returns FA_ERR_UNSUPPORTED.
  *  - Zero-initialise fa_params (memset or `= {0}`): every optional field then means
@@ -113,9 +113,13 @@ typedef enum fa_status {
     FA_ERR_DEVICE_CHECK = 6  /* a device-side argument check failed (device status) */
 } fa_status;
 
-/* Input element types */
+/* Input element types.  bf16 and fp16 (dew-flash-attn PyPI page, usage: inputs in bf16
+ * or fp16; fa4-jax PyPI page, restrictions: fp16/bf16) run every path of fa_fwd and fa_bwd
+ * alike: o, dq, dk and dv have the inputs' type, accumulation and lse stay fp32.  e4m3 is
+ * the FP8 forward above. */
 #define FA_DTYPE_BF16 0
 #define FA_DTYPE_E4M3 1
+#define FA_DTYPE_F16 2
 
 /* Flags */
 #define FA_FLAG_VALIDATE_CU 1u  /* check cu_seqlens on the device; result in the status word */
@@ -148,7 +152,7 @@ typedef struct fa_params {
     int page_size;                  /* keys per page (block_table only) */
     int max_blocks_per_seq;         /* row stride of block_table */
     int num_pages;                  /* pages in each of the k and v pools */
-    /* Input element type (FA_DTYPE_*; 0 = bf16).  See the FP8 forward above. */
+    /* Input element type (FA_DTYPE_*; 0 = bf16).  See the FP8 forward above and the types. */
     int dtype;
     const float *q_descale;         /* FA_DTYPE_E4M3 only: device fp32 [B * h_kv] or NULL (= 1) */
     const float *k_descale;
@@ -168,7 +172,7 @@ fa_status fa_fwd(const fa_params *p, const void *q, const void *k, const void *v
                  void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
 
 /* Backward of L = sum(O * dout).  o and lse must be what fa_fwd returned for the
- * same inputs.  dq: layout of q; dk, dv: layout of k (all written, bf16).
+ * same inputs.  dq: layout of q; dk, dv: layout of k (all written, in the inputs' type).
  * dsinks: fp32 [h_q], written when p->sinks is given (must then be non-NULL). */
 fa_status fa_bwd(const fa_params *p, const void *q, const void *k, const void *v, const void *o,
                  const float *lse, const void *dout, void *dq, void *dk, void *dv, float *dsinks,

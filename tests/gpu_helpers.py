@@ -20,10 +20,11 @@ BF16_HALF_ULP = 2.0 ** -8
 LSE_ABS = 1e-3
 
 
-def to_dev(bits):
+def to_dev(bits, dtype="bf16"):
+    """uint16 bit patterns -> a CUDA tensor of bf16 (or fp16 for dtype "f16")."""
     import torch
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
-    return t.view(torch.bfloat16).cuda()
+    return t.view(torch.float16 if dtype == "f16" else torch.bfloat16).cuda()
 
 
 def from_dev(t) -> np.ndarray:
@@ -33,7 +34,8 @@ def from_dev(t) -> np.ndarray:
 
 def dev_inputs(w):
     import torch
-    d = dict(q=to_dev(w["q"]), k=to_dev(w["k"]), v=to_dev(w["v"]), dout=to_dev(w["dout"]))
+    t = w.get("dtype", "bf16")
+    d = dict(q=to_dev(w["q"], t), k=to_dev(w["k"], t), v=to_dev(w["v"], t), dout=to_dev(w["dout"], t))
     d["sinks"] = None if w["sinks"] is None else torch.from_numpy(w["sinks"]).cuda()
     d["cu_q"] = None if w["cu_q"] is None else torch.from_numpy(w["cu_q"]).cuda()
     d["cu_k"] = None if w["cu_k"] is None else torch.from_numpy(w["cu_k"]).cuda()
@@ -98,4 +100,4 @@ def run_gpu(w, bwd=True, flags=0):
 
 
 def f64(w, key):
-    return inputs.bf16_to_f64(w[key])
+    return (inputs.f16_to_f64 if w.get("dtype") == "f16" else inputs.bf16_to_f64)(w[key])

@@ -206,3 +206,32 @@ def test_binding_checks_dtypes():
         fa.forward(q, q, q, descale=(None, None, None))
     with pytest.raises(TypeError):
         fa.backward(k8, k8, k8, q, None, q)
+
+
+def test_f16_is_planned_like_bf16():
+    # fp16 inputs take the same paths and the same workspace as bf16 ones, forward and backward
+    for kw in (dict(), dict(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=64), dict(d=256), dict(s_q=1, s_kv=4096),
+               dict(cu_seqlens_q=0x2000, cu_seqlens_k=0x2000)):
+        assert fa.fa_fwd_workspace_size(params(dtype=fa.FA_DTYPE_F16, **kw)) == fa.fa_fwd_workspace_size(params(**kw))
+    for kw in (dict(), dict(d=64, flags=fa.FA_FLAG_DETERMINISTIC), dict(cu_seqlens_q=0x2000, cu_seqlens_k=0x2000)):
+        assert fa.fa_bwd_workspace_size(params(dtype=fa.FA_DTYPE_F16, **kw)) == fa.fa_bwd_workspace_size(params(**kw))
+    assert call_fwd(params(dtype=fa.FA_DTYPE_F16), ws_bytes=16) == fa.FA_ERR_WORKSPACE
+    assert call_bwd(params(dtype=fa.FA_DTYPE_F16), ws_bytes=16) == fa.FA_ERR_WORKSPACE
+    assert call_bwd(params(dtype=fa.FA_DTYPE_F16, d=256)) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_binding_checks_f16_types():
+    torch = pytest.importorskip("torch")
+    b = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    h = torch.zeros(1, 8, 2, 128, dtype=torch.float16)
+    f = torch.zeros(1, 8, 2, 128, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        fa.forward(h, b, b)                # mixed fp16 / bf16
+    with pytest.raises(TypeError):
+        fa.forward(f, f, f)                # fp32 is not an input type
+    with pytest.raises(TypeError):
+        fa.forward(h, h, h, descale=(None, None, None))
+    with pytest.raises(TypeError):
+        fa.backward(h, h, h, b, None, h)   # o of another type
+    with pytest.raises(TypeError):
+        fa.backward(h, h, h, h, None, h, grads=(b, h, h, None))
