@@ -74,8 +74,48 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the driver): the SM
+    clock, its maximum and the active clock-event reasons of one GPU, found by PCI id."""
+    CLOCK_SM = 1
+    # nvmlClocksEventReasons bits of the four reasons the timing rules name
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, pci_bus_id: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError(f"no NVML device at {pci_bus_id}")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(mx)) != 0:
+            raise OSError("nvmlDeviceGetMaxClockInfo failed")
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        sm, rs = self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.ct.byref(sm)) != 0:
+            return None
+        if self.reasons_fn(self.h, self.ct.byref(rs)) != 0:
+            return None
+        return float(sm.value), {nm for bit, nm in self.REASONS.items() if rs.value & bit}
+
+
+def _pci_bus_id(dev_index: int) -> str:
+    import torch
+    pr = torch.cuda.get_device_properties(dev_index)
+    return f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """SM clocks and clock-event reasons sampled DURING the timed region: every 2 ms by a
+    thread reading NVML (the timed region is tens of milliseconds), else every 200 ms by
+    nvidia-smi.  The GPU is the CUDA device's own (matched by PCI id)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -83,18 +123,46 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.out = None
+        self.nvml = None
+        self.samples = []
+        self.stop = threading.Event()
+        self.thread = None
+        try:
+            self.pci = _pci_bus_id(index)
+        except Exception:  # noqa: BLE001 - an older torch without PCI properties
+            self.pci = None
+        try:
+            self.nvml = _Nvml(self.pci) if self.pci else None
+        except (OSError, AttributeError):
+            self.nvml = None
+
+    def _poll(self):
+        while not self.stop.is_set():
+            x = self.nvml.sample()
+            if x is not None:
+                self.samples.append(x)
+            self.stop.wait(0.002)
 
     def __enter__(self):
+        if self.nvml is not None:
+            self.nvml.sample()  # first read before the region: the library is then warm
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+                ["nvidia-smi", f"--id={self.pci or self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader", "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -103,6 +171,14 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            if not self.samples:
+                return None
+            reasons = set().union(*(r for _, r in self.samples))
+            return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.nvml.max_mhz,
+                    "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml, every 2 ms"}
+        if self.out is None:
+            return None
         self.out.flush()
         self.out.seek(0)
         sm, mx, reasons = [], None, set()
@@ -122,7 +198,8 @@ class ClockSampler:
         os.unlink(self.out.name)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvidia-smi, every 200 ms"}
 
 
 # ----------------------------------------------------------------------------------------------
@@ -248,6 +325,8 @@ def run_ours(args):
         line["workloads"] = {n: measure_workload(dev, n) for n in SWEEP + OTHER}
         line["deterministic_bwd"] = {n: measure_workload(dev, n, bwd_flags=fa.FA_FLAG_DETERMINISTIC)
                                      for n in ("sweep_s8192_causal", "sweep_s2048", "gqa_window_causal", "varlen")}
+        line["f16"] = {n: measure_workload(dev, n, dtype="f16")
+                       for n in ("sweep_s8192_causal", "sweep_s8192", "sweep_s2048", "gqa_window_causal", "varlen")}
         line["e4m3_fwd"] = {n: measure_fp8(dev, n) for n in ("sweep_s8192_causal", "sweep_s8192", "sweep_s16384",
                                                               "sweep_s2048", "decode_d128_sq64")}
     if rank == 0 and not args.no_cpu:
@@ -332,10 +411,11 @@ def run_e2e(args, fa, kw, ins, outs, flops, world, dev):
 # every other workload: forward and forward+backward TFLOPS (context beside the headline)
 # ----------------------------------------------------------------------------------------------
 
-def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0):
+def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0, dtype="bf16"):
     """fwd and fwd+bwd of one prefill workload with seeded on-device inputs (the same recipe
     seeds, drawn by torch's generator); L2 flushed before every timed step.  bwd_flags:
-    fa_params flags of the backward (FA_FLAG_DETERMINISTIC for the fixed-order dQ sums)."""
+    fa_params flags of the backward (FA_FLAG_DETERMINISTIC for the fixed-order dQ sums);
+    dtype: "bf16" or "f16" inputs (the same draws, rounded to that type)."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
     w = inputs.workload(name)
@@ -350,10 +430,11 @@ def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0):
         wf = dict(w)
         qs, ks = (w["B"], w["s_q"], w["h_q"], w["d"]), (w["B"], w["s_kv"], w["h_kv"], w["d"])
         cu_d = None
-    q = inputs.normal_bf16_torch(sd(inputs.Q), qs, dev)
-    k = inputs.normal_bf16_torch(sd(inputs.K), ks, dev)
-    v = inputs.normal_bf16_torch(sd(inputs.V), ks, dev)
-    do = inputs.normal_bf16_torch(sd(inputs.DO), qs, dev)
+    draw = inputs.normal_f16_torch if dtype == "f16" else inputs.normal_bf16_torch
+    q = draw(sd(inputs.Q), qs, dev)
+    k = draw(sd(inputs.K), ks, dev)
+    v = draw(sd(inputs.V), ks, dev)
+    do = draw(sd(inputs.DO), qs, dev)
     sinks = None
     if w.get("sinks"):
         g = torch.Generator(device=dev)

@@ -201,6 +201,14 @@ def normal_bf16_torch(seed: int, shape, device):
     return torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
+def normal_f16_torch(seed: int, shape, device):
+    """The same draws as normal_bf16_torch, rounded to fp16 instead."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32).to(torch.float16)
+
+
 def page_table(seed: int, B: int, max_blocks: int, num_pages: int) -> np.ndarray:
     """Block table of a paged key/value cache: int32 [B, max_blocks] page indices, a
     seeded draw of distinct pages (a permutation of the pool, cut to B * max_blocks)."""
