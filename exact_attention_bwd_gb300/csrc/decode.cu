@@ -288,52 +288,89 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
     }
 }
 
-// One warp per output row: merge the splits' partials by their log-sum-exp and fold in
-// the sink, which joins the denominator exactly once.
-template <bool F16>
-__global__ void combine_kernel(const CombineArgs a) {
+// Merges the splits' partials of each output row by their log-sum-exp and folds in the
+// sink, which joins the denominator exactly once.  A row is taken by L lanes (32, or 16 at
+// d = 64, two rows per warp), each holding 4 consecutive columns per step (two steps at
+// d = 256), so every warp instruction reads whole 128-byte lines.  The split statistics
+// are spread over the row's lanes and reduced by shuffles (one memory round trip), and the
+// partial rows are read four splits at a time so several loads are in flight per lane.
+constexpr int kCombineWarps = 8;
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
+    constexpr int L = D >= 128 ? 32 : D / 4;  // lanes per row
+    constexpr int RPW = 32 / L;                // rows per warp
+    constexpr int V = D / (4 * L);             // float4 columns per lane
     const Problem& p = a.p;
     const long nrows = (long)p.B * p.h_q * p.s_q;
-    const long row = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    const int lane = threadIdx.x & 31;
-    if (row >= nrows) return;
-    const int i = (int)(row % p.s_q);
-    const int h = (int)((row / p.s_q) % p.h_q);
-    const int b = (int)(row / ((long)p.s_q * p.h_q));
+    const int lane = threadIdx.x & 31, l = lane % L;
+    const long row = ((long)blockIdx.x * kCombineWarps + threadIdx.x / 32) * RPW + lane / L;
+    const bool live = row < nrows;
+    const long r = live ? row : 0;  // rows past the end compute on row 0 and store nothing
+    const int n = a.n_splits;
+    const float* lp = a.lse_part + r;
     float mx = -INFINITY;
-    for (int sp = 0; sp < a.n_splits; ++sp) mx = fmaxf(mx, a.lse_part[sp * nrows + row]);
+    for (int sp = l; sp < n; sp += L) mx = fmaxf(mx, lp[(long)sp * nrows]);
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const int h = (int)((r / p.s_q) % p.h_q);
     const float sink = p.sinks ? p.sinks[h] : -INFINITY;
     const float m_all = fmaxf(mx, sink);
     float den = 0.f;
-    for (int sp = 0; sp < a.n_splits; ++sp) {
-        const float x = a.lse_part[sp * nrows + row];
+    for (int sp = l; sp < n; sp += L) {
+        const float x = lp[(long)sp * nrows];
         den += (x == -INFINITY) ? 0.f : __expf(x - m_all);
     }
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float den_keys = den;
     if (p.sinks) den += __expf(sink - m_all);
     const float lse = den > 0.f ? m_all + __logf(den) : -INFINITY;
-    const int D = p.d;
-    uint16_t* out = a.o + (((long)b * p.s_q + i) * p.h_q + h) * D;
-    for (int c = lane * 4; c < D; c += 128) {
-        float4 o = make_float4(0, 0, 0, 0);
-        if (den_keys > 0.f) {
-            for (int sp = 0; sp < a.n_splits; ++sp) {
-                const float x = a.lse_part[sp * nrows + row];
-                if (x == -INFINITY) continue;
-                const float w = __expf(x - m_all) / den;
-                const float4 v = *reinterpret_cast<const float4*>(a.o_part + (sp * nrows + row) * D + c);
-                o.x += w * v.x;
-                o.y += w * v.y;
-                o.z += w * v.z;
-                o.w += w * v.w;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+
+    float4 acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (den_keys > 0.f) {
+        const float* op = a.o_part + r * D + 4 * l;
+        const long split_stride = nrows * D;
+        for (int sp0 = 0; sp0 < n; sp0 += 4) {
+            float w[4];
+            float4 x[4][V];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int sp = sp0 + k;
+                const float lk = sp < n ? lp[(long)sp * nrows] : -INFINITY;
+                // an empty split's partial row may never have been written: not read at all
+                w[k] = lk == -INFINITY ? 0.f : __expf(lk - m_all) * inv;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    x[k][v] = lk == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                              : *reinterpret_cast<const float4*>(op + sp * split_stride + 4 * L * v);
             }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    acc[v].x = fmaf(w[k], x[k][v].x, acc[v].x);
+                    acc[v].y = fmaf(w[k], x[k][v].y, acc[v].y);
+                    acc[v].z = fmaf(w[k], x[k][v].z, acc[v].z);
+                    acc[v].w = fmaf(w[k], x[k][v].w, acc[v].w);
+                }
         }
-        uint2 packed;
-        packed.x = pack16<F16>(o.x, o.y);
-        packed.y = pack16<F16>(o.z, o.w);
-        *reinterpret_cast<uint2*>(out + c) = packed;
     }
-    if (lane == 0 && a.lse) a.lse[((long)b * p.h_q + h) * p.s_q + i] = lse;
+    if (!live) return;
+    const int i = (int)(row % p.s_q);
+    const int b = (int)(row / ((long)p.s_q * p.h_q));
+    uint16_t* out = a.o + (((long)b * p.s_q + i) * p.h_q + h) * D + 4 * l;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        uint2 packed;
+        packed.x = pack16<F16>(acc[v].x, acc[v].y);
+        packed.y = pack16<F16>(acc[v].z, acc[v].w);
+        *reinterpret_cast<uint2*>(out + 4 * L * v) = packed;
+    }
+    if (l == 0 && a.lse) a.lse[row] = lse;  // [B, h_q, s_q]: the row index itself
 }
 
 }  // namespace
@@ -373,13 +410,24 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
 int decode_rows_max(int d) { return d == 256 ? 4 : 8; }
 int decode_ctas_per_sm(int d, int rows) { return (d == 256 || rows > 4) ? 1 : 2; }
 
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+template <int D>
+static cudaError_t launch_combine_d(const CombineArgs& a, cudaStream_t st) {
     const long nrows = (long)a.p.B * a.p.h_q * a.p.s_q;
-    const int rows_per_block = 8;
+    const long rows_per_block = (long)kCombineWarps * (D >= 128 ? 1 : 2);
     const long blocks = (nrows + rows_per_block - 1) / rows_per_block;
-    auto kernel = a.p.dtype == FA_DTYPE_F16 ? combine_kernel<true> : combine_kernel<false>;
-    kernel<<<(unsigned)blocks, rows_per_block * 32, 0, st>>>(a);
+    if (blocks == 0) return cudaSuccess;
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? combine_kernel<D, true> : combine_kernel<D, false>;
+    kernel<<<(unsigned)blocks, kCombineWarps * 32, 0, st>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+    switch (a.p.d) {
+        case 64: return launch_combine_d<64>(a, st);
+        case 128: return launch_combine_d<128>(a, st);
+        case 256: return launch_combine_d<256>(a, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace fa

@@ -177,8 +177,9 @@ def test_large_groups(h_q, h_kv, d, causal):
                       sinks=True))
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_decode_long_cache(d):
     """One query row per head against a quarter-million-key cache (the split count caps at
-    64 splits, each spanning many key tiles)."""
+    64 splits, each spanning many key tiles; the combine then spreads more splits than it
+    has lanes per row over each lane)."""
     compare(make_case(112, d, B=1, s_q=1, s_kv=262144, h_q=8, h_kv=2, d=d, causal=True), bwd=False)
