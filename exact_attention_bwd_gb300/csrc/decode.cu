@@ -290,87 +290,111 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
 
 // Merges the splits' partials of each output row by their log-sum-exp and folds in the
 // sink, which joins the denominator exactly once.  A row is taken by L lanes (32, or 16 at
-// d = 64, two rows per warp), each holding 4 consecutive columns per step (two steps at
-// d = 256), so every warp instruction reads whole 128-byte lines.  The split statistics
-// are spread over the row's lanes and reduced by shuffles (one memory round trip), and the
-// partial rows are read four splits at a time so several loads are in flight per lane.
+// d = 64), each holding 4 consecutive columns per step (two steps at d = 256), so every
+// warp instruction reads whole 128-byte lines; a lane group takes RL rows.  The splits are
+// merged in one pass, four at a time with a running maximum: every load of a batch (the
+// splits' log-sum-exps and partial rows of all RL rows) is independent of the others, so
+// a lane has them all in flight at once instead of waiting for the statistics first.
 constexpr int kCombineWarps = 8;
 
+template <int D>
+struct CombineCfg {
+    static constexpr int L = D >= 128 ? 32 : D / 4;  // lanes per row
+    static constexpr int V = D / (4 * L);             // float4 columns per lane
+    static constexpr int RL = D >= 256 ? 1 : 2;       // rows per lane group
+    static constexpr int ROWS_PER_BLOCK = kCombineWarps * (32 / L) * RL;
+};
+
 template <int D, bool F16>
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
-    constexpr int L = D >= 128 ? 32 : D / 4;  // lanes per row
-    constexpr int RPW = 32 / L;                // rows per warp
-    constexpr int V = D / (4 * L);             // float4 columns per lane
+__global__ void __launch_bounds__(kCombineWarps * 32, 3) combine_kernel(const CombineArgs a) {
+    using C = CombineCfg<D>;
+    constexpr int L = C::L, V = C::V, RL = C::RL;
     const Problem& p = a.p;
     const long nrows = (long)p.B * p.h_q * p.s_q;
     const int lane = threadIdx.x & 31, l = lane % L;
-    const long row = ((long)blockIdx.x * kCombineWarps + threadIdx.x / 32) * RPW + lane / L;
-    const bool live = row < nrows;
-    const long r = live ? row : 0;  // rows past the end compute on row 0 and store nothing
+    const long row0 = (((long)blockIdx.x * kCombineWarps + threadIdx.x / 32) * (32 / L) + lane / L) * RL;
     const int n = a.n_splits;
-    const float* lp = a.lse_part + r;
-    float mx = -INFINITY;
-    for (int sp = l; sp < n; sp += L) mx = fmaxf(mx, lp[(long)sp * nrows]);
+    float m[RL], den[RL];
+    float4 acc[RL][V];
 #pragma unroll
-    for (int o = L / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const int h = (int)((r / p.s_q) % p.h_q);
-    const float sink = p.sinks ? p.sinks[h] : -INFINITY;
-    const float m_all = fmaxf(mx, sink);
-    float den = 0.f;
-    for (int sp = l; sp < n; sp += L) {
-        const float x = lp[(long)sp * nrows];
-        den += (x == -INFINITY) ? 0.f : __expf(x - m_all);
+    for (int q = 0; q < RL; ++q) {
+        m[q] = -INFINITY;
+        den[q] = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[q][v] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    for (int sp0 = 0; sp0 < n; sp0 += 4) {
+        float lk[RL][4];
+        float4 x[RL][4][V];
 #pragma unroll
-    for (int o = L / 2; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    const float den_keys = den;
-    if (p.sinks) den += __expf(sink - m_all);
-    const float lse = den > 0.f ? m_all + __logf(den) : -INFINITY;
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-
-    float4 acc[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (den_keys > 0.f) {
-        const float* op = a.o_part + r * D + 4 * l;
-        const long split_stride = nrows * D;
-        for (int sp0 = 0; sp0 < n; sp0 += 4) {
-            float w[4];
-            float4 x[4][V];
+        for (int q = 0; q < RL; ++q) {
+            const long r = min(row0 + q, nrows - 1);  // rows past the end read the last row, store nothing
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int sp = sp0 + k;
-                const float lk = sp < n ? lp[(long)sp * nrows] : -INFINITY;
-                // an empty split's partial row may never have been written: not read at all
-                w[k] = lk == -INFINITY ? 0.f : __expf(lk - m_all) * inv;
+                const bool in = sp < n;
+                lk[q][k] = in ? a.lse_part[(long)sp * nrows + r] : -INFINITY;
+                const float* src = a.o_part + ((long)sp * nrows + r) * D + 4 * l;
 #pragma unroll
                 for (int v = 0; v < V; ++v)
-                    x[k][v] = lk == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                              : *reinterpret_cast<const float4*>(op + sp * split_stride + 4 * L * v);
+                    x[q][k][v] = in ? *reinterpret_cast<const float4*>(src + 4 * L * v) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < RL; ++q) {
+            const float mn = fmaxf(m[q], fmaxf(fmaxf(lk[q][0], lk[q][1]), fmaxf(lk[q][2], lk[q][3])));
+            if (mn == -INFINITY) continue;  // no keys in any split so far
+            const float sc = m[q] == -INFINITY ? 0.f : __expf(m[q] - mn);
+            den[q] *= sc;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                acc[q][v].x *= sc;
+                acc[q][v].y *= sc;
+                acc[q][v].z *= sc;
+                acc[q][v].w *= sc;
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
+            for (int k = 0; k < 4; ++k) {
+                // an empty split (-inf) adds nothing; its partial row may never have been
+                // written, so it is skipped rather than multiplied by zero
+                if (lk[q][k] == -INFINITY) continue;
+                const float w = __expf(lk[q][k] - mn);
+                den[q] += w;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    acc[v].x = fmaf(w[k], x[k][v].x, acc[v].x);
-                    acc[v].y = fmaf(w[k], x[k][v].y, acc[v].y);
-                    acc[v].z = fmaf(w[k], x[k][v].z, acc[v].z);
-                    acc[v].w = fmaf(w[k], x[k][v].w, acc[v].w);
+                    acc[q][v].x = fmaf(w, x[q][k][v].x, acc[q][v].x);
+                    acc[q][v].y = fmaf(w, x[q][k][v].y, acc[q][v].y);
+                    acc[q][v].z = fmaf(w, x[q][k][v].z, acc[q][v].z);
+                    acc[q][v].w = fmaf(w, x[q][k][v].w, acc[q][v].w);
                 }
+            }
+            m[q] = mn;
         }
     }
-    if (!live) return;
-    const int i = (int)(row % p.s_q);
-    const int b = (int)(row / ((long)p.s_q * p.h_q));
-    uint16_t* out = a.o + (((long)b * p.s_q + i) * p.h_q + h) * D + 4 * l;
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-        uint2 packed;
-        packed.x = pack16<F16>(acc[v].x, acc[v].y);
-        packed.y = pack16<F16>(acc[v].z, acc[v].w);
-        *reinterpret_cast<uint2*>(out + 4 * L * v) = packed;
+    for (int q = 0; q < RL; ++q) {
+        const long row = row0 + q;
+        if (row >= nrows) break;
+        const int i = (int)(row % p.s_q);
+        const int h = (int)((row / p.s_q) % p.h_q);
+        const int b = (int)(row / ((long)p.s_q * p.h_q));
+        const float sink = p.sinks ? p.sinks[h] : -INFINITY;
+        const float m_all = fmaxf(m[q], sink);
+        const float sc = m[q] == -INFINITY ? 0.f : __expf(m[q] - m_all);
+        const float den_keys = den[q] * sc;
+        const float dn = den_keys + (p.sinks && m_all != -INFINITY ? __expf(sink - m_all) : 0.f);
+        const float lse = dn > 0.f ? m_all + __logf(dn) : -INFINITY;
+        const float f = den_keys > 0.f ? sc / dn : 0.f;
+        uint16_t* out = a.o + (((long)b * p.s_q + i) * p.h_q + h) * D + 4 * l;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            uint2 packed;
+            packed.x = pack16<F16>(acc[q][v].x * f, acc[q][v].y * f);
+            packed.y = pack16<F16>(acc[q][v].z * f, acc[q][v].w * f);
+            *reinterpret_cast<uint2*>(out + 4 * L * v) = packed;
+        }
+        if (l == 0 && a.lse) a.lse[row] = lse;  // [B, h_q, s_q]: the row index itself
     }
-    if (l == 0 && a.lse) a.lse[row] = lse;  // [B, h_q, s_q]: the row index itself
 }
 
 }  // namespace
@@ -413,7 +437,7 @@ int decode_ctas_per_sm(int d, int rows) { return (d == 256 || rows > 4) ? 1 : 2;
 template <int D>
 static cudaError_t launch_combine_d(const CombineArgs& a, cudaStream_t st) {
     const long nrows = (long)a.p.B * a.p.h_q * a.p.s_q;
-    const long rows_per_block = (long)kCombineWarps * (D >= 128 ? 1 : 2);
+    const long rows_per_block = CombineCfg<D>::ROWS_PER_BLOCK;
     const long blocks = (nrows + rows_per_block - 1) / rows_per_block;
     if (blocks == 0) return cudaSuccess;
     auto kernel = a.p.dtype == FA_DTYPE_F16 ? combine_kernel<D, true> : combine_kernel<D, false>;
