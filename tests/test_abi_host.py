@@ -235,3 +235,34 @@ def test_binding_checks_f16_types():
         fa.backward(h, h, h, b, None, h)   # o of another type
     with pytest.raises(TypeError):
         fa.backward(h, h, h, h, None, h, grads=(b, h, h, None))
+
+
+def test_params_layout_and_constants_match_the_header(tmp_path):
+    """The ctypes mirror of fa_params has the C struct's size and field offsets, and the
+    binding's constants equal the header's (a plain C compile of include/fa.h)."""
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in fa.FaParams._fields_]
+    consts = [n for n in dir(fa) if re.fullmatch(r"FA_(OK|ERR_\w+|FLAG_\w+|DTYPE_\w+)", n)]
+    src = ["#include <stdio.h>", "#include <stddef.h>", '#include "fa.h"', "int main(void) {",
+           '  printf("size %zu\\n", sizeof(fa_params));']
+    src += [f'  printf("off {f} %zu\\n", offsetof(fa_params, {f}));' for f in fields]
+    src += [f'  printf("const {n} %lld\\n", (long long)({n}));' for n in consts]
+    src += ["  return 0;", "}"]
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(src) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(c), "-o", str(exe)],
+                   check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        kind, *rest = line.split()
+        got[(kind, rest[0]) if kind != "size" else ("size", "")] = int(rest[-1])
+    assert got[("size", "")] == ctypes.sizeof(fa.FaParams)
+    for f in fields:
+        assert got[("off", f)] == getattr(fa.FaParams, f).offset, f
+    assert len(consts) == 13  # 7 status codes, 3 flags, 3 element types
+    for n in consts:
+        assert got[("const", n)] == getattr(fa, n), n
