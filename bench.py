@@ -311,9 +311,7 @@ def run_ours(args):
         "kernel_ms": per_kernel,
         "roofline": roof,
         "e2e": e2e,
-        # per step: fwd, bwd_pre, bwd_main, plus the dQ conversion below d = 128 (at d = 128 the
-        # main kernel writes dQ) and the sink-gradient reduction with sinks
-        "gpu_launches": (3 + (w["d"] != 128) + bool(w.get("sinks"))) * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "step_ms": {"median": statistics.median(times), "mean": statistics.mean(times),
                     "std": statistics.pstdev(times), "min": min(times), "max": max(times)},

@@ -285,7 +285,7 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
 struct BwdPlan {
     bool empty = true;
     int n_qtiles = 0, n_kvblocks = 0, n_bands = 1;
-    size_t off_delta = 0, off_lse2 = 0, off_dq = 0, off_sink = 0, off_count = 0, off_done = 0;
+    size_t off_delta = 0, off_lse2 = 0, off_dq = 0, off_sink = 0, off_count = 0;
     size_t ws_bytes = kStatusBytes;
 };
 
@@ -326,10 +326,6 @@ fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     if (flags & FA_FLAG_DETERMINISTIC) {  // one counter per (key/value head, query tile)
         pl.off_count = pl.ws_bytes;
         pl.ws_bytes += align256((size_t)p.h_kv * pl.n_qtiles * 4);
-    }
-    if (p.d == 128) {  // d = 128: landed-contribution counters per (query tile, 32-column slice)
-        pl.off_done = pl.ws_bytes;
-        pl.ws_bytes += align256((size_t)p.h_kv * pl.n_qtiles * 4 * 4);
     }
     return FA_OK;
 }
@@ -553,7 +549,6 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.dsinks = p.sinks ? dsinks : nullptr;
     a.sink_t = p.sinks ? reinterpret_cast<float*>(ws + pl.off_sink) : nullptr;
     a.dq_count = (in->flags & FA_FLAG_DETERMINISTIC) ? reinterpret_cast<int*>(ws + pl.off_count) : nullptr;
-    a.dq_done = p.d == 128 ? reinterpret_cast<int*>(ws + pl.off_done) : nullptr;
     a.status = status;
 
     const int tokens_q = p.cu_q ? p.T_q : p.s_q;

@@ -85,46 +85,6 @@ __device__ __forceinline__ void block_qtiles(const Problem& p, const SeqView& sv
     qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
 }
 
-// Number of key blocks of the sequence whose query-tile range (block_qtiles) contains
-// query tile t: the blocks that add into the tile's dQ rows.  Solved for the blocks: with
-// s0 / s1 the tile's first and last position, block blk takes part when its first key
-// blk * 128 is at most s1 + off + right (right >= 0) and its last key min(blk * 128 + 127,
-// nk - 1) is at least s0 + off - left (left >= 0); those blocks form one range.
-__device__ __forceinline__ int dq_contributors(const Problem& p, const SeqView& sv, const Band& band, int t) {
-    const int nblk = cdiv(sv.nk, kRows);
-    const int s0 = t * p.P, s1 = min(s0 + p.P, sv.nq) - 1;
-    if (nblk <= 0 || s1 < s0) return 0;
-    int b_lo = 0, b_hi = nblk - 1;
-    if (p.left >= 0) {
-        const int x = s0 + band.off - p.left;  // first key a position of the tile sees
-        if (x > sv.nk - 1) return 0;
-        b_lo = max(x, 0) / kRows;
-    }
-    if (p.right >= 0) {
-        const int y = s1 + band.off + p.right;  // last key a position of the tile sees
-        if (y < 0) return 0;
-        b_hi = min(b_hi, y / kRows);
-    }
-    return max(0, b_hi - b_lo + 1);
-}
-
-// Writes the dQ rows of one 32-column slice of query tile t (the calling warp's lane =
-// column dcol): dQ = scale * accumulator, rounded to the inputs' 16-bit type.  Called once
-// every contribution to the slice has landed and is visible to the warp.
-template <int D, bool F16>
-__device__ __forceinline__ void dq_write_slice(const BwdArgs& a, const SeqView& sv, int g, int tbase, int t,
-                                               int dcol) {
-    const Problem& p = a.p;
-    const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
-    const float* src = a.dq_acc + trow * D + dcol;
-    const int rows = min(p.P, sv.nq - t * p.P) * p.G;  // packed rows of valid positions
-#pragma unroll 8
-    for (int r = 0; r < rows; ++r) {
-        const int i = t * p.P + r / p.G, h = g * p.G + r % p.G;
-        a.dq[(token_row(p, sv, i) * p.h_q + h) * D + dcol] = round16<F16>(p.scale * __ldcg(src + (long)r * D));
-    }
-}
-
 // Deterministic dQ order.  Every query tile receives the contributions of the key blocks
 // that see it in descending block order, each block's contribution complete before the
 // next one starts, so the fp32 sums are formed in the same order on every run.  A key
@@ -294,26 +254,6 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
             DqOrder order;
             order.next = blk + 1;
-            // The warp that lands the last contribution to a (query tile, 32-column slice)
-            // writes the slice's dQ rows.  Default order: a per-slice counter, incremented one
-            // step late (after the next tile's TMEM drain), so the fence that publishes a
-            // tile's reductions finds them long completed instead of stalling the drain.
-            // Deterministic order: the last block in the order is known in advance.
-            int* done = a.dq_done + ((long)g * a.n_qtiles + tbase) * 4 + (warp & 3);
-            auto land = [&](int tl) {
-                __threadfence();
-                __syncwarp();
-                int old = 0;
-                if (lane == 0) {
-                    old = atomicAdd(done + 4 * tl, 1);
-                    __threadfence();
-                }
-                old = __shfl_sync(0xffffffffu, old, 0);
-                __syncwarp();
-                if (old == dq_contributors(p, sv, band, tl) - 1) dq_write_slice<D, F16>(a, sv, g, tbase, tl, dcol);
-            };
-            int pend = -1;  // default order: the tile whose count this warp still owes
-            bool ok = true;
             for (int it = 0; it < nsteps; ++it) {
                 const int t = qt0 + it;
                 const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
@@ -321,7 +261,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 if constexpr (DET) need = 4 * dq_predecessors(p, sv, band, order, t);
                 {
                     const bool w = mbar_wait(&s.dq_full, it & 1, ab);
-                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                    if (!__all_sync(0xffffffffu, w)) break;
                 }
                 tc_fence_after();
                 uint32_t qa[64], qb[64];
@@ -330,29 +270,15 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 // the columns are free as soon as they are in registers
                 tc_fence_before();
                 mbar_arrive(&s.dq_free);
-                if constexpr (!DET) {
-                    if (pend >= 0) land(pend);
-                    pend = t;
-                }
                 int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
-                if (DET && !dq_turn_wait(cnt, need, ab)) { ok = false; break; }
+                if (DET && !dq_turn_wait(cnt, need, ab)) break;
                 // for each query row the 32 lanes of a warp add to 32 consecutive floats
                 float* acc = a.dq_acc + trow * D + dcol;
 #pragma unroll
                 for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qa[r]));
 #pragma unroll
                 for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
-                if constexpr (DET) {
-                    dq_turn_done(cnt);
-                    // every later block has added into this tile: the last contribution is ours
-                    if (need == 4 * (dq_contributors(p, sv, band, t) - 1)) {
-                        __threadfence();
-                        dq_write_slice<D, F16>(a, sv, g, tbase, t, dcol);
-                    }
-                }
-            }
-            if constexpr (!DET) {
-                if (ok && pend >= 0) land(pend);
+                if constexpr (DET) dq_turn_done(cnt);
             }
         }
     } else if (warp < 4) {
@@ -675,7 +601,6 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
     const bool live = decode_qtile(p, idx, seq, t);
     const long trow = ((long)g * a.n_qtiles + idx) * 128;
     if (a.dq_count && threadIdx.x == 0) a.dq_count[(long)g * a.n_qtiles + idx] = 0;
-    if (a.dq_done && threadIdx.x < 4) a.dq_done[((long)g * a.n_qtiles + idx) * 4 + threadIdx.x] = 0;
     if (!live) {
         a.lse2_t[trow + threadIdx.x] = INFINITY;
         a.delta_t[trow + threadIdx.x] = 0.f;
@@ -683,18 +608,6 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
         return;
     }
     const SeqView sv = seq_view(p, seq);
-    if constexpr (D == 128) {
-        // the main kernel writes a tile's dQ rows when its last contribution lands; a tile
-        // that no key block adds into gets its zero rows here
-        if (a.dq_done && dq_contributors(p, sv, Band{sv.nk - sv.nq, p.left, p.right, sv.nk}, t) == 0) {
-            const int r = threadIdx.x, i = t * p.P + r / p.G, h = g * p.G + r % p.G;
-            if (r < p.P * p.G && i < sv.nq) {
-                uint4* row = reinterpret_cast<uint4*>(a.dq + (token_row(p, sv, i) * p.h_q + h) * D);
-#pragma unroll
-                for (int x = 0; x < D / 8; ++x) row[x] = make_uint4(0, 0, 0, 0);
-            }
-        }
-    }
     // a warp takes its 32 rows RPI at a time: LPR lanes per row, 16 bytes (8 elements) of O
     // and dO each, so every load instruction moves whole 128-byte lines
     constexpr int LPR = D / 8, RPI = 32 / LPR;
@@ -831,13 +744,10 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st) {
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t st) {
     dim3 grid(a.n_qtiles, a.p.h_kv);
     if (a.n_qtiles == 0) return cudaSuccess;
-    // d = 128: the main kernel has written dQ already (dq_done)
-    if (!a.dq_done) {
-        const bool f16 = a.p.dtype == FA_DTYPE_F16;
-        auto kernel = a.p.d == 64 ? (f16 ? bwd_post_kernel<64, true> : bwd_post_kernel<64, false>)
-                                  : (f16 ? bwd_post_kernel<128, true> : bwd_post_kernel<128, false>);
-        kernel<<<grid, 128, 0, st>>>(a);
-    }
+    const bool f16 = a.p.dtype == FA_DTYPE_F16;
+    auto kernel = a.p.d == 64 ? (f16 ? bwd_post_kernel<64, true> : bwd_post_kernel<64, false>)
+                              : (f16 ? bwd_post_kernel<128, true> : bwd_post_kernel<128, false>);
+    kernel<<<grid, 128, 0, st>>>(a);
     if (a.dsinks) bwd_dsink_kernel<<<a.p.h_q, 256, 0, st>>>(a);
     return cudaGetLastError();
 }

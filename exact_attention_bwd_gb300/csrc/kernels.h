@@ -101,9 +101,6 @@ struct BwdArgs {
     float* sink_t;         // [h_kv, n_qtiles, 128]  per-row sink-gradient terms (with sinks)
     int* dq_count;         // [h_kv, n_qtiles] dQ contributions landed per query tile, or null:
                            // non-null = deterministic order (key blocks in descending order)
-    int* dq_done;          // d = 128: [h_kv, n_qtiles, 4] key blocks whose dQ contributions to
-                           // each 32-column slice of a query tile have landed; the last one
-                           // writes the slice's dQ rows (no separate conversion pass), else null
     int* status;
 };
 

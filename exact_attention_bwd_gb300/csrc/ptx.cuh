@@ -674,10 +674,6 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
     }
 }
 template <bool F16>
-__device__ __forceinline__ uint16_t round16(float x) {
-    return (uint16_t)(pack16<F16>(x, 0.f) & 0xFFFFu);
-}
-template <bool F16>
 __device__ __forceinline__ float lo16(uint32_t w) {
     if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
     else return bf16_lo(w);
