@@ -291,19 +291,21 @@ struct BwdPlan {
 
 fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     pl = BwdPlan();
-    if (p.d != 64 && p.d != 128) return FA_ERR_UNSUPPORTED;
+    if (p.d != 64 && p.d != 128 && p.d != 256) return FA_ERR_UNSUPPORTED;
+    if (p.d == 256 && (flags & FA_FLAG_DETERMINISTIC)) return FA_ERR_UNSUPPORTED;  // fixed dQ order: d <= 128
     if (p.block_table) return FA_ERR_UNSUPPORTED;  // paged caches: forward only
     if (p.dtype == FA_DTYPE_E4M3) return FA_ERR_UNSUPPORTED;      // e4m3: forward only
     const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
     const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
     if (p.B == 0 || (rows_total == 0 && keys_total == 0)) return FA_OK;
     pl.empty = false;
+    const int kvb = p.d == 256 ? 64 : kTileRows;  // keys per CTA (d = 256: 64)
     if (p.cu_q) {
         pl.n_qtiles = p.T_q / p.P + p.B;
-        pl.n_kvblocks = p.T_k / kTileRows + p.B;
+        pl.n_kvblocks = p.T_k / kvb + p.B;
     } else {
         pl.n_qtiles = p.B * ((p.s_q + p.P - 1) / p.P);
-        pl.n_kvblocks = (p.s_kv + kTileRows - 1) / kTileRows;
+        pl.n_kvblocks = (p.s_kv + kvb - 1) / kvb;
         // a (batch, key/value head) unit's CTAs all read its Q and dO tiles and add into its
         // dQ accumulator rows (16-bit Q + dO, fp32 accumulator: 8 bytes per row and column);
         // take as many units at a time as keep that within half the L2, in bands of
@@ -558,8 +560,8 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     const bool f16 = p.dtype == FA_DTYPE_F16;
     if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16) ||
         !encode_bhsd(&tdo, dout, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16) ||
-        !encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, 128, f16) ||
-        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, 128, f16))
+        !encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, p.d == 256 ? 64 : 128, f16) ||
+        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, p.d == 256 ? 64 : 128, f16))
         return FA_ERR_CUDA;
     cudaError_t e = timed(kBwdPre, st, [&] { return launch_bwd_pre(a, st); });
     if (e != cudaSuccess) return FA_ERR_CUDA;

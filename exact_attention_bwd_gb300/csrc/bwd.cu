@@ -577,6 +577,337 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 }
 
 // ------------------------------------------------------------------------------------------
+// backward at d = 256: one CTA per 64-key block, query rows on the tensor-memory lanes
+// ------------------------------------------------------------------------------------------
+// The d <= 128 layout (128-key block, the key rows on the lanes, dK and dV accumulated in
+// tensor memory at full width) does not fit at d = 256: the two 256-column accumulators
+// alone fill the 512 columns.  Here a CTA owns 64 keys and the GEMMs are oriented so that
+// every accumulator has M = 128 on the lanes:
+//   S = Q K^T, dP = dO V^T          M = 128 query rows, N = 64 keys       (64 + 64 columns)
+//   dV^T += dO^T P, dK^T += Q^T dS  M = 128 of d (two halves), N = 64     (128 + 128 columns)
+//   dQ^T = K^T dS^T                 M = 128 of d (two halves, one after the other), N = 128
+//                                   query rows, drained between the halves (128 columns)
+// P and dS go through shared memory ([query row][64 keys], 128-byte swizzle), where they
+// serve as the MN-major B operand of dV^T / dK^T and the K-major B operand of dQ^T.  Shared
+// memory holds Q, dO (64 KB each, one buffer), K, V (32 KB each) and P, dS (16 KB each).
+//
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 owns the TMEM
+// allocation, warps 4-7 the compute group (thread = TMEM lane: a query row for P / dS, a
+// column of d for the dQ^T drain and the dK / dV epilogue).
+constexpr int kThreadsBwd256 = 256;
+constexpr int kKeys256 = 64;  // keys per block
+
+struct __align__(1024) BwdSmem256 {
+    uint8_t q[4][128 * 128];       // [128 packed rows][64 cols] x 4 chunks of d
+    uint8_t dO[4][128 * 128];
+    uint8_t k[4][kKeys256 * 128];  // [64 keys][64 cols] x 4 chunks of d
+    uint8_t v[4][kKeys256 * 128];
+    uint8_t p[128 * 128];          // P:  [128 query rows][64 keys]
+    uint8_t ds[128 * 128];         // dS: [128 query rows][64 keys]
+    float stat[2][128];            // LSE * log2(e) and D of the tile's rows
+    uint64_t kv_full, q_full, q_empty, do_full, do_empty, s_full, dp_full, pds_full, pds_free, dq_full, dq_free,
+        dkv_full;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(BwdSmem256) <= 232448, "d = 256 backward: shared memory over the 227 KB limit");
+
+// Query tiles [qt0, qt1) whose positions have a band reaching 64-key block `blk`.
+__device__ __forceinline__ void block_qtiles64(const Problem& p, const SeqView& sv, const Band& band, int blk,
+                                               int& qt0, int& qt1) {
+    const int j0 = blk * kKeys256;
+    const int j1 = min(j0 + kKeys256, sv.nk) - 1;
+    int i_lo = 0, i_hi = sv.nq - 1;
+    if (p.right >= 0) i_lo = max(i_lo, j0 - band.off - p.right);
+    if (p.left >= 0) i_hi = min(i_hi, j1 - band.off + p.left);
+    qt0 = (i_hi >= i_lo) ? i_lo / p.P : 0;
+    qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kThreadsBwd256, 1)
+    bwd256_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
+    constexpr int D = 256;
+    // TMEM columns
+    constexpr uint32_t C_S = 0, C_DP = 64, C_DV = 128, C_DK = 256, C_DQ = 384;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the layout fills the shared memory: no room to realign by hand
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0 && a.status) atomicCAS(a.status, 0, kStatusDeviceCheck);
+        return;
+    }
+    BwdSmem256& s = *reinterpret_cast<BwdSmem256*>(smem_raw);
+    const Problem& p = a.p;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int g, seq, blk;
+    {
+        const int idx = blockIdx.x;
+        if (p.cu_q) {
+            g = idx % p.h_kv;
+            blk = idx / p.h_kv;
+            seq = owner_sequence(p.cu_k, p.B, blk, kKeys256);
+            blk -= p.cu_k[seq] / kKeys256 + seq;
+        } else {
+            int unit;
+            band_order(idx, p.h_kv * p.B, a.n_bands, a.n_kvblocks, unit, blk);
+            g = unit % p.h_kv;
+            seq = unit / p.h_kv;
+        }
+    }
+    const SeqView sv = seq_view(p, seq);
+    const int j0 = blk * kKeys256;
+    if (j0 >= sv.nk) return;  // idle packed-batch block
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
+    const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
+    int qt0, qt1;
+    block_qtiles64(p, sv, band, blk, qt0, qt1);
+    const int nsteps = qt1 - qt0;
+    const int tbase = qtile_base(p, seq);
+
+    Abort ab{&s.abort_flag, a.status};
+    if (tid == 0) {
+        s.abort_flag = 0;
+        mbar_init(&s.kv_full, 1);
+        mbar_init(&s.q_full, 1);
+        mbar_init(&s.q_empty, 1);
+        mbar_init(&s.do_full, 1);
+        mbar_init(&s.do_empty, 1);
+        mbar_init(&s.s_full, 1);
+        mbar_init(&s.dp_full, 1);
+        mbar_init(&s.pds_full, 128);
+        mbar_init(&s.pds_free, 1);
+        mbar_init(&s.dq_full, 1);
+        mbar_init(&s.dq_free, 128);
+        mbar_init(&s.dkv_full, 1);
+        fence_mbar_init();
+    }
+    if (p.P * p.G < 128) {
+        // rows past P*G of a query tile are never written by TMA: zero them once
+        for (int c = 0; c < 4; ++c)
+            for (int x = p.P * p.G * 128 + tid * 16; x < 128 * 128; x += kThreadsBwd256 * 16) {
+                *reinterpret_cast<uint4*>(&s.q[c][x]) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(&s.dO[c][x]) = make_uint4(0, 0, 0, 0);
+            }
+        fence_proxy_async_smem();
+    }
+    if (warp == 2) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0 && nsteps > 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            tma_prefetch_desc(&tmdo);
+            mbar_expect_tx(&s.kv_full, 2 * 4 * kKeys256 * 128);
+            for (int c = 0; c < 4; ++c) {
+                tma_load_4d(s.k[c], &tmk, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
+                tma_load_4d(s.v[c], &tmv, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
+            }
+            const uint32_t tile_bytes = (uint32_t)(p.P * p.G) * 128u * 4u;  // one Q or dO tile
+            int q_issued = 0, do_issued = 0;
+            for (int it = 0; it < nsteps; ++it) {
+                const uint32_t ph = it & 1;
+                const int row = sv.q0 + (qt0 + it) * p.P;
+                if (!mbar_wait(&s.q_empty, ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.q_full, tile_bytes + 2 * 128 * 4);
+                for (int c = 0; c < 4; ++c) tma_load_4d(s.q[c], &tmq, &s.q_full, c * 64, g * p.G, row, sv.tma_b);
+                {
+                    const long trow = ((long)g * a.n_qtiles + tbase + qt0 + it) * 128;
+                    bulk_load(s.stat[0], a.lse2_t + trow, 512, &s.q_full);
+                    bulk_load(s.stat[1], a.delta_t + trow, 512, &s.q_full);
+                }
+                ++q_issued;
+                if (!mbar_wait(&s.do_empty, ph ^ 1, ab)) break;
+                mbar_expect_tx(&s.do_full, tile_bytes);
+                for (int c = 0; c < 4; ++c) tma_load_4d(s.dO[c], &tmdo, &s.do_full, c * 64, g * p.G, row, sv.tma_b);
+                ++do_issued;
+            }
+            // the copies still in flight: the last phase of each buffer
+            if (q_issued > 0) mbar_wait_quiet(&s.q_full, (q_issued - 1) & 1);
+            if (do_issued > 0) mbar_wait_quiet(&s.do_full, (do_issued - 1) & 1);
+            mbar_wait_quiet(&s.kv_full, 0);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0 && nsteps > 0) {
+            constexpr uint32_t id_s = idesc_16(128, kKeys256, false, false, F16);   // S, dP: K-major both
+            constexpr uint32_t id_kv = idesc_16(128, kKeys256, true, true, F16);    // dV^T, dK^T: MN-major both
+            constexpr uint32_t id_dq = idesc_16(128, 128, true, false, F16);        // dQ^T: A MN-major, B K-major
+            const uint64_t qd_k = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
+            const uint64_t dod_k = sdesc_sw128(smem_u32(s.dO[0]), 16, 1024);
+            const uint64_t kd_k = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
+            const uint64_t vd_k = sdesc_sw128(smem_u32(s.v[0]), 16, 1024);
+            const uint64_t pd_mn = sdesc_sw128(smem_u32(s.p), 128 * 128, 1024);
+            const uint64_t dsd_mn = sdesc_sw128(smem_u32(s.ds), 128 * 128, 1024);
+            const uint64_t dsd_k = sdesc_sw128(smem_u32(s.ds), 16, 1024);
+            bool ok = mbar_wait(&s.kv_full, 0, ab);
+            int ndq = 0;  // dQ^T halves issued so far
+            for (int it = 0; ok && it < nsteps; ++it) {
+                const uint32_t par = it & 1;
+                if (!(ok = mbar_wait(&s.q_full, par, ab))) break;
+                if (!(ok = mbar_wait(&s.do_full, par, ab))) break;
+                tc_fence_after();
+                // S = Q K^T, dP = dO V^T (K = 256: four 64-column chunks of each operand)
+                mma_ss_k16k8_x16(tmem + C_S, qd_k, kd_k, id_s, 0u);
+                tc_commit(&s.s_full);
+                mma_ss_k16k8_x16(tmem + C_DP, dod_k, vd_k, id_s, 0u);
+                tc_commit(&s.dp_full);
+                // P and dS in shared memory (the compute group has also read S and dP out)
+                if (!(ok = mbar_wait(&s.pds_full, par, ab))) break;
+                tc_fence_after();
+                const uint32_t acc = it > 0 ? 1u : 0u;
+                for (int h = 0; h < 2; ++h) {
+                    // dV^T_h += dO_h^T P, dK^T_h += Q_h^T dS (the h-th 128 columns of d)
+                    mma_ss_mnmn_x8(tmem + C_DV + 64 * h, sdesc_sw128(smem_u32(s.dO[2 * h]), 128 * 128, 1024), pd_mn,
+                                   id_kv, acc);
+                    mma_ss_mnmn_x8(tmem + C_DK + 64 * h, sdesc_sw128(smem_u32(s.q[2 * h]), 128 * 128, 1024), dsd_mn,
+                                   id_kv, acc);
+                }
+                for (int h = 0; h < 2; ++h) {
+                    // dQ^T_h = K_h^T dS^T into the one dQ^T column block, drained in between
+                    if (ndq > 0 && !(ok = mbar_wait(&s.dq_free, (ndq - 1) & 1, ab))) break;
+                    tc_fence_after();
+                    mma_ss_mnk_x4(tmem + C_DQ, sdesc_sw128(smem_u32(s.k[2 * h]), kKeys256 * 128, 1024), dsd_k, id_dq,
+                                  0u);
+                    tc_commit(&s.dq_full);
+                    ++ndq;
+                }
+                if (!ok) break;
+                // Q, dO, P and dS of this step are read once these MMAs complete
+                tc_commit(&s.q_empty);
+                tc_commit(&s.do_empty);
+                tc_commit(&s.pds_free);
+            }
+            tc_commit(&s.dkv_full);
+            mbar_wait_quiet(&s.dkv_full, 0);
+        }
+    } else if (warp >= 4) {
+        // ================= compute group =================
+        const int wq = warp & 3;
+        const int r = (wq << 5) | lane;  // TMEM lane: query row (P, dS) or column of d (drains)
+        const uint32_t lane_base = (uint32_t)(wq << 5) << 16;
+        const float c = p.scale_log2;
+        bool ok = true;
+        int ndq = 0;
+        for (int it = 0; it < nsteps; ++it) {
+            const uint32_t par = it & 1;
+            const int t = qt0 + it;
+            const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
+            {
+                bool w = mbar_wait(&s.q_full, par, ab);  // the LSE / D rows land with Q
+                w = w && mbar_wait(&s.s_full, par, ab);
+                w = w && mbar_wait(&s.dp_full, par, ab);
+                if (it > 0) w = w && mbar_wait(&s.pds_free, par ^ 1, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            tc_fence_after();
+            // ---- P = exp2(S c - LSE2) on the allowed keys, dS = P (dP - D); row r ----
+            {
+                const int i = t * p.P + r / p.G;  // query position of this row
+                const bool row_ok = r < p.P * p.G && i < sv.nq;
+                // allowed keys of the row, as columns [c_lo, c_hi) of this block
+                const int c_lo = row_ok ? band.lo(i) - j0 : 0;
+                const int c_hi = row_ok ? band.hi(i) + 1 - j0 : 0;
+                const float l2 = s.stat[0][r], dl = s.stat[1][r];
+                uint32_t sr[64], dr[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + C_S, sr);
+                tmem_ld_32x32b_x64(tmem + lane_base + C_DP, dr);
+                // S and dP are in registers: the next step's S / dP may overwrite them once
+                // this step's P and dS are handed over (pds_full)
+                uint8_t* prow = s.p + r * 128;
+                uint8_t* drow = s.ds + r * 128;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {  // 16-byte units of 8 keys
+                    float pv[8], dv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int cc = 8 * u + e;
+                        const float pe = (cc >= c_lo && cc < c_hi) ? ex2(fmaf(__uint_as_float(sr[cc]), c, -l2)) : 0.f;
+                        pv[e] = pe;
+                        dv[e] = pe * (__uint_as_float(dr[cc]) - dl);
+                    }
+                    const int unit = (u ^ (r & 7)) << 4;
+                    *reinterpret_cast<uint4*>(prow + unit) = make_uint4(
+                        pack16<F16>(pv[0], pv[1]), pack16<F16>(pv[2], pv[3]), pack16<F16>(pv[4], pv[5]),
+                        pack16<F16>(pv[6], pv[7]));
+                    *reinterpret_cast<uint4*>(drow + unit) = make_uint4(
+                        pack16<F16>(dv[0], dv[1]), pack16<F16>(dv[2], dv[3]), pack16<F16>(dv[4], dv[5]),
+                        pack16<F16>(dv[6], dv[7]));
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&s.pds_full);
+            // ---- dQ^T halves: lane = column of d within the half, columns = query rows ----
+            for (int h = 0; h < 2; ++h) {
+                {
+                    const bool w = mbar_wait(&s.dq_full, ndq & 1, ab);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                }
+                ++ndq;
+                tc_fence_after();
+                uint32_t qa[64], qb[64];
+                tmem_ld_32x32b_x64(tmem + lane_base + C_DQ, qa);
+                tmem_ld_32x32b_x64(tmem + lane_base + C_DQ + 64, qb);
+                tc_fence_before();
+                mbar_arrive(&s.dq_free);
+                // for each query row the 32 lanes of a warp add to 32 consecutive floats
+                float* acc = a.dq_acc + trow * D + 128 * h + r;
+#pragma unroll
+                for (int x = 0; x < 64; ++x) atomicAdd(acc + (long)x * D, __uint_as_float(qa[x]));
+#pragma unroll
+                for (int x = 0; x < 64; ++x) atomicAdd(acc + (long)(64 + x) * D, __uint_as_float(qb[x]));
+            }
+            if (!ok) break;
+        }
+        // ---- epilogue: dV, dK of the block's 64 keys (lane = column of d within a half) ----
+        if (nsteps > 0 && ok) {
+            const bool w = mbar_wait(&s.dkv_full, 0, ab);
+            ok = __all_sync(0xffffffffu, w);
+            tc_fence_after();
+        }
+        const int nkeys = min(kKeys256, sv.nk - j0);
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+            uint16_t* base = which == 0 ? a.dv : a.dk;
+            const float mul = which == 0 ? 1.f : p.scale;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v[64];
+                if (nsteps > 0 && ok) {
+                    tmem_ld_32x32b_x64(tmem + lane_base + (which == 0 ? C_DV : C_DK) + 64 * h, v);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 64; ++x) v[x] = 0u;
+                }
+                // key rows are consecutive within a sequence: one stride of h_kv * d elements
+                uint16_t* dst = base + (key_row(p, sv, j0) * p.h_kv + g) * D + 128 * h + r;
+                const long stride = (long)p.h_kv * D;
+#pragma unroll
+                for (int x = 0; x < 64; ++x, dst += stride)
+                    if (x < nkeys) *dst = round16<F16>(__uint_as_float(v[x]) * mul);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
 // preprocess: one CTA (128 threads) per (tiled query tile, key/value head)
 // ------------------------------------------------------------------------------------------
 // Decodes a tiled query-tile index into (sequence, tile within it); false for an idle tile.
@@ -718,9 +1049,23 @@ static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const 
     return cudaGetLastError();
 }
 
+static cudaError_t launch_main256(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t st) {
+    const size_t smem = sizeof(BwdSmem256);
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd256_kernel<true> : bwd256_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
+    kernel<<<(unsigned)n, kThreadsBwd256, smem, st>>>(a, tq, tk, tv, tdo);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, cudaStream_t st) {
     switch (a.p.d) {
+        case 256:
+            // the fixed dQ order is not built at d = 256 (the planner refuses the flag)
+            return a.dq_count ? cudaErrorInvalidValue : launch_main256(a, tq, tk, tv, tdo, st);
         case 64:
             return a.dq_count ? launch_main_d<64, true>(a, tq, tk, tv, tdo, st)
                               : launch_main_d<64, false>(a, tq, tk, tv, tdo, st);
@@ -735,8 +1080,9 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st) {
     dim3 grid(a.n_qtiles, a.p.h_kv);
     if (a.n_qtiles == 0) return cudaSuccess;
     const bool f16 = a.p.dtype == FA_DTYPE_F16;
-    auto kernel = a.p.d == 64 ? (f16 ? bwd_pre_kernel<64, true> : bwd_pre_kernel<64, false>)
-                              : (f16 ? bwd_pre_kernel<128, true> : bwd_pre_kernel<128, false>);
+    auto kernel = a.p.d == 64    ? (f16 ? bwd_pre_kernel<64, true> : bwd_pre_kernel<64, false>)
+                  : a.p.d == 128 ? (f16 ? bwd_pre_kernel<128, true> : bwd_pre_kernel<128, false>)
+                                 : (f16 ? bwd_pre_kernel<256, true> : bwd_pre_kernel<256, false>);
     kernel<<<grid, 128, 0, st>>>(a);
     return cudaGetLastError();
 }
@@ -745,8 +1091,9 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t st) {
     dim3 grid(a.n_qtiles, a.p.h_kv);
     if (a.n_qtiles == 0) return cudaSuccess;
     const bool f16 = a.p.dtype == FA_DTYPE_F16;
-    auto kernel = a.p.d == 64 ? (f16 ? bwd_post_kernel<64, true> : bwd_post_kernel<64, false>)
-                              : (f16 ? bwd_post_kernel<128, true> : bwd_post_kernel<128, false>);
+    auto kernel = a.p.d == 64    ? (f16 ? bwd_post_kernel<64, true> : bwd_post_kernel<64, false>)
+                  : a.p.d == 128 ? (f16 ? bwd_post_kernel<128, true> : bwd_post_kernel<128, false>)
+                                 : (f16 ? bwd_post_kernel<256, true> : bwd_post_kernel<256, false>);
     kernel<<<grid, 128, 0, st>>>(a);
     if (a.dsinks) bwd_dsink_kernel<<<a.p.h_q, 256, 0, st>>>(a);
     return cudaGetLastError();

@@ -335,6 +335,29 @@ __device__ __forceinline__ void mma_ss_mnmn_x8(uint32_t d_tmem, uint64_t a, uint
         : "memory");
 }
 
+// A MN-major, B K-major (one 128-byte row of K per B row), 4 steps (K = 64)
+__device__ __forceinline__ void mma_ss_mnk_x4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 128; mov.b64 da, {ta, %4}; add.u32 tb, %5, 2; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 256; mov.b64 da, {ta, %4}; add.u32 tb, %5, 4; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 384; mov.b64 da, {ta, %4}; add.u32 tb, %5, 6; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
 // A K-major 16 KB chunks, B K-major 8 KB chunks, 16 steps (K = 256)
 __device__ __forceinline__ void mma_ss_k16k8_x16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
     const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
@@ -672,6 +695,10 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
     } else {
         return pack_bf16(lo, hi);
     }
+}
+template <bool F16>
+__device__ __forceinline__ uint16_t round16(float x) {
+    return (uint16_t)(pack16<F16>(x, 0.f) & 0xFFFFu);
 }
 template <bool F16>
 __device__ __forceinline__ float lo16(uint32_t w) {

@@ -105,7 +105,9 @@ def test_workspace_too_small():
 
 def test_backward_rejects():
     assert call_bwd(params(sinks=0x3000), dsinks=None) == fa.FA_ERR_INVALID_ARG
-    assert call_bwd(params(d=256)) == fa.FA_ERR_UNSUPPORTED
+    assert call_bwd(params(d=192)) == fa.FA_ERR_UNSUPPORTED
+    # d = 256 has no fixed-order (deterministic) dQ
+    assert call_bwd(params(d=256, flags=fa.FA_FLAG_DETERMINISTIC)) == fa.FA_ERR_UNSUPPORTED
     assert call_bwd(params(h_q=3, h_kv=2)) == fa.FA_ERR_INVALID_ARG
     assert call_bwd(params(), q=MISAL) == fa.FA_ERR_INVALID_ARG
 
@@ -217,7 +219,7 @@ def test_f16_is_planned_like_bf16():
         assert fa.fa_bwd_workspace_size(params(dtype=fa.FA_DTYPE_F16, **kw)) == fa.fa_bwd_workspace_size(params(**kw))
     assert call_fwd(params(dtype=fa.FA_DTYPE_F16), ws_bytes=16) == fa.FA_ERR_WORKSPACE
     assert call_bwd(params(dtype=fa.FA_DTYPE_F16), ws_bytes=16) == fa.FA_ERR_WORKSPACE
-    assert call_bwd(params(dtype=fa.FA_DTYPE_F16, d=256)) == fa.FA_ERR_UNSUPPORTED
+    assert call_bwd(params(dtype=fa.FA_DTYPE_F16, d=256), ws_bytes=16) == fa.FA_ERR_WORKSPACE
 
 
 def test_binding_checks_f16_types():
@@ -266,3 +268,14 @@ def test_params_layout_and_constants_match_the_header(tmp_path):
     assert len(consts) == 13  # 7 status codes, 3 flags, 3 element types
     for n in consts:
         assert got[("const", n)] == getattr(fa, n), n
+
+
+def test_d256_backward_workspace():
+    """d = 256: 64-key blocks; the workspace holds the same per-row statistics and a dQ
+    accumulator of 128 rows x 256 fp32 columns per (query tile, key/value head)."""
+    p = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=256)
+    tiles = 2 * -(-300 // 64)   # P = 64 positions per 128-row tile (G = 2)
+    stat = 2 * tiles * 128 * 4
+    align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert fa.fa_bwd_workspace_size(p) == 256 + 2 * align(stat) + align(2 * tiles * 128 * 256 * 4)
+    assert call_bwd(p, ws_bytes=16) == fa.FA_ERR_WORKSPACE
