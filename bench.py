@@ -329,6 +329,8 @@ def run_ours(args):
                        for n in ("sweep_s8192_causal", "sweep_s8192", "sweep_s2048", "gqa_window_causal", "varlen")}
         line["e4m3_fwd"] = {n: measure_fp8(dev, n) for n in ("sweep_s8192_causal", "sweep_s8192", "sweep_s16384",
                                                               "sweep_s2048", "decode_d128_sq64")}
+    if not args.no_sweep:
+        line["d256"] = measure_d256(dev)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = oracle_sample(w)
     if rank == 0:
@@ -411,7 +413,7 @@ def run_e2e(args, fa, kw, ins, outs, flops, world, dev):
 # every other workload: forward and forward+backward TFLOPS (context beside the headline)
 # ----------------------------------------------------------------------------------------------
 
-def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0, dtype="bf16"):
+def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0, dtype="bf16", check_status=False):
     """fwd and fwd+bwd of one prefill workload with seeded on-device inputs (the same recipe
     seeds, drawn by torch's generator); L2 flushed before every timed step.  bwd_flags:
     fa_params flags of the backward (FA_FLAG_DETERMINISTIC for the fixed-order dQ sums);
@@ -459,12 +461,33 @@ def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0, dtype="bf16"):
         if it >= warmup:
             tf.append(e0.elapsed_time(e1))
             tb.append(e1.elapsed_time(e2))
+    if check_status and (fa.device_status(wsf) != 0 or fa.device_status(wsb) != 0):
+        raise RuntimeError(f"{name}: device status nonzero after the timed steps")
     ff = metrics.fwd_flops(wf)
     mf, mb = statistics.mean(tf), statistics.mean(tb)
     del q, k, v, do, o, lse, wsf, dq, dk, dv, wsb
     torch.cuda.empty_cache()
     return {"fwd_ms": round(mf, 4), "bwd_ms": round(mb, 4), "fwd_TFLOPS": round(ff / (mf * 1e-3) / 1e12, 1),
             "fwd_bwd_TFLOPS": round(3.5 * ff / ((mf + mb) * 1e-3) / 1e12, 1)}
+
+
+def measure_d256(dev):
+    """fwd and fwd+bwd at head dim 256, with the backward's own rate against the bf16 peak.
+    Run last among the GPU sections; a failure is recorded in the section, not raised."""
+    from exact_attention_bwd_gb300 import binding as fa
+    pk = peaks()
+    out = {}
+    for name in ("d256_s8192_causal", "d256_s4096"):
+        try:
+            r = measure_workload(dev, name, check_status=True)
+            ff = metrics.fwd_flops(inputs.workload(name))
+            bt = 2.5 * ff / (r["bwd_ms"] * 1e-3) / 1e12
+            r.update(bwd_TFLOPS=round(bt, 1), bwd_frac_of_peak=round(bt / pk["bf16"], 4),
+                     fwd_frac_of_peak=round(r["fwd_TFLOPS"] / pk["bf16"], 4))
+            out[name] = r
+        except (RuntimeError, fa.FaError) as e:
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+    return out
 
 
 def measure_fp8(dev, name, steps=8, warmup=3):

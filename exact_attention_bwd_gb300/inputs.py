@@ -145,6 +145,11 @@ WORKLOADS = {
     # packed varlen
     "varlen": dict(wid=4, variant=0, B=256, T=32768, h_q=32, h_kv=32, d=128, causal=True,
                    window=(-1, -1), sinks=False, varlen=True),
+    # head dim 256, forward and backward (16k tokens, 16 heads)
+    "d256_s8192_causal": dict(wid=6, variant=0, B=2, s_q=8192, s_kv=8192, h_q=16, h_kv=16, d=256,
+                              causal=True, window=(-1, -1), sinks=False, varlen=False),
+    "d256_s4096": dict(wid=6, variant=1, B=4, s_q=4096, s_kv=4096, h_q=16, h_kv=16, d=256,
+                       causal=False, window=(-1, -1), sinks=False, varlen=False),
     # decode / chunked prefill against a long cache
     **{f"decode_d{d}_sq{sq}": dict(wid=5, variant=(0 if d == 128 else 2) + (0 if sq == 1 else 1),
                                    B=64, s_q=sq, s_kv=32768, h_q=32, h_kv=8, d=d, causal=True,

@@ -56,7 +56,8 @@
  *    limit and records FA_ERR_TIMEOUT in the workspace status word, which
  *    fa_read_device_status reports.
  *  - Supported: bf16 and fp16 (and e4m3 for the forward at d = 128, see below); head dim d in
- *    {64, 128, 256} for the forward, {64, 128} for the backward; h_q / h_kv <= 128.
+ *    {64, 128, 256} for the forward and the backward (FA_FLAG_DETERMINISTIC: d <= 128);
+ *    h_q / h_kv <= 128.
  *    Anything else returns FA_ERR_UNSUPPORTED.
  *  - Zero-initialise fa_params (memset or `= {0}`): every optional field then means
  *    "not used".
@@ -130,7 +131,8 @@ typedef enum fa_status {
  * vllm-project/flash-attention README (changelog 2.4).  A key block's CTA waits (bounded,
  * like every wait: FA_ERR_TIMEOUT) for the later blocks' contributions, which the launch
  * puts at lower CTA indices; slower than the default, markedly so without a causal mask.
- * The sink gradient is summed in a fixed order with or without the flag. */
+ * The sink gradient is summed in a fixed order with or without the flag.  d <= 128 only:
+ * with d = 256 fa_bwd returns FA_ERR_UNSUPPORTED. */
 #define FA_FLAG_DETERMINISTIC 4u
 
 typedef struct fa_params {
