@@ -16,15 +16,18 @@
 // Restrictions: GQA backward accumulates dK/dV in fp32).  dQ is accumulated in an fp32
 // workspace with atomic adds and converted by the postprocess kernel.
 //
-// Main-kernel warp roles (384 threads):
+// Main-kernel warp roles (d <= 128, 512 threads):
 //   warp 0      TMA producer: K and V once, then Q_i and dO_i through a two-stage ring
 //   warp 1      MMA issuer: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q,
-//               dQ_i = dS K, all into TMEM
+//               dQ_i (dQ^T_i = K^T dS^T at d = 128), all into TMEM
 //   warp 2      owns the TMEM allocation
 //   warps 4-11  two groups of 128: thread = key row; group c takes query columns
 //               [64c, 64c+64): P^T = exp2(S^T * c - LSE2), dS^T = P^T (dP^T - D) into
-//               shared memory; then thread = query row for the dQ tile, columns split in
-//               halves between the groups, reduced into the workspace.
+//               shared memory; at d = 64 also the dQ tile (thread = query row, columns
+//               split in halves between the groups), reduced into the workspace
+//   warps 12-15 d = 128: drain dQ^T_i (thread = column of d) and reduce it into the
+//               workspace
+// d = 256 has its own kernel (bwd256_kernel below).
 #include "common.cuh"
 
 namespace fa {
