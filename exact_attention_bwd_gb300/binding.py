@@ -49,6 +49,7 @@ class FaParams(ctypes.Structure):
         ("max_blocks_per_seq", ctypes.c_int), ("num_pages", ctypes.c_int),
         ("dtype", ctypes.c_int), ("q_descale", ctypes.c_void_p), ("k_descale", ctypes.c_void_p),
         ("v_descale", ctypes.c_void_p), ("seqused_q", ctypes.c_void_p),
+        ("wait_limit_ns", ctypes.c_ulonglong),
     ]
 
 
@@ -162,7 +163,7 @@ def _ptr(t):
 
 def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None,
                 cu_k=None, flags=0, seqused_k=None, block_table=None, s_kv=None, dtype=None, q_descale=None,
-                k_descale=None, v_descale=None, seqused_q=None) -> FaParams:
+                k_descale=None, v_descale=None, seqused_q=None, wait_limit_ns=0) -> FaParams:
     """fa_params from tensor shapes: [B,S,H,D] dense or [T,H,D] packed (with cu_q / cu_k).
 
     With a block_table ([B, max_blocks_per_seq] int32), k is a page pool
@@ -196,6 +197,7 @@ def make_params(q, k, *, causal=False, window=(-1, -1), softmax_scale=None, sink
     p.q_descale = None if q_descale is None else q_descale.data_ptr()
     p.k_descale = None if k_descale is None else k_descale.data_ptr()
     p.v_descale = None if v_descale is None else v_descale.data_ptr()
+    p.wait_limit_ns = int(wait_limit_ns)
     if block_table is not None:
         p.block_table = block_table.data_ptr()
         p.page_size, p.num_pages = int(page_size), int(num_pages)
@@ -216,7 +218,7 @@ def _stream():
 
 def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None, cu_k=None,
             flags=0, out=None, lse=None, workspace=None, seqused_k=None, block_table=None, s_kv=None,
-            descale=None, seqused_q=None):
+            descale=None, seqused_q=None, wait_limit_ns=0):
     """Runs fa_fwd on torch CUDA tensors; returns (o, lse, workspace).
 
     q, k, v are all bfloat16, all float16, or all uint8 = e4m3 bytes (FA_DTYPE_E4M3);
@@ -233,7 +235,7 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
                     cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv,
                     dtype=_type_code(q.dtype), q_descale=dq_, k_descale=dk_, v_descale=dv_,
-                    seqused_q=seqused_q)
+                    seqused_q=seqused_q, wait_limit_ns=wait_limit_ns)
     nbytes = fa_fwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_fwd_workspace_size")
@@ -251,7 +253,8 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
 
 
 def backward(q, k, v, o, lse, dout, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None,
-             cu_q=None, cu_k=None, flags=0, workspace=None, grads=None, seqused_q=None, seqused_k=None):
+             cu_q=None, cu_k=None, flags=0, workspace=None, grads=None, seqused_q=None, seqused_k=None,
+             wait_limit_ns=0):
     """Runs fa_bwd on torch CUDA tensors; returns (dq, dk, dv, dsinks, workspace).
 
     q, k, v, o, dout (and dq, dk, dv when given) are all bfloat16 or all float16."""
@@ -265,7 +268,8 @@ def backward(q, k, v, o, lse, dout, *, causal=False, window=(-1, -1), softmax_sc
         if t.dtype != q.dtype:
             raise TypeError(f"the backward's tensors must share q's type {q.dtype}; {name} is {t.dtype}")
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
-                    cu_k=cu_k, flags=flags, seqused_q=seqused_q, seqused_k=seqused_k, dtype=_type_code(q.dtype))
+                    cu_k=cu_k, flags=flags, seqused_q=seqused_q, seqused_k=seqused_k, dtype=_type_code(q.dtype),
+                    wait_limit_ns=wait_limit_ns)
     nbytes = fa_bwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_bwd_workspace_size")

@@ -124,6 +124,9 @@ cudaError_t timed(KernelId id, cudaStream_t st, F&& launch) {
 // ------------------------------------------------------------------------------------------
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Default bound on each pipeline wait of a kernel (2 s; fa_params.wait_limit_ns = 0).
+constexpr unsigned long long kWaitLimitNsDefault = 2000000000ull;
+
 // Host-visible total token counts of a packed call are not known without reading the
 // offsets; the caller passes them as s_q / s_kv (T_q, T_k).
 fa_status normalise(const fa_params* in, Problem& p) {
@@ -161,6 +164,7 @@ fa_status normalise(const fa_params* in, Problem& p) {
         p.T_k = a.s_kv;
     }
     p.dtype = a.dtype;
+    p.wait_ns = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNsDefault;
     // KV-cache forms: a per-sequence used length, and a paged cache (dense q only)
     p.seqused_q = a.seqused_q;
     p.seqused_k = a.seqused_k;
@@ -442,6 +446,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         c.lse_part = lse_part;
         c.o = reinterpret_cast<uint16_t*>(o);
         c.lse = lse;
+        c.status = status;
         e = timed(kCombine, st, [&] { return launch_combine(c, st); });
         return cuda_status(e);
     }
@@ -502,6 +507,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         c.lse_part = lse_part;
         c.o = reinterpret_cast<uint16_t*>(o);
         c.lse = lse;
+        c.status = status;
         e = timed(kCombine, st, [&] { return launch_combine(c, st); });
     }
     return cuda_status(e);

@@ -136,7 +136,7 @@ __device__ __forceinline__ bool dq_turn_wait(const int* cnt, int need, const Abo
                 ok = false;
                 break;
             }
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > ab.limit) {
                 ab.raise(kStatusTimeout);
                 ok = false;
                 break;
@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     BwdSmem<D>& s = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // an earlier kernel or CTA of the call failed (a device check of the offsets, a
+    // timeout): do not start, and read nothing the offsets point at
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     // 1-D grid.  Dense: the (batch, key/value head) units are split into n_bands bands of
     // near-equal size (the first hb % n_bands bands one unit larger); inside a band the unit
     // varies fastest and the key block slowest, so the key blocks that see the most query
@@ -195,8 +198,6 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     const SeqView sv = seq_view(p, seq);
     const int j0 = blk * kRows;
     if (j0 >= sv.nk) return;  // idle packed-batch block
-    // an earlier CTA of this launch gave up: do not start new work
-    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     const int j1 = min(j0 + kRows, sv.nk) - 1;
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
     int qt0, qt1;  // query tiles whose positions have a band reaching [j0, j1]
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     const int nsteps = qt1 - qt0;
     const int tbase = qtile_base(p, seq);
 
-    Abort ab{&s.abort_flag, a.status};
+    Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
         s.abort_flag = 0;
         mbar_init(&s.kv_full, 1);
@@ -643,6 +644,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
     BwdSmem256& s = *reinterpret_cast<BwdSmem256*>(smem_raw);
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;  // the call already failed
     int g, seq, blk;
     {
         const int idx = blockIdx.x;
@@ -661,14 +663,13 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
     const SeqView sv = seq_view(p, seq);
     const int j0 = blk * kKeys256;
     if (j0 >= sv.nk) return;  // idle packed-batch block
-    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
     int qt0, qt1;
     block_qtiles64(p, sv, band, blk, qt0, qt1);
     const int nsteps = qt1 - qt0;
     const int tbase = qtile_base(p, seq);
 
-    Abort ab{&s.abort_flag, a.status};
+    Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
         s.abort_flag = 0;
         mbar_init(&s.kv_full, 1);
@@ -931,6 +932,9 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
     const Problem& p = a.p;
     const int idx = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the offset check (FA_FLAG_VALIDATE_CU) ran first on this stream: when it failed,
+    // touch nothing (the later kernels of the call skip as well)
+    if (*reinterpret_cast<volatile const int*>(a.status) != 0) return;
     int seq, t;
     const bool live = decode_qtile(p, idx, seq, t);
     const long trow = ((long)g * a.n_qtiles + idx) * 128;
@@ -992,6 +996,7 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
 // tiles of its key/value head, in a fixed order (strided per-thread sums, then a tree).
 __global__ void __launch_bounds__(256) bwd_dsink_kernel(const BwdArgs a) {
     const Problem& p = a.p;
+    if (*reinterpret_cast<volatile const int*>(a.status) != 0) return;  // the call failed: dsinks stay 0
     const int h = blockIdx.x, g = h / p.G, hh = h % p.G;
     // head h holds rows hh + G k (k < P) of every tile of its key/value head
     const long n = (long)a.n_qtiles * p.P;
@@ -1016,6 +1021,7 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
     const Problem& p = a.p;
     const int idx = blockIdx.x, g = blockIdx.y;
+    if (*reinterpret_cast<volatile const int*>(a.status) != 0) return;  // the call failed: dQ not written
     int seq, t;
     if (!decode_qtile(p, idx, seq, t)) return;
     const SeqView sv = seq_view(p, seq);

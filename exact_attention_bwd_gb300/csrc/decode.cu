@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
     const int unit = blockIdx.x / a.n_splits;
     const int g = unit % p.h_kv, b = unit / p.h_kv;
     const int R = p.s_q * p.G;
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     const SeqView sv = seq_view(p, b);  // dense; nq, nk below s_q, s_kv when the slot is partly filled
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
 
@@ -93,8 +94,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
     const int t_begin = j_begin / BK;
     const int n_tiles = j_end > j_begin ? (j_end - 1) / BK + 1 - t_begin : 0;
 
-    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
-    Abort ab{&s.abort_flag, a.status};
+    Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
         s.abort_flag = 0;
         for (int i = 0; i < C::STAGES; ++i) {
@@ -310,6 +310,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3) combine_kernel(const Co
     using C = CombineCfg<D>;
     constexpr int L = C::L, V = C::V, RL = C::RL;
     const Problem& p = a.p;
+    // an earlier kernel of the call failed: its partials are incomplete, write nothing
+    if (a.status && *reinterpret_cast<volatile const int*>(a.status) != 0) return;
     const long nrows = (long)p.B * p.h_q * p.s_q;
     const int lane = threadIdx.x & 31, l = lane % L;
     const long row0 = (((long)blockIdx.x * kCombineWarps + threadIdx.x / 32) * (32 / L) + lane / L) * RL;

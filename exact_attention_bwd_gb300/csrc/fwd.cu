@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
 
     // ---------------- setup ----------------
-    Abort ab{&s.abort_flag, a.status};
+    Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
         s.abort_flag = 0;
         mbar_init(&s.q_full, 1);

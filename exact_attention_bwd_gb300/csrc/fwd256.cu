@@ -53,6 +53,9 @@ __global__ void __launch_bounds__(kThreads256, 1)
     Smem256& s = *reinterpret_cast<Smem256*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // an earlier kernel or CTA of the call failed (a device check, a timeout): read nothing
+    // the offsets point at
+    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
 
     // ---------------- work unit ----------------
     // 1-D grid, heaviest work first (see the d <= 128 kernel)
@@ -78,7 +81,6 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const SeqView sv = seq_view(p, seq);
     const int s0 = blk * p.P;
     if (s0 >= sv.nq) return;  // idle packed-batch block
-    if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
     int t0, t1;
     kv_tile_range(band, s0, min(s0 + p.P, sv.nq) - 1, BN, t0, t1);
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     }
     const int ntiles = t1 - t0;
 
-    Abort ab{&s.abort_flag, a.status};
+    Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
         s.abort_flag = 0;
         mbar_init(&s.q_full, 1);

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
     const int warp = tid >> 5, lane = tid & 31;
     if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
 
-    Abort ab{&s.abort_flag, a.status};
+    Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
         s.abort_flag = 0;
         mbar_init(&s.q_full, 1);

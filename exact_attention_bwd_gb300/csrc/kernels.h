@@ -28,6 +28,7 @@ struct Problem {
     const int32_t* block_table;  // [B * max_blocks] pages of a paged K/V cache, or null
     int page_size, max_blocks;
     int dtype;                // input element type (FA_DTYPE_*)
+    unsigned long long wait_ns;  // bound on each pipeline wait (ns) before a CTA gives up
 };
 
 // ------------------------------------------------------------------------------------------
@@ -75,6 +76,7 @@ struct CombineArgs {
     const float* lse_part;
     uint16_t* o;       // bf16 or fp16 (as the inputs)
     float* lse;
+    const int* status; // the call's status word: nonzero = an earlier kernel failed, do nothing
 };
 
 // ------------------------------------------------------------------------------------------

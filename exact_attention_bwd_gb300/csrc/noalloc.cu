@@ -8,12 +8,16 @@
 // This entry point uses a fixed scratch array compiled into the library instead.
 //
 // The array lives in device global memory of every GPU that loads the library, for the
-// life of the process.  Its device address is looked up once per device, on that
-// device's first call (see device_scratch), so that first call should not be made while
-// a stream is being captured.  Every call shares the one array: calls whose work
-// overlaps on the GPU (different streams, or different host threads) race on it.  The
-// forward resets the status word at the start of each call and overwrites every partial
+// life of the process.  Its device address is looked up once per device context, on the
+// first call in that context (see device_scratch), so that first call should not be made
+// while a stream is being captured.  A context destroyed and made again (cudaDeviceReset
+// and the next runtime call) loads the module afresh and may place the array elsewhere;
+// the lookup is then repeated, keyed by the driver's context id, which is never reused.
+// Every call shares the one array: calls whose work overlaps on the GPU (different
+// streams, or different host threads) race on it.  The forward resets the status word at the start of each call and overwrites every partial
 // result it later reads, so nothing carried over from an earlier call is used.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -28,18 +32,49 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchSlot {
+    void* ptr = nullptr;            // device address of g_scratch in context `ctx_id`
+    unsigned long long ctx_id = 0;  // the driver's unique id of that context (0 = none)
+};
+ScratchSlot g_slot[kMaxDevices];
 
-// Device address of g_scratch on the current device (looked up once per device, with
-// that device current).  Returns null when the lookup fails.
+// Unique id of the calling thread's current CUDA context, or 0 when there is none yet or
+// the driver entry points are unavailable.
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_scratch on device `dev` (current): looked up with that device current
+// on its first call, and again whenever the device's context has changed since.  Returns
+// null when the lookup fails.
 void* device_scratch(int dev) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchSlot& s = g_slot[dev];
+    const unsigned long long id = current_context_id();
+    if (!s.ptr || id == 0 || id != s.ctx_id) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = ptr;
+        s.ptr = ptr;
+        s.ctx_id = current_context_id();  // the lookup has made the context current
     }
-    return g_scratch_ptr[dev];
+    return s.ptr;
 }
 
 }  // namespace

@@ -16,8 +16,9 @@ namespace fa {
 // ------------------------------------------------------------------------------------------
 enum : int { kStatusOk = 0, kStatusTimeout = 5, kStatusDeviceCheck = 6 };
 
-// A stalled pipeline gives up after this long; one wait never legitimately takes more
-// than a few microseconds.
+// A stalled pipeline gives up after this long (the default of a call's wait limit, and the
+// fixed limit of the drain at exit); one wait never legitimately takes more than a few
+// microseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -70,6 +71,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 struct Abort {
     volatile int* flag;   // shared memory
     int* status;          // global memory (may be null)
+    unsigned long long limit;  // ns a pipeline wait may take before the CTA gives up
     __device__ __forceinline__ bool raised() const { return *flag != 0; }
     __device__ __forceinline__ void raise(int code) const {
         *flag = 1;
@@ -85,15 +87,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (ab.raised()) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > ab.limit) {
             ab.raise(kStatusTimeout);
             return false;
         }
     }
 }
 
-// Bounded wait used while draining at exit: gives up after the time limit, without
-// touching the abort state (the CTA is already on its way out).
+// Bounded wait used while draining at exit: gives up after the fixed 2 s limit (not the
+// call's limit: every copy and MMA already issued must land before the CTA exits),
+// without touching the abort state (the CTA is already on its way out).
 __device__ __forceinline__ bool mbar_wait_quiet(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();

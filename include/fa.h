@@ -53,8 +53,11 @@
  *  - Errors: arguments are checked on the host before anything is launched; a
  *    violation returns a code and launches nothing.  No C++ exception crosses this
  *    ABI and no kernel traps: a kernel whose pipeline stalls gives up after a time
- *    limit and records FA_ERR_TIMEOUT in the workspace status word, which
- *    fa_read_device_status reports.
+ *    limit (fa_params.wait_limit_ns) and records FA_ERR_TIMEOUT in the workspace status
+ *    word, which fa_read_device_status reports.  Every kernel of a call reads the status
+ *    word first and does nothing when it is set, so a failed offset check
+ *    (FA_FLAG_VALIDATE_CU) or a timeout leaves the outputs of the rest of the call
+ *    unwritten.
  *  - Supported: bf16 and fp16 (and e4m3 for the forward at d = 128, see below); head dim d in
  *    {64, 128, 256} for the forward and the backward (FA_FLAG_DETERMINISTIC: d <= 128);
  *    h_q / h_kv <= 128.
@@ -160,6 +163,14 @@ typedef struct fa_params {
     const float *k_descale;
     const float *v_descale;
     const int32_t *seqused_q;       /* device int32 [B], or NULL (see partly filled slots) */
+    /* Bound, in nanoseconds, on each wait of a kernel's pipeline (a stage of copies or
+     * MMAs that should have landed); 0 selects 2 s.  A wait that runs past it makes the CTA
+     * give up: it records FA_ERR_TIMEOUT in the status word, lets its own copies and MMAs
+     * land, frees its tensor memory and returns, and the call's later kernels do nothing.
+     * A limit below the kernels' own latencies (a few microseconds) turns every call into
+     * such a failure, which is how the failure path is exercised; outputs of a failed call
+     * are unspecified. */
+    unsigned long long wait_limit_ns;
 } fa_params;
 
 /* Bytes of workspace fa_fwd / fa_bwd need for these parameters (>= 256: the first
@@ -204,8 +215,9 @@ fa_status fa_profile_read(const char *kernel, float *ms);
  * are those of fa_fwd.  Allocates nothing.  Returns FA_ERR_WORKSPACE, launching nothing,
  * when the problem needs more scratch than the array holds (fa_fwd_workspace_size(p)
  * larger than FA_NOALLOC_SCRATCH_BYTES); FA_ERR_CUDA if the array's address cannot be
- * had.  The first call on each device looks the array's address up, so make it before
- * any stream capture.  All calls share the array and it keeps the last call's contents:
+ * had.  The first call on each device looks the array's address up (and again after the
+ * device's context was destroyed and made anew, e.g. by cudaDeviceReset), so make the
+ * first call, and the first after such a reset, before any stream capture.  All calls share the array and it keeps the last call's contents:
  * each call resets what must start at zero, but calls that overlap on the GPU race on
  * it, so serialise them (one stream, or events between streams).  The kernels' status
  * word also lives in the array and is not readable through this ABI. */
