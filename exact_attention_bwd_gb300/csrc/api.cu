@@ -201,6 +201,9 @@ struct FwdPlan {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Head dimensions with kernels: 64 and 128 (two query tiles per CTA), 192 and 256 (one).
+bool supported_d(int d) { return d == 64 || d == 128 || d == 192 || d == 256; }
+
 // Chooses the number of KV splits that minimises (waves) x (tiles per split), with a
 // small charge per split for the partial results written and read back.
 int choose_splits(long ctas, int tiles, int slots, double part_cost_per_split) {
@@ -224,7 +227,7 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
     if (p.B == 0 || rows_total == 0) return FA_OK;  // nothing to compute
     const bool dense = p.cu_q == nullptr;
     const int R = p.s_q * p.G;  // query rows per key/value head (dense)
-    if (dense && p.dtype != FA_DTYPE_E4M3 && (p.d == 64 || p.d == 128 || p.d == 256) && R <= decode_rows_max(p.d)) {
+    if (dense && p.dtype != FA_DTYPE_E4M3 && supported_d(p.d) && R <= decode_rows_max(p.d)) {
         pl.path = FwdPath::kDecode;
         const int tiles = (p.s_kv + kDecodeKeys - 1) / kDecodeKeys;
         const long units = (long)p.B * p.h_kv;
@@ -240,12 +243,12 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
                       align256(pl.part_rows * pl.n_splits * 4);
         return FA_OK;
     }
-    if (p.d != 64 && p.d != 128 && p.d != 256) return FA_ERR_UNSUPPORTED;
+    if (!supported_d(p.d)) return FA_ERR_UNSUPPORTED;
     pl.path = FwdPath::kTensor;
-    // d <= 128: two 128-row query tiles and 128-key tiles per CTA; d = 256: one query
-    // tile and 64-key tiles (the 256-column accumulator fills half the tensor memory)
-    const int rows_per_cta = (p.d == 256 ? 1 : 2) * p.P;
-    const int kv_tile = p.d == 256 ? 64 : kTileRows;
+    // d <= 128: two 128-row query tiles and 128-key tiles per CTA; d = 192 / 256: one query
+    // tile and 64-key tiles (the d-column accumulator fills much of the tensor memory)
+    const int rows_per_cta = (p.d >= 192 ? 1 : 2) * p.P;
+    const int kv_tile = p.d >= 192 ? 64 : kTileRows;
     if (dense) {
         pl.n_blocks = (p.s_q + rows_per_cta - 1) / rows_per_cta;
         const int tiles = (p.s_kv + kv_tile - 1) / kv_tile;
@@ -295,15 +298,15 @@ struct BwdPlan {
 
 fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     pl = BwdPlan();
-    if (p.d != 64 && p.d != 128 && p.d != 256) return FA_ERR_UNSUPPORTED;
-    if (p.d == 256 && (flags & FA_FLAG_DETERMINISTIC)) return FA_ERR_UNSUPPORTED;  // fixed dQ order: d <= 128
+    if (!supported_d(p.d)) return FA_ERR_UNSUPPORTED;
+    if (p.d >= 192 && (flags & FA_FLAG_DETERMINISTIC)) return FA_ERR_UNSUPPORTED;  // fixed dQ order: d <= 128
     if (p.block_table) return FA_ERR_UNSUPPORTED;  // paged caches: forward only
     if (p.dtype == FA_DTYPE_E4M3) return FA_ERR_UNSUPPORTED;      // e4m3: forward only
     const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;
     const long keys_total = p.cu_q ? (long)p.T_k : (long)p.B * p.s_kv;
     if (p.B == 0 || (rows_total == 0 && keys_total == 0)) return FA_OK;
     pl.empty = false;
-    const int kvb = p.d == 256 ? 64 : kTileRows;  // keys per CTA (d = 256: 64)
+    const int kvb = p.d >= 192 ? 64 : kTileRows;  // keys per CTA (d = 192 / 256: 64)
     if (p.cu_q) {
         pl.n_qtiles = p.T_q / p.P + p.B;
         pl.n_kvblocks = p.T_k / kvb + p.B;
@@ -415,7 +418,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     const int tokens_k = p.cu_q ? p.T_k : p.s_kv;
     const int bdim = p.cu_q ? 1 : p.B;
     CUtensorMap tk, tv;
-    const int kv_box = (pl.path == FwdPath::kDecode || p.d == 256) ? 64 : 128;
+    const int kv_box = (pl.path == FwdPath::kDecode || p.d >= 192) ? 64 : 128;
     // a paged cache is a [num_pages][page_size][h_kv][d] pool: the map's key and outer
     // dimensions are the row within a page and the page
     const int kv_rows = p.block_table ? p.page_size : tokens_k;
@@ -566,8 +569,8 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     const bool f16 = p.dtype == FA_DTYPE_F16;
     if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16) ||
         !encode_bhsd(&tdo, dout, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16) ||
-        !encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, p.d == 256 ? 64 : 128, f16) ||
-        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, p.d == 256 ? 64 : 128, f16))
+        !encode_bhsd(&tk, k, p.d, p.h_kv, tokens_k, bdim, 1, p.d >= 192 ? 64 : 128, f16) ||
+        !encode_bhsd(&tv, v, p.d, p.h_kv, tokens_k, bdim, 1, p.d >= 192 ? 64 : 128, f16))
         return FA_ERR_CUDA;
     cudaError_t e = timed(kBwdPre, st, [&] { return launch_bwd_pre(a, st); });
     if (e != cudaSuccess) return FA_ERR_CUDA;

@@ -581,11 +581,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 }
 
 // ------------------------------------------------------------------------------------------
-// backward at d = 256: one CTA per 64-key block, query rows on the tensor-memory lanes
+// backward at d = 192 and 256: one CTA per 64-key block, query rows on the tensor-memory lanes
 // ------------------------------------------------------------------------------------------
 // The d <= 128 layout (128-key block, the key rows on the lanes, dK and dV accumulated in
 // tensor memory at full width) does not fit at d = 256: the two 256-column accumulators
-// alone fill the 512 columns.  Here a CTA owns 64 keys and the GEMMs are oriented so that
+// alone fill the 512 columns (and at d = 192 the two 192-column ones, with S and dP,
+// leave no room for dQ).  Here a CTA owns 64 keys and the GEMMs are oriented so that
 // every accumulator has M = 128 on the lanes:
 //   S = Q K^T, dP = dO V^T          M = 128 query rows, N = 64 keys       (64 + 64 columns)
 //   dV^T += dO^T P, dK^T += Q^T dS  M = 128 of d (two halves), N = 64     (128 + 128 columns)
@@ -598,6 +599,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 // Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 owns the TMEM
 // allocation, warps 4-7 the compute group (thread = TMEM lane: a query row for P / dS, a
 // column of d for the dQ^T drain and the dK / dV epilogue).
+//
+// d = 192 runs the same layout with three 64-column chunks of Q, dO, K and V: S and dP
+// take K = 192 (no padding), while the GEMMs with d on the lanes keep their two 128-row
+// halves, the second of which reads a fourth chunk of Q, dO and K that is zero in shared
+// memory (written once, never loaded); its rows 192..255 come out zero and are neither
+// reduced nor stored.
 constexpr int kThreadsBwd256 = 256;
 constexpr int kKeys256 = 64;  // keys per block
 
@@ -628,11 +635,12 @@ __device__ __forceinline__ void block_qtiles64(const Problem& p, const SeqView& 
     qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
 }
 
-template <bool F16>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsBwd256, 1)
     bwd256_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
-    constexpr int D = 256;
+    static_assert(D == 192 || D == 256, "wide-head backward: d = 192 or 256");
+    constexpr int KCH = D / 64;  // chunks loaded; a zero fourth chunk pads d = 192
     // TMEM columns
     constexpr uint32_t C_S = 0, C_DP = 64, C_DV = 128, C_DK = 256, C_DQ = 384;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -688,13 +696,22 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
     }
     if (p.P * p.G < 128) {
         // rows past P*G of a query tile are never written by TMA: zero them once
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < KCH; ++c)
             for (int x = p.P * p.G * 128 + tid * 16; x < 128 * 128; x += kThreadsBwd256 * 16) {
                 *reinterpret_cast<uint4*>(&s.q[c][x]) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4*>(&s.dO[c][x]) = make_uint4(0, 0, 0, 0);
             }
-        fence_proxy_async_smem();
     }
+    if constexpr (KCH < 4) {
+        // d = 192: the fourth chunk of Q, dO and K (read by the second d-half GEMMs) is zero
+        for (int x = tid * 16; x < 128 * 128; x += kThreadsBwd256 * 16) {
+            *reinterpret_cast<uint4*>(&s.q[3][x]) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(&s.dO[3][x]) = make_uint4(0, 0, 0, 0);
+        }
+        for (int x = tid * 16; x < kKeys256 * 128; x += kThreadsBwd256 * 16)
+            *reinterpret_cast<uint4*>(&s.k[3][x]) = make_uint4(0, 0, 0, 0);
+    }
+    if (p.P * p.G < 128 || KCH < 4) fence_proxy_async_smem();
     if (warp == 2) {
         tmem_alloc(&s.tmem_base, 512);
         tmem_relinquish();
@@ -711,19 +728,19 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
             tma_prefetch_desc(&tmdo);
-            mbar_expect_tx(&s.kv_full, 2 * 4 * kKeys256 * 128);
-            for (int c = 0; c < 4; ++c) {
+            mbar_expect_tx(&s.kv_full, 2 * KCH * kKeys256 * 128);
+            for (int c = 0; c < KCH; ++c) {
                 tma_load_4d(s.k[c], &tmk, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
                 tma_load_4d(s.v[c], &tmv, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
             }
-            const uint32_t tile_bytes = (uint32_t)(p.P * p.G) * 128u * 4u;  // one Q or dO tile
+            const uint32_t tile_bytes = (uint32_t)(p.P * p.G) * 128u * KCH;  // one Q or dO tile
             int q_issued = 0, do_issued = 0;
             for (int it = 0; it < nsteps; ++it) {
                 const uint32_t ph = it & 1;
                 const int row = sv.q0 + (qt0 + it) * p.P;
                 if (!mbar_wait(&s.q_empty, ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.q_full, tile_bytes + 2 * 128 * 4);
-                for (int c = 0; c < 4; ++c) tma_load_4d(s.q[c], &tmq, &s.q_full, c * 64, g * p.G, row, sv.tma_b);
+                for (int c = 0; c < KCH; ++c) tma_load_4d(s.q[c], &tmq, &s.q_full, c * 64, g * p.G, row, sv.tma_b);
                 {
                     const long trow = ((long)g * a.n_qtiles + tbase + qt0 + it) * 128;
                     bulk_load(s.stat[0], a.lse2_t + trow, 512, &s.q_full);
@@ -732,7 +749,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 ++q_issued;
                 if (!mbar_wait(&s.do_empty, ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.do_full, tile_bytes);
-                for (int c = 0; c < 4; ++c) tma_load_4d(s.dO[c], &tmdo, &s.do_full, c * 64, g * p.G, row, sv.tma_b);
+                for (int c = 0; c < KCH; ++c) tma_load_4d(s.dO[c], &tmdo, &s.do_full, c * 64, g * p.G, row, sv.tma_b);
                 ++do_issued;
             }
             // the copies still in flight: the last phase of each buffer
@@ -760,10 +777,16 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 if (!(ok = mbar_wait(&s.q_full, par, ab))) break;
                 if (!(ok = mbar_wait(&s.do_full, par, ab))) break;
                 tc_fence_after();
-                // S = Q K^T, dP = dO V^T (K = 256: four 64-column chunks of each operand)
-                mma_ss_k16k8_x16(tmem + C_S, qd_k, kd_k, id_s, 0u);
-                tc_commit(&s.s_full);
-                mma_ss_k16k8_x16(tmem + C_DP, dod_k, vd_k, id_s, 0u);
+                // S = Q K^T, dP = dO V^T (K = d: KCH 64-column chunks of each operand)
+                if constexpr (KCH == 4) {
+                    mma_ss_k16k8_x16(tmem + C_S, qd_k, kd_k, id_s, 0u);
+                    tc_commit(&s.s_full);
+                    mma_ss_k16k8_x16(tmem + C_DP, dod_k, vd_k, id_s, 0u);
+                } else {
+                    mma_ss_k16k8_x12(tmem + C_S, qd_k, kd_k, id_s, 0u);
+                    tc_commit(&s.s_full);
+                    mma_ss_k16k8_x12(tmem + C_DP, dod_k, vd_k, id_s, 0u);
+                }
                 tc_commit(&s.dp_full);
                 // P and dS in shared memory (the compute group has also read S and dP out)
                 if (!(ok = mbar_wait(&s.pds_full, par, ab))) break;
@@ -865,11 +888,14 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 tc_fence_before();
                 mbar_arrive(&s.dq_free);
                 // for each query row the 32 lanes of a warp add to 32 consecutive floats
-                float* acc = a.dq_acc + trow * D + 128 * h + r;
+                // (at d = 192 the second half's lanes 64..127 hold the zero padding rows)
+                if (128 * h + r < D) {
+                    float* acc = a.dq_acc + trow * D + 128 * h + r;
 #pragma unroll
-                for (int x = 0; x < 64; ++x) atomicAdd(acc + (long)x * D, __uint_as_float(qa[x]));
+                    for (int x = 0; x < 64; ++x) atomicAdd(acc + (long)x * D, __uint_as_float(qa[x]));
 #pragma unroll
-                for (int x = 0; x < 64; ++x) atomicAdd(acc + (long)(64 + x) * D, __uint_as_float(qb[x]));
+                    for (int x = 0; x < 64; ++x) atomicAdd(acc + (long)(64 + x) * D, __uint_as_float(qb[x]));
+                }
             }
             if (!ok) break;
         }
@@ -893,6 +919,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
 #pragma unroll
                     for (int x = 0; x < 64; ++x) v[x] = 0u;
                 }
+                if (128 * h + r >= D) continue;  // d = 192: a padding row of the second half
                 // key rows are consecutive within a sequence: one stride of h_kv * d elements
                 uint16_t* dst = base + (key_row(p, sv, j0) * p.h_kv + g) * D + 128 * h + r;
                 const long stride = (long)p.h_kv * D;
@@ -946,9 +973,11 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
         return;
     }
     const SeqView sv = seq_view(p, seq);
-    // a warp takes its 32 rows RPI at a time: LPR lanes per row, 16 bytes (8 elements) of O
-    // and dO each, so every load instruction moves whole 128-byte lines
-    constexpr int LPR = D / 8, RPI = 32 / LPR;
+    // a warp takes its 32 rows RPI at a time: LPR lanes per row (a power of two), VPL
+    // 16-byte units (8 elements) of O and dO each per lane, so every load instruction moves
+    // whole 128-byte lines
+    constexpr int LPR = D == 192 ? 8 : D / 8, RPI = 32 / LPR, VPL = D / (8 * LPR);
+    static_assert(LPR * RPI == 32 && VPL * 8 * LPR == D, "row split of the preprocess");
     const int sub = lane / LPR, ch = lane % LPR;
 #pragma unroll 4
     for (int rr = 0; rr < 32; rr += RPI) {
@@ -960,16 +989,20 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
         long tok = 0;
         if (valid) {
             tok = token_row(p, sv, i);
-            const uint4 ov = *reinterpret_cast<const uint4*>(a.o + (tok * p.h_q + h) * D + 8 * ch);
-            const uint4 dv = *reinterpret_cast<const uint4*>(a.dout + (tok * p.h_q + h) * D + 8 * ch);
-            dsum = fmaf(lo16<F16>(ov.x), lo16<F16>(dv.x), dsum);
-            dsum = fmaf(hi16<F16>(ov.x), hi16<F16>(dv.x), dsum);
-            dsum = fmaf(lo16<F16>(ov.y), lo16<F16>(dv.y), dsum);
-            dsum = fmaf(hi16<F16>(ov.y), hi16<F16>(dv.y), dsum);
-            dsum = fmaf(lo16<F16>(ov.z), lo16<F16>(dv.z), dsum);
-            dsum = fmaf(hi16<F16>(ov.z), hi16<F16>(dv.z), dsum);
-            dsum = fmaf(lo16<F16>(ov.w), lo16<F16>(dv.w), dsum);
-            dsum = fmaf(hi16<F16>(ov.w), hi16<F16>(dv.w), dsum);
+#pragma unroll
+            for (int u = 0; u < VPL; ++u) {
+                const long off = (tok * p.h_q + h) * D + 8 * ch + 8 * LPR * u;
+                const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
+                const uint4 dv = *reinterpret_cast<const uint4*>(a.dout + off);
+                dsum = fmaf(lo16<F16>(ov.x), lo16<F16>(dv.x), dsum);
+                dsum = fmaf(hi16<F16>(ov.x), hi16<F16>(dv.x), dsum);
+                dsum = fmaf(lo16<F16>(ov.y), lo16<F16>(dv.y), dsum);
+                dsum = fmaf(hi16<F16>(ov.y), hi16<F16>(dv.y), dsum);
+                dsum = fmaf(lo16<F16>(ov.z), lo16<F16>(dv.z), dsum);
+                dsum = fmaf(hi16<F16>(ov.z), hi16<F16>(dv.z), dsum);
+                dsum = fmaf(lo16<F16>(ov.w), lo16<F16>(dv.w), dsum);
+                dsum = fmaf(hi16<F16>(ov.w), hi16<F16>(dv.w), dsum);
+            }
         }
         // sum over the row's LPR lanes (all lanes take part: rows differ in validity)
 #pragma unroll
@@ -1058,10 +1091,11 @@ static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const 
     return cudaGetLastError();
 }
 
+template <int D>
 static cudaError_t launch_main256(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem256);
-    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd256_kernel<true> : bwd256_kernel<false>;
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd256_kernel<D, true> : bwd256_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
@@ -1072,9 +1106,11 @@ static cudaError_t launch_main256(const BwdArgs& a, const CUtensorMap& tq, const
 cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, cudaStream_t st) {
     switch (a.p.d) {
+        case 192:
+            // the fixed dQ order is not built at d = 192 / 256 (the planner refuses the flag)
+            return a.dq_count ? cudaErrorInvalidValue : launch_main256<192>(a, tq, tk, tv, tdo, st);
         case 256:
-            // the fixed dQ order is not built at d = 256 (the planner refuses the flag)
-            return a.dq_count ? cudaErrorInvalidValue : launch_main256(a, tq, tk, tv, tdo, st);
+            return a.dq_count ? cudaErrorInvalidValue : launch_main256<256>(a, tq, tk, tv, tdo, st);
         case 64:
             return a.dq_count ? launch_main_d<64, true>(a, tq, tk, tv, tdo, st)
                               : launch_main_d<64, false>(a, tq, tk, tv, tdo, st);
@@ -1091,6 +1127,7 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t st) {
     const bool f16 = a.p.dtype == FA_DTYPE_F16;
     auto kernel = a.p.d == 64    ? (f16 ? bwd_pre_kernel<64, true> : bwd_pre_kernel<64, false>)
                   : a.p.d == 128 ? (f16 ? bwd_pre_kernel<128, true> : bwd_pre_kernel<128, false>)
+                  : a.p.d == 192 ? (f16 ? bwd_pre_kernel<192, true> : bwd_pre_kernel<192, false>)
                                  : (f16 ? bwd_pre_kernel<256, true> : bwd_pre_kernel<256, false>);
     kernel<<<grid, 128, 0, st>>>(a);
     return cudaGetLastError();
@@ -1102,6 +1139,7 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t st) {
     const bool f16 = a.p.dtype == FA_DTYPE_F16;
     auto kernel = a.p.d == 64    ? (f16 ? bwd_post_kernel<64, true> : bwd_post_kernel<64, false>)
                   : a.p.d == 128 ? (f16 ? bwd_post_kernel<128, true> : bwd_post_kernel<128, false>)
+                  : a.p.d == 192 ? (f16 ? bwd_post_kernel<192, true> : bwd_post_kernel<192, false>)
                                  : (f16 ? bwd_post_kernel<256, true> : bwd_post_kernel<256, false>);
     kernel<<<grid, 128, 0, st>>>(a);
     if (a.dsinks) bwd_dsink_kernel<<<a.p.h_q, 256, 0, st>>>(a);

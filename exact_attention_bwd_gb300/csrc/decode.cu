@@ -1,6 +1,6 @@
 // Decode-shaped forward (few query rows per key/value head) and the split-KV combine.
 //
-// With s_q * (h_q / h_kv) <= 8 query rows per key/value head (4 at d = 256) the work is a stream over
+// With s_q * (h_q / h_kv) <= 8 query rows per key/value head (4 at d = 192, 256) the work is a stream over
 // the key/value cache: about 2 multiply-adds per byte read, far below what the tensor
 // cores would need, so this path runs on the CUDA cores and is sized to keep HBM busy.
 // The cache of one (batch, key/value head) is split across CTAs, each CTA writes a
@@ -25,8 +25,8 @@ struct DecCfg {
     static constexpr int EPL = D / 32;                 // head-dim elements per lane
     static constexpr int R = 4 * RG;                   // query rows held (padded)
     // two CTAs per SM where the stages fit in half the shared memory
-    static constexpr int STAGES = (D == 256) ? 3 : (D == 128 ? 3 : 6);
-    static constexpr int MIN_BLOCKS = (D == 256 || RG > 1) ? 1 : 2;
+    static constexpr int STAGES = (D >= 128) ? 3 : 6;
+    static constexpr int MIN_BLOCKS = (D >= 192 || RG > 1) ? 1 : 2;
 };
 
 template <int D, int RG>
@@ -46,11 +46,20 @@ __device__ __forceinline__ int sw128(int row, int col) {
 
 // EPL consecutive 16-bit values (fp16 if F16, else bf16) of row `row` starting at column
 // `col` of a swizzled tile, widened to fp32 (EPL = 2, 4 or 8: one 4-, 8- or 16-byte load
-// that stays in a unit).
+// that stays in a unit; EPL = 6, at d = 192: three 4-byte loads, since six values starting
+// at an even column can straddle a 16-byte unit or a 64-column chunk).
 template <int EPL, int CHUNK, bool F16>
 __device__ __forceinline__ void load_row_slice(const uint8_t* tile, int row, int col, float* out) {
     const uint8_t* src = tile + (col >> 6) * CHUNK + sw128(row, col & 63);
-    if constexpr (EPL == 2) {
+    if constexpr (EPL == 6) {
+#pragma unroll
+        for (int e = 0; e < 6; e += 2) {
+            const int c = col + e;
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + (c >> 6) * CHUNK + sw128(row, c & 63));
+            out[e] = lo16<F16>(w);
+            out[e + 1] = hi16<F16>(w);
+        }
+    } else if constexpr (EPL == 2) {
         const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
         out[0] = lo16<F16>(w);
         out[1] = hi16<F16>(w);
@@ -299,9 +308,9 @@ constexpr int kCombineWarps = 8;
 
 template <int D>
 struct CombineCfg {
-    static constexpr int L = D >= 128 ? 32 : D / 4;  // lanes per row
+    static constexpr int L = D == 192 ? 16 : (D >= 128 ? 32 : D / 4);  // lanes per row (a power of two)
     static constexpr int V = D / (4 * L);             // float4 columns per lane
-    static constexpr int RL = D >= 256 ? 1 : 2;       // rows per lane group
+    static constexpr int RL = D >= 192 ? 1 : 2;       // rows per lane group
     static constexpr int ROWS_PER_BLOCK = kCombineWarps * (32 / L) * RL;
 };
 
@@ -416,7 +425,7 @@ template <int D>
 static cudaError_t launch_decode_d(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
     const int R = a.p.s_q * a.p.G;
     if (R <= 4) return launch_decode_dr<D, 1>(a, tk, tv, st);
-    if constexpr (D != 256) {
+    if constexpr (D <= 128) {
         if (R <= 8) return launch_decode_dr<D, 2>(a, tk, tv, st);
     }
     return cudaErrorInvalidValue;
@@ -426,6 +435,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
     switch (a.p.d) {
         case 64: return launch_decode_d<64>(a, tk, tv, st);
         case 128: return launch_decode_d<128>(a, tk, tv, st);
+        case 192: return launch_decode_d<192>(a, tk, tv, st);
         case 256: return launch_decode_d<256>(a, tk, tv, st);
         default: return cudaErrorInvalidValue;
     }
@@ -433,8 +443,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUte
 
 // The per-lane state (query rows and output accumulators) grows with the rows; past these
 // counts the registers spill, and the tensor-core path takes the problem instead.
-int decode_rows_max(int d) { return d == 256 ? 4 : 8; }
-int decode_ctas_per_sm(int d, int rows) { return (d == 256 || rows > 4) ? 1 : 2; }
+int decode_rows_max(int d) { return d >= 192 ? 4 : 8; }
+int decode_ctas_per_sm(int d, int rows) { return (d >= 192 || rows > 4) ? 1 : 2; }
 
 template <int D>
 static cudaError_t launch_combine_d(const CombineArgs& a, cudaStream_t st) {
@@ -451,6 +461,7 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
     switch (a.p.d) {
         case 64: return launch_combine_d<64>(a, st);
         case 128: return launch_combine_d<128>(a, st);
+        case 192: return launch_combine_d<192>(a, st);
         case 256: return launch_combine_d<256>(a, st);
         default: return cudaErrorInvalidValue;
     }

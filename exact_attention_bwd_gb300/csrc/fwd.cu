@@ -535,6 +535,7 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMa
     switch (a.p.d) {
         case 64: return f16 ? launch_fwd_d<64, true>(a, tq, tk, tv, st) : launch_fwd_d<64, false>(a, tq, tk, tv, st);
         case 128: return f16 ? launch_fwd_d<128, true>(a, tq, tk, tv, st) : launch_fwd_d<128, false>(a, tq, tk, tv, st);
+        case 192:
         case 256: return launch_fwd256(a, tq, tk, tv, st);
         default: return cudaErrorInvalidValue;
     }

@@ -1,12 +1,15 @@
-// Forward attention for head dimension 256 on the tcgen05 tensor cores.
+// Forward attention for head dimensions 192 and 256 on the tcgen05 tensor cores.
 //
-// The accumulator of one 128-row query tile is 256 TMEM columns wide, so a CTA holds a
-// single query tile.  Tensor memory: O in columns [0, 256), two 64-column S buffers in
-// [256, 384), and the Q tile itself in [384, 512) (16-bit pairs, one row per lane), so
-// S = Q K^T takes its A operand from tensor memory and reads only K from shared memory.
-// Q arrives by TMA in the first 64 KB ring slot; the softmax warps copy their rows into
-// tensor memory, after which that slot joins the key/value ring as its third stage.
-// Keys and values stream in 64-row tiles (32 KB each at d = 256).  The MMA thread runs one
+// The accumulator of one 128-row query tile is d TMEM columns wide, so a CTA holds a
+// single query tile.  Tensor memory: O in columns [0, d), two 64-column S buffers in
+// [256, 384), and the Q tile itself from column 384 on (16-bit pairs, one row per lane,
+// d / 2 columns), so S = Q K^T takes its A operand from tensor memory and reads only K
+// from shared memory.  Q arrives by TMA in the first ring slot (a Q tile is as large as a
+// K plus a V tile); the softmax warps copy their rows into tensor memory, after which that
+// slot joins the key/value ring.  Keys and values stream in 64-row tiles (32 KB each at
+// d = 256, 24 KB at d = 192, which leaves room for a fourth slot).  d = 192 is one of the
+// head sizes the pages pad to (dew-flash-attn PyPI page, the FA3 head-dim padding to
+// 64 / 128 / 192 / 256); here it runs as three 64-column chunks, not padded.  The MMA thread runs one
 // tile ahead: S(j+1) is computed while the softmax group works on S(j), then
 // O += P(j) V(j).  Rows are packed across the G query heads of the key/value head exactly
 // as in the d <= 128 kernel, and the online softmax is the same (running max / running
@@ -18,39 +21,46 @@ namespace fa {
 namespace {
 
 constexpr int kThreads256 = 256;
-constexpr int D = 256;
 constexpr int BN = 64;               // keys per KV tile
-constexpr int KCH = D / 64;          // 64-column chunks
 constexpr int Q_CHUNK = 128 * 128;   // [128 rows][64 cols] 16-bit
 constexpr int KV_CHUNK = BN * 128;   // [64 rows][64 cols] 16-bit
-constexpr int KV_BYTES = KCH * KV_CHUNK;  // one K or V tile (32 KB)
-constexpr int STAGES = 3;            // ring slots of K + V (64 KB each); slot 0 first holds Q
-constexpr int SLOT_BYTES = 2 * KV_BYTES;
-static_assert(KCH * Q_CHUNK == SLOT_BYTES, "the Q tile fills one ring slot");
 constexpr uint32_t C_O = 0;
 constexpr uint32_t C_S = 256;        // S buffer b at columns 256 + 64 b
 constexpr uint32_t C_Q = 384;        // Q: column c holds elements 2c, 2c+1 of the row
 
-// ring slot and use count of KV tile `it`: tiles 0 and 1 take slots 1 and 2, tile 2 the
-// slot Q came in, and so on round the ring
-__device__ __forceinline__ int slot_of(int it) { return (it + 1) % STAGES; }
-__device__ __forceinline__ uint32_t use_parity(int it) { return (uint32_t)(it / STAGES) & 1u; }
+template <int D>
+struct Cfg256 {
+    static constexpr int KCH = D / 64;              // 64-column chunks
+    static constexpr int KV_BYTES = KCH * KV_CHUNK; // one K or V tile (32 KB at d = 256)
+    static constexpr int SLOT_BYTES = 2 * KV_BYTES; // ring slot: K then V; slot 0 first holds Q
+    static constexpr int STAGES = D == 256 ? 3 : 4;
+    static_assert(KCH * Q_CHUNK == SLOT_BYTES, "the Q tile fills one ring slot");
+    static_assert(C_Q + D / 2 <= 512 && C_O + D <= C_S, "tensor-memory columns overlap");
+    // ring slot and use count of KV tile `it`: tiles 0 .. STAGES-2 take slots 1 .. STAGES-1,
+    // tile STAGES-1 the slot Q came in, and so on round the ring
+    static __device__ __forceinline__ int slot_of(int it) { return (it + 1) % STAGES; }
+    static __device__ __forceinline__ uint32_t use_parity(int it) { return (uint32_t)(it / STAGES) & 1u; }
+};
 
+template <int D>
 struct __align__(1024) Smem256 {
-    uint8_t ring[STAGES][SLOT_BYTES];  // K at 0, V at KV_BYTES
+    uint8_t ring[Cfg256<D>::STAGES][Cfg256<D>::SLOT_BYTES];  // K at 0, V at KV_BYTES
     uint64_t q_full, q_tmem;
-    uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+    uint64_t k_full[Cfg256<D>::STAGES], k_empty[Cfg256<D>::STAGES], v_full[Cfg256<D>::STAGES],
+        v_empty[Cfg256<D>::STAGES];
     uint64_t s_full[2], p_full[2], pv_done, o_full, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
-template <bool F16>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads256, 1)
     fwd256_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
+    using C = Cfg256<D>;
+    constexpr int KCH = C::KCH, KV_BYTES = C::KV_BYTES, SLOT_BYTES = C::SLOT_BYTES, STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
-    Smem256& s = *reinterpret_cast<Smem256*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem256<D>& s = *reinterpret_cast<Smem256<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Problem& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // an earlier kernel or CTA of the call failed (a device check, a timeout): read nothing
@@ -137,8 +147,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
                 tma_load_4d(&s.ring[0][c * Q_CHUNK], &tmq, &s.q_full, c * 64, g * p.G, sv.q0 + s0, sv.tma_b);
             int k_issued = 0, v_issued = 0;
             for (int it = 0; it < ntiles; ++it) {
-                const int st = slot_of(it);
-                const uint32_t ph = use_parity(it);
+                const int st = C::slot_of(it);
+                const uint32_t ph = C::use_parity(it);
                 int row, outer;
                 kv_tile_coord(p, sv, (t0 + it) * BN, row, outer);
                 // slot 0 is free for keys once the softmax warps have copied Q out of it
@@ -157,9 +167,9 @@ __global__ void __launch_bounds__(kThreads256, 1)
             // wait for every copy still in flight before the CTA may exit
             for (int back = 1; back <= STAGES; ++back) {
                 if (k_issued - back >= 0)
-                    mbar_wait_quiet(&s.k_full[slot_of(k_issued - back)], use_parity(k_issued - back));
+                    mbar_wait_quiet(&s.k_full[C::slot_of(k_issued - back)], C::use_parity(k_issued - back));
                 if (v_issued - back >= 0)
-                    mbar_wait_quiet(&s.v_full[slot_of(v_issued - back)], use_parity(v_issued - back));
+                    mbar_wait_quiet(&s.v_full[C::slot_of(v_issued - back)], C::use_parity(v_issued - back));
             }
             mbar_wait_quiet(&s.q_full, 0);
         }
@@ -173,24 +183,27 @@ __global__ void __launch_bounds__(kThreads256, 1)
             const uint64_t vd0 = sdesc_sw128(smem_u32(s.ring[0] + KV_BYTES), KV_CHUNK, 1024);
             constexpr uint32_t kSlot = SLOT_BYTES >> 4;
             auto issue_s = [&](int it) {  // S(it) = Q K(it)^T into buffer it & 1
-                const int st = slot_of(it);
-                mma_ts_lin_k8_x16(tmem + C_S + 64 * (it & 1), tmem + C_Q, kd0 + (uint64_t)(st * kSlot), idS, 0u);
+                const int st = C::slot_of(it);
+                if constexpr (D == 256)
+                    mma_ts_lin_k8_x16(tmem + C_S + 64 * (it & 1), tmem + C_Q, kd0 + (uint64_t)(st * kSlot), idS, 0u);
+                else
+                    mma_ts_lin_k8_x12(tmem + C_S + 64 * (it & 1), tmem + C_Q, kd0 + (uint64_t)(st * kSlot), idS, 0u);
                 tc_commit(&s.s_full[it & 1]);
                 tc_commit(&s.k_empty[st]);
             };
             bool ok = mbar_wait(&s.q_tmem, 0, ab);
-            if (ok && (ok = mbar_wait(&s.k_full[slot_of(0)], 0, ab))) {
+            if (ok && (ok = mbar_wait(&s.k_full[C::slot_of(0)], 0, ab))) {
                 tc_fence_after();
                 issue_s(0);
             }
             for (int it = 0; ok && it < ntiles; ++it) {
                 if (it + 1 < ntiles) {
-                    if (!(ok = mbar_wait(&s.k_full[slot_of(it + 1)], use_parity(it + 1), ab))) break;
+                    if (!(ok = mbar_wait(&s.k_full[C::slot_of(it + 1)], C::use_parity(it + 1), ab))) break;
                     tc_fence_after();
                     issue_s(it + 1);  // its buffer held P(it-1), read by PV(it-1) issued earlier
                 }
-                const int st = slot_of(it), b = it & 1;
-                if (!(ok = mbar_wait(&s.v_full[st], use_parity(it), ab))) break;
+                const int st = C::slot_of(it), b = it & 1;
+                if (!(ok = mbar_wait(&s.v_full[st], C::use_parity(it), ab))) break;
                 // buffer b is used at iterations b, b + 2, ...: this is its (it >> 1)-th phase
                 if (!(ok = mbar_wait(&s.p_full[b], (it >> 1) & 1, ab))) break;
                 tc_fence_after();
@@ -374,15 +387,25 @@ __global__ void __launch_bounds__(kThreads256, 1)
 
 }  // namespace
 
-cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          cudaStream_t st) {
-    const size_t smem = sizeof(Smem256) + 1024;
-    auto kernel = a.p.dtype == FA_DTYPE_F16 ? fwd256_kernel<true> : fwd256_kernel<false>;
+template <int D>
+static cudaError_t launch_fwd_wide(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, cudaStream_t st) {
+    const size_t smem = sizeof(Smem256<D>) + 1024;
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? fwd256_kernel<D, true> : fwd256_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = a.p.cu_q ? (long)a.n_blocks * a.p.h_kv : (long)a.n_blocks * a.n_splits * a.p.h_kv * a.p.B;
     kernel<<<(unsigned)n, kThreads256, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
+}
+
+cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          cudaStream_t st) {
+    switch (a.p.d) {
+        case 192: return launch_fwd_wide<192>(a, tq, tk, tv, st);
+        case 256: return launch_fwd_wide<256>(a, tq, tk, tv, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace fa

@@ -79,13 +79,32 @@ struct Abort {
     }
 };
 
+// try_wait whose suspension lasts at most about `hint_ns` (instead of the hardware's own
+// limit, which can exceed a short wait limit).
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and raises
 // the CTA's abort) when the limit passes or another wait of the CTA already gave up.
+// Each try suspends the thread for at most about the limit (the hardware's own suspension
+// limit could outlast a short one), and resumes it as soon as the phase completes.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = ab.limit < 0xFFFFFFFFull ? (uint32_t)ab.limit : 0xFFFFFFFFu;
+    if (mbar_try_wait_for(bar, parity, hint)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_for(bar, parity, hint)) return true;
         if (ab.raised()) return false;
         if (globaltimer() - t0 > ab.limit) {
             ab.raise(kStatusTimeout);
@@ -408,6 +427,45 @@ __device__ __forceinline__ void mma_ss_k16k8_x16(uint32_t d_tmem, uint64_t a, ui
         : "memory");
 }
 
+// A K-major 16 KB chunks, B K-major 8 KB chunks, 12 steps (K = 192)
+__device__ __forceinline__ void mma_ss_k16k8_x12(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32), blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 da, db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; mov.b64 da, {ta, %4}; add.u32 tb, %5, 0; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p0;\n"
+        "add.u32 ta, %3, 2; mov.b64 da, {ta, %4}; add.u32 tb, %5, 2; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 4; mov.b64 da, {ta, %4}; add.u32 tb, %5, 4; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 6; mov.b64 da, {ta, %4}; add.u32 tb, %5, 6; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1024; mov.b64 da, {ta, %4}; add.u32 tb, %5, 512; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1026; mov.b64 da, {ta, %4}; add.u32 tb, %5, 514; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1028; mov.b64 da, {ta, %4}; add.u32 tb, %5, 516; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 1030; mov.b64 da, {ta, %4}; add.u32 tb, %5, 518; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2048; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1024; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2050; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1026; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2052; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1028; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "add.u32 ta, %3, 2054; mov.b64 da, {ta, %4}; add.u32 tb, %5, 1030; mov.b64 db, {tb, %6};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
 // A from TMEM at columns a + 8 k, B K-major in 8 KB chunks (+32 B per step, next chunk
 // every 4 steps), 16 steps (K = 256)
 __device__ __forceinline__ void mma_ts_lin_k8_x16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc0) {
@@ -450,6 +508,46 @@ __device__ __forceinline__ void mma_ts_lin_k8_x16(uint32_t d_tmem, uint32_t a_tm
         "add.u32 ta, %3, 112; add.u32 tb, %4, 1540; mov.b64 db, {tb, %5};\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
         "add.u32 ta, %3, 120; add.u32 tb, %4, 1542; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "}\n"
+        :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(a_tmem), "r"(blo), "r"(bhi)
+        : "memory");
+}
+
+// A from TMEM at columns a + 8 k, B K-major in 8 KB chunks (+32 B per step, next chunk
+// every 4 steps), 12 steps (K = 192)
+__device__ __forceinline__ void mma_ts_lin_k8_x12(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+    asm volatile(
+        "{\n"
+        ".reg .pred p0, p1;\n"
+        ".reg .b32 ta, tb;\n"
+        ".reg .b64 db;\n"
+        "setp.ne.b32 p0, %2, 0;\n"
+        "setp.eq.b32 p1, %1, %1;\n"
+        "add.u32 ta, %3, 0; add.u32 tb, %4, 0; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p0;\n"
+        "add.u32 ta, %3, 8; add.u32 tb, %4, 2; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 16; add.u32 tb, %4, 4; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 24; add.u32 tb, %4, 6; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 32; add.u32 tb, %4, 512; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 40; add.u32 tb, %4, 514; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 48; add.u32 tb, %4, 516; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 56; add.u32 tb, %4, 518; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 64; add.u32 tb, %4, 1024; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 72; add.u32 tb, %4, 1026; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 80; add.u32 tb, %4, 1028; mov.b64 db, {tb, %5};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
+        "add.u32 ta, %3, 88; add.u32 tb, %4, 1030; mov.b64 db, {tb, %5};\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %1, p1;\n"
         "}\n"
         :: "r"(d_tmem), "r"(idesc), "r"(acc0), "r"(a_tmem), "r"(blo), "r"(bhi)

@@ -105,9 +105,10 @@ def test_workspace_too_small():
 
 def test_backward_rejects():
     assert call_bwd(params(sinks=0x3000), dsinks=None) == fa.FA_ERR_INVALID_ARG
-    assert call_bwd(params(d=192)) == fa.FA_ERR_UNSUPPORTED
-    # d = 256 has no fixed-order (deterministic) dQ
+    assert call_bwd(params(d=160)) == fa.FA_ERR_UNSUPPORTED
+    # d = 192 and 256 have no fixed-order (deterministic) dQ
     assert call_bwd(params(d=256, flags=fa.FA_FLAG_DETERMINISTIC)) == fa.FA_ERR_UNSUPPORTED
+    assert call_bwd(params(d=192, flags=fa.FA_FLAG_DETERMINISTIC)) == fa.FA_ERR_UNSUPPORTED
     assert call_bwd(params(h_q=3, h_kv=2)) == fa.FA_ERR_INVALID_ARG
     assert call_bwd(params(), q=MISAL) == fa.FA_ERR_INVALID_ARG
 
@@ -268,6 +269,17 @@ def test_params_layout_and_constants_match_the_header(tmp_path):
     assert len(consts) == 13  # 7 status codes, 3 flags, 3 element types
     for n in consts:
         assert got[("const", n)] == getattr(fa, n), n
+
+
+def test_d192_is_planned():
+    """d = 192 runs forward (dense, packed, decode and split shapes) and backward."""
+    for kw in (dict(d=192), dict(d=192, s_q=1, s_kv=4096), dict(d=192, s_q=64, s_kv=8192, causal=1)):
+        assert fa.fa_fwd_workspace_size(params(**kw)) >= 256, kw
+    p = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=192)
+    tiles = 2 * -(-300 // 64)
+    stat = 2 * tiles * 128 * 4
+    align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert fa.fa_bwd_workspace_size(p) == 256 + 2 * align(stat) + align(2 * tiles * 128 * 192 * 4)
 
 
 def test_d256_backward_workspace():
