@@ -68,16 +68,22 @@ def library_path() -> str:
 
 
 def load(build_if_missing: bool = True):
-    """Loads (building first if stale) the CUDA library; raises if that is impossible."""
+    """Loads (building first if stale) the CUDA library; raises if that is impossible.
+
+    With FA_TRACE=1 in the environment the trace build (libfa_gb300_trace.so, whose
+    kernels record per-role event traces into the workspace; see trace.py) is loaded
+    instead of the product library."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
+        trace = os.environ.get("FA_TRACE", "") == "1"
+        path = _build.TRACE_LIB if trace else _build.LIB
         if build_if_missing:
-            _build.build()
-        if not os.path.exists(_build.LIB):
-            raise RuntimeError(f"CUDA library {_build.LIB} is missing; run exact_attention_bwd_gb300/build.py")
-        lib = ctypes.CDLL(_build.LIB)
+            _build.build(trace=trace)
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing; run exact_attention_bwd_gb300/build.py")
+        lib = ctypes.CDLL(path)
         P = ctypes.POINTER(FaParams)
         vp, sz = ctypes.c_void_p, ctypes.c_size_t
         lib.fa_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]

@@ -12,6 +12,7 @@
 
 #include "../../include/fa.h"
 #include "kernels.h"
+#include "trace.cuh"
 
 namespace fa {
 namespace {
@@ -196,6 +197,7 @@ struct FwdPlan {
     size_t part_rows = 0;  // rows of the split partials
     int s_pad = 0;         // e4m3: keys per V^T row (s_kv rounded up to 16)
     size_t off_vt = 0;     // e4m3: workspace offset of V^T
+    size_t off_trace = 0;  // trace builds: the per-role event records (tensor-core path)
     size_t ws_bytes = kStatusBytes;
 };
 
@@ -283,6 +285,10 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
         pl.off_vt = pl.ws_bytes;
         pl.ws_bytes += align256((size_t)p.B * p.h_kv * p.d * pl.s_pad);
     }
+#ifdef FA_TRACE
+    pl.off_trace = pl.ws_bytes;
+    pl.ws_bytes += align256(kTraceBytes);
+#endif
     return FA_OK;
 }
 
@@ -292,7 +298,7 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
 struct BwdPlan {
     bool empty = true;
     int n_qtiles = 0, n_kvblocks = 0, n_bands = 1;
-    size_t off_delta = 0, off_lse2 = 0, off_dq = 0, off_sink = 0, off_count = 0;
+    size_t off_delta = 0, off_lse2 = 0, off_dq = 0, off_sink = 0, off_count = 0, off_trace = 0;
     size_t ws_bytes = kStatusBytes;
 };
 
@@ -336,6 +342,10 @@ fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
         pl.off_count = pl.ws_bytes;
         pl.ws_bytes += align256((size_t)p.h_kv * pl.n_qtiles * 4);
     }
+#ifdef FA_TRACE
+    pl.off_trace = pl.ws_bytes;
+    pl.ws_bytes += align256(kTraceBytes);
+#endif
     return FA_OK;
 }
 
@@ -364,7 +374,11 @@ using namespace fa;
 
 extern "C" {
 
+#ifdef FA_TRACE
+const char* fa_version(void) { return "fa_gb300 0.1 (sm_103a, tcgen05) trace build"; }
+#else
 const char* fa_version(void) { return "fa_gb300 0.1 (sm_103a, tcgen05)"; }
+#endif
 
 const char* fa_status_string(fa_status s) {
     switch (s) {
@@ -498,6 +512,10 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.status = status;
+#ifdef FA_TRACE
+    a.trace = reinterpret_cast<unsigned long long*>(ws + pl.off_trace);
+    if (cudaMemsetAsync(a.trace, 0, kTraceBytes, st) != cudaSuccess) return FA_ERR_CUDA;
+#endif
     cudaError_t e = timed(kFwd, st, [&] {
         return p.dtype == FA_DTYPE_E4M3 ? launch_fwd_e4m3(a, tq, tk, tv, st) : launch_fwd(a, tq, tk, tv, st);
     });
@@ -561,6 +579,10 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.sink_t = p.sinks ? reinterpret_cast<float*>(ws + pl.off_sink) : nullptr;
     a.dq_count = (in->flags & FA_FLAG_DETERMINISTIC) ? reinterpret_cast<int*>(ws + pl.off_count) : nullptr;
     a.status = status;
+#ifdef FA_TRACE
+    a.trace = reinterpret_cast<unsigned long long*>(ws + pl.off_trace);
+    if (cudaMemsetAsync(a.trace, 0, kTraceBytes, st) != cudaSuccess) return FA_ERR_CUDA;
+#endif
 
     const int tokens_q = p.cu_q ? p.T_q : p.s_q;
     const int tokens_k = p.cu_q ? p.T_k : p.s_kv;

@@ -29,6 +29,7 @@
 //               workspace
 // d = 256 has its own kernel (bwd256_kernel below).
 #include "common.cuh"
+#include "trace.cuh"
 
 namespace fa {
 namespace {
@@ -258,13 +259,16 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
             DqOrder order;
             order.next = blk + 1;
+            Tracer tr;
+            tr.init(warp == 12 ? a.trace : nullptr, 3);
+            tr.item(blockIdx.x);
             for (int it = 0; it < nsteps; ++it) {
                 const int t = qt0 + it;
                 const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
                 int need = 0;
                 if constexpr (DET) need = 4 * dq_predecessors(p, sv, band, order, t);
                 {
-                    const bool w = mbar_wait(&s.dq_full, it & 1, ab);
+                    const bool w = twait(tr, kBDqFull, &s.dq_full, it & 1, ab);
                     if (!__all_sync(0xffffffffu, w)) break;
                 }
                 tc_fence_after();
@@ -283,6 +287,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 #pragma unroll
                 for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
                 if constexpr (DET) dq_turn_done(cnt);
+                tr.mark(kMDqReduced);
             }
         }
     } else if (warp < 4) {
@@ -291,6 +296,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && nsteps > 0) {
+            Tracer tr;
+            tr.init(a.trace, 0);
+            tr.item(blockIdx.x);
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 const int st = it & 1;
                 const uint32_t ph = (it >> 1) & 1;
                 const int row = sv.q0 + (qt0 + it) * p.P;
-                if (!mbar_wait(&s.q_empty[st], ph ^ 1, ab)) break;
+                if (!twait(tr, kBQEmpty, &s.q_empty[st], ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.q_full[st], qbytes);
                 for (int c = 0; c < C::KCH; ++c)
                     tma_load_4d(s.q[st] + c * C::CHUNK, &tmq, &s.q_full[st], c * 64, g * p.G, row, sv.tma_b);
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     bulk_load(s.stat[st][1], a.delta_t + trow, 512, &s.q_full[st]);
                 }
                 ++q_issued;
-                if (!mbar_wait(&s.do_empty[st], ph ^ 1, ab)) break;
+                if (!twait(tr, kBDoEmpty, &s.do_empty[st], ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.do_full[st], tile_bytes);
                 for (int c = 0; c < C::KCH; ++c)
                     tma_load_4d(s.dO[st] + c * C::CHUNK, &tmdo, &s.do_full[st], c * 64, g * p.G, row, sv.tma_b);
@@ -340,7 +348,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             // whose 64-row accumulator would need the M = 64 lane layout
             constexpr uint32_t id_dq = C::DQ_T ? idesc_16(128, 128, true, true, F16) : idesc_16(128, D, true, true, F16);
             const uint32_t ka = smem_u32(s.k), va = smem_u32(s.v);
-            bool ok = mbar_wait(&s.kv_full, 0, ab);
+            Tracer tr;
+            tr.init(a.trace, 1);
+            tr.item(blockIdx.x);
+            bool ok = twait(tr, kBKvFull, &s.kv_full, 0, ab);
             tc_fence_after();
             // each GEMM goes out as one MMA burst (ptx.cuh): base descriptors only, the step
             // offsets are immediates inside the asm block
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             };
             // issue order per step i:  dP^T_i, dV_i, S^T_{i+1}, dQ^T_i, dK_i  (S^T_0 first)
             // S^T_{i+1} goes before dQ^T_i / dK_i so that the next step's P^T overlaps them
-            if (ok && (ok = mbar_wait(&s.q_full[0], 0, ab))) {
+            if (ok && (ok = twait(tr, kBQFull, &s.q_full[0], 0, ab))) {
                 tc_fence_after();
                 issue_st(0);
             }
@@ -366,30 +377,30 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 const uint32_t par = it & 1;
                 const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
                 // dP^T = V dO_i^T (its columns held dQ^T_{i-1} when D == 128)
-                if (!(ok = mbar_wait(&s.do_full[st], ph, ab))) break;
+                if (!(ok = twait(tr, kBDoFull, &s.do_full[st], ph, ab))) break;
                 if (C::DQ_OVER_DP && it > 0) {
-                    if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
+                    if (!(ok = twait(tr, kBDqFree, &s.dq_free, par ^ 1, ab))) break;
                 }
                 tc_fence_after();
                 if constexpr (D == 128) mma_ss_kk16_x8(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
                 else mma_ss_kk16_x4(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
                 tc_commit(&s.dp_full);
                 // dV += P^T dO_i (query pairs of group c sit at columns 64c + 8k, k < 4)
-                if (!(ok = mbar_wait(&s.p_full, par, ab))) break;
+                if (!(ok = twait(tr, kBPFull, &s.p_full, par, ab))) break;
                 tc_fence_after();
                 mma_ts_p_mn_x8(tmem + C::C_DV, tmem + C::C_S, sdesc_sw128(da, C::CHUNK, 1024), id_dv, it > 0 ? 1u : 0u);
                 tc_commit(&s.do_empty[st]);
                 // S^T_{i+1}: its columns held P^T_i, read by dV_i issued just above
                 if (it + 1 < nsteps) {
-                    if (!(ok = mbar_wait(&s.q_full[st ^ 1], ((it + 1) >> 1) & 1, ab))) break;
+                    if (!(ok = twait(tr, kBQFull, &s.q_full[st ^ 1], ((it + 1) >> 1) & 1, ab))) break;
                     tc_fence_after();
                     issue_st(it + 1);
                 }
                 // dQ^T_i = K^T dS^T, then dK += dS^T Q_i: dQ goes first so that its drain by the
                 // dQ warps (which frees the dP^T columns for the next step) overlaps dK
-                if (!(ok = mbar_wait(&s.ds_full, par, ab))) break;
+                if (!(ok = twait(tr, kBDsFull, &s.ds_full, par, ab))) break;
                 if (!C::DQ_OVER_DP && it > 0) {
-                    if (!(ok = mbar_wait(&s.dq_free, par ^ 1, ab))) break;
+                    if (!(ok = twait(tr, kBDqFree, &s.dq_free, par ^ 1, ab))) break;
                 }
                 tc_fence_after();
                 if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: A = K tile (MN-major), B = dS^T (MN-major)
@@ -417,6 +428,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         bool ok = true;
         DqOrder order;
         order.next = blk + 1;
+        Tracer tr;
+        tr.init(warp == 4 ? a.trace : nullptr, 2);
+        tr.item(blockIdx.x);
         for (int it = 0; it < nsteps; ++it) {
             const uint32_t par = it & 1;
             const int t = qt0 + it;                 // query tile within the sequence
@@ -431,8 +445,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             // ---- P^T ----
             {
                 // the stage's LSE / D rows landed with Q_i (already complete by the time S^T is)
-                bool w = mbar_wait(&s.q_full[st], (it >> 1) & 1, ab);
-                w = w && mbar_wait(&s.s_full, par, ab);
+                bool w = twait(tr, kBQFull, &s.q_full[st], (it >> 1) & 1, ab);
+                w = w && twait(tr, kBSFull, &s.s_full, par, ab);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             tc_fence_after();
@@ -473,11 +487,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             mbar_arrive(&s.p_full);
             // ---- dS^T = P^T (dP^T - D) -> shared memory ----
             {
-                const bool w = mbar_wait(&s.dp_full, par, ab);
+                const bool w = twait(tr, kBDpFull, &s.dp_full, par, ab);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             if (it > 0) {
-                const bool w = mbar_wait(&s.ds_free, par ^ 1, ab);
+                const bool w = twait(tr, kBDsFree, &s.ds_free, par ^ 1, ab);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             tc_fence_after();
@@ -509,6 +523,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.ds_full);
+            tr.mark(kMStepDone);
             // ---- dQ_i (d = 64 only; for d = 128 the dQ warp group drains it) ----
             if constexpr (!C::DQ_T) {
                 {
@@ -537,10 +552,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
         // ---- epilogue: dK, dV for this key tile ----
         if (nsteps > 0 && ok) {
-            const bool w = mbar_wait(&s.dkv_full, 0, ab);
+            const bool w = twait(tr, kBDkvFull, &s.dkv_full, 0, ab);
             ok = __all_sync(0xffffffffu, w);
             tc_fence_after();
         }
+        tr.mark(kMEpilogue);
         const bool row_ok = j <= j1;
         const long krow = key_row(p, sv, j);
 #pragma unroll
@@ -724,6 +740,9 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0 && nsteps > 0) {
+            Tracer tr;
+            tr.init(a.trace, 0);
+            tr.item(blockIdx.x);
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
@@ -738,7 +757,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
             for (int it = 0; it < nsteps; ++it) {
                 const uint32_t ph = it & 1;
                 const int row = sv.q0 + (qt0 + it) * p.P;
-                if (!mbar_wait(&s.q_empty, ph ^ 1, ab)) break;
+                if (!twait(tr, kBQEmpty, &s.q_empty, ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.q_full, tile_bytes + 2 * 128 * 4);
                 for (int c = 0; c < KCH; ++c) tma_load_4d(s.q[c], &tmq, &s.q_full, c * 64, g * p.G, row, sv.tma_b);
                 {
@@ -747,7 +766,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                     bulk_load(s.stat[1], a.delta_t + trow, 512, &s.q_full);
                 }
                 ++q_issued;
-                if (!mbar_wait(&s.do_empty, ph ^ 1, ab)) break;
+                if (!twait(tr, kBDoEmpty, &s.do_empty, ph ^ 1, ab)) break;
                 mbar_expect_tx(&s.do_full, tile_bytes);
                 for (int c = 0; c < KCH; ++c) tma_load_4d(s.dO[c], &tmdo, &s.do_full, c * 64, g * p.G, row, sv.tma_b);
                 ++do_issued;
@@ -770,12 +789,15 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
             const uint64_t pd_mn = sdesc_sw128(smem_u32(s.p), 128 * 128, 1024);
             const uint64_t dsd_mn = sdesc_sw128(smem_u32(s.ds), 128 * 128, 1024);
             const uint64_t dsd_k = sdesc_sw128(smem_u32(s.ds), 16, 1024);
-            bool ok = mbar_wait(&s.kv_full, 0, ab);
+            Tracer tr;
+            tr.init(a.trace, 1);
+            tr.item(blockIdx.x);
+            bool ok = twait(tr, kBKvFull, &s.kv_full, 0, ab);
             int ndq = 0;  // dQ^T halves issued so far
             for (int it = 0; ok && it < nsteps; ++it) {
                 const uint32_t par = it & 1;
-                if (!(ok = mbar_wait(&s.q_full, par, ab))) break;
-                if (!(ok = mbar_wait(&s.do_full, par, ab))) break;
+                if (!(ok = twait(tr, kBQFull, &s.q_full, par, ab))) break;
+                if (!(ok = twait(tr, kBDoFull, &s.do_full, par, ab))) break;
                 tc_fence_after();
                 // S = Q K^T, dP = dO V^T (K = d: KCH 64-column chunks of each operand)
                 if constexpr (KCH == 4) {
@@ -789,7 +811,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 }
                 tc_commit(&s.dp_full);
                 // P and dS in shared memory (the compute group has also read S and dP out)
-                if (!(ok = mbar_wait(&s.pds_full, par, ab))) break;
+                if (!(ok = twait(tr, kBPdsFull, &s.pds_full, par, ab))) break;
                 tc_fence_after();
                 const uint32_t acc = it > 0 ? 1u : 0u;
                 for (int h = 0; h < 2; ++h) {
@@ -801,7 +823,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 }
                 for (int h = 0; h < 2; ++h) {
                     // dQ^T_h = K_h^T dS^T into the one dQ^T column block, drained in between
-                    if (ndq > 0 && !(ok = mbar_wait(&s.dq_free, (ndq - 1) & 1, ab))) break;
+                    if (ndq > 0 && !(ok = twait(tr, kBDqFree, &s.dq_free, (ndq - 1) & 1, ab))) break;
                     tc_fence_after();
                     mma_ss_mnk_x4(tmem + C_DQ, sdesc_sw128(smem_u32(s.k[2 * h]), kKeys256 * 128, 1024), dsd_k, id_dq,
                                   0u);
@@ -825,15 +847,18 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
         const float c = p.scale_log2;
         bool ok = true;
         int ndq = 0;
+        Tracer tr;
+        tr.init(warp == 4 ? a.trace : nullptr, 2);
+        tr.item(blockIdx.x);
         for (int it = 0; it < nsteps; ++it) {
             const uint32_t par = it & 1;
             const int t = qt0 + it;
             const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
             {
-                bool w = mbar_wait(&s.q_full, par, ab);  // the LSE / D rows land with Q
-                w = w && mbar_wait(&s.s_full, par, ab);
-                w = w && mbar_wait(&s.dp_full, par, ab);
-                if (it > 0) w = w && mbar_wait(&s.pds_free, par ^ 1, ab);
+                bool w = twait(tr, kBQFull, &s.q_full, par, ab);  // the LSE / D rows land with Q
+                w = w && twait(tr, kBSFull, &s.s_full, par, ab);
+                w = w && twait(tr, kBDpFull, &s.dp_full, par, ab);
+                if (it > 0) w = w && twait(tr, kBPdsFree, &s.pds_free, par ^ 1, ab);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             tc_fence_after();
@@ -874,10 +899,11 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.pds_full);
+            tr.mark(kMSoftmaxDone);
             // ---- dQ^T halves: lane = column of d within the half, columns = query rows ----
             for (int h = 0; h < 2; ++h) {
                 {
-                    const bool w = mbar_wait(&s.dq_full, ndq & 1, ab);
+                    const bool w = twait(tr, kBDqFull, &s.dq_full, ndq & 1, ab);
                     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 }
                 ++ndq;
@@ -896,6 +922,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
 #pragma unroll
                     for (int x = 0; x < 64; ++x) atomicAdd(acc + (long)(64 + x) * D, __uint_as_float(qb[x]));
                 }
+                tr.mark(kMDqReduced);
             }
             if (!ok) break;
         }

@@ -34,6 +34,7 @@
 // previous item's S MMAs, which read the Q tiles, have completed) and o_free[k] (the
 // epilogue has read O_k out of tensor memory before the next P V overwrites it).
 #include "fwd_items.cuh"
+#include "trace.cuh"
 
 namespace fa {
 namespace {
@@ -128,6 +129,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
+            Tracer tr;
+            tr.init(a.trace, 0);
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
@@ -138,8 +141,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
              idx += step, step = 2 * (int)gridDim.x - step) {
                 const FwdItem w = fwd_item(a, idx);
                 if (!w.live || w.u1 <= w.u0) continue;
+                tr.item(idx);
                 // the previous item's Q tiles are free once its S MMAs have completed
-                if (n_q > 0 && !(ok = mbar_wait(&s.q_empty, (n_q - 1) & 1, ab))) break;
+                if (n_q > 0 && !(ok = twait(tr, kBQEmpty, &s.q_empty, (n_q - 1) & 1, ab))) break;
                 uint32_t qbytes = 0;
                 for (int k = 0; k < 2; ++k)
                     if (w.ti[k].t1 > w.ti[k].t0) qbytes += qbox * C::KCH;
@@ -156,12 +160,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     const uint32_t ph = (gt / C::STAGES) & 1;
                     int krow, kouter;
                     kv_tile_coord(p, w.sv, j * BN, krow, kouter);
-                    if (!(ok = mbar_wait(&s.k_empty[st], ph ^ 1, ab))) break;
+                    if (!(ok = twait(tr, kBKEmpty, &s.k_empty[st], ph ^ 1, ab))) break;
                     mbar_expect_tx(&s.k_full[st], C::TILE_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
                         tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, w.g, krow, kouter);
                     ++k_issued;
-                    if (!(ok = mbar_wait(&s.v_empty[st], ph ^ 1, ab))) break;
+                    if (!(ok = twait(tr, kBVEmpty, &s.v_empty[st], ph ^ 1, ab))) break;
                     mbar_expect_tx(&s.v_full[st], C::TILE_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
                         tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, w.g, krow, kouter);
@@ -186,6 +190,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         // Everything the issue path touches lives in registers (no per-tile arrays indexed
         // at run time), so consecutive MMAs go out back to back.
         if (lane == 0) {
+            Tracer tr;
+            tr.init(a.trace, 1);
             constexpr uint32_t idS = idesc_16(128, BN, false, false, F16);
             constexpr uint32_t idO = idesc_16(128, D, false, true, F16);
             constexpr uint32_t kStageStep = (uint32_t)C::TILE_BYTES >> 4;  // descriptor units per stage
@@ -221,12 +227,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     if (!w.live) u1 = u0;
                 }
                 if (u1 <= u0) continue;
-                ok = mbar_wait(&s.q_full, n_q & 1, ab);
+                tr.item(idx);
+                ok = twait(tr, kBQFull, &s.q_full, n_q & 1, ab);
                 ++n_q;
                 tc_fence_after();
                 {
                     const int st0 = gt % C::STAGES;
-                    if (ok && (ok = mbar_wait(&s.k_full[st0], (gt / C::STAGES) & 1, ab))) {
+                    if (ok && (ok = twait(tr, kBKFull, &s.k_full[st0], (gt / C::STAGES) & 1, ab))) {
                         // prologue: S_k for the first KV tile (the S columns held the previous
                         // item's last P, read by P V MMAs issued earlier)
                         tc_fence_after();
@@ -253,15 +260,15 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     const uint64_t kd1 = kd_base + (uint64_t)(st1 * kStageStep);
                     const bool next = j + 1 < u1;
                     bool k_ready = false;
-                    ok = mbar_wait(&s.v_full[st], ph, ab);
+                    ok = twait(tr, kBVFull, &s.v_full[st], ph, ab);
                     tc_fence_after();
                     // tile 0: O_0 += P_0 V_j, then S_0 for the next key tile
                     if (ok && j >= ta0 && j < ta1) {
-                        ok = mbar_wait(&s.p_full[0], pc0 & 1, ab);
+                        ok = twait(tr, kBPFull, &s.p_full[0], pc0 & 1, ab);
                         ++pc0;
                         // the first P V of the item overwrites O_0: the previous item's
                         // epilogue must have read it
-                        if (ok && j == ta0 && oc0 > 0) ok = mbar_wait(&s.o_free[0], (oc0 - 1) & 1, ab);
+                        if (ok && j == ta0 && oc0 > 0) ok = twait(tr, kBOFree, &s.o_free[0], (oc0 - 1) & 1, ab);
                         tc_fence_after();
                         if (ok) {
                             issue_pv(256, 0, vd, j > ta0 ? 1u : 0u);
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         }
                     }
                     if (ok && next && j + 1 >= ta0 && j + 1 < ta1) {
-                        ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                        ok = twait(tr, kBKFull, &s.k_full[st1], ph1, ab);
                         tc_fence_after();
                         k_ready = true;
                         if (ok) {
@@ -282,9 +289,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     }
                     // tile 1
                     if (ok && j >= tb0 && j < tb1) {
-                        ok = mbar_wait(&s.p_full[1], pc1 & 1, ab);
+                        ok = twait(tr, kBPFull, &s.p_full[1], pc1 & 1, ab);
                         ++pc1;
-                        if (ok && j == tb0 && oc1 > 0) ok = mbar_wait(&s.o_free[1], (oc1 - 1) & 1, ab);
+                        if (ok && j == tb0 && oc1 > 0) ok = twait(tr, kBOFree, &s.o_free[1], (oc1 - 1) & 1, ab);
                         tc_fence_after();
                         if (ok) {
                             issue_pv(384, 128, vd, j > tb0 ? 1u : 0u);
@@ -296,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     }
                     if (ok && next && j + 1 >= tb0 && j + 1 < tb1) {
                         if (!k_ready) {
-                            ok = mbar_wait(&s.k_full[st1], ph1, ab);
+                            ok = twait(tr, kBKFull, &s.k_full[st1], ph1, ab);
                             tc_fence_after();
                             k_ready = true;
                         }
@@ -335,6 +342,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const float c = p.scale_log2;
         uint32_t scount = 0, ocount = 0;  // S tiles and O tiles received (carried across items)
         bool ok = true;
+        Tracer tr;
+        tr.init((warp & 3) == 0 ? a.trace : nullptr, 2 + k);
         for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
              idx += step, step = 2 * (int)gridDim.x - step) {
         // only the loop bounds and the row's key band stay live across the key loop; the
@@ -343,6 +352,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         {
             const FwdItem w = fwd_item(a, idx);
             if (!w.live) continue;
+            tr.item(idx);
             my_t0 = k ? w.ti[1].t0 : w.ti[0].t0;
             my_t1 = k ? w.ti[1].t1 : w.ti[0].t1;
             const int i = (k ? w.ti[1].s0 : w.ti[0].s0) + r / p.G;
@@ -352,7 +362,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
         float m_used = -INFINITY, l = 0.f;
         for (int j = my_t0; j < my_t1; ++j) {
-            const bool w = mbar_wait(&s.s_full[k], scount & 1, ab);
+            const bool w = twait(tr, kBSFull, &s.s_full[k], scount & 1, ab);
             if (!__all_sync(0xffffffffu, w)) {
                 ok = false;
                 break;
@@ -424,6 +434,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.p_full[k]);
+            tr.mark(kMSoftmaxDone);
         }
         // ---------------- epilogue ----------------
         int idx2 = idx;
@@ -436,7 +447,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const bool row_valid = (k ? w.ti[1].active : w.ti[0].active) && (r < p.P * p.G) && i < sv.nq;
         const bool has_o = my_t1 > my_t0;  // uniform over the warp group
         if (has_o && ok) {
-            const bool wt = mbar_wait(&s.o_full[k], ocount & 1, ab);
+            const bool wt = twait(tr, kBOFull, &s.o_full[k], ocount & 1, ab);
             ++ocount;
             ok = __all_sync(0xffffffffu, wt);
             tc_fence_after();
@@ -494,6 +505,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.o_free[k]);
+            tr.mark(kMEpilogueDone);
         } else if (row_valid) {
             if (!split_mode) {
                 uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;

@@ -54,6 +54,7 @@ struct FwdArgs {
     const float* q_descale;
     const float* k_descale;
     const float* v_descale;
+    unsigned long long* trace;  // trace builds only: the workspace's trace region (else null)
 };
 
 // ------------------------------------------------------------------------------------------
@@ -104,6 +105,7 @@ struct BwdArgs {
     int* dq_count;         // [h_kv, n_qtiles] dQ contributions landed per query tile, or null:
                            // non-null = deterministic order (key blocks in descending order)
     int* status;
+    unsigned long long* trace;  // trace builds only: the workspace's trace region (else null)
 };
 
 // host-side launchers (defined next to each kernel)

@@ -9,9 +9,11 @@ Here:
   bounds even without the check.  The status word must read FA_ERR_DEVICE_CHECK and
   every output must keep the canary bytes it started with: no kernel after the check
   may touch them.
-- wait_limit_ns = 1: every kernel's first wait on its pipeline runs out at once, so each
-  CTA takes its give-up path (record FA_ERR_TIMEOUT, let its copies and MMAs land, free its
-  tensor memory, return).  The status word must read FA_ERR_TIMEOUT, and the next call
+- wait_limit_ns = 1: the first wait of a kernel's pipeline that is not complete when it
+  starts runs out at once, so the CTA takes its give-up path (record FA_ERR_TIMEOUT, let its
+  copies and MMAs land, free its tensor memory, return); the cases are shaped so that such
+  a wait comes early (a consumer waits for the first copies or MMAs, a producer for ring
+  slots).  The status word must read FA_ERR_TIMEOUT, and the next call
   with the default limit, on the same device and streams, must match the oracle: a CTA
   that had left tensor memory allocated or a copy in flight would break it.
 No GPU fault, trap or hang is involved: the waits are bounded and the offsets in range.
@@ -100,7 +102,9 @@ TIMEOUT_CASES = [
     ("fwd_d128_two_tiles", dict(d=128, s_q=600, s_kv=600), None),
     ("fwd_d256", dict(d=256), None),
     ("fwd_split_keys", dict(d=128, s_q=64, s_kv=4100, h_q=8), None),
-    ("decode", dict(d=128, s_q=1, s_kv=3000, h_q=8), None),
+    # a long cache in few units: each split streams many key tiles, so the producer
+    # waits for ring slots (with one tile per split nothing ever waits)
+    ("decode", dict(d=128, B=1, s_q=1, s_kv=65536, h_q=8), None),
     ("bwd_d64", dict(d=64, sinks=True), 0),
     ("bwd_d128", dict(d=128, s_q=600, s_kv=600), 0),
     ("bwd_d128_deterministic", dict(d=128, s_q=600, s_kv=600), 4),
