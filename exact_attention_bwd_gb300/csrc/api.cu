@@ -194,6 +194,7 @@ struct FwdPlan {
     FwdPath path = FwdPath::kEmpty;
     int n_blocks = 0, n_splits = 1, split_tiles = 0;
     int unit_major = 0;
+    int tokens = 0;        // packed batch with cu_seqlens_q == cu_seqlens_k: token tiles
     size_t part_rows = 0;  // rows of the split partials
     int s_pad = 0;         // e4m3: keys per V^T row (s_kv rounded up to 16)
     size_t off_vt = 0;     // e4m3: workspace offset of V^T
@@ -277,6 +278,10 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
             pl.ws_bytes = kStatusBytes + align256(pl.part_rows * pl.n_splits * p.d * 4) +
                           align256(pl.part_rows * pl.n_splits * 4);
         }
+    } else if (p.cu_q == p.cu_k && p.d <= 128) {
+        // queries and keys packed alike: tiles run over the packed token axis
+        pl.tokens = 1;
+        pl.n_blocks = (p.T_q + rows_per_cta - 1) / rows_per_cta;
     } else {
         pl.n_blocks = p.T_q / rows_per_cta + p.B;
     }
@@ -501,6 +506,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.n_splits = pl.n_splits;
     a.split_tiles = pl.split_tiles;
     a.unit_major = pl.unit_major;
+    a.tokens = pl.tokens;
     {
         const long items = p.cu_q ? (long)pl.n_blocks * p.h_kv : (long)pl.n_blocks * pl.n_splits * p.h_kv * p.B;
         a.n_items = (int)items;

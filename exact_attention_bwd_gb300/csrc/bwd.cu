@@ -814,6 +814,18 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 if (!(ok = twait(tr, kBPdsFull, &s.pds_full, par, ab))) break;
                 tc_fence_after();
                 const uint32_t acc = it > 0 ? 1u : 0u;
+                // dQ^T_h = K_h^T dS^T into the one dQ^T column block, drained between the halves
+                auto issue_dq = [&](int h) -> bool {
+                    if (ndq > 0 && !twait(tr, kBDqFree, &s.dq_free, (ndq - 1) & 1, ab)) return false;
+                    tc_fence_after();
+                    mma_ss_mnk_x4(tmem + C_DQ, sdesc_sw128(smem_u32(s.k[2 * h]), kKeys256 * 128, 1024), dsd_k, id_dq,
+                                  0u);
+                    tc_commit(&s.dq_full);
+                    ++ndq;
+                    return true;
+                };
+                // the first dQ^T half goes first, so that its drain overlaps dV^T and dK^T
+                if (!(ok = issue_dq(0))) break;
                 for (int h = 0; h < 2; ++h) {
                     // dV^T_h += dO_h^T P, dK^T_h += Q_h^T dS (the h-th 128 columns of d)
                     mma_ss_mnmn_x8(tmem + C_DV + 64 * h, sdesc_sw128(smem_u32(s.dO[2 * h]), 128 * 128, 1024), pd_mn,
@@ -821,19 +833,12 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                     mma_ss_mnmn_x8(tmem + C_DK + 64 * h, sdesc_sw128(smem_u32(s.q[2 * h]), 128 * 128, 1024), dsd_mn,
                                    id_kv, acc);
                 }
-                for (int h = 0; h < 2; ++h) {
-                    // dQ^T_h = K_h^T dS^T into the one dQ^T column block, drained in between
-                    if (ndq > 0 && !(ok = twait(tr, kBDqFree, &s.dq_free, (ndq - 1) & 1, ab))) break;
-                    tc_fence_after();
-                    mma_ss_mnk_x4(tmem + C_DQ, sdesc_sw128(smem_u32(s.k[2 * h]), kKeys256 * 128, 1024), dsd_k, id_dq,
-                                  0u);
-                    tc_commit(&s.dq_full);
-                    ++ndq;
-                }
-                if (!ok) break;
-                // Q, dO, P and dS of this step are read once these MMAs complete
+                // Q and dO of this step are read once these complete (dQ^T reads K and dS only):
+                // the next step's copies start while the second dQ^T half runs and drains
                 tc_commit(&s.q_empty);
                 tc_commit(&s.do_empty);
+                if (!(ok = issue_dq(1))) break;
+                // P and dS are read once the second dQ^T half completes
                 tc_commit(&s.pds_free);
             }
             tc_commit(&s.dkv_full);

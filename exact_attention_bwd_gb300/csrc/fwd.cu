@@ -10,6 +10,9 @@
 //   warp 1       MMA issuer (one thread): S_k = Q_k K^T into TMEM, O_k += P_k V with P_k
 //                read back from TMEM
 //   warp 2       owns the TMEM allocation
+//   warp 3       tile scheduler: decodes this CTA's work items ahead of the other roles into
+//                a small ring in shared memory (the item, each row's allowed key interval),
+//                so that no role spends its own latency on the decode
 //   warps 4..7   softmax of tile 0, warps 8..11 softmax of tile 1: each thread owns one
 //                row (one TMEM lane); exp2-based online softmax with lazy rescaling
 //
@@ -28,7 +31,11 @@
 // query tiles, and a key range in split mode) in heaviest-first order with a grid stride
 // (alternating direction from round to round under a causal mask, see first_step);
 // a packed batch's items are found by binary search over its offsets (dew-flash-attn PyPI
-// page, "Packed sequences"), and idle items cost only their decode.  Barrier phases carry
+// page, "Packed sequences"), and idle items cost only their decode.  When the queries and
+// keys are packed alike (cu_seqlens_q and cu_seqlens_k the same array) the query tiles run
+// over the packed token axis instead: a tile holds P consecutive tokens, which may belong
+// to several short sequences, each row masked to its own sequence's band, so a batch of
+// short sequences costs only its tokens rather than a tile per sequence.  Barrier phases carry
 // over from item to item, so the next item's Q load and first S = Q K^T overlap the
 // previous item's epilogue; two barriers hand the shared resources over: q_empty (the
 // previous item's S MMAs, which read the Q tiles, have completed) and o_free[k] (the
@@ -56,6 +63,18 @@ struct FwdCfg {
     // TMEM columns: S_k at 128k, O_k at 256 + 128k
 };
 
+// One decoded work item, as the scheduler warp hands it to the other roles.
+struct ItemInfo {
+    int idx, end;       // item index; end = 1: no more items for this CTA
+    int g, split, b;    // key/value head, key split, batch or sequence
+    int q0, k0, tma_b;  // first query / key row of the sequence, outer TMA coordinate
+    int u0, u1;         // union key-tile range of the two tiles (u1 <= u0: none)
+    int s0[2], t0[2], t1[2];  // first query position and key-tile range of each tile
+};
+constexpr int kItemSlots = 3;
+// arrivals that free an item slot: producer, MMA issuer and the eight softmax warps
+constexpr int kItemReaders = 10;
+
 template <int D>
 struct __align__(1024) FwdSmem {
     uint8_t q[2][FwdCfg<D>::TILE_BYTES];
@@ -67,6 +86,9 @@ struct __align__(1024) FwdSmem {
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
     uint64_t q_empty;
     uint64_t drain;
+    uint64_t item_full[kItemSlots], item_empty[kItemSlots];
+    ItemInfo item[kItemSlots];
+    int2 band[kItemSlots][2][128];  // (jlo, jhi) of every row of both query tiles
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -103,6 +125,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
         mbar_init(&s.q_empty, 1);
         mbar_init(&s.drain, 1);
+        for (int i = 0; i < kItemSlots; ++i) {
+            mbar_init(&s.item_full[i], 1);
+            mbar_init(&s.item_empty[i], kItemReaders);
+        }
         fence_mbar_init();
     }
     if (p.P * p.G < 128) {
@@ -137,38 +163,40 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             const uint32_t qbox = (uint32_t)(p.P * p.G) * 128u;  // bytes of one 64-col Q box
             int gt = 0, n_q = 0, k_issued = 0, v_issued = 0;    // key tiles, Q loads, copies issued
             bool ok = true;
-            for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
-             idx += step, step = 2 * (int)gridDim.x - step) {
-                const FwdItem w = fwd_item(a, idx);
-                if (!w.live || w.u1 <= w.u0) continue;
+            for (int n = 0; ok; ++n) {
+                const int slot = n % kItemSlots;
+                if (!(ok = mbar_wait(&s.item_full[slot], (n / kItemSlots) & 1, ab))) break;
+                const ItemInfo& it = s.item[slot];
+                const int end = it.end, idx = it.idx, g = it.g, u0 = it.u0, u1 = it.u1;
+                const SeqView sv{it.b, it.q0, 0, it.k0, 0, it.tma_b};
+                const int qr0 = it.q0 + it.s0[0], qr1 = it.q0 + it.s0[1];
+                const bool on0 = it.t1[0] > it.t0[0], on1 = it.t1[1] > it.t0[1];
+                mbar_arrive(&s.item_empty[slot]);
+                if (end) break;
+                if (u1 <= u0) continue;
                 tr.item(idx);
                 // the previous item's Q tiles are free once its S MMAs have completed
                 if (n_q > 0 && !(ok = twait(tr, kBQEmpty, &s.q_empty, (n_q - 1) & 1, ab))) break;
-                uint32_t qbytes = 0;
-                for (int k = 0; k < 2; ++k)
-                    if (w.ti[k].t1 > w.ti[k].t0) qbytes += qbox * C::KCH;
-                mbar_expect_tx(&s.q_full, qbytes);
-                for (int k = 0; k < 2; ++k) {
-                    if (w.ti[k].t1 <= w.ti[k].t0) continue;
-                    for (int c = 0; c < C::KCH; ++c)
-                        tma_load_4d(&s.q[k][c * C::CHUNK_BYTES], &tmq, &s.q_full, c * 64, w.g * p.G,
-                                    w.sv.q0 + w.ti[k].s0, w.sv.tma_b);
+                mbar_expect_tx(&s.q_full, qbox * C::KCH * ((on0 ? 1u : 0u) + (on1 ? 1u : 0u)));
+                for (int c = 0; c < C::KCH; ++c) {
+                    if (on0) tma_load_4d(&s.q[0][c * C::CHUNK_BYTES], &tmq, &s.q_full, c * 64, g * p.G, qr0, sv.tma_b);
+                    if (on1) tma_load_4d(&s.q[1][c * C::CHUNK_BYTES], &tmq, &s.q_full, c * 64, g * p.G, qr1, sv.tma_b);
                 }
                 ++n_q;
-                for (int j = w.u0; j < w.u1; ++j, ++gt) {
+                for (int j = u0; j < u1; ++j, ++gt) {
                     const int st = gt % C::STAGES;
                     const uint32_t ph = (gt / C::STAGES) & 1;
                     int krow, kouter;
-                    kv_tile_coord(p, w.sv, j * BN, krow, kouter);
+                    kv_tile_coord(p, sv, j * BN, krow, kouter);
                     if (!(ok = twait(tr, kBKEmpty, &s.k_empty[st], ph ^ 1, ab))) break;
                     mbar_expect_tx(&s.k_full[st], C::TILE_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
-                        tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, w.g, krow, kouter);
+                        tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, g, krow, kouter);
                     ++k_issued;
                     if (!(ok = twait(tr, kBVEmpty, &s.v_empty[st], ph ^ 1, ab))) break;
                     mbar_expect_tx(&s.v_full[st], C::TILE_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
-                        tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, w.g, krow, kouter);
+                        tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, g, krow, kouter);
                     ++v_issued;
                 }
             }
@@ -212,20 +240,16 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             uint32_t oc0 = 0, oc1 = 0;  // O tiles completed per query tile (o_full commits)
             int gt = 0, n_q = 0;        // key tiles, items consumed
             bool ok = true;
-            for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
-             idx += step, step = 2 * (int)gridDim.x - step) {
+            for (int n = 0; ok; ++n) {
                 // the item's key-tile ranges are all the issue loop needs
-                int ta0, ta1, tb0, tb1, u0, u1;
-                {
-                    const FwdItem w = fwd_item(a, idx);
-                    ta0 = w.ti[0].t0;
-                    ta1 = w.ti[0].t1;
-                    tb0 = w.ti[1].t0;
-                    tb1 = w.ti[1].t1;
-                    u0 = w.u0;
-                    u1 = w.u1;
-                    if (!w.live) u1 = u0;
-                }
+                const int slot = n % kItemSlots;
+                if (!(ok = mbar_wait(&s.item_full[slot], (n / kItemSlots) & 1, ab))) break;
+                const ItemInfo& itm = s.item[slot];
+                const int end = itm.end, idx = itm.idx;
+                const int ta0 = itm.t0[0], ta1 = itm.t1[0], tb0 = itm.t0[1], tb1 = itm.t1[1];
+                const int u0 = itm.u0, u1 = itm.u1;
+                mbar_arrive(&s.item_empty[slot]);
+                if (end) break;
                 if (u1 <= u0) continue;
                 tr.item(idx);
                 ok = twait(tr, kBQFull, &s.q_full, n_q & 1, ab);
@@ -330,6 +354,92 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tc_commit(&s.drain);
             mbar_wait_quiet(&s.drain, 0);
         }
+    } else if (warp == 3) {
+        // ================= tile scheduler =================
+        // Walks the CTA's items (a grid stride, alternating direction under `snake`) and hands
+        // each live one to the other roles through the item ring: lane 0 writes the item, every
+        // lane the allowed key interval of 8 of its 256 rows.  In token mode the key-tile ranges
+        // come from those intervals (their hull), since a tile's rows may span sequences.
+        int n = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x, step = first_step(a.snake); idx < a.n_items;
+             idx += step, step = 2 * (int)gridDim.x - step) {
+            FwdItem w = fwd_item(a, idx);
+            if (!w.live) continue;
+            const int slot = n % kItemSlots;
+            if (n >= kItemSlots) {
+                const bool wt = mbar_wait(&s.item_empty[slot], ((n / kItemSlots) - 1) & 1, ab);
+                if (!__all_sync(0xffffffffu, wt)) {
+                    ok = false;
+                    break;
+                }
+            }
+#pragma unroll 1
+            for (int k = 0; k < 2; ++k) {
+                int lo_min = kNoRow, hi_max = -1;
+#pragma unroll 1
+                for (int m = 0; m < 4; ++m) {
+                    const int r = lane + 32 * m;
+                    int jlo, jhi;
+                    fwd_row_band(a, w, k, r, jlo, jhi);
+                    s.band[slot][k][r] = make_int2(jlo, jhi);
+                    if (jlo <= jhi) {
+                        lo_min = min(lo_min, jlo);
+                        hi_max = max(hi_max, jhi);
+                    }
+                }
+                if (a.tokens) {
+                    lo_min = __reduce_min_sync(0xffffffffu, lo_min);
+                    hi_max = __reduce_max_sync(0xffffffffu, hi_max);
+                    w.ti[k].t0 = lo_min <= hi_max ? lo_min / BN : 0;
+                    w.ti[k].t1 = lo_min <= hi_max ? hi_max / BN + 1 : 0;
+                }
+            }
+            if (a.tokens) {
+                w.u0 = 0x7fffffff;
+                w.u1 = 0;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (w.ti[k].t1 > w.ti[k].t0) {
+                        w.u0 = min(w.u0, w.ti[k].t0);
+                        w.u1 = max(w.u1, w.ti[k].t1);
+                    }
+                if (w.u1 == 0) w.u0 = 0;
+            }
+            if (lane == 0) {
+                ItemInfo& it = s.item[slot];
+                it.idx = idx;
+                it.end = 0;
+                it.g = w.g;
+                it.split = w.split;
+                it.b = w.sv.b;
+                it.q0 = w.sv.q0;
+                it.k0 = w.sv.k0;
+                it.tma_b = w.sv.tma_b;
+                it.u0 = w.u0;
+                it.u1 = w.u1;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    it.s0[k] = w.ti[k].s0;
+                    it.t0[k] = w.ti[k].t0;
+                    it.t1[k] = w.ti[k].t1;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.item_full[slot]);
+            ++n;
+        }
+        if (ok) {
+            // the end marker
+            const int slot = n % kItemSlots;
+            bool wt = true;
+            if (n >= kItemSlots) wt = mbar_wait(&s.item_empty[slot], ((n / kItemSlots) - 1) & 1, ab);
+            if (__all_sync(0xffffffffu, wt)) {
+                if (lane == 0) s.item[slot].end = 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.item_full[slot]);
+            }
+        }
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
@@ -344,22 +454,26 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         bool ok = true;
         Tracer tr;
         tr.init((warp & 3) == 0 ? a.trace : nullptr, 2 + k);
-        for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
-             idx += step, step = 2 * (int)gridDim.x - step) {
-        // only the loop bounds and the row's key band stay live across the key loop; the
-        // epilogue decodes the item again (cheap) instead of holding it in registers
-        int my_t0, my_t1, jlo, jhi;
+        for (int n = 0; ok; ++n) {
+        // the item comes decoded from the scheduler warp; only the loop bounds, the row's key
+        // band and its sink stay live across the key loop, the epilogue reads the rest again
+        // from the item slot (held until the epilogue is done)
+        const int slot = n % kItemSlots;
         {
-            const FwdItem w = fwd_item(a, idx);
-            if (!w.live) continue;
-            tr.item(idx);
-            my_t0 = k ? w.ti[1].t0 : w.ti[0].t0;
-            my_t1 = k ? w.ti[1].t1 : w.ti[0].t1;
-            const int i = (k ? w.ti[1].s0 : w.ti[0].s0) + r / p.G;
-            const bool rv = (k ? w.ti[1].active : w.ti[0].active) && (r < p.P * p.G) && i < w.sv.nq;
-            jlo = rv ? w.band.lo(i) : 1;
-            jhi = rv ? w.band.hi(i) : 0;
+            const bool wt = mbar_wait(&s.item_full[slot], (n / kItemSlots) & 1, ab);
+            if (!__all_sync(0xffffffffu, wt)) {
+                ok = false;
+                break;
+            }
         }
+        if (s.item[slot].end) break;
+        tr.item(s.item[slot].idx);
+        const int my_t0 = s.item[slot].t0[k], my_t1 = s.item[slot].t1[k];
+        const int2 rb = s.band[slot][k][r];
+        const int jlo = rb.x, jhi = rb.y;
+        // the sink's logit, fetched now so that its latency hides behind the key loop
+        float sink2 = 0.f;
+        if (p.sinks && a.n_splits == 1 && jlo != kNoRow) sink2 = p.sinks[s.item[slot].g * p.G + r % p.G] * kLog2e;
         float m_used = -INFINITY, l = 0.f;
         for (int j = my_t0; j < my_t1; ++j) {
             const bool w = twait(tr, kBSFull, &s.s_full[k], scount & 1, ab);
@@ -375,9 +489,18 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             uint32_t sr[128];
             tmem_ld_32x32b_x128(tS, sr);
             if (edge) {
+                // the row's allowed columns [lo, hi] of this tile (a row without keys has
+                // lo > 127 and hi < 0) as a bit mask per 32-column chunk, applied without
+                // branches: one bit test and one select per element
+                const int lo = jlo - j0, hi = jhi - j0;
 #pragma unroll
-                for (int cc = 0; cc < BN; ++cc)
-                    if (j0 + cc < jlo || j0 + cc > jhi) sr[cc] = __float_as_uint(-INFINITY);
+                for (int cb = 0; cb < BN; cb += 32) {
+                    const int c0 = max(lo - cb, 0), c1 = min(hi - cb, 31);
+                    const uint32_t keep = c0 > c1 ? 0u : (0xffffffffu >> (31 - c1)) & (0xffffffffu << c0);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (!(keep & (1u << t))) sr[cb + t] = __float_as_uint(-INFINITY);
+                }
             }
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -437,14 +560,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tr.mark(kMSoftmaxDone);
         }
         // ---------------- epilogue ----------------
-        int idx2 = idx;
-        asm volatile("" : "+r"(idx2));  // a fresh decode, not the one held before the loop
-        const FwdItem w = fwd_item(a, idx2);
-        const SeqView& sv = w.sv;
-        const int g = w.g, split = w.split;
-        const int i = (k ? w.ti[1].s0 : w.ti[0].s0) + r / p.G;  // query position
-        const int h = g * p.G + r % p.G;                         // query head
-        const bool row_valid = (k ? w.ti[1].active : w.ti[0].active) && (r < p.P * p.G) && i < sv.nq;
+        const ItemInfo& itm = s.item[slot];
+        const SeqView sv{itm.b, itm.q0, 0, 0, 0, 0};
+        const int g = itm.g, split = itm.split;
+        const int i = itm.s0[k] + r / p.G;  // query position (a packed row in token mode)
+        const int h = g * p.G + r % p.G;    // query head
+        const bool row_valid = jlo != kNoRow;
         const bool has_o = my_t1 > my_t0;  // uniform over the warp group
         if (has_o && ok) {
             const bool wt = twait(tr, kBOFull, &s.o_full[k], ocount & 1, ab);
@@ -455,7 +576,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const bool split_mode = a.n_splits > 1;
         float oscale = 0.f, lse = -INFINITY;
         if (!split_mode && p.sinks && row_valid) {
-            const float s2 = p.sinks[h] * kLog2e;
+            const float s2 = sink2;
             const float mf = fmaxf(m_used, s2);
             const float wgt = (m_used == -INFINITY) ? 0.f : ex2(m_used - mf);
             const float lt = l * wgt + ex2(s2 - mf);
@@ -475,36 +596,34 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             }
         }
         if (has_o && ok) {
-            // warp-collective TMEM reads; only valid rows store
-#pragma unroll
-            for (int cb = 0; cb < D; cb += 32) {
-                uint32_t orr[32];
-                tmem_ld_32x32b_x32(tO + cb, orr);
-                if (!row_valid) continue;
+            // the whole O row into registers (warp-collective TMEM reads), then O_k is free for
+            // the next item's P V while the row is scaled and stored; only valid rows store
+            uint32_t orr[D];
+            if constexpr (D == 128) tmem_ld_32x32b_x128(tO, orr);
+            else tmem_ld_32x32b_x64(tO, orr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.o_free[k]);
+            if (row_valid) {
                 if (!split_mode) {
-                    uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
+                    uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
+                    for (int t = 0; t < D / 8; ++t) {
                         uint4 wv;
                         wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
                         wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
                         wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
                         wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
-                        reinterpret_cast<uint4*>(orow)[t] = wv;
+                        orow[t] = wv;
                     }
                 } else {
-                    float* op = a.o_part + ((long)split * nrows + prow) * D + cb;
+                    float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t)
-                        reinterpret_cast<float4*>(op)[t] = make_float4(
-                            __uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
-                            __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
+                    for (int t = 0; t < D / 4; ++t)
+                        op[t] = make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
+                                            __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
                 }
             }
-            // O_k is in registers and stored: the next item's P V may overwrite it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.o_free[k]);
             tr.mark(kMEpilogueDone);
         } else if (row_valid) {
             if (!split_mode) {
@@ -517,6 +636,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 for (int t = 0; t < D / 4; ++t) reinterpret_cast<float4*>(op)[t] = make_float4(0, 0, 0, 0);
             }
         }
+        // the item slot is read for the last time: hand it back to the scheduler
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.item_empty[slot]);
         }  // items
     }
 

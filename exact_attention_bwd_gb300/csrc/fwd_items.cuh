@@ -32,6 +32,24 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
     FwdItem w;
     int seq, blk;
     w.split = 0;
+    if (p.cu_q && a.tokens) {
+        // token tiles: query tile k of block blk holds packed rows [(2 blk + k) P, + P), whatever
+        // sequences they belong to; key coordinates are packed rows too.  The key-tile ranges
+        // follow from the rows' own bands (fwd_row_band), so they are left empty here.
+        w.g = idx % p.h_kv;
+        blk = a.n_blocks - 1 - idx / p.h_kv;  // later tokens first
+        w.sv = SeqView{0, 0, p.T_q, 0, p.T_k, 0};
+        w.band = Band{0, p.left, p.right, p.T_k};
+        w.u0 = w.u1 = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            w.ti[k].s0 = (2 * blk + k) * p.P;
+            w.ti[k].active = w.ti[k].s0 < p.T_q;
+            w.ti[k].t0 = w.ti[k].t1 = 0;
+        }
+        w.live = blk * 2 * p.P < p.T_q;
+        return w;
+    }
     if (p.cu_q) {
         w.g = idx % p.h_kv;
         const int bs = 2 * p.P;
@@ -75,6 +93,54 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
     if (w.u1 == 0) w.u0 = 0;
     w.live = blk * 2 * p.P < w.sv.nq;
     return w;
+}
+
+// Largest sequence s in [0, nseq) with cu[s] <= row: the sequence that holds packed row
+// `row` (empty sequences at the same offset come before it).
+__device__ __forceinline__ int row_sequence(const int32_t* cu, int nseq, int row) {
+    int lo = 0, hi = nseq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= row)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Allowed keys of row r (TMEM lane) of query tile k of item w, in the key coordinates of
+// the item's key tiles (sequence-local, or packed rows in token mode): [jlo, jhi].  A row
+// that holds no query (padding past P G rows, past the sequence or its used length) gets
+// jlo = kNoRow; a query with no allowed key gets jlo = kNoKeys; both get jhi = -1.
+constexpr int kNoRow = 0x7fffffff;
+constexpr int kNoKeys = 0x7ffffffe;
+__device__ __forceinline__ void fwd_row_band(const FwdArgs& a, const FwdItem& w, int k, int r, int& jlo, int& jhi) {
+    const Problem& p = a.p;
+    jlo = kNoRow;
+    jhi = -1;
+    if (!w.ti[k].active || r >= p.P * p.G) return;
+    const int i = w.ti[k].s0 + r / p.G;
+    int lo, hi;
+    if (p.cu_q && a.tokens) {
+        if (i >= p.T_q) return;
+        const SeqView sv = seq_view(p, row_sequence(p.cu_q, p.B, i));
+        const int il = i - sv.q0;
+        if (il >= sv.nq) return;
+        const Band bd{sv.nk - sv.nq, p.left, p.right, sv.nk};
+        lo = sv.k0 + bd.lo(il);
+        hi = sv.k0 + bd.hi(il);
+    } else {
+        if (i >= w.sv.nq) return;
+        lo = w.band.lo(i);
+        hi = w.band.hi(i);
+    }
+    if (hi < lo) {
+        jlo = kNoKeys;
+        return;
+    }
+    jlo = lo;
+    jhi = hi;
 }
 
 // The persistent loop's items: a plain grid stride (idx = c, c + G, c + 2G, ...), or with

@@ -38,13 +38,19 @@ def from_dev(t) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def dev_inputs(w):
+def dev_inputs(w, share_cu=True):
+    """Device copies of a workload's inputs.  When the query and key offsets are equal,
+    one device array serves as both (unless share_cu is False), which is how a caller
+    signals queries and keys packed alike and what lets the d <= 128 kernels tile the
+    packed token axis; separate arrays with equal contents take the per-sequence tiles."""
     import torch
     t = w.get("dtype", "bf16")
     d = dict(q=to_dev(w["q"], t), k=to_dev(w["k"], t), v=to_dev(w["v"], t), dout=to_dev(w["dout"], t))
     d["sinks"] = None if w["sinks"] is None else torch.from_numpy(w["sinks"]).cuda()
     d["cu_q"] = None if w["cu_q"] is None else torch.from_numpy(w["cu_q"]).cuda()
     d["cu_k"] = None if w["cu_k"] is None else torch.from_numpy(w["cu_k"]).cuda()
+    if share_cu and d["cu_q"] is not None and np.array_equal(w["cu_q"], w["cu_k"]):
+        d["cu_k"] = d["cu_q"]
     return d
 
 
@@ -107,12 +113,12 @@ class Guarded:
         assert np.all(tail == 0xFF), f"{name}: a write landed past the end (first at byte +{np.argmax(tail != 0xFF)})"
 
 
-def run_gpu(w, bwd=True, flags=0):
+def run_gpu(w, bwd=True, flags=0, share_cu=True):
     """fa_fwd (+ fa_bwd) through the binding, every output and workspace guarded; returns
     numpy fp64 results."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
-    d = dev_inputs(w)
+    d = dev_inputs(w, share_cu=share_cu)
     kw = dict(causal=w["causal"], window=w["window"], softmax_scale=w["scale"], sinks=d["sinks"],
               cu_q=d["cu_q"], cu_k=d["cu_k"], flags=flags)
     q, k, v = d["q"], d["k"], d["v"]

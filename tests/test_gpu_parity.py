@@ -27,12 +27,12 @@ def make_case(wid, variant, *, B=1, s_q=128, s_kv=None, h_q=2, h_kv=None, d=64, 
     return inputs.make(w)
 
 
-def compare(w, bwd=True, flags=0, fa_rule=()):
+def compare(w, bwd=True, flags=0, fa_rule=(), share_cu=True):
     """Element-wise parity with the oracle.  Outputs named in `fa_rule` are judged by the
     pages' secondary rule instead: max error at most twice that of the bf16-operand
     emulation (tests/bf16_emulation.py) — for shapes where bf16 rounding of the GEMM
     operands alone exceeds the absolute bound."""
-    got = run_gpu(w, bwd=bwd, flags=flags)
+    got = run_gpu(w, bwd=bwd, flags=flags, share_cu=share_cu)
     q, k, v, do = f64(w, "q"), f64(w, "k"), f64(w, "v"), f64(w, "dout")
     kw = oracle_args(w)
     o, lse, _ = oracle.fwd(q, k, v, **kw)
@@ -99,11 +99,31 @@ def test_group_sizes(h_q, h_kv, d):
     compare(make_case(103, h_q + 10 * h_kv, B=2, s_q=250, h_q=h_q, h_kv=h_kv, d=d, causal=True, sinks=True))
 
 
+@pytest.mark.parametrize("share_cu", [True, False])
 @pytest.mark.parametrize("d", [64, 128])
-def test_packed_batch(d):
-    # the pages' offsets [0, 17, 300, 428] plus empty and one-token sequences
+def test_packed_batch(d, share_cu):
+    """The pages' offsets [0, 17, 300, 428] plus empty and one-token sequences; one offsets
+    array for queries and keys (token tiles) and two equal ones (tiles per sequence)."""
     lengths = [17, 283, 128, 0, 1, 0, 300, 129]
-    compare(make_case(104, d, h_q=4, h_kv=2, d=d, causal=True, lengths=lengths))
+    compare(make_case(104, d, h_q=4, h_kv=2, d=d, causal=True, lengths=lengths), share_cu=share_cu)
+
+
+def _short_lengths(seed, n, long_len):
+    rng = np.random.default_rng(seed)
+    lengths = [int(x) for x in rng.integers(0, 40, size=n)]
+    lengths[n // 3] = long_len  # one long sequence among many short ones and some empty
+    return lengths
+
+
+@pytest.mark.parametrize("d,causal,window,sinks,h_q,h_kv", [
+    (64, True, (-1, -1), False, 4, 2), (128, True, (-1, -1), True, 2, 2), (64, False, (-1, -1), True, 8, 2),
+    (128, False, (30, 10), True, 4, 1), (64, True, (20, 0), False, 16, 2)])
+def test_packed_many_short_sequences(d, causal, window, sinks, h_q, h_kv):
+    """Token tiles: 128-row query tiles that hold the ends and middles of many short
+    sequences (lengths 0 to 39, one of 600), each row masked to its own sequence."""
+    lengths = _short_lengths(d + h_q + int(causal), 60, 600)
+    compare(make_case(113, d + 7 * h_q + int(causal) + 3 * int(sinks), h_q=h_q, h_kv=h_kv, d=d, causal=causal,
+                      window=window, sinks=sinks, lengths=lengths))
 
 
 def test_packed_batch_different_q_k_packing():
