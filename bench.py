@@ -331,6 +331,9 @@ def run_ours(args):
                                                               "sweep_s2048", "decode_d128_sq64")}
     if not args.no_sweep:
         line["d256"] = measure_d256(dev)
+    if "decode" in line:
+        # the decode targets' figures once more, compactly, near the end of the line
+        line["decode_frac_hbm"] = {n: r.get("frac_hbm") for n, r in line["decode"].items()}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = oracle_sample(w)
     if rank == 0:
@@ -467,8 +470,16 @@ def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0, dtype="bf16", ch
     mf, mb = statistics.mean(tf), statistics.mean(tb)
     del q, k, v, do, o, lse, wsf, dq, dk, dv, wsb
     torch.cuda.empty_cache()
+    pk = peaks()
+    # both roofs: the tensor rate and the HBM rate of the algorithmic bytes (for the shapes
+    # near the ridge point, e.g. the grouped-query sliding-window workloads)
+    fgb = metrics.fwd_bytes(wf) / (mf * 1e-3) / 1e9
+    bgb = metrics.bwd_bytes(wf) / (mb * 1e-3) / 1e9
     return {"fwd_ms": round(mf, 4), "bwd_ms": round(mb, 4), "fwd_TFLOPS": round(ff / (mf * 1e-3) / 1e12, 1),
-            "fwd_bwd_TFLOPS": round(3.5 * ff / ((mf + mb) * 1e-3) / 1e12, 1)}
+            "fwd_bwd_TFLOPS": round(3.5 * ff / ((mf + mb) * 1e-3) / 1e12, 1),
+            "fwd_frac_tensor": round(ff / (mf * 1e-3) / 1e12 / pk["bf16"], 4),
+            "fwd_GB_per_s": round(fgb, 1), "fwd_frac_hbm": round(fgb / pk["hbm"], 4),
+            "bwd_GB_per_s": round(bgb, 1), "bwd_frac_hbm": round(bgb / pk["hbm"], 4)}
 
 
 def measure_d256(dev):

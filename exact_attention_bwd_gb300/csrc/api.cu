@@ -303,6 +303,7 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
 struct BwdPlan {
     bool empty = true;
     int n_qtiles = 0, n_kvblocks = 0, n_bands = 1;
+    int tokens = 0;  // packed batch with cu_seqlens_q == cu_seqlens_k: token blocks and tiles
     size_t off_delta = 0, off_lse2 = 0, off_dq = 0, off_sink = 0, off_count = 0, off_trace = 0;
     size_t ws_bytes = kStatusBytes;
 };
@@ -318,7 +319,12 @@ fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     if (p.B == 0 || (rows_total == 0 && keys_total == 0)) return FA_OK;
     pl.empty = false;
     const int kvb = p.d >= 192 ? 64 : kTileRows;  // keys per CTA (d = 192 / 256: 64)
-    if (p.cu_q) {
+    if (p.cu_q && p.cu_q == p.cu_k && p.d <= 128 && !(flags & FA_FLAG_DETERMINISTIC)) {
+        // queries and keys packed alike: key blocks and query tiles run over the packed axis
+        pl.tokens = 1;
+        pl.n_qtiles = (p.T_q + p.P - 1) / p.P;
+        pl.n_kvblocks = (p.T_k + kvb - 1) / kvb;
+    } else if (p.cu_q) {
         pl.n_qtiles = p.T_q / p.P + p.B;
         pl.n_kvblocks = p.T_k / kvb + p.B;
     } else {
@@ -572,6 +578,7 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.n_qtiles = pl.n_qtiles;
     a.n_kvblocks = pl.n_kvblocks;
     a.n_bands = pl.n_bands;
+    a.tokens = pl.tokens;
     a.o = reinterpret_cast<const uint16_t*>(o);
     a.lse = lse;
     a.dout = reinterpret_cast<const uint16_t*>(dout);

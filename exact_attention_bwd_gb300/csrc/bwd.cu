@@ -89,6 +89,38 @@ __device__ __forceinline__ void block_qtiles(const Problem& p, const SeqView& sv
     qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
 }
 
+// Token mode: the packed query rows [qlo, qhi] whose band holds packed key row j (qlo > qhi
+// when none: a key past the batch, past its sequence's used keys, or seen by no query).
+__device__ __forceinline__ void token_key_queries(const Problem& p, int j, int& qlo, int& qhi) {
+    qlo = 1;
+    qhi = 0;
+    if (j >= p.T_k) return;
+    const SeqView sv = seq_view(p, row_sequence(p.cu_k, p.B, j));
+    const int jl = j - sv.k0;
+    if (jl >= sv.nk) return;
+    const int off = sv.nk - sv.nq;
+    const int i_min = p.right >= 0 ? max(0, jl - off - p.right) : 0;
+    const int i_max = p.left >= 0 ? min(sv.nq - 1, jl - off + p.left) : sv.nq - 1;
+    if (i_min > i_max) return;
+    qlo = sv.q0 + i_min;
+    qhi = sv.q0 + i_max;
+}
+
+// Token mode: the query tiles [qt0, qt1) (P packed rows each) that some key of the block
+// [j0, j1] sees.  Within a sequence a key's first and last query rise with the key, and a
+// later sequence's rows follow an earlier one's, so the first key's first query and the last
+// key's last query bound the rest; when either key sees no query, its sequence's first (or
+// last) row stands in.
+__device__ __forceinline__ void token_block_qtiles(const Problem& p, int j0, int j1, int& qt0, int& qt1) {
+    int a_lo, a_hi, b_lo, b_hi;
+    token_key_queries(p, j0, a_lo, a_hi);
+    token_key_queries(p, j1, b_lo, b_hi);
+    const int qstart = a_lo <= a_hi ? a_lo : p.cu_q[row_sequence(p.cu_k, p.B, j0)];
+    const int qend = b_lo <= b_hi ? b_hi : p.cu_q[row_sequence(p.cu_k, p.B, j1) + 1] - 1;
+    qt0 = qend >= qstart ? qstart / p.P : 0;
+    qt1 = qend >= qstart ? qend / p.P + 1 : 0;
+}
+
 // Deterministic dQ order.  Every query tile receives the contributions of the key blocks
 // that see it in descending block order, each block's contribution complete before the
 // next one starts, so the fp32 sums are formed in the same order on every run.  A key
@@ -154,7 +186,7 @@ __device__ __forceinline__ void dq_turn_done(int* cnt) {
     if ((threadIdx.x & 31) == 0) atomicAdd(cnt, 1);
 }
 
-template <int D, bool DET, bool F16>
+template <int D, bool DET, bool F16, bool TOK>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
     bwd_main_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
@@ -178,11 +210,19 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     // tiles under a causal mask (the first ones) start first, while the query tiles, dO
     // tiles and dQ accumulator rows that a band's CTAs share stay in L2.
     int g, seq, blk;
+    // token mode (TOK): key blocks and query tiles over the packed token axis; never with DET
+    constexpr bool tokens = TOK;
+    static_assert(!(DET && TOK), "the fixed dQ order uses blocks per sequence");
     {
         const int idx = blockIdx.x;
         // deterministic order: a sequence's later key blocks first (lower CTA indices)
         constexpr bool rev = DET;
-        if (p.cu_q) {
+        if (tokens) {
+            // token mode: key block blk holds packed key rows [128 blk, 128 blk + 128)
+            g = idx % p.h_kv;
+            blk = idx / p.h_kv;
+            seq = 0;
+        } else if (p.cu_q) {
             g = idx % p.h_kv;
             blk = idx / p.h_kv;
             if (rev) blk = a.n_kvblocks - 1 - blk;
@@ -196,15 +236,18 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             if (rev) blk = a.n_kvblocks - 1 - blk;
         }
     }
-    const SeqView sv = seq_view(p, seq);
+    const SeqView sv = tokens ? SeqView{0, 0, p.T_q, 0, p.T_k, 0} : seq_view(p, seq);
     const int j0 = blk * kRows;
     if (j0 >= sv.nk) return;  // idle packed-batch block
     const int j1 = min(j0 + kRows, sv.nk) - 1;
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
     int qt0, qt1;  // query tiles whose positions have a band reaching [j0, j1]
-    block_qtiles(p, sv, band, blk, qt0, qt1);
+    if (tokens)
+        token_block_qtiles(p, j0, j1, qt0, qt1);
+    else
+        block_qtiles(p, sv, band, blk, qt0, qt1);
     const int nsteps = qt1 - qt0;
-    const int tbase = qtile_base(p, seq);
+    const int tbase = tokens ? 0 : qtile_base(p, seq);
 
     Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
@@ -428,6 +471,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         bool ok = true;
         DqOrder order;
         order.next = blk + 1;
+        // token mode: this key's queries as packed rows (its own sequence's band)
+        int tq_lo = 1, tq_hi = 0;
+        if (tokens) token_key_queries(p, j, tq_lo, tq_hi);
         Tracer tr;
         tr.init(warp == 4 ? a.trace : nullptr, 2);
         tr.item(blockIdx.x);
@@ -441,7 +487,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             const float* dlt = s.stat[st][1] + 64 * cg;
             // edge test: does the band cut this (query tile, key tile) pair?
             const int iq_first = s0, iq_last = min(s0 + p.P, sv.nq) - 1;
-            const bool interior = j0 >= band.lo(iq_last) && j0 + kRows - 1 <= band.hi(iq_first);
+            const bool interior = !tokens && j0 >= band.lo(iq_last) && j0 + kRows - 1 <= band.hi(iq_first);
             // ---- P^T ----
             {
                 // the stage's LSE / D rows landed with Q_i (already complete by the time S^T is)
@@ -468,10 +514,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     // packed columns (column = G (i - s0) + head) it is the column range
                     // [G (i_min - s0), G (i_max + 1 - s0)), taken relative to this group's
                     // first column
-                    const int i_min = p.right >= 0 ? j - band.off - p.right : 0;
-                    const int i_max = j >= sv.nk ? i_min - 1 : (p.left >= 0 ? j - band.off + p.left : sv.nq - 1);
-                    const int c_lo = (i_min - s0) * p.G - 64 * cg;
-                    const int c_hi = (i_max + 1 - s0) * p.G - 64 * cg;
+                    int c_lo, c_hi;
+                    if constexpr (TOK) {
+                        // the key's queries as packed rows (none: an empty column range)
+                        c_lo = tq_lo > tq_hi ? 0 : (tq_lo - s0) * p.G - 64 * cg;
+                        c_hi = tq_lo > tq_hi ? 0 : (tq_hi + 1 - s0) * p.G - 64 * cg;
+                    } else {
+                        const int i_min = p.right >= 0 ? j - band.off - p.right : 0;
+                        const int i_max = j >= sv.nk ? i_min - 1 : (p.left >= 0 ? j - band.off + p.left : sv.nq - 1);
+                        c_lo = (i_min - s0) * p.G - 64 * cg;
+                        c_hi = (i_max + 1 - s0) * p.G - 64 * cg;
+                    }
 #pragma unroll
                     for (int cc = 0; cc < 64; ++cc)
                         if (cc < c_lo || cc >= c_hi) pf[cc] = 0.f;
@@ -557,7 +610,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             tc_fence_after();
         }
         tr.mark(kMEpilogue);
-        const bool row_ok = j <= j1;
+        // rows past the block's keys, or (token mode) past the key's sequence's used keys,
+        // are not written
+        bool row_ok = j <= j1;
+        if (tokens && row_ok && p.seqused_k) {
+            const SeqView ks = seq_view(p, row_sequence(p.cu_k, p.B, j));
+            row_ok = j - ks.k0 < ks.nk;
+        }
         const long krow = key_row(p, sv, j);
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
@@ -974,7 +1033,14 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
 // preprocess: one CTA (128 threads) per (tiled query tile, key/value head)
 // ------------------------------------------------------------------------------------------
 // Decodes a tiled query-tile index into (sequence, tile within it); false for an idle tile.
-__device__ __forceinline__ bool decode_qtile(const Problem& p, int idx, int& seq, int& t) {
+// Token mode: the tile is the packed rows [idx P, idx P + P) (sequence 0's view spans them all).
+__device__ __forceinline__ bool decode_qtile(const BwdArgs& a, int idx, int& seq, int& t) {
+    const Problem& p = a.p;
+    if (p.cu_q && a.tokens) {
+        seq = 0;
+        t = idx;
+        return idx * p.P < p.T_q;
+    }
     if (p.cu_q) {
         seq = owner_sequence(p.cu_q, p.B, idx, p.P);
         t = idx - (p.cu_q[seq] / p.P + seq);
@@ -983,6 +1049,23 @@ __device__ __forceinline__ bool decode_qtile(const Problem& p, int idx, int& seq
     const int per = cdiv(p.s_q, p.P);
     seq = idx / per;
     t = idx % per;
+    return true;
+}
+
+// The view the pre- and postprocess index a query tile's rows with, and whether local row
+// i of it holds a query: in token mode the view spans the packed rows, and a row past its
+// own sequence's used queries (seqused_q) holds none.
+__device__ __forceinline__ SeqView qtile_view(const BwdArgs& a, int seq) {
+    const Problem& p = a.p;
+    return (p.cu_q && a.tokens) ? SeqView{0, 0, p.T_q, 0, p.T_k, 0} : seq_view(p, seq);
+}
+__device__ __forceinline__ bool query_row_used(const BwdArgs& a, const SeqView& sv, int i) {
+    const Problem& p = a.p;
+    if (i >= sv.nq) return false;
+    if (p.cu_q && a.tokens && p.seqused_q) {
+        const SeqView own = seq_view(p, row_sequence(p.cu_q, p.B, i));
+        return i - own.q0 < own.nq;
+    }
     return true;
 }
 
@@ -995,7 +1078,7 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
     // touch nothing (the later kernels of the call skip as well)
     if (*reinterpret_cast<volatile const int*>(a.status) != 0) return;
     int seq, t;
-    const bool live = decode_qtile(p, idx, seq, t);
+    const bool live = decode_qtile(a, idx, seq, t);
     const long trow = ((long)g * a.n_qtiles + idx) * 128;
     if (a.dq_count && threadIdx.x == 0) a.dq_count[(long)g * a.n_qtiles + idx] = 0;
     if (!live) {
@@ -1004,7 +1087,7 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
         if (a.sink_t) a.sink_t[trow + threadIdx.x] = 0.f;
         return;
     }
-    const SeqView sv = seq_view(p, seq);
+    const SeqView sv = qtile_view(a, seq);
     // a warp takes its 32 rows RPI at a time: LPR lanes per row (a power of two), VPL
     // 16-byte units (8 elements) of O and dO each per lane, so every load instruction moves
     // whole 128-byte lines
@@ -1016,7 +1099,7 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(const BwdArgs a) {
         const int r = warp * 32 + rr + sub;
         const int i = t * p.P + r / p.G;
         const int h = g * p.G + r % p.G;
-        const bool valid = r < p.P * p.G && i < sv.nq;
+        const bool valid = r < p.P * p.G && query_row_used(a, sv, i);
         float dsum = 0.f;
         long tok = 0;
         if (valid) {
@@ -1088,15 +1171,15 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
     const int idx = blockIdx.x, g = blockIdx.y;
     if (*reinterpret_cast<volatile const int*>(a.status) != 0) return;  // the call failed: dQ not written
     int seq, t;
-    if (!decode_qtile(p, idx, seq, t)) return;
-    const SeqView sv = seq_view(p, seq);
+    if (!decode_qtile(a, idx, seq, t)) return;
+    const SeqView sv = qtile_view(a, seq);
     const long trow = ((long)g * a.n_qtiles + idx) * 128;
     constexpr int V = 8;  // columns per thread step
     for (int x = threadIdx.x; x < 128 * D / V; x += 128) {
         const int r = x / (D / V), cb = (x % (D / V)) * V;
         const int i = t * p.P + r / p.G;
         const int h = g * p.G + r % p.G;
-        if (r >= p.P * p.G || i >= sv.nq) continue;
+        if (r >= p.P * p.G || !query_row_used(a, sv, i)) continue;
         const float4 u0 = *reinterpret_cast<const float4*>(a.dq_acc + (trow + r) * D + cb);
         const float4 u1 = *reinterpret_cast<const float4*>(a.dq_acc + (trow + r) * D + cb + 4);
         const float sc = p.scale;
@@ -1111,11 +1194,11 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(const BwdArgs a) {
 
 }  // namespace
 
-template <int D, bool DET>
+template <int D, bool DET, bool TOK>
 static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem<D>);
-    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd_main_kernel<D, DET, true> : bwd_main_kernel<D, DET, false>;
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd_main_kernel<D, DET, true, TOK> : bwd_main_kernel<D, DET, false, TOK>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
@@ -1144,11 +1227,13 @@ cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUten
         case 256:
             return a.dq_count ? cudaErrorInvalidValue : launch_main256<256>(a, tq, tk, tv, tdo, st);
         case 64:
-            return a.dq_count ? launch_main_d<64, true>(a, tq, tk, tv, tdo, st)
-                              : launch_main_d<64, false>(a, tq, tk, tv, tdo, st);
+            if (a.dq_count) return launch_main_d<64, true, false>(a, tq, tk, tv, tdo, st);
+            return a.tokens ? launch_main_d<64, false, true>(a, tq, tk, tv, tdo, st)
+                            : launch_main_d<64, false, false>(a, tq, tk, tv, tdo, st);
         case 128:
-            return a.dq_count ? launch_main_d<128, true>(a, tq, tk, tv, tdo, st)
-                              : launch_main_d<128, false>(a, tq, tk, tv, tdo, st);
+            if (a.dq_count) return launch_main_d<128, true, false>(a, tq, tk, tv, tdo, st);
+            return a.tokens ? launch_main_d<128, false, true>(a, tq, tk, tv, tdo, st)
+                            : launch_main_d<128, false, false>(a, tq, tk, tv, tdo, st);
         default: return cudaErrorInvalidValue;
     }
 }

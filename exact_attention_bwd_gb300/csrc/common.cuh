@@ -45,6 +45,20 @@ __device__ __forceinline__ int owner_sequence(const int32_t* cu, int nseq, int g
     return lo;
 }
 
+// Largest sequence s in [0, nseq) with cu[s] <= row: the sequence that holds packed row
+// `row` (empty sequences at the same offset come before it).
+__device__ __forceinline__ int row_sequence(const int32_t* cu, int nseq, int row) {
+    int lo = 0, hi = nseq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= row)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 // Banded work order over hb (batch, key/value head) units of per_unit items each: the
 // units form n_bands bands of near-equal size (the first hb % n_bands bands one unit
 // larger), taken one after the other; inside a band the unit varies fastest, so the items

@@ -95,20 +95,6 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
     return w;
 }
 
-// Largest sequence s in [0, nseq) with cu[s] <= row: the sequence that holds packed row
-// `row` (empty sequences at the same offset come before it).
-__device__ __forceinline__ int row_sequence(const int32_t* cu, int nseq, int row) {
-    int lo = 0, hi = nseq - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cu[mid] <= row)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
 // Allowed keys of row r (TMEM lane) of query tile k of item w, in the key coordinates of
 // the item's key tiles (sequence-local, or packed rows in token mode): [jlo, jhi].  A row
 // that holds no query (padding past P G rows, past the sequence or its used length) gets

@@ -92,6 +92,8 @@ struct BwdArgs {
     int n_bands;           // dense grid order: the (batch, kv head) units form this many bands of
                            // near-equal size, key block slowest within a band, so a band's
                            // query-side data stays in L2
+    int tokens;            // packed batch with queries and keys packed alike: key blocks and query
+                           // tiles run over the packed token axis (d <= 128 kernel)
     // 16-bit tensors hold bf16 or fp16 (Problem::dtype) like the inputs
     const uint16_t* o;
     const float* lse;

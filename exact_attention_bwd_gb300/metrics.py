@@ -44,3 +44,25 @@ def fwd_flops(w: dict) -> float:
 
 def bwd_flops(w: dict) -> float:
     return 2.5 * fwd_flops(w)
+
+
+def _tokens(w: dict):
+    """(query rows, key rows) over the batch: B s_q and B s_kv, or the packed totals."""
+    if w.get("varlen") or w.get("cu_q") is not None:
+        return int(w["cu_q"][-1]) if w.get("cu_q") is not None else w["T"], \
+            int(w["cu_k"][-1]) if w.get("cu_k") is not None else w["T"]
+    return w["B"] * w["s_q"], w["B"] * w["s_kv"]
+
+
+def fwd_bytes(w: dict, elem: int = 2) -> float:
+    """Algorithmic HBM bytes of the forward: Q, K, V read once, O written (16-bit elements)
+    and the fp32 LSE written."""
+    tq, tk = _tokens(w)
+    return elem * (2 * tq * w["h_q"] * w["d"] + 2 * tk * w["h_kv"] * w["d"]) + 4 * tq * w["h_q"]
+
+
+def bwd_bytes(w: dict, elem: int = 2) -> float:
+    """Algorithmic HBM bytes of the backward: Q, O, dO read and dQ written; K, V read and
+    dK, dV written (16-bit elements); the fp32 LSE read."""
+    tq, tk = _tokens(w)
+    return elem * (4 * tq * w["h_q"] * w["d"] + 4 * tk * w["h_kv"] * w["d"]) + 4 * tq * w["h_q"]

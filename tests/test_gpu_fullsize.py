@@ -82,7 +82,7 @@ def run_full(w, bwd=True):
     return res
 
 
-SWEEP = [(s, c) for s in (512, 2048, 8192, 16384) for c in (True, False)]
+SWEEP = [(s, c) for s in (512, 1024, 2048, 4096, 8192, 16384) for c in (True, False)]
 
 
 @pytest.mark.parametrize("s,causal", SWEEP, ids=[f"s{s}-{'causal' if c else 'full'}" for s, c in SWEEP])

@@ -283,3 +283,47 @@ def test_seqused_q_decode():
         q0, q1 = ref["cu_q"][b], ref["cu_q"][b + 1]
         check(f"O[{b}]", o[b, :used_q[b]], ref["o"][q0:q1])
         check_lse(f"LSE[{b}]", lse[b, :, :used_q[b]], ref["lse"][:, q0:q1])
+
+
+@pytest.mark.parametrize("d,causal,window,sinks", [(64, True, (-1, -1), True), (128, False, (40, 10), False)])
+def test_seqused_packed_token_tiles(d, causal, window, sinks):
+    """A packed batch whose queries and keys share one offsets array (token tiles) with
+    partly used slots: each slot uses its first seqused_q[b] queries and seqused_k[b] keys,
+    forward and backward, against the oracle on the packed batch of the used rows."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    slots = [40, 3, 0, 200, 17, 90, 1, 130]
+    rng = np.random.default_rng(inputs.seed_of(WID, 70 + d, USED))
+    used_q = np.array([rng.integers(0, n + 1) for n in slots], np.int32)
+    used_k = np.array([rng.integers(0, n + 1) for n in slots], np.int32)
+    used_q[3], used_k[3] = 200, 120
+    w = inputs.make(dict(wid=WID, variant=80 + d, B=len(slots), s_q=0, s_kv=0, h_q=4, h_kv=2, d=d, causal=causal,
+                         window=window, sinks=sinks, varlen=True, lengths=slots))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    cu = dev(w["cu_q"])
+    tq, tk, tv, tdo = (to_dev(w[t]) for t in ("q", "k", "v", "dout"))
+    kw = dict(causal=causal, window=window, softmax_scale=w["scale"], sinks=None if w["sinks"] is None else dev(w["sinks"]),
+              cu_q=cu, cu_k=cu, seqused_q=dev(used_q), seqused_k=dev(used_k))
+    o, lse, ws = fa.forward(tq, tk, tv, **kw)
+    dq, dk, dv, ds, ws2 = fa.backward(tq, tk, tv, o, lse, tdo, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK and fa.device_status(ws2) == fa.FA_OK
+    # the oracle's problem: the used rows of every slot, packed
+    cu_h = w["cu_q"]
+    cat = lambda x, n: np.concatenate([x[cu_h[b]:cu_h[b] + n[b]] for b in range(len(slots))])  # noqa: E731
+    q, k, v, do = (inputs.bf16_to_f64(w[t]) for t in ("q", "k", "v", "dout"))
+    rcq, rck = inputs.cu_seqlens(used_q), inputs.cu_seqlens(used_k)
+    okw = dict(scale=w["scale"], causal=causal, window=window, cu_q=rcq, cu_k=rck,
+               sinks=None if w["sinks"] is None else w["sinks"].astype(np.float64))
+    args = (cat(q, used_q), cat(k, used_k), cat(v, used_k))
+    ro, rl, _ = oracle.fwd(*args, **okw)
+    rdq, rdk, rdv, rds = oracle.bwd(*args, cat(do, used_q), **okw)
+    o, lse, dq, dk, dv = from_dev(o), lse.cpu().numpy().astype(np.float64), from_dev(dq), from_dev(dk), from_dev(dv)
+    check("O", cat(o, used_q), ro)
+    check_lse("LSE", np.concatenate([lse[:, cu_h[b]:cu_h[b] + used_q[b]] for b in range(len(slots))], axis=1), rl)
+    check("dQ", cat(dq, used_q), rdq)
+    check("dK", cat(dk, used_k), rdk)
+    check("dV", cat(dv, used_k), rdv)
+    if sinks:
+        err = float(np.abs(ds.cpu().numpy() - rds).max())
+        assert err <= 2e-2 * max(1.0, float(np.abs(rds).max()))
