@@ -23,10 +23,9 @@
 //   warp 2      owns the TMEM allocation
 //   warps 4-11  two groups of 128: thread = key row; group c takes query columns
 //               [64c, 64c+64): P^T = exp2(S^T * c - LSE2), dS^T = P^T (dP^T - D) into
-//               shared memory; at d = 64 also the dQ tile (thread = query row, columns
-//               split in halves between the groups), reduced into the workspace
-//   warps 12-15 d = 128: drain dQ^T_i (thread = column of d) and reduce it into the
-//               workspace
+//               shared memory
+//   warps 12-15 drain dQ_i and reduce it into the workspace: d = 128 as dQ^T_i (thread =
+//               column of d), d = 64 as dQ_i (thread = query row)
 // d = 256 has its own kernel (bwd256_kernel below).
 #include "common.cuh"
 #include "trace.cuh"
@@ -265,7 +264,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         mbar_init(&s.ds_full, 256);
         mbar_init(&s.ds_free, 1);
         mbar_init(&s.dq_full, 1);
-        mbar_init(&s.dq_free, C::DQ_T ? 128 : 256);
+        mbar_init(&s.dq_free, 128);  // the dQ group's threads
         mbar_init(&s.dkv_full, 1);
         fence_mbar_init();
     }
@@ -291,7 +290,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     // registers: 512 x 128 at launch, redistributed per warp group (the change is made at
     // the top of each group's branch): the two compute groups 160; d = 128: producer/MMA 48
     // and the dQ group, which holds a whole 128-row dQ^T column in registers, 144
-    // (128*48 + 256*160 + 128*144 = 65536); d = 64 (no dQ group work): 64 and 128.  Splits
+    // (128*48 + 256*160 + 128*144 = 65536); d = 64 (a 64-column dQ row per thread): 64 and 128.  Splits
     // that leave a group short make it spill, which costs more than the registers save.
     if (warp >= 12) {
         if constexpr (D == 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 144;\n" ::: "memory");
@@ -331,6 +330,36 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                 for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
                 if constexpr (DET) dq_turn_done(cnt);
                 tr.mark(kMDqReduced);
+            }
+        } else {
+            // d = 64: dQ_i with the query rows on the lanes (64 columns of d per row), drained
+            // here too, so that the compute groups go on to the next step's P^T meanwhile
+            const int qr = ((warp & 3) << 5) | lane;  // TMEM lane = query row of the tile
+            const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+            DqOrder order;
+            order.next = blk + 1;
+            for (int it = 0; it < nsteps; ++it) {
+                const int t = qt0 + it;
+                const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
+                int need = 0;
+                if constexpr (DET) need = 4 * dq_predecessors(p, sv, band, order, t);
+                {
+                    const bool w = mbar_wait(&s.dq_full, it & 1, ab);
+                    if (!__all_sync(0xffffffffu, w)) break;
+                }
+                tc_fence_after();
+                uint32_t qv[D];
+                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ, qv);
+                tc_fence_before();
+                mbar_arrive(&s.dq_free);
+                int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
+                if (DET && !dq_turn_wait(cnt, need, ab)) break;
+                float4* acc = reinterpret_cast<float4*>(a.dq_acc + (trow + qr) * D);
+#pragma unroll
+                for (int t4 = 0; t4 < D / 4; ++t4)
+                    atomicAdd(acc + t4, make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
+                                                    __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
+                if constexpr (DET) dq_turn_done(cnt);
             }
         }
     } else if (warp < 4) {
@@ -577,31 +606,6 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             tc_fence_before();
             mbar_arrive(&s.ds_full);
             tr.mark(kMStepDone);
-            // ---- dQ_i (d = 64 only; for d = 128 the dQ warp group drains it) ----
-            if constexpr (!C::DQ_T) {
-                {
-                    const bool w = mbar_wait(&s.dq_full, par, ab);
-                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                }
-                tc_fence_after();
-                const int qr = jr;  // TMEM lane = query row of the tile
-                uint32_t qv[D / 2];
-                tmem_ld_32x32b_x32(tmem + lane_base + C::C_DQ + (D / 2) * cg, qv);
-                tc_fence_before();
-                mbar_arrive(&s.dq_free);
-                int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
-                if (DET && !dq_turn_wait(cnt, 8 * dq_predecessors(p, sv, band, order, t), ab)) {
-                    ok = false;
-                    break;
-                }
-                float* acc = a.dq_acc + (trow + qr) * D + (D / 2) * cg;
-#pragma unroll
-                for (int t4 = 0; t4 < D / 8; ++t4)
-                    atomicAdd(reinterpret_cast<float4*>(acc) + t4,
-                              make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
-                                          __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
-                if constexpr (DET) dq_turn_done(cnt);
-            }
         }
         // ---- epilogue: dK, dV for this key tile ----
         if (nsteps > 0 && ok) {
