@@ -38,7 +38,12 @@
  * attention never crosses sequences, zero-length sequences are legal, and the
  * LSE is laid out [h_q, T_q].  The offsets are read on the device and are not
  * checked unless FA_FLAG_VALIDATE_CU is set (tokens they do not cover get
- * unspecified outputs, as on the pages).
+ * unspecified outputs, as on the pages).  Passing the same array as cu_seqlens_q and
+ * cu_seqlens_k (queries and keys packed alike, as in self-attention over a packed batch)
+ * lets the d <= 128 kernels tile the packed token axis itself: a 128-row tile then holds
+ * several short sequences, each row masked to its own sequence, so a batch of short
+ * sequences costs about its tokens rather than a tile per sequence.  Two arrays with equal
+ * contents give the same results, with tiles per sequence.
  *
  * Conventions common to every call:
  *  - Layouts: dense tensors are contiguous [B, S, H, D] (bf16 or fp16); packed ones [T, H, D].
@@ -59,8 +64,9 @@
  *    (FA_FLAG_VALIDATE_CU) or a timeout leaves the outputs of the rest of the call
  *    unwritten.
  *  - Supported: bf16 and fp16 (and e4m3 for the forward at d = 128, see below); head dim d in
- *    {64, 128, 256} for the forward and the backward (FA_FLAG_DETERMINISTIC: d <= 128);
- *    h_q / h_kv <= 128.
+ *    {64, 128, 192, 256} for the forward and the backward (FA_FLAG_DETERMINISTIC: d <= 128);
+ *    h_q / h_kv <= 128.  d = 192 is one of the head sizes the pages pad to (dew-flash-attn
+ *    PyPI page, the FA3 head-dim padding to 64 / 128 / 192 / 256).
  *    Anything else returns FA_ERR_UNSUPPORTED.
  *  - Zero-initialise fa_params (memset or `= {0}`): every optional field then means
  *    "not used".
