@@ -579,6 +579,8 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.n_kvblocks = pl.n_kvblocks;
     a.n_bands = pl.n_bands;
     a.tokens = pl.tokens;
+    a.n_units = (int)((long)pl.n_kvblocks * p.h_kv * (p.cu_q ? 1 : p.B));
+    a.n_ctas = a.n_units < sm_count() ? a.n_units : sm_count();
     a.o = reinterpret_cast<const uint16_t*>(o);
     a.lse = lse;
     a.dout = reinterpret_cast<const uint16_t*>(dout);

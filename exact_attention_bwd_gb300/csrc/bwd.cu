@@ -62,7 +62,7 @@ struct __align__(1024) BwdSmem {
     float stat[2][2][128];       // per Q stage: LSE * log2(e) and D of the tile's 128 rows
     uint64_t kv_full;
     uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
-    uint64_t s_full, dp_full, p_full, ds_full, ds_free, dq_full, dq_free, dkv_full;
+    uint64_t s_full, dp_full, p_full, ds_full, ds_free, dq_full, dq_free, dkv_full, dkv_free, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -185,6 +185,58 @@ __device__ __forceinline__ void dq_turn_done(int* cnt) {
     if ((threadIdx.x & 31) == 0) atomicAdd(cnt, 1);
 }
 
+// One key block of the d <= 128 backward: its (key/value head, sequence, block), the
+// sequence view and band, its keys [j0, j1] and the query tiles [qt0, qt0 + nsteps) that
+// see it.  Work unit idx is numbered as the grid was before the kernel became persistent:
+// dense units in L2-sized bands (see band_order), packed blocks over cu_k, token blocks over
+// the packed key axis; with the fixed dQ order a sequence's later blocks come first.
+struct BwdBlock {
+    int g, blk, seq, qt0, nsteps, tbase, j0, j1;
+    SeqView sv;
+    Band band;
+    bool live;  // false: an idle block of a packed batch (nothing to compute or write)
+};
+
+template <bool DET, bool TOK>
+__device__ __forceinline__ BwdBlock bwd_block(const BwdArgs& a, int idx) {
+    const Problem& p = a.p;
+    BwdBlock b;
+    if (TOK) {
+        // token mode: key block blk holds packed key rows [128 blk, 128 blk + 128)
+        b.g = idx % p.h_kv;
+        b.blk = idx / p.h_kv;
+        b.seq = 0;
+    } else if (p.cu_q) {
+        b.g = idx % p.h_kv;
+        int blk = idx / p.h_kv;
+        if (DET) blk = a.n_kvblocks - 1 - blk;
+        b.seq = owner_sequence(p.cu_k, p.B, blk, kRows);
+        b.blk = blk - (p.cu_k[b.seq] / kRows + b.seq);
+    } else {
+        int unit, blk;
+        band_order(idx, p.h_kv * p.B, a.n_bands, a.n_kvblocks, unit, blk);
+        b.g = unit % p.h_kv;
+        b.seq = unit / p.h_kv;
+        b.blk = DET ? a.n_kvblocks - 1 - blk : blk;
+    }
+    b.sv = TOK ? SeqView{0, 0, p.T_q, 0, p.T_k, 0} : seq_view(p, b.seq);
+    b.j0 = b.blk * kRows;
+    b.live = b.j0 < b.sv.nk;
+    b.j1 = min(b.j0 + kRows, b.sv.nk) - 1;
+    b.band = Band{b.sv.nk - b.sv.nq, p.left, p.right, b.sv.nk};
+    int qt1 = 0;
+    b.qt0 = 0;
+    if (b.live) {
+        if (TOK)
+            token_block_qtiles(p, b.j0, b.j1, b.qt0, qt1);
+        else
+            block_qtiles(p, b.sv, b.band, b.blk, b.qt0, qt1);
+    }
+    b.nsteps = qt1 - b.qt0;
+    b.tbase = TOK ? 0 : qtile_base(p, b.seq);
+    return b;
+}
+
 template <int D, bool DET, bool F16, bool TOK>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
     bwd_main_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -203,50 +255,18 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     // an earlier kernel or CTA of the call failed (a device check of the offsets, a
     // timeout): do not start, and read nothing the offsets point at
     if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
-    // 1-D grid.  Dense: the (batch, key/value head) units are split into n_bands bands of
-    // near-equal size (the first hb % n_bands bands one unit larger); inside a band the unit
-    // varies fastest and the key block slowest, so the key blocks that see the most query
-    // tiles under a causal mask (the first ones) start first, while the query tiles, dO
-    // tiles and dQ accumulator rows that a band's CTAs share stay in L2.
-    int g, seq, blk;
     // token mode (TOK): key blocks and query tiles over the packed token axis; never with DET
     constexpr bool tokens = TOK;
     static_assert(!(DET && TOK), "the fixed dQ order uses blocks per sequence");
-    {
-        const int idx = blockIdx.x;
-        // deterministic order: a sequence's later key blocks first (lower CTA indices)
-        constexpr bool rev = DET;
-        if (tokens) {
-            // token mode: key block blk holds packed key rows [128 blk, 128 blk + 128)
-            g = idx % p.h_kv;
-            blk = idx / p.h_kv;
-            seq = 0;
-        } else if (p.cu_q) {
-            g = idx % p.h_kv;
-            blk = idx / p.h_kv;
-            if (rev) blk = a.n_kvblocks - 1 - blk;
-            seq = owner_sequence(p.cu_k, p.B, blk, kRows);
-            blk -= p.cu_k[seq] / kRows + seq;
-        } else {
-            int unit;
-            band_order(idx, p.h_kv * p.B, a.n_bands, a.n_kvblocks, unit, blk);
-            g = unit % p.h_kv;
-            seq = unit / p.h_kv;
-            if (rev) blk = a.n_kvblocks - 1 - blk;
-        }
-    }
-    const SeqView sv = tokens ? SeqView{0, 0, p.T_q, 0, p.T_k, 0} : seq_view(p, seq);
-    const int j0 = blk * kRows;
-    if (j0 >= sv.nk) return;  // idle packed-batch block
-    const int j1 = min(j0 + kRows, sv.nk) - 1;
-    const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
-    int qt0, qt1;  // query tiles whose positions have a band reaching [j0, j1]
-    if (tokens)
-        token_block_qtiles(p, j0, j1, qt0, qt1);
-    else
-        block_qtiles(p, sv, band, blk, qt0, qt1);
-    const int nsteps = qt1 - qt0;
-    const int tbase = tokens ? 0 : qtile_base(p, seq);
+    // Persistent: the CTA walks work units blockIdx.x, + gridDim.x, ... (heaviest first, in
+    // L2-sized bands for dense batches).  With the fixed dQ order the launch has one CTA per
+    // unit, so a CTA waits only on CTAs dispatched before it.  Every role keeps a running
+    // count of the steps (query tiles) and blocks it has been through, so that the barrier
+    // phases carry on from block to block; two barriers hand a block's resources to the next:
+    // dkv_full (the block's last MMAs, which read K and V and finish dK and dV, have
+    // completed: the next K/V may load) and dkv_free (the compute groups have read dK and
+    // dV out of tensor memory: the next block's first dV / dK may overwrite them).
+    const int n_units = a.n_units;
 
     Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
@@ -266,6 +286,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         mbar_init(&s.dq_full, 1);
         mbar_init(&s.dq_free, 128);  // the dQ group's threads
         mbar_init(&s.dkv_full, 1);
+        mbar_init(&s.dkv_free, 256);  // the compute groups' threads
+        mbar_init(&s.drain, 1);
         fence_mbar_init();
     }
     if (p.P * p.G < 128) {
@@ -290,129 +312,135 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     // registers: 512 x 128 at launch, redistributed per warp group (the change is made at
     // the top of each group's branch): the two compute groups 160; d = 128: producer/MMA 48
     // and the dQ group, which holds a whole 128-row dQ^T column in registers, 144
-    // (128*48 + 256*160 + 128*144 = 65536); d = 64 (a 64-column dQ row per thread): 64 and 128.  Splits
-    // that leave a group short make it spill, which costs more than the registers save.
+    // (128*48 + 256*160 + 128*144 = 65536); d = 64 (a 64-column dQ row per thread): 64 and
+    // 128.  Splits that leave a group short make it spill, which costs more than the
+    // registers save.
     if (warp >= 12) {
         if constexpr (D == 128) asm volatile("setmaxnreg.inc.sync.aligned.u32 144;\n" ::: "memory");
         else asm volatile("setmaxnreg.dec.sync.aligned.u32 128;\n" ::: "memory");
-        // ================= dQ group: drains dQ^T_i and reduces it into the workspace =================
-        if constexpr (C::DQ_T) {
-            const int dcol = ((warp & 3) << 5) | lane;  // TMEM lane = column d of dQ
-            const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+        // ================= dQ group: drains dQ_i and reduces it into the workspace =================
+        // d = 128: dQ^T_i (TMEM lane = column of d); d = 64: dQ_i (TMEM lane = query row of the
+        // tile, 64 columns of d per row), drained here so the compute groups go on meanwhile
+        const int tl = ((warp & 3) << 5) | lane;  // this thread's TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+        Tracer tr;
+        tr.init(warp == 12 ? a.trace : nullptr, 3);
+        int gs = 0;  // steps of earlier blocks
+        bool ok = true;
+        for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+            const BwdBlock bk = bwd_block<DET, TOK>(a, idx);
+            if (bk.nsteps <= 0) continue;
+            tr.item(idx);
             DqOrder order;
-            order.next = blk + 1;
-            Tracer tr;
-            tr.init(warp == 12 ? a.trace : nullptr, 3);
-            tr.item(blockIdx.x);
-            for (int it = 0; it < nsteps; ++it) {
-                const int t = qt0 + it;
-                const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
+            order.next = bk.blk + 1;
+            for (int it = 0; it < bk.nsteps; ++it) {
+                const int i = gs + it;
+                const int t = bk.qt0 + it;
+                const long trow = ((long)bk.g * a.n_qtiles + bk.tbase + t) * 128;
                 int need = 0;
-                if constexpr (DET) need = 4 * dq_predecessors(p, sv, band, order, t);
+                if constexpr (DET) need = 4 * dq_predecessors(p, bk.sv, bk.band, order, t);
                 {
-                    const bool w = twait(tr, kBDqFull, &s.dq_full, it & 1, ab);
-                    if (!__all_sync(0xffffffffu, w)) break;
+                    const bool w = twait(tr, kBDqFull, &s.dq_full, i & 1, ab);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 }
                 tc_fence_after();
-                uint32_t qa[64], qb[64];
-                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ, qa);
-                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ + 64, qb);
-                // the columns are free as soon as they are in registers
-                tc_fence_before();
-                mbar_arrive(&s.dq_free);
-                int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
-                if (DET && !dq_turn_wait(cnt, need, ab)) break;
-                // for each query row the 32 lanes of a warp add to 32 consecutive floats
-                float* acc = a.dq_acc + trow * D + dcol;
+                int* cnt = DET ? a.dq_count + (long)bk.g * a.n_qtiles + bk.tbase + t : nullptr;
+                if constexpr (C::DQ_T) {
+                    uint32_t qa[64], qb[64];
+                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ, qa);
+                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ + 64, qb);
+                    // the columns are free as soon as they are in registers
+                    tc_fence_before();
+                    mbar_arrive(&s.dq_free);
+                    if (DET && !dq_turn_wait(cnt, need, ab)) { ok = false; break; }
+                    // for each query row the 32 lanes of a warp add to 32 consecutive floats
+                    float* acc = a.dq_acc + trow * D + tl;
 #pragma unroll
-                for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qa[r]));
+                    for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qa[r]));
 #pragma unroll
-                for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
+                    for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
+                } else {
+                    uint32_t qv[D];
+                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ, qv);
+                    tc_fence_before();
+                    mbar_arrive(&s.dq_free);
+                    if (DET && !dq_turn_wait(cnt, need, ab)) { ok = false; break; }
+                    float4* acc = reinterpret_cast<float4*>(a.dq_acc + (trow + tl) * D);
+#pragma unroll
+                    for (int t4 = 0; t4 < D / 4; ++t4)
+                        atomicAdd(acc + t4, make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
+                                                        __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
+                }
                 if constexpr (DET) dq_turn_done(cnt);
                 tr.mark(kMDqReduced);
             }
-        } else {
-            // d = 64: dQ_i with the query rows on the lanes (64 columns of d per row), drained
-            // here too, so that the compute groups go on to the next step's P^T meanwhile
-            const int qr = ((warp & 3) << 5) | lane;  // TMEM lane = query row of the tile
-            const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-            DqOrder order;
-            order.next = blk + 1;
-            for (int it = 0; it < nsteps; ++it) {
-                const int t = qt0 + it;
-                const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;
-                int need = 0;
-                if constexpr (DET) need = 4 * dq_predecessors(p, sv, band, order, t);
-                {
-                    const bool w = mbar_wait(&s.dq_full, it & 1, ab);
-                    if (!__all_sync(0xffffffffu, w)) break;
-                }
-                tc_fence_after();
-                uint32_t qv[D];
-                tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ, qv);
-                tc_fence_before();
-                mbar_arrive(&s.dq_free);
-                int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
-                if (DET && !dq_turn_wait(cnt, need, ab)) break;
-                float4* acc = reinterpret_cast<float4*>(a.dq_acc + (trow + qr) * D);
-#pragma unroll
-                for (int t4 = 0; t4 < D / 4; ++t4)
-                    atomicAdd(acc + t4, make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
-                                                    __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
-                if constexpr (DET) dq_turn_done(cnt);
-            }
+            gs += bk.nsteps;
         }
     } else if (warp < 4) {
     if constexpr (D == 128) asm volatile("setmaxnreg.dec.sync.aligned.u32 48;\n" ::: "memory");
     else asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
-        if (lane == 0 && nsteps > 0) {
+        if (lane == 0) {
             Tracer tr;
             tr.init(a.trace, 0);
-            tr.item(blockIdx.x);
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
             tma_prefetch_desc(&tmdo);
-            mbar_expect_tx(&s.kv_full, 2 * C::TILE);
-            for (int c = 0; c < C::KCH; ++c) {
-                tma_load_4d(s.k + c * C::CHUNK, &tmk, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
-                tma_load_4d(s.v + c * C::CHUNK, &tmv, &s.kv_full, c * 64, g, sv.k0 + j0, sv.tma_b);
-            }
             const uint32_t tile_bytes = (uint32_t)(p.P * p.G) * 128u * C::KCH;  // one Q or dO tile
             const uint32_t qbytes = tile_bytes + 2 * 128 * 4;                       // Q plus LSE2, D rows
-            int q_issued = 0, do_issued = 0;
-            for (int it = 0; it < nsteps; ++it) {
-                const int st = it & 1;
-                const uint32_t ph = (it >> 1) & 1;
-                const int row = sv.q0 + (qt0 + it) * p.P;
-                if (!twait(tr, kBQEmpty, &s.q_empty[st], ph ^ 1, ab)) break;
-                mbar_expect_tx(&s.q_full[st], qbytes);
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_4d(s.q[st] + c * C::CHUNK, &tmq, &s.q_full[st], c * 64, g * p.G, row, sv.tma_b);
-                {
-                    const long trow = ((long)g * a.n_qtiles + tbase + qt0 + it) * 128;
-                    bulk_load(s.stat[st][0], a.lse2_t + trow, 512, &s.q_full[st]);
-                    bulk_load(s.stat[st][1], a.delta_t + trow, 512, &s.q_full[st]);
+            int q_issued = 0, do_issued = 0, kv_issued = 0;  // copies issued (also the step / block counts)
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+                const BwdBlock bk = bwd_block<DET, TOK>(a, idx);
+                if (bk.nsteps <= 0) continue;
+                tr.item(idx);
+                for (int it = 0; it < bk.nsteps; ++it) {
+                    const int i = q_issued;  // global step
+                    const int st = i & 1;
+                    const uint32_t ph = (i >> 1) & 1;
+                    const int row = bk.sv.q0 + (bk.qt0 + it) * p.P;
+                    if (!(ok = twait(tr, kBQEmpty, &s.q_empty[st], ph ^ 1, ab))) break;
+                    mbar_expect_tx(&s.q_full[st], qbytes);
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_4d(s.q[st] + c * C::CHUNK, &tmq, &s.q_full[st], c * 64, bk.g * p.G, row, bk.sv.tma_b);
+                    {
+                        const long trow = ((long)bk.g * a.n_qtiles + bk.tbase + bk.qt0 + it) * 128;
+                        bulk_load(s.stat[st][0], a.lse2_t + trow, 512, &s.q_full[st]);
+                        bulk_load(s.stat[st][1], a.delta_t + trow, 512, &s.q_full[st]);
+                    }
+                    ++q_issued;
+                    if (it == 0) {
+                        // this block's K and V, once the previous block's last MMAs (which read
+                        // them) have completed; the first Q went out before, as its ring slot
+                        // frees while the previous block still runs
+                        if (kv_issued > 0 && !(ok = twait(tr, kBDkvFull, &s.dkv_full, (kv_issued - 1) & 1, ab))) break;
+                        mbar_expect_tx(&s.kv_full, 2 * C::TILE);
+                        for (int c = 0; c < C::KCH; ++c) {
+                            tma_load_4d(s.k + c * C::CHUNK, &tmk, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0, bk.sv.tma_b);
+                            tma_load_4d(s.v + c * C::CHUNK, &tmv, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0, bk.sv.tma_b);
+                        }
+                        ++kv_issued;
+                    }
+                    if (!(ok = twait(tr, kBDoEmpty, &s.do_empty[st], ph ^ 1, ab))) break;
+                    mbar_expect_tx(&s.do_full[st], tile_bytes);
+                    for (int c = 0; c < C::KCH; ++c)
+                        tma_load_4d(s.dO[st] + c * C::CHUNK, &tmdo, &s.do_full[st], c * 64, bk.g * p.G, row, bk.sv.tma_b);
+                    ++do_issued;
                 }
-                ++q_issued;
-                if (!twait(tr, kBDoEmpty, &s.do_empty[st], ph ^ 1, ab)) break;
-                mbar_expect_tx(&s.do_full[st], tile_bytes);
-                for (int c = 0; c < C::KCH; ++c)
-                    tma_load_4d(s.dO[st] + c * C::CHUNK, &tmdo, &s.do_full[st], c * 64, g * p.G, row, sv.tma_b);
-                ++do_issued;
             }
+            // the copies still in flight: the latest phase of each ring stage and of K/V
             for (int back = 1; back <= 2; ++back) {
                 if (q_issued - back >= 0) mbar_wait_quiet(&s.q_full[(q_issued - back) & 1], ((q_issued - back) >> 1) & 1);
                 if (do_issued - back >= 0)
                     mbar_wait_quiet(&s.do_full[(do_issued - back) & 1], ((do_issued - back) >> 1) & 1);
             }
-            mbar_wait_quiet(&s.kv_full, 0);
+            if (kv_issued > 0) mbar_wait_quiet(&s.kv_full, (kv_issued - 1) & 1);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
-        if (lane == 0 && nsteps > 0) {
+        if (lane == 0) {
             constexpr uint32_t id_s = idesc_16(128, 128, false, false, F16);  // S^T, dP^T: K-major both
             constexpr uint32_t id_dv = idesc_16(128, D, false, true, F16);    // A from TMEM, B MN-major
             constexpr uint32_t id_dk = idesc_16(128, D, false, true, F16);    // A K-major, B MN-major
@@ -422,70 +450,85 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             const uint32_t ka = smem_u32(s.k), va = smem_u32(s.v);
             Tracer tr;
             tr.init(a.trace, 1);
-            tr.item(blockIdx.x);
-            bool ok = twait(tr, kBKvFull, &s.kv_full, 0, ab);
-            tc_fence_after();
             // each GEMM goes out as one MMA burst (ptx.cuh): base descriptors only, the step
             // offsets are immediates inside the asm block
             const uint64_t kd_k = sdesc_sw128(ka, 16, 1024), vd_k = sdesc_sw128(va, 16, 1024);
             const uint64_t kd_mn = sdesc_sw128(ka, C::CHUNK, 1024);
             const uint32_t sa = smem_u32(s.dst[0]);
             const uint64_t sd_k = sdesc_sw128(sa, 16, 1024), sd_mn = sdesc_sw128(sa, 128 * 128, 1024);
-            auto issue_st = [&](int it) {  // S^T_it = K Q_it^T into the S^T columns
-                const uint64_t qd = sdesc_sw128(smem_u32(s.q[it & 1]), 16, 1024);
+            auto issue_st = [&](int i) {  // S^T_i = K Q_i^T into the S^T columns
+                const uint64_t qd = sdesc_sw128(smem_u32(s.q[i & 1]), 16, 1024);
                 if constexpr (D == 128) mma_ss_kk16_x8(tmem + C::C_S, kd_k, qd, id_s, 0u);
                 else mma_ss_kk16_x4(tmem + C::C_S, kd_k, qd, id_s, 0u);
                 tc_commit(&s.s_full);
             };
-            // issue order per step i:  dP^T_i, dV_i, S^T_{i+1}, dQ^T_i, dK_i  (S^T_0 first)
-            // S^T_{i+1} goes before dQ^T_i / dK_i so that the next step's P^T overlaps them
-            if (ok && (ok = twait(tr, kBQFull, &s.q_full[0], 0, ab))) {
+            int gs = 0, nb = 0;  // steps and blocks of earlier blocks
+            bool ok = true;
+            for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+                const int nsteps = bwd_block<DET, TOK>(a, idx).nsteps;
+                if (nsteps <= 0) continue;
+                tr.item(idx);
+                if (!(ok = twait(tr, kBKvFull, &s.kv_full, nb & 1, ab))) break;
                 tc_fence_after();
-                issue_st(0);
-            }
-            for (int it = 0; ok && it < nsteps; ++it) {
-                const int st = it & 1;
-                const uint32_t ph = (it >> 1) & 1;
-                const uint32_t par = it & 1;
-                const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
-                // dP^T = V dO_i^T (its columns held dQ^T_{i-1} when D == 128)
-                if (!(ok = twait(tr, kBDoFull, &s.do_full[st], ph, ab))) break;
-                if (C::DQ_OVER_DP && it > 0) {
-                    if (!(ok = twait(tr, kBDqFree, &s.dq_free, par ^ 1, ab))) break;
-                }
+                // issue order per step i:  dP^T_i, dV_i, S^T_{i+1}, dQ^T_i, dK_i  (S^T_0 first);
+                // S^T_{i+1} goes before dQ^T_i / dK_i so that the next step's P^T overlaps them
+                if (!(ok = twait(tr, kBQFull, &s.q_full[gs & 1], (gs >> 1) & 1, ab))) break;
                 tc_fence_after();
-                if constexpr (D == 128) mma_ss_kk16_x8(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
-                else mma_ss_kk16_x4(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
-                tc_commit(&s.dp_full);
-                // dV += P^T dO_i (query pairs of group c sit at columns 64c + 8k, k < 4)
-                if (!(ok = twait(tr, kBPFull, &s.p_full, par, ab))) break;
-                tc_fence_after();
-                mma_ts_p_mn_x8(tmem + C::C_DV, tmem + C::C_S, sdesc_sw128(da, C::CHUNK, 1024), id_dv, it > 0 ? 1u : 0u);
-                tc_commit(&s.do_empty[st]);
-                // S^T_{i+1}: its columns held P^T_i, read by dV_i issued just above
-                if (it + 1 < nsteps) {
-                    if (!(ok = twait(tr, kBQFull, &s.q_full[st ^ 1], ((it + 1) >> 1) & 1, ab))) break;
+                issue_st(gs);
+                for (int it = 0; ok && it < nsteps; ++it) {
+                    const int i = gs + it;  // global step
+                    const int st = i & 1;
+                    const uint32_t ph = (i >> 1) & 1;
+                    const uint32_t par = i & 1;
+                    const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
+                    // dP^T = V dO_i^T (its columns held dQ^T_{i-1} when D == 128)
+                    if (!(ok = twait(tr, kBDoFull, &s.do_full[st], ph, ab))) break;
+                    if (C::DQ_OVER_DP && i > 0) {
+                        if (!(ok = twait(tr, kBDqFree, &s.dq_free, par ^ 1, ab))) break;
+                    }
                     tc_fence_after();
-                    issue_st(it + 1);
+                    if constexpr (D == 128) mma_ss_kk16_x8(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
+                    else mma_ss_kk16_x4(tmem + C::C_DP, vd_k, sdesc_sw128(da, 16, 1024), id_s, 0u);
+                    tc_commit(&s.dp_full);
+                    // dV += P^T dO_i (query pairs of group c sit at columns 64c + 8k, k < 4); the
+                    // block's first dV overwrites the accumulators, which the compute groups
+                    // must have read out for the previous block
+                    if (!(ok = twait(tr, kBPFull, &s.p_full, par, ab))) break;
+                    if (it == 0 && nb > 0 && !(ok = twait(tr, kBDkvFree, &s.dkv_free, (nb - 1) & 1, ab))) break;
+                    tc_fence_after();
+                    mma_ts_p_mn_x8(tmem + C::C_DV, tmem + C::C_S, sdesc_sw128(da, C::CHUNK, 1024), id_dv, it > 0 ? 1u : 0u);
+                    tc_commit(&s.do_empty[st]);
+                    // S^T_{i+1}: its columns held P^T_i, read by dV_i issued just above
+                    if (it + 1 < nsteps) {
+                        if (!(ok = twait(tr, kBQFull, &s.q_full[st ^ 1], ((i + 1) >> 1) & 1, ab))) break;
+                        tc_fence_after();
+                        issue_st(i + 1);
+                    }
+                    // dQ^T_i = K^T dS^T, then dK += dS^T Q_i: dQ goes first so that its drain by the
+                    // dQ warps (which frees the dP^T columns for the next step) overlaps dK
+                    if (!(ok = twait(tr, kBDsFull, &s.ds_full, par, ab))) break;
+                    if (!C::DQ_OVER_DP && i > 0) {
+                        if (!(ok = twait(tr, kBDqFree, &s.dq_free, par ^ 1, ab))) break;
+                    }
+                    tc_fence_after();
+                    if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: A = K tile (MN-major), B = dS^T (MN-major)
+                        mma_ss_mnmn_x8(tmem + C::C_DQ, kd_mn, sd_mn, id_dq, 0u);
+                    else                    // dQ = dS K: A = dS (MN-major), B = K tile (MN-major)
+                        mma_ss_mnmn_x8(tmem + C::C_DQ, sd_mn, kd_mn, id_dq, 0u);
+                    tc_commit(&s.dq_full);
+                    mma_ss_kmn16_x8(tmem + C::C_DK, sd_k, sdesc_sw128(qa, C::CHUNK, 1024), id_dk, it > 0 ? 1u : 0u);
+                    tc_commit(&s.q_empty[st]);
+                    tc_commit(&s.ds_free);
                 }
-                // dQ^T_i = K^T dS^T, then dK += dS^T Q_i: dQ goes first so that its drain by the
-                // dQ warps (which frees the dP^T columns for the next step) overlaps dK
-                if (!(ok = twait(tr, kBDsFull, &s.ds_full, par, ab))) break;
-                if (!C::DQ_OVER_DP && it > 0) {
-                    if (!(ok = twait(tr, kBDqFree, &s.dq_free, par ^ 1, ab))) break;
-                }
-                tc_fence_after();
-                if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: A = K tile (MN-major), B = dS^T (MN-major)
-                    mma_ss_mnmn_x8(tmem + C::C_DQ, kd_mn, sd_mn, id_dq, 0u);
-                else                    // dQ = dS K: A = dS (MN-major), B = K tile (MN-major)
-                    mma_ss_mnmn_x8(tmem + C::C_DQ, sd_mn, kd_mn, id_dq, 0u);
-                tc_commit(&s.dq_full);
-                mma_ss_kmn16_x8(tmem + C::C_DK, sd_k, sdesc_sw128(qa, C::CHUNK, 1024), id_dk, it > 0 ? 1u : 0u);
-                tc_commit(&s.q_empty[st]);
-                tc_commit(&s.ds_free);
+                if (!ok) break;
+                // dK and dV of the block are final, and K and V are read, once these complete
+                tc_commit(&s.dkv_full);
+                gs += nsteps;
+                ++nb;
             }
-            tc_commit(&s.dkv_full);
-            mbar_wait_quiet(&s.dkv_full, 0);
+            // let every issued MMA finish before the CTA tears down
+            tc_commit(&s.drain);
+            mbar_wait_quiet(&s.drain, 0);
         }
     }
     } else {
@@ -495,158 +538,178 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int wq = warp & 3;
         const int jr = (wq << 5) | lane;           // key row of this thread (TMEM lane)
         const uint32_t lane_base = (uint32_t)(wq << 5) << 16;
-        const int j = j0 + jr;
         const float c = p.scale_log2;
         bool ok = true;
-        DqOrder order;
-        order.next = blk + 1;
-        // token mode: this key's queries as packed rows (its own sequence's band)
-        int tq_lo = 1, tq_hi = 0;
-        if (tokens) token_key_queries(p, j, tq_lo, tq_hi);
         Tracer tr;
         tr.init(warp == 4 ? a.trace : nullptr, 2);
-        tr.item(blockIdx.x);
-        for (int it = 0; it < nsteps; ++it) {
-            const uint32_t par = it & 1;
-            const int t = qt0 + it;                 // query tile within the sequence
-            const int s0 = t * p.P;                 // its first query position
-            const long trow = ((long)g * a.n_qtiles + tbase + t) * 128;  // tiled row base
-            const int st = it & 1;
-            const float* lse2 = s.stat[st][0] + 64 * cg;
-            const float* dlt = s.stat[st][1] + 64 * cg;
-            // edge test: does the band cut this (query tile, key tile) pair?
-            const int iq_first = s0, iq_last = min(s0 + p.P, sv.nq) - 1;
-            const bool interior = !tokens && j0 >= band.lo(iq_last) && j0 + kRows - 1 <= band.hi(iq_first);
-            // ---- P^T ----
-            {
-                // the stage's LSE / D rows landed with Q_i (already complete by the time S^T is)
-                bool w = twait(tr, kBQFull, &s.q_full[st], (it >> 1) & 1, ab);
-                w = w && twait(tr, kBSFull, &s.s_full, par, ab);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            }
-            tc_fence_after();
-            float pf[64];
-            {
-                uint32_t sr[64];
-                tmem_ld_32x32b_x64(tmem + lane_base + C::C_S + 64 * cg, sr);
-#pragma unroll
-                for (int cc = 0; cc < 64; cc += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(lse2 + cc);
-                    pf[cc + 0] = ex2(fmaf(__uint_as_float(sr[cc + 0]), c, -l4.x));
-                    pf[cc + 1] = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -l4.y));
-                    pf[cc + 2] = ex2(fmaf(__uint_as_float(sr[cc + 2]), c, -l4.z));
-                    pf[cc + 3] = ex2(fmaf(__uint_as_float(sr[cc + 3]), c, -l4.w));
+        int gs = 0, nb = 0;  // steps and blocks of earlier blocks
+        for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+            const BwdBlock bk = bwd_block<DET, TOK>(a, idx);
+            if (!bk.live) continue;  // an idle block of a packed batch writes nothing
+            tr.item(idx);
+            const int j = bk.j0 + jr;
+            // token mode: this key's queries as packed rows (its own sequence's band)
+            int tq_lo = 1, tq_hi = 0;
+            if (tokens) token_key_queries(p, j, tq_lo, tq_hi);
+            for (int it = 0; it < bk.nsteps; ++it) {
+                const int i = gs + it;                  // global step
+                const uint32_t par = i & 1;
+                const int t = bk.qt0 + it;              // query tile within the sequence
+                const int s0 = t * p.P;                 // its first query position
+                const int st = i & 1;
+                const float* lse2 = s.stat[st][0] + 64 * cg;
+                const float* dlt = s.stat[st][1] + 64 * cg;
+                // edge test: does the band cut this (query tile, key tile) pair?
+                const int iq_first = s0, iq_last = min(s0 + p.P, bk.sv.nq) - 1;
+                const bool interior =
+                    !tokens && bk.j0 >= bk.band.lo(iq_last) && bk.j0 + kRows - 1 <= bk.band.hi(iq_first);
+                // ---- P^T ----
+                {
+                    // the stage's LSE / D rows landed with Q_i (already complete by the time S^T is)
+                    bool w = twait(tr, kBQFull, &s.q_full[st], (i >> 1) & 1, ab);
+                    w = w && twait(tr, kBSFull, &s.s_full, par, ab);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 }
-                if (!interior) {
-                    // the query positions whose band holds key j form one interval
-                    // [i_min, i_max] (lo and hi are monotone in the position); in this tile's
-                    // packed columns (column = G (i - s0) + head) it is the column range
-                    // [G (i_min - s0), G (i_max + 1 - s0)), taken relative to this group's
-                    // first column
-                    int c_lo, c_hi;
-                    if constexpr (TOK) {
-                        // the key's queries as packed rows (none: an empty column range)
-                        c_lo = tq_lo > tq_hi ? 0 : (tq_lo - s0) * p.G - 64 * cg;
-                        c_hi = tq_lo > tq_hi ? 0 : (tq_hi + 1 - s0) * p.G - 64 * cg;
-                    } else {
-                        const int i_min = p.right >= 0 ? j - band.off - p.right : 0;
-                        const int i_max = j >= sv.nk ? i_min - 1 : (p.left >= 0 ? j - band.off + p.left : sv.nq - 1);
-                        c_lo = (i_min - s0) * p.G - 64 * cg;
-                        c_hi = (i_max + 1 - s0) * p.G - 64 * cg;
+                tc_fence_after();
+                float pf[64];
+                {
+                    uint32_t sr[64];
+                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_S + 64 * cg, sr);
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + cc);
+                        pf[cc + 0] = ex2(fmaf(__uint_as_float(sr[cc + 0]), c, -l4.x));
+                        pf[cc + 1] = ex2(fmaf(__uint_as_float(sr[cc + 1]), c, -l4.y));
+                        pf[cc + 2] = ex2(fmaf(__uint_as_float(sr[cc + 2]), c, -l4.z));
+                        pf[cc + 3] = ex2(fmaf(__uint_as_float(sr[cc + 3]), c, -l4.w));
                     }
+                    if (!interior) {
+                        // the query positions whose band holds key j form one interval
+                        // [i_min, i_max] (lo and hi are monotone in the position); in this tile's
+                        // packed columns (column = G (i - s0) + head) it is the column range
+                        // [G (i_min - s0), G (i_max + 1 - s0)), taken relative to this group's
+                        // first column
+                        int c_lo, c_hi;
+                        if constexpr (TOK) {
+                            // the key's queries as packed rows (none: an empty column range)
+                            c_lo = tq_lo > tq_hi ? 0 : (tq_lo - s0) * p.G - 64 * cg;
+                            c_hi = tq_lo > tq_hi ? 0 : (tq_hi + 1 - s0) * p.G - 64 * cg;
+                        } else {
+                            const int i_min = p.right >= 0 ? j - bk.band.off - p.right : 0;
+                            const int i_max =
+                                j >= bk.sv.nk ? i_min - 1 : (p.left >= 0 ? j - bk.band.off + p.left : bk.sv.nq - 1);
+                            c_lo = (i_min - s0) * p.G - 64 * cg;
+                            c_hi = (i_max + 1 - s0) * p.G - 64 * cg;
+                        }
 #pragma unroll
-                    for (int cc = 0; cc < 64; ++cc)
-                        if (cc < c_lo || cc >= c_hi) pf[cc] = 0.f;
+                        for (int cc = 0; cc < 64; ++cc)
+                            if (cc < c_lo || cc >= c_hi) pf[cc] = 0.f;
+                    }
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 2) pk[cc / 2] = pack16<F16>(pf[cc], pf[cc + 1]);
+                    // P^T of query columns [64cg, 64cg+64) goes over the first half of the S^T
+                    // columns this group has just read (the other group never touches them)
+                    tmem_st_32x32b_x32(tmem + lane_base + C::C_S + 64 * cg, pk);
                 }
-                uint32_t pk[32];
+                tc_fence_before();
+                mbar_arrive(&s.p_full);
+                // ---- dS^T = P^T (dP^T - D) -> shared memory ----
+                {
+                    const bool w = twait(tr, kBDpFull, &s.dp_full, par, ab);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                }
+                if (i > 0) {
+                    const bool w = twait(tr, kBDsFree, &s.ds_free, par ^ 1, ab);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                }
+                tc_fence_after();
+                {
+                    uint8_t* drow = s.dst[cg] + jr * 128;
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 2) pk[cc / 2] = pack16<F16>(pf[cc], pf[cc + 1]);
-                // P^T of query columns [64cg, 64cg+64) goes over the first half of the S^T
-                // columns this group has just read (the other group never touches them)
-                tmem_st_32x32b_x32(tmem + lane_base + C::C_S + 64 * cg, pk);
-            }
-            tc_fence_before();
-            mbar_arrive(&s.p_full);
-            // ---- dS^T = P^T (dP^T - D) -> shared memory ----
-            {
-                const bool w = twait(tr, kBDpFull, &s.dp_full, par, ab);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            }
-            if (it > 0) {
-                const bool w = twait(tr, kBDsFree, &s.ds_free, par ^ 1, ab);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            }
-            tc_fence_after();
-            {
-                uint8_t* drow = s.dst[cg] + jr * 128;
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t dr[32];
+                        tmem_ld_32x32b_x32(tmem + lane_base + C::C_DP + 64 * cg + 32 * hf, dr);
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t dr[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DP + 64 * cg + 32 * hf, dr);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {  // 16-byte units of 8 columns
-                        const int cb = 32 * hf + 8 * u;
-                        const float4 d0 = *reinterpret_cast<const float4*>(dlt + cb);
-                        const float4 d1 = *reinterpret_cast<const float4*>(dlt + cb + 4);
-                        uint4 w;
-                        w.x = pack16<F16>(pf[cb + 0] * (__uint_as_float(dr[8 * u + 0]) - d0.x),
-                                        pf[cb + 1] * (__uint_as_float(dr[8 * u + 1]) - d0.y));
-                        w.y = pack16<F16>(pf[cb + 2] * (__uint_as_float(dr[8 * u + 2]) - d0.z),
-                                        pf[cb + 3] * (__uint_as_float(dr[8 * u + 3]) - d0.w));
-                        w.z = pack16<F16>(pf[cb + 4] * (__uint_as_float(dr[8 * u + 4]) - d1.x),
-                                        pf[cb + 5] * (__uint_as_float(dr[8 * u + 5]) - d1.y));
-                        w.w = pack16<F16>(pf[cb + 6] * (__uint_as_float(dr[8 * u + 6]) - d1.z),
-                                        pf[cb + 7] * (__uint_as_float(dr[8 * u + 7]) - d1.w));
-                        const int unit = (cb >> 3) ^ (jr & 7);
-                        *reinterpret_cast<uint4*>(drow + unit * 16) = w;
+                        for (int u = 0; u < 4; ++u) {  // 16-byte units of 8 columns
+                            const int cb = 32 * hf + 8 * u;
+                            const float4 d0 = *reinterpret_cast<const float4*>(dlt + cb);
+                            const float4 d1 = *reinterpret_cast<const float4*>(dlt + cb + 4);
+                            uint4 w;
+                            w.x = pack16<F16>(pf[cb + 0] * (__uint_as_float(dr[8 * u + 0]) - d0.x),
+                                            pf[cb + 1] * (__uint_as_float(dr[8 * u + 1]) - d0.y));
+                            w.y = pack16<F16>(pf[cb + 2] * (__uint_as_float(dr[8 * u + 2]) - d0.z),
+                                            pf[cb + 3] * (__uint_as_float(dr[8 * u + 3]) - d0.w));
+                            w.z = pack16<F16>(pf[cb + 4] * (__uint_as_float(dr[8 * u + 4]) - d1.x),
+                                            pf[cb + 5] * (__uint_as_float(dr[8 * u + 5]) - d1.y));
+                            w.w = pack16<F16>(pf[cb + 6] * (__uint_as_float(dr[8 * u + 6]) - d1.z),
+                                            pf[cb + 7] * (__uint_as_float(dr[8 * u + 7]) - d1.w));
+                            const int unit = (cb >> 3) ^ (jr & 7);
+                            *reinterpret_cast<uint4*>(drow + unit * 16) = w;
+                        }
                     }
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&s.ds_full);
+                tr.mark(kMStepDone);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&s.ds_full);
-            tr.mark(kMStepDone);
-        }
-        // ---- epilogue: dK, dV for this key tile ----
-        if (nsteps > 0 && ok) {
-            const bool w = twait(tr, kBDkvFull, &s.dkv_full, 0, ab);
-            ok = __all_sync(0xffffffffu, w);
-            tc_fence_after();
-        }
-        tr.mark(kMEpilogue);
-        // rows past the block's keys, or (token mode) past the key's sequence's used keys,
-        // are not written
-        bool row_ok = j <= j1;
-        if (tokens && row_ok && p.seqused_k) {
-            const SeqView ks = seq_view(p, row_sequence(p.cu_k, p.B, j));
-            row_ok = j - ks.k0 < ks.nk;
-        }
-        const long krow = key_row(p, sv, j);
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            uint16_t* dst = (which == 0 ? a.dv : a.dk) + (krow * p.h_kv + g) * D + (D / 2) * cg;
-            const float mul = which == 0 ? 1.f : p.scale;
-            const uint32_t col = (which == 0 ? C::C_DV : C::C_DK) + (D / 2) * cg;
-#pragma unroll
-            for (int cb = 0; cb < D / 2; cb += 32) {
-                uint32_t v[32];
-                if (nsteps > 0 && ok) {
-                    tmem_ld_32x32b_x32(tmem + lane_base + col + cb, v);
+            if (!ok) break;
+            // ---- epilogue: dK, dV for this key block ----
+            const bool have = bk.nsteps > 0;  // uniform over the CTA
+            if (have) {
+                const bool w = twait(tr, kBDkvFull, &s.dkv_full, nb & 1, ab);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+            }
+            tr.mark(kMEpilogue);
+            // rows past the block's keys, or (token mode) past the key's sequence's used keys,
+            // are not written
+            bool row_ok = j <= bk.j1;
+            if (tokens && row_ok && p.seqused_k) {
+                const SeqView ks = seq_view(p, row_sequence(p.cu_k, p.B, j));
+                row_ok = j - ks.k0 < ks.nk;
+            }
+            const long krow = key_row(p, bk.sv, j);
+            // this group's half of the dV and dK row into registers; then the accumulators are
+            // free for the next block while the rows are scaled and stored
+            uint32_t vv[D / 2], kk[D / 2];
+            if (have) {
+                if constexpr (D == 128) {
+                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_DV + (D / 2) * cg, vv);
+                    tmem_ld_32x32b_x64(tmem + lane_base + C::C_DK + (D / 2) * cg, kk);
                 } else {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] = 0u;
+                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DV + (D / 2) * cg, vv);
+                    tmem_ld_32x32b_x32(tmem + lane_base + C::C_DK + (D / 2) * cg, kk);
                 }
-                if (row_ok) {
+                tc_fence_before();
+                mbar_arrive(&s.dkv_free);
+            } else {
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        uint4 w;
-                        w.x = pack16<F16>(__uint_as_float(v[8 * t + 0]) * mul, __uint_as_float(v[8 * t + 1]) * mul);
-                        w.y = pack16<F16>(__uint_as_float(v[8 * t + 2]) * mul, __uint_as_float(v[8 * t + 3]) * mul);
-                        w.z = pack16<F16>(__uint_as_float(v[8 * t + 4]) * mul, __uint_as_float(v[8 * t + 5]) * mul);
-                        w.w = pack16<F16>(__uint_as_float(v[8 * t + 6]) * mul, __uint_as_float(v[8 * t + 7]) * mul);
-                        reinterpret_cast<uint4*>(dst + cb)[t] = w;
-                    }
+                for (int t = 0; t < D / 2; ++t) vv[t] = kk[t] = 0u;
+            }
+            if (row_ok) {
+                uint4* dvp = reinterpret_cast<uint4*>(a.dv + (krow * p.h_kv + bk.g) * D + (D / 2) * cg);
+                uint4* dkp = reinterpret_cast<uint4*>(a.dk + (krow * p.h_kv + bk.g) * D + (D / 2) * cg);
+                const float mul = p.scale;
+#pragma unroll
+                for (int t = 0; t < D / 16; ++t) {
+                    uint4 w;
+                    w.x = pack16<F16>(__uint_as_float(vv[8 * t + 0]), __uint_as_float(vv[8 * t + 1]));
+                    w.y = pack16<F16>(__uint_as_float(vv[8 * t + 2]), __uint_as_float(vv[8 * t + 3]));
+                    w.z = pack16<F16>(__uint_as_float(vv[8 * t + 4]), __uint_as_float(vv[8 * t + 5]));
+                    w.w = pack16<F16>(__uint_as_float(vv[8 * t + 6]), __uint_as_float(vv[8 * t + 7]));
+                    dvp[t] = w;
+                    w.x = pack16<F16>(__uint_as_float(kk[8 * t + 0]) * mul, __uint_as_float(kk[8 * t + 1]) * mul);
+                    w.y = pack16<F16>(__uint_as_float(kk[8 * t + 2]) * mul, __uint_as_float(kk[8 * t + 3]) * mul);
+                    w.z = pack16<F16>(__uint_as_float(kk[8 * t + 4]) * mul, __uint_as_float(kk[8 * t + 5]) * mul);
+                    w.w = pack16<F16>(__uint_as_float(kk[8 * t + 6]) * mul, __uint_as_float(kk[8 * t + 7]) * mul);
+                    dkp[t] = w;
                 }
+            }
+            if (have) {
+                gs += bk.nsteps;
+                ++nb;
             }
         }
     }
@@ -1202,10 +1265,13 @@ template <int D, bool DET, bool TOK>
 static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem<D>);
+    static_assert(sizeof(BwdSmem<D>) <= 232448, "backward: shared memory over the 227 KB limit");
     auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd_main_kernel<D, DET, true, TOK> : bwd_main_kernel<D, DET, false, TOK>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
+    // persistent CTAs (at most one per SM); the fixed dQ order takes one CTA per unit
+    const long n = DET ? (long)a.n_units : (long)a.n_ctas;
+    if (n <= 0) return cudaSuccess;
     kernel<<<(unsigned)n, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
     return cudaGetLastError();
 }

@@ -454,98 +454,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         bool ok = true;
         Tracer tr;
         tr.init((warp & 3) == 0 ? a.trace : nullptr, 2 + k);
-        // Epilogue of an item: O / l (with the sink) to the outputs, LSE, then the item slot
-        // goes back to the scheduler.  It runs one item late, after the next item's first P
-        // (see the key loop), so that waiting for the last P V and storing O overlap work of
-        // the next item instead of sitting on the chain.
-        struct Pending {
-            bool on;
-            int slot;
-            float m, l, sink2;
-        };
-        Pending pend{false, 0, 0.f, 0.f, 0.f};
-        auto finish = [&](const Pending& e) {
-            const ItemInfo& itm = s.item[e.slot];
-            const SeqView sv{itm.b, itm.q0, 0, 0, 0, 0};
-            const int g = itm.g, split = itm.split;
-            const int i = itm.s0[k] + r / p.G;  // query position (a packed row in token mode)
-            const int h = g * p.G + r % p.G;    // query head
-            const bool e_valid = s.band[e.slot][k][r].x != kNoRow;
-            bool have = itm.t1[k] > itm.t0[k] && ok;  // uniform over the warp group
-            if (have) {
-                const bool wt = twait(tr, kBOFull, &s.o_full[k], ocount & 1, ab);
-                ++ocount;
-                have = __all_sync(0xffffffffu, wt);
-                if (!have) ok = false;
-                tc_fence_after();
-            }
-            const bool split_mode = a.n_splits > 1;
-            float oscale = 0.f, lse = -INFINITY;
-            if (!split_mode && p.sinks && e_valid) {
-                const float mf = fmaxf(e.m, e.sink2);
-                const float wgt = (e.m == -INFINITY) ? 0.f : ex2(e.m - mf);
-                const float lt = e.l * wgt + ex2(e.sink2 - mf);
-                oscale = wgt / lt;
-                lse = (mf + log2f(lt)) * kLn2;
-            } else if (e.l > 0.f) {
-                oscale = 1.f / e.l;
-                lse = (e.m + log2f(e.l)) * kLn2;
-            }
-            const long nrows = (long)p.B * p.h_q * p.s_q;
-            const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;  // split-mode row (dense only)
-            if (e_valid) {
-                if (!split_mode) {
-                    if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
-                } else {
-                    a.lse_part[(long)split * nrows + prow] = lse;
-                }
-            }
-            if (have) {
-                // the whole O row into registers (warp-collective TMEM reads), then O_k is free
-                // for the next item's P V while the row is scaled and stored
-                uint32_t orr[D];
-                if constexpr (D == 128) tmem_ld_32x32b_x128(tO, orr);
-                else tmem_ld_32x32b_x64(tO, orr);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.o_free[k]);
-                if (e_valid) {
-                    if (!split_mode) {
-                        uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
-#pragma unroll
-                        for (int t = 0; t < D / 8; ++t) {
-                            uint4 wv;
-                            wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
-                            wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
-                            wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
-                            wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
-                            orow[t] = wv;
-                        }
-                    } else {
-                        float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
-#pragma unroll
-                        for (int t = 0; t < D / 4; ++t)
-                            op[t] = make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
-                                                __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
-                    }
-                }
-                tr.mark(kMEpilogueDone);
-            } else if (e_valid) {
-                // no key tile (or a failed wait): zero rows
-                if (!split_mode) {
-                    uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
-#pragma unroll
-                    for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(0, 0, 0, 0);
-                } else {
-                    float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
-#pragma unroll
-                    for (int t = 0; t < D / 4; ++t) op[t] = make_float4(0, 0, 0, 0);
-                }
-            }
-            // the item slot is read for the last time: hand it back to the scheduler
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.item_empty[e.slot]);
-        };
         for (int n = 0; ok; ++n) {
         // the item comes decoded from the scheduler warp; only the loop bounds, the row's key
         // band and its sink stay live across the key loop, the epilogue reads the rest again
@@ -650,19 +558,88 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.p_full[k]);
             tr.mark(kMSoftmaxDone);
-            // the previous item's epilogue, now that this item's first P is handed over: its
-            // O read (and o_free) unblocks this item's first P V, and its stores overlap the
-            // round trip to this item's next S
-            if (pend.on) {
-                finish(pend);
-                pend.on = false;
+        }
+        // ---------------- epilogue ----------------
+        const ItemInfo& itm = s.item[slot];
+        const SeqView sv{itm.b, itm.q0, 0, 0, 0, 0};
+        const int g = itm.g, split = itm.split;
+        const int i = itm.s0[k] + r / p.G;  // query position (a packed row in token mode)
+        const int h = g * p.G + r % p.G;    // query head
+        const bool row_valid = jlo != kNoRow;
+        const bool has_o = my_t1 > my_t0;  // uniform over the warp group
+        if (has_o && ok) {
+            const bool wt = twait(tr, kBOFull, &s.o_full[k], ocount & 1, ab);
+            ++ocount;
+            ok = __all_sync(0xffffffffu, wt);
+            tc_fence_after();
+        }
+        const bool split_mode = a.n_splits > 1;
+        float oscale = 0.f, lse = -INFINITY;
+        if (!split_mode && p.sinks && row_valid) {
+            const float s2 = sink2;
+            const float mf = fmaxf(m_used, s2);
+            const float wgt = (m_used == -INFINITY) ? 0.f : ex2(m_used - mf);
+            const float lt = l * wgt + ex2(s2 - mf);
+            oscale = wgt / lt;
+            lse = (mf + log2f(lt)) * kLn2;
+        } else if (l > 0.f) {
+            oscale = 1.f / l;
+            lse = (m_used + log2f(l)) * kLn2;
+        }
+        const long nrows = (long)p.B * p.h_q * p.s_q;
+        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;  // split-mode row (dense only)
+        if (row_valid) {
+            if (!split_mode) {
+                if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
+            } else {
+                a.lse_part[(long)split * nrows + prow] = lse;
             }
         }
-        // an item without key tiles: the previous epilogue has not run yet
-        if (pend.on) finish(pend);
-        pend = Pending{true, slot, m_used, l, sink2};
+        if (has_o && ok) {
+            // the whole O row into registers (warp-collective TMEM reads), then O_k is free for
+            // the next item's P V while the row is scaled and stored; only valid rows store
+            uint32_t orr[D];
+            if constexpr (D == 128) tmem_ld_32x32b_x128(tO, orr);
+            else tmem_ld_32x32b_x64(tO, orr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.o_free[k]);
+            if (row_valid) {
+                if (!split_mode) {
+                    uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
+#pragma unroll
+                    for (int t = 0; t < D / 8; ++t) {
+                        uint4 wv;
+                        wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
+                        wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
+                        wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
+                        wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
+                        orow[t] = wv;
+                    }
+                } else {
+                    float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
+#pragma unroll
+                    for (int t = 0; t < D / 4; ++t)
+                        op[t] = make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
+                                            __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
+                }
+            }
+            tr.mark(kMEpilogueDone);
+        } else if (row_valid) {
+            if (!split_mode) {
+                uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
+#pragma unroll
+                for (int t = 0; t < D / 8; ++t) reinterpret_cast<uint4*>(orow)[t] = make_uint4(0, 0, 0, 0);
+            } else {
+                float* op = a.o_part + ((long)split * nrows + prow) * D;
+#pragma unroll
+                for (int t = 0; t < D / 4; ++t) reinterpret_cast<float4*>(op)[t] = make_float4(0, 0, 0, 0);
+            }
+        }
+        // the item slot is read for the last time: hand it back to the scheduler
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.item_empty[slot]);
         }  // items
-        if (pend.on) finish(pend);
     }
 
     tc_fence_before();

@@ -94,6 +94,8 @@ struct BwdArgs {
                            // query-side data stays in L2
     int tokens;            // packed batch with queries and keys packed alike: key blocks and query
                            // tiles run over the packed token axis (d <= 128 kernel)
+    int n_units;           // work units (key blocks x kv heads [x batch])
+    int n_ctas;            // persistent CTAs of the d <= 128 main kernel (at most one per SM)
     // 16-bit tensors hold bf16 or fp16 (Problem::dtype) like the inputs
     const uint16_t* o;
     const float* lse;

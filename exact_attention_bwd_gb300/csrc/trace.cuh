@@ -35,7 +35,7 @@ enum TraceEvent : uint32_t {
 enum TraceBarrier : uint32_t {
     kBQFull = 1, kBQEmpty, kBKFull, kBKEmpty, kBVFull, kBVEmpty, kBSFull, kBPFull, kBOFull, kBOFree,
     kBDoFull, kBDoEmpty, kBKvFull, kBDpFull, kBDsFull, kBDsFree, kBDqFull, kBDqFree, kBDkvFull, kBQTmem,
-    kBPvDone, kBPdsFull, kBPdsFree,
+    kBPvDone, kBPdsFull, kBPdsFree, kBDkvFree,
 };
 
 // marks (arguments of kEvMark)

@@ -24,7 +24,7 @@ REGION_BYTES = CTAS * ROLES * SLOTS * 16
 EV_ITEM, EV_WAIT, EV_GOT, EV_MARK = 1, 2, 3, 4
 BARRIERS = ["q_full", "q_empty", "k_full", "k_empty", "v_full", "v_empty", "s_full", "p_full", "o_full", "o_free",
             "do_full", "do_empty", "kv_full", "dp_full", "ds_full", "ds_free", "dq_full", "dq_free", "dkv_full",
-            "q_tmem", "pv_done", "pds_full", "pds_free"]
+            "q_tmem", "pv_done", "pds_full", "pds_free", "dkv_free"]
 MARKS = ["issue_s", "issue_pv", "issue_dp", "issue_dv", "issue_dq", "issue_dk", "softmax_done", "epilogue",
          "epilogue_done", "dq_reduced", "step_done"]
 ROLE_NAMES = {"fwd": ["producer", "mma", "softmax tile 0", "softmax tile 1"],
