@@ -435,7 +435,8 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     if (keys_total > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int* status = reinterpret_cast<int*>(workspace);
-    if ((rc = cuda_status(cudaMemsetAsync(status, 0, sizeof(int), st))) != FA_OK) return rc;
+    // the status word and, next to it, the counter from which persistent CTAs take work
+    if ((rc = cuda_status(cudaMemsetAsync(status, 0, 2 * sizeof(int), st))) != FA_OK) return rc;
     if ((rc = maybe_validate(p, in->flags, status, st)) != FA_OK) return rc;
     if (pl.path == FwdPath::kEmpty) return FA_OK;
 
@@ -524,6 +525,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.status = status;
+    a.work_counter = status + 1;
 #ifdef FA_TRACE
     a.trace = reinterpret_cast<unsigned long long*>(ws + pl.off_trace);
     if (cudaMemsetAsync(a.trace, 0, kTraceBytes, st) != cudaSuccess) return FA_ERR_CUDA;
@@ -567,7 +569,8 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
         return FA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int* status = reinterpret_cast<int*>(workspace);
-    if ((rc = cuda_status(cudaMemsetAsync(status, 0, sizeof(int), st))) != FA_OK) return rc;
+    // the status word and, next to it, the counter from which persistent CTAs take work
+    if ((rc = cuda_status(cudaMemsetAsync(status, 0, 2 * sizeof(int), st))) != FA_OK) return rc;
     if (p.sinks && (rc = cuda_status(cudaMemsetAsync(dsinks, 0, sizeof(float) * p.h_q, st))) != FA_OK) return rc;
     if ((rc = maybe_validate(p, in->flags, status, st)) != FA_OK) return rc;
     if (pl.empty) return FA_OK;
@@ -594,6 +597,7 @@ fa_status fa_bwd(const fa_params* in, const void* q, const void* k, const void* 
     a.sink_t = p.sinks ? reinterpret_cast<float*>(ws + pl.off_sink) : nullptr;
     a.dq_count = (in->flags & FA_FLAG_DETERMINISTIC) ? reinterpret_cast<int*>(ws + pl.off_count) : nullptr;
     a.status = status;
+    a.work_counter = status + 1;
 #ifdef FA_TRACE
     a.trace = reinterpret_cast<unsigned long long*>(ws + pl.off_trace);
     if (cudaMemsetAsync(a.trace, 0, kTraceBytes, st) != cudaSuccess) return FA_ERR_CUDA;

@@ -52,6 +52,11 @@ struct BwdCfg {
     static constexpr bool DQ_T = (D == 128);                   // dQ computed transposed (lanes = d)
 };
 
+// The work-unit ring of the d <= 128 main kernel: slots, and the arrivals that free one
+// (producer, MMA issuer, the eight compute warps and the four dQ warps).
+constexpr int kUnitSlots = 4;
+constexpr int kUnitReaders = 14;
+
 template <int D>
 struct __align__(1024) BwdSmem {
     uint8_t k[BwdCfg<D>::TILE];
@@ -63,6 +68,8 @@ struct __align__(1024) BwdSmem {
     uint64_t kv_full;
     uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
     uint64_t s_full, dp_full, p_full, ds_full, ds_free, dq_full, dq_free, dkv_full, dkv_free, drain;
+    uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
+    int unit[kUnitSlots];  // work units handed out by the scheduler warp (-1: no more)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -197,6 +204,23 @@ struct BwdBlock {
     bool live;  // false: an idle block of a packed batch (nothing to compute or write)
 };
 
+// The n-th work unit this role takes from the scheduler's ring (-1: none left, or a failed
+// wait, which also clears ok).  Every thread of a calling warp (or the single calling thread
+// of the producer / MMA roles) reads the slot; lane 0 frees it.
+template <class Smem>
+__device__ __forceinline__ int take_unit(Smem& s, int n, const Abort& ab, bool& ok) {
+    const int slot = n % kUnitSlots;
+    const bool w = mbar_wait(&s.unit_full[slot], (n / kUnitSlots) & 1, ab);
+    if (!__all_sync(__activemask(), w)) {
+        ok = false;
+        return -1;
+    }
+    const int idx = s.unit[slot];
+    __syncwarp(__activemask());
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.unit_empty[slot]);
+    return idx;
+}
+
 template <bool DET, bool TOK>
 __device__ __forceinline__ BwdBlock bwd_block(const BwdArgs& a, int idx) {
     const Problem& p = a.p;
@@ -258,9 +282,11 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     // token mode (TOK): key blocks and query tiles over the packed token axis; never with DET
     constexpr bool tokens = TOK;
     static_assert(!(DET && TOK), "the fixed dQ order uses blocks per sequence");
-    // Persistent: the CTA walks work units blockIdx.x, + gridDim.x, ... (heaviest first, in
-    // L2-sized bands for dense batches).  With the fixed dQ order the launch has one CTA per
-    // unit, so a CTA waits only on CTAs dispatched before it.  Every role keeps a running
+    // Persistent: one CTA per SM; its scheduler warp takes work units one at a time from the
+    // call's counter (units are numbered heaviest first, in L2-sized bands for dense batches,
+    // so the CTAs share the work out greedily) and hands them to the other roles through a
+    // small ring.  With the fixed dQ order the launch has one CTA per unit instead (unit =
+    // CTA index), so a CTA waits only on CTAs dispatched before it.  Every role keeps a running
     // count of the steps (query tiles) and blocks it has been through, so that the barrier
     // phases carry on from block to block; two barriers hand a block's resources to the next:
     // dkv_full (the block's last MMAs, which read K and V and finish dK and dV, have
@@ -288,6 +314,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         mbar_init(&s.dkv_full, 1);
         mbar_init(&s.dkv_free, 256);  // the compute groups' threads
         mbar_init(&s.drain, 1);
+        for (int i = 0; i < kUnitSlots; ++i) {
+            mbar_init(&s.unit_full[i], 1);
+            mbar_init(&s.unit_empty[i], kUnitReaders);
+        }
         fence_mbar_init();
     }
     if (p.P * p.G < 128) {
@@ -327,7 +357,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         tr.init(warp == 12 ? a.trace : nullptr, 3);
         int gs = 0;  // steps of earlier blocks
         bool ok = true;
-        for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+        for (int n = 0; ok; ++n) {
+            const int idx = take_unit(s, n, ab, ok);
+            if (idx < 0) break;
             const BwdBlock bk = bwd_block<DET, TOK>(a, idx);
             if (bk.nsteps <= 0) continue;
             tr.item(idx);
@@ -392,7 +424,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             const uint32_t qbytes = tile_bytes + 2 * 128 * 4;                       // Q plus LSE2, D rows
             int q_issued = 0, do_issued = 0, kv_issued = 0;  // copies issued (also the step / block counts)
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+            for (int n = 0; ok; ++n) {
+                const int idx = take_unit(s, n, ab, ok);
+                if (idx < 0) break;
                 const BwdBlock bk = bwd_block<DET, TOK>(a, idx);
                 if (bk.nsteps <= 0) continue;
                 tr.item(idx);
@@ -464,7 +498,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             };
             int gs = 0, nb = 0;  // steps and blocks of earlier blocks
             bool ok = true;
-            for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+            for (int n = 0; ok; ++n) {
+                const int idx = take_unit(s, n, ab, ok);
+                if (idx < 0) break;
                 const int nsteps = bwd_block<DET, TOK>(a, idx).nsteps;
                 if (nsteps <= 0) continue;
                 tr.item(idx);
@@ -530,6 +566,20 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
             tc_commit(&s.drain);
             mbar_wait_quiet(&s.drain, 0);
         }
+    } else if (warp == 3) {
+        // ================= scheduler: hands out the work units =================
+        if (lane == 0) {
+            for (int n = 0;; ++n) {
+                int idx;
+                if constexpr (DET) idx = n == 0 ? (int)blockIdx.x : n_units;
+                else idx = atomicAdd(a.work_counter, 1);
+                const int slot = n % kUnitSlots;
+                if (n >= kUnitSlots && !mbar_wait(&s.unit_empty[slot], ((n / kUnitSlots) - 1) & 1, ab)) break;
+                s.unit[slot] = idx < n_units ? idx : -1;
+                mbar_arrive(&s.unit_full[slot]);
+                if (idx >= n_units) break;
+            }
+        }
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 160;\n" ::: "memory");
@@ -543,7 +593,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         Tracer tr;
         tr.init(warp == 4 ? a.trace : nullptr, 2);
         int gs = 0, nb = 0;  // steps and blocks of earlier blocks
-        for (int idx = blockIdx.x; ok && idx < n_units; idx += gridDim.x) {
+        for (int n = 0; ok; ++n) {
+            const int idx = take_unit(s, n, ab, ok);
+            if (idx < 0) break;
             const BwdBlock bk = bwd_block<DET, TOK>(a, idx);
             if (!bk.live) continue;  // an idle block of a packed batch writes nothing
             tr.item(idx);

@@ -51,6 +51,7 @@ struct FwdArgs {
     float* o_part;     // split mode: [n_splits, rows, d] fp32
     float* lse_part;   // split mode: [n_splits, rows] fp32 (natural log, no sink)
     int* status;
+    int* work_counter; // zeroed by the call: persistent CTAs take item indices from it in turn
     // e4m3 inputs only: per (batch, kv head) factors that turn the stored values into the
     // true ones (x = stored * descale), [B * h_kv] fp32 or null (= 1)
     const float* q_descale;
@@ -111,6 +112,7 @@ struct BwdArgs {
     int* dq_count;         // [h_kv, n_qtiles] dQ contributions landed per query tile, or null:
                            // non-null = deterministic order (key blocks in descending order)
     int* status;
+    int* work_counter;     // zeroed by the call: persistent CTAs take work units from it in turn
     unsigned long long* trace;  // trace builds only: the workspace's trace region (else null)
 };
 
