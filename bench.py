@@ -237,10 +237,14 @@ def run_ours(args):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
     q, k, v, dout = up(w["q"]), up(w["k"]), up(w["v"]), up(w["dout"])
-    kw = dict(causal=w["causal"], window=w["window"], softmax_scale=w["scale"])
+    # sinks and packed offsets for the workloads that have them (one offsets array serves
+    # queries and keys, which are packed alike)
+    sinks = None if w["sinks"] is None else torch.from_numpy(w["sinks"]).to(dev)
+    cu = None if w["cu_q"] is None else torch.from_numpy(w["cu_q"]).to(dev)
+    kw = dict(causal=w["causal"], window=w["window"], softmax_scale=w["scale"], sinks=sinks, cu_q=cu, cu_k=cu)
     o, lse, ws_f = fa.forward(q, k, v, **kw)
-    dq, dk, dv, _, ws_b = fa.backward(q, k, v, o, lse, dout, **kw)
-    grads = (dq, dk, dv, None)
+    dq, dk, dv, dsk, ws_b = fa.backward(q, k, v, o, lse, dout, **kw)
+    grads = (dq, dk, dv, dsk)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -334,7 +338,7 @@ def run_ours(args):
     if "decode" in line:
         # the decode targets' figures once more, compactly, near the end of the line
         line["decode_frac_hbm"] = {n: r.get("frac_hbm") for n, r in line["decode"].items()}
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and not args.no_cpu and w["cu_q"] is None:
         line["cpu_baseline"] = oracle_sample(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -361,6 +365,7 @@ def run_e2e(args, fa, kw, ins, outs, flops, world, dev):
     dev_in = [[torch.empty_like(t) for t in (q, k, v, dout)] for _ in range(2)]
     dev_out = [[torch.empty_like(o), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
                 torch.empty_like(v)] for _ in range(2)]
+    dsk = None if kw.get("sinks") is None else torch.empty_like(kw["sinks"])
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_cmp = [torch.cuda.Event() for _ in range(2)]
@@ -384,7 +389,7 @@ def run_e2e(args, fa, kw, ins, outs, flops, world, dev):
                 qb, kb, vb, dob = dev_in[b]
                 ob, lb, dqb, dkb, dvb = dev_out[b]
                 fa.forward(qb, kb, vb, **kw, out=ob, lse=lb, workspace=ws_f)
-                fa.backward(qb, kb, vb, ob, lb, dob, **kw, workspace=ws_b, grads=(dqb, dkb, dvb, None))
+                fa.backward(qb, kb, vb, ob, lb, dob, **kw, workspace=ws_b, grads=(dqb, dkb, dvb, dsk))
                 ev_cmp[b].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_cmp[b])

@@ -282,11 +282,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     // token mode (TOK): key blocks and query tiles over the packed token axis; never with DET
     constexpr bool tokens = TOK;
     static_assert(!(DET && TOK), "the fixed dQ order uses blocks per sequence");
-    // Persistent: one CTA per SM; its scheduler warp takes work units one at a time from the
-    // call's counter (units are numbered heaviest first, in L2-sized bands for dense batches,
-    // so the CTAs share the work out greedily) and hands them to the other roles through a
-    // small ring.  With the fixed dQ order the launch has one CTA per unit instead (unit =
-    // CTA index), so a CTA waits only on CTAs dispatched before it.  Every role keeps a running
+    // Persistent (a.persist): one CTA per SM, whose scheduler warp walks the work units with a
+    // grid stride (units are numbered heaviest first, in L2-sized bands for dense batches)
+    // and hands them to the other roles through a small ring.  Otherwise the launch has one
+    // CTA per unit (unit = CTA index): always with the fixed dQ order, so that a CTA waits
+    // only on CTAs dispatched before it, and for long causal dense problems, where one unit
+    // per CTA measured faster (the hardware's dispatch of CTAs as SMs free up).  Every role keeps a running
     // count of the steps (query tiles) and blocks it has been through, so that the barrier
     // phases carry on from block to block; two barriers hand a block's resources to the next:
     // dkv_full (the block's last MMAs, which read K and V and finish dK and dV, have
@@ -570,9 +571,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         // ================= scheduler: hands out the work units =================
         if (lane == 0) {
             for (int n = 0;; ++n) {
-                int idx;
-                if constexpr (DET) idx = n == 0 ? (int)blockIdx.x : n_units;
-                else idx = atomicAdd(a.work_counter, 1);
+                // a grid stride over the units (a launch with one CTA per unit takes one)
+                const int idx = (int)blockIdx.x + n * (int)gridDim.x;
                 const int slot = n % kUnitSlots;
                 if (n >= kUnitSlots && !mbar_wait(&s.unit_empty[slot], ((n / kUnitSlots) - 1) & 1, ab)) break;
                 s.unit[slot] = idx < n_units ? idx : -1;
@@ -1321,8 +1321,8 @@ static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const 
     auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd_main_kernel<D, DET, true, TOK> : bwd_main_kernel<D, DET, false, TOK>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    // persistent CTAs (at most one per SM); the fixed dQ order takes one CTA per unit
-    const long n = DET ? (long)a.n_units : (long)a.n_ctas;
+    // persistent CTAs (at most one per SM), or one CTA per unit
+    const long n = (DET || !a.persist) ? (long)a.n_units : (long)a.n_ctas;
     if (n <= 0) return cudaSuccess;
     kernel<<<(unsigned)n, kThreadsBwd, smem, st>>>(a, tq, tk, tv, tdo);
     return cudaGetLastError();

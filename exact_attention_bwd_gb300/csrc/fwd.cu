@@ -28,8 +28,8 @@
 // edge evaluate the mask per element.
 //
 // Scheduling is persistent: one CTA per SM walks the work items (a key/value head's two
-// query tiles, and a key range in split mode), numbered heaviest first and taken one at a
-// time from a counter in the workspace, so the long items go first and the CTAs even out;
+// query tiles, and a key range in split mode) in heaviest-first order with a grid stride
+// (alternating direction from round to round under a causal mask, see first_step);
 // a packed batch's items are found by binary search over its offsets (dew-flash-attn PyPI
 // page, "Packed sequences"), and idle items cost only their decode.  When the queries and
 // keys are packed alike (cu_seqlens_q and cu_seqlens_k the same array) the query tiles run
@@ -356,18 +356,15 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
     } else if (warp == 3) {
         // ================= tile scheduler =================
-        // Takes the next item index from the call's work counter (items are numbered heaviest
-        // first, so the CTAs share the work out greedily, the long items first) and hands each
-        // live item to the other roles through the item ring: lane 0 writes the item, every
+        // Walks the CTA's items (a grid stride, alternating direction under `snake`; taking
+        // items from a shared counter instead measured slower on most shapes) and hands each
+        // live one to the other roles through the item ring: lane 0 writes the item, every
         // lane the allowed key interval of 8 of its 256 rows.  In token mode the key-tile ranges
         // come from those intervals (their hull), since a tile's rows may span sequences.
         int n = 0;
         bool ok = true;
-        while (true) {
-            int idx = 0;
-            if (lane == 0) idx = atomicAdd(a.work_counter, 1);
-            idx = __shfl_sync(0xffffffffu, idx, 0);
-            if (idx >= a.n_items) break;
+        for (int idx = blockIdx.x, step = first_step(a.snake); idx < a.n_items;
+             idx += step, step = 2 * (int)gridDim.x - step) {
             FwdItem w = fwd_item(a, idx);
             if (!w.live) continue;
             const int slot = n % kItemSlots;

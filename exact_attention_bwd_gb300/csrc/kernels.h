@@ -51,7 +51,6 @@ struct FwdArgs {
     float* o_part;     // split mode: [n_splits, rows, d] fp32
     float* lse_part;   // split mode: [n_splits, rows] fp32 (natural log, no sink)
     int* status;
-    int* work_counter; // zeroed by the call: persistent CTAs take item indices from it in turn
     // e4m3 inputs only: per (batch, kv head) factors that turn the stored values into the
     // true ones (x = stored * descale), [B * h_kv] fp32 or null (= 1)
     const float* q_descale;
@@ -97,6 +96,7 @@ struct BwdArgs {
                            // tiles run over the packed token axis (d <= 128 kernel)
     int n_units;           // work units (key blocks x kv heads [x batch])
     int n_ctas;            // persistent CTAs of the d <= 128 main kernel (at most one per SM)
+    int persist;           // 1: n_ctas persistent CTAs walk the units; 0: one CTA per unit
     // 16-bit tensors hold bf16 or fp16 (Problem::dtype) like the inputs
     const uint16_t* o;
     const float* lse;
@@ -112,7 +112,6 @@ struct BwdArgs {
     int* dq_count;         // [h_kv, n_qtiles] dQ contributions landed per query tile, or null:
                            // non-null = deterministic order (key blocks in descending order)
     int* status;
-    int* work_counter;     // zeroed by the call: persistent CTAs take work units from it in turn
     unsigned long long* trace;  // trace builds only: the workspace's trace region (else null)
 };
 
