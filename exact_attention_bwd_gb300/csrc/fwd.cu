@@ -60,10 +60,7 @@ struct FwdCfg {
     static constexpr int CHUNK_BYTES = 128 * 128;       // one [128 rows][64 cols] chunk
     static constexpr int STAGES = (D == 64) ? 4 : 2;
     static constexpr int TMEM_COLS = 512;
-    // O buffers per query tile: at d = 64 an O tile takes 64 columns, so each tile has two
-    // and an item's epilogue can run after the next item has started on the other
-    static constexpr int NOB = D == 64 ? 2 : 1;
-    // TMEM columns: S_k at 128k, O_k (buffer b) at 256 + 128k + 64b
+    // TMEM columns: S_k at 128k, O_k at 256 + 128k
 };
 
 // One decoded work item, as the scheduler warp hands it to the other roles.
@@ -86,13 +83,12 @@ struct __align__(1024) FwdSmem {
     uint64_t q_full;
     uint64_t k_full[FwdCfg<D>::STAGES], k_empty[FwdCfg<D>::STAGES];
     uint64_t v_full[FwdCfg<D>::STAGES], v_empty[FwdCfg<D>::STAGES];
-    uint64_t s_full[2], p_full[2], o_full[2][FwdCfg<D>::NOB], o_free[2][FwdCfg<D>::NOB];
+    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
     uint64_t q_empty;
     uint64_t drain;
     uint64_t item_full[kItemSlots], item_empty[kItemSlots];
     ItemInfo item[kItemSlots];
     int2 band[kItemSlots][2][128];  // (jlo, jhi) of every row of both query tiles
-    float3 pend[256];               // softmax thread t: (m, l, sink) of its item whose epilogue waits
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -124,10 +120,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         for (int k = 0; k < 2; ++k) {
             mbar_init(&s.s_full[k], 1);
             mbar_init(&s.p_full[k], 4);  // one arrive per softmax warp
-            for (int b = 0; b < C::NOB; ++b) {
-                mbar_init(&s.o_full[k][b], 1);
-                mbar_init(&s.o_free[k][b], 4);  // one arrive per softmax warp
-            }
+            mbar_init(&s.o_full[k], 1);
+            mbar_init(&s.o_free[k], 4);  // one arrive per softmax warp
         }
         mbar_init(&s.q_empty, 1);
         mbar_init(&s.drain, 1);
@@ -243,7 +237,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 mma_ts_lin_mn_x8(tmem + ocol, tmem + pcol, vd, idO, acc0);
             };
             uint32_t pc0 = 0, pc1 = 0;  // P tiles consumed per query tile
-            uint32_t oc0 = 0, oc1 = 0;  // O tiles started per query tile (buffer oc % NOB)
+            uint32_t oc0 = 0, oc1 = 0;  // O tiles completed per query tile (o_full commits)
             int gt = 0, n_q = 0;        // key tiles, items consumed
             bool ok = true;
             for (int n = 0; ok; ++n) {
@@ -298,15 +292,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         ++pc0;
                         // the first P V of the item overwrites O_0: the previous item's
                         // epilogue must have read it
-                        // the first P V of the item overwrites its O buffer: the epilogue of the
-                        // buffer's previous use must have read it
-                        if (ok && j == ta0 && oc0 >= (uint32_t)C::NOB)
-                            ok = twait(tr, kBOFree, &s.o_free[0][oc0 % C::NOB], (oc0 / C::NOB - 1) & 1, ab);
+                        if (ok && j == ta0 && oc0 > 0) ok = twait(tr, kBOFree, &s.o_free[0], (oc0 - 1) & 1, ab);
                         tc_fence_after();
                         if (ok) {
-                            issue_pv(256 + 64 * (oc0 % C::NOB), 0, vd, j > ta0 ? 1u : 0u);
+                            issue_pv(256, 0, vd, j > ta0 ? 1u : 0u);
                             if (j == ta1 - 1) {
-                                tc_commit(&s.o_full[0][oc0 % C::NOB]);
+                                tc_commit(&s.o_full[0]);
                                 ++oc0;
                             }
                         }
@@ -324,13 +315,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     if (ok && j >= tb0 && j < tb1) {
                         ok = twait(tr, kBPFull, &s.p_full[1], pc1 & 1, ab);
                         ++pc1;
-                        if (ok && j == tb0 && oc1 >= (uint32_t)C::NOB)
-                            ok = twait(tr, kBOFree, &s.o_free[1][oc1 % C::NOB], (oc1 / C::NOB - 1) & 1, ab);
+                        if (ok && j == tb0 && oc1 > 0) ok = twait(tr, kBOFree, &s.o_free[1], (oc1 - 1) & 1, ab);
                         tc_fence_after();
                         if (ok) {
-                            issue_pv(384 + 64 * (oc1 % C::NOB), 128, vd, j > tb0 ? 1u : 0u);
+                            issue_pv(384, 128, vd, j > tb0 ? 1u : 0u);
                             if (j == tb1 - 1) {
-                                tc_commit(&s.o_full[1][oc1 % C::NOB]);
+                                tc_commit(&s.o_full[1]);
                                 ++oc1;
                             }
                         }
@@ -459,108 +449,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
         const uint32_t tS = tmem + lane_base + 128 * k;
-        const uint32_t tO0 = tmem + lane_base + 256 + 128 * k;  // O buffer 0 of this tile
+        const uint32_t tO = tmem + lane_base + 256 + 128 * k;
         const float c = p.scale_log2;
-        uint32_t scount = 0;  // S tiles received (carried across items)
-        uint32_t ostart = 0;  // O tiles started (items with a key tile): buffer ostart % NOB
+        uint32_t scount = 0, ocount = 0;  // S tiles and O tiles received (carried across items)
         bool ok = true;
         Tracer tr;
         tr.init((warp & 3) == 0 ? a.trace : nullptr, 2 + k);
-        // The epilogue of an item: O / l (with the sink) to the outputs, LSE, then the item
-        // slot goes back to the scheduler.  With two O buffers (d = 64) it runs one item late,
-        // after the next item's first P: the next item's P V writes the other buffer, so
-        // waiting for the last P V and storing O overlap the next item's start.
-        struct Pending {
-            int slot;
-            int ouse;  // this tile's O use of the item (-1: no key tile)
-            float m, l, sink2;
-        };
-        // the item whose epilogue waits (d = 64): its slot and O use packed in one register,
-        // (m, l, sink) in shared memory; -1 = none
-        int pend_id = -1;
-        float3* const pend_row = &s.pend[tid - 128];
-        auto finish = [&](const Pending& e) {
-            const ItemInfo& itm = s.item[e.slot];
-            const SeqView sv{itm.b, itm.q0, 0, 0, 0, 0};
-            const int g = itm.g, split = itm.split;
-            const int i = itm.s0[k] + r / p.G;  // query position (a packed row in token mode)
-            const int h = g * p.G + r % p.G;    // query head
-            const bool row_valid = s.band[e.slot][k][r].x != kNoRow;
-            const int ob = e.ouse >= 0 ? e.ouse % C::NOB : 0;
-            bool have = e.ouse >= 0 && ok;  // uniform over the warp group
-            if (have) {
-                const bool wt = twait(tr, kBOFull, &s.o_full[k][ob], (e.ouse / C::NOB) & 1, ab);
-                have = __all_sync(0xffffffffu, wt);
-                if (!have) ok = false;
-                tc_fence_after();
-            }
-            const bool split_mode = a.n_splits > 1;
-            float oscale = 0.f, lse = -INFINITY;
-            if (!split_mode && p.sinks && row_valid) {
-                const float mf = fmaxf(e.m, e.sink2);
-                const float wgt = (e.m == -INFINITY) ? 0.f : ex2(e.m - mf);
-                const float lt = e.l * wgt + ex2(e.sink2 - mf);
-                oscale = wgt / lt;
-                lse = (mf + log2f(lt)) * kLn2;
-            } else if (e.l > 0.f) {
-                oscale = 1.f / e.l;
-                lse = (e.m + log2f(e.l)) * kLn2;
-            }
-            const long nrows = (long)p.B * p.h_q * p.s_q;
-            const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;  // split-mode row (dense only)
-            if (row_valid) {
-                if (!split_mode) {
-                    if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
-                } else {
-                    a.lse_part[(long)split * nrows + prow] = lse;
-                }
-            }
-            if (have) {
-                // the whole O row into registers (warp-collective TMEM reads), then the buffer
-                // is free for a later item's P V while the row is scaled and stored
-                uint32_t orr[D];
-                if constexpr (D == 128) tmem_ld_32x32b_x128(tO0, orr);
-                else tmem_ld_32x32b_x64(tO0 + 64 * ob, orr);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.o_free[k][ob]);
-                if (row_valid) {
-                    if (!split_mode) {
-                        uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
-#pragma unroll
-                        for (int t = 0; t < D / 8; ++t) {
-                            uint4 wv;
-                            wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
-                            wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
-                            wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
-                            wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
-                            orow[t] = wv;
-                        }
-                    } else {
-                        float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
-#pragma unroll
-                        for (int t = 0; t < D / 4; ++t)
-                            op[t] = make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
-                                                __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
-                    }
-                }
-                tr.mark(kMEpilogueDone);
-            } else if (row_valid) {
-                // no key tile (or a failed wait): zero rows
-                if (!split_mode) {
-                    uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
-#pragma unroll
-                    for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(0, 0, 0, 0);
-                } else {
-                    float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
-#pragma unroll
-                    for (int t = 0; t < D / 4; ++t) op[t] = make_float4(0, 0, 0, 0);
-                }
-            }
-            // the item slot is read for the last time: hand it back to the scheduler
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.item_empty[e.slot]);
-        };
         for (int n = 0; ok; ++n) {
         // the item comes decoded from the scheduler warp; only the loop bounds, the row's key
         // band and its sink stay live across the key loop, the epilogue reads the rest again
@@ -582,9 +476,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         float sink2 = 0.f;
         if (p.sinks && a.n_splits == 1 && jlo != kNoRow) sink2 = p.sinks[s.item[slot].g * p.G + r % p.G] * kLog2e;
         float m_used = -INFINITY, l = 0.f;
-        const int ouse = my_t1 > my_t0 ? (int)ostart : -1;  // this item's O use, if any
-        const uint32_t tO = tO0 + 64 * (ouse >= 0 ? ouse % C::NOB : 0);
-        if (ouse >= 0) ++ostart;
         for (int j = my_t0; j < my_t1; ++j) {
             const bool w = twait(tr, kBSFull, &s.s_full[k], scount & 1, ab);
             if (!__all_sync(0xffffffffu, w)) {
@@ -668,28 +559,88 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.p_full[k]);
             tr.mark(kMSoftmaxDone);
-            if (C::NOB > 1 && pend_id >= 0) {
-                const float3 v = *pend_row;
-                finish(Pending{pend_id & 15, (pend_id >> 4) - 1, v.x, v.y, v.z});
-                pend_id = -1;
-            }
         }
         // ---------------- epilogue ----------------
-        if constexpr (C::NOB > 1) {
-            if (pend_id >= 0) {  // an item without key tiles left the previous one pending
-                const float3 v = *pend_row;
-                finish(Pending{pend_id & 15, (pend_id >> 4) - 1, v.x, v.y, v.z});
+        const ItemInfo& itm = s.item[slot];
+        const SeqView sv{itm.b, itm.q0, 0, 0, 0, 0};
+        const int g = itm.g, split = itm.split;
+        const int i = itm.s0[k] + r / p.G;  // query position (a packed row in token mode)
+        const int h = g * p.G + r % p.G;    // query head
+        const bool row_valid = jlo != kNoRow;
+        const bool has_o = my_t1 > my_t0;  // uniform over the warp group
+        if (has_o && ok) {
+            const bool wt = twait(tr, kBOFull, &s.o_full[k], ocount & 1, ab);
+            ++ocount;
+            ok = __all_sync(0xffffffffu, wt);
+            tc_fence_after();
+        }
+        const bool split_mode = a.n_splits > 1;
+        float oscale = 0.f, lse = -INFINITY;
+        if (!split_mode && p.sinks && row_valid) {
+            const float s2 = sink2;
+            const float mf = fmaxf(m_used, s2);
+            const float wgt = (m_used == -INFINITY) ? 0.f : ex2(m_used - mf);
+            const float lt = l * wgt + ex2(s2 - mf);
+            oscale = wgt / lt;
+            lse = (mf + log2f(lt)) * kLn2;
+        } else if (l > 0.f) {
+            oscale = 1.f / l;
+            lse = (m_used + log2f(l)) * kLn2;
+        }
+        const long nrows = (long)p.B * p.h_q * p.s_q;
+        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;  // split-mode row (dense only)
+        if (row_valid) {
+            if (!split_mode) {
+                if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
+            } else {
+                a.lse_part[(long)split * nrows + prow] = lse;
             }
-            *pend_row = make_float3(m_used, l, sink2);
-            pend_id = slot | ((ouse + 1) << 4);
-        } else {
-            finish(Pending{slot, ouse, m_used, l, sink2});
         }
+        if (has_o && ok) {
+            // the whole O row into registers (warp-collective TMEM reads), then O_k is free for
+            // the next item's P V while the row is scaled and stored; only valid rows store
+            uint32_t orr[D];
+            if constexpr (D == 128) tmem_ld_32x32b_x128(tO, orr);
+            else tmem_ld_32x32b_x64(tO, orr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.o_free[k]);
+            if (row_valid) {
+                if (!split_mode) {
+                    uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
+#pragma unroll
+                    for (int t = 0; t < D / 8; ++t) {
+                        uint4 wv;
+                        wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
+                        wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
+                        wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
+                        wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
+                        orow[t] = wv;
+                    }
+                } else {
+                    float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
+#pragma unroll
+                    for (int t = 0; t < D / 4; ++t)
+                        op[t] = make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
+                                            __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
+                }
+            }
+            tr.mark(kMEpilogueDone);
+        } else if (row_valid) {
+            if (!split_mode) {
+                uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
+#pragma unroll
+                for (int t = 0; t < D / 8; ++t) reinterpret_cast<uint4*>(orow)[t] = make_uint4(0, 0, 0, 0);
+            } else {
+                float* op = a.o_part + ((long)split * nrows + prow) * D;
+#pragma unroll
+                for (int t = 0; t < D / 4; ++t) reinterpret_cast<float4*>(op)[t] = make_float4(0, 0, 0, 0);
+            }
+        }
+        // the item slot is read for the last time: hand it back to the scheduler
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.item_empty[slot]);
         }  // items
-        if (C::NOB > 1 && pend_id >= 0) {
-            const float3 v = *pend_row;
-            finish(Pending{pend_id & 15, (pend_id >> 4) - 1, v.x, v.y, v.z});
-        }
     }
 
     tc_fence_before();

@@ -97,11 +97,12 @@ __device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity
 
 // Waits for the phase with the given parity to complete.  Returns false (and raises
 // the CTA's abort) when the limit passes or another wait of the CTA already gave up.
-// Each try suspends the thread for at most about the limit (the hardware's own suspension
-// limit could outlast a short one), and resumes it as soon as the phase completes.
+// The first try is the plain one (the hardware picks how long it suspends; most waits end
+// there).  The retries suspend for at most about the limit each, so that a short limit is
+// not outlasted by one hardware suspension.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab) {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint32_t hint = ab.limit < 0xFFFFFFFFull ? (uint32_t)ab.limit : 0xFFFFFFFFu;
-    if (mbar_try_wait_for(bar, parity, hint)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
         if (mbar_try_wait_for(bar, parity, hint)) return true;
