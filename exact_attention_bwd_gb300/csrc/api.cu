@@ -195,6 +195,7 @@ struct FwdPlan {
     int n_blocks = 0, n_splits = 1, split_tiles = 0;
     int unit_major = 0;
     int tokens = 0;        // packed batch with cu_seqlens_q == cu_seqlens_k: token tiles
+    int kt = 128;          // keys per key tile of the d <= 128 kernel (64: two CTAs per SM)
     size_t part_rows = 0;  // rows of the split partials
     int s_pad = 0;         // e4m3: keys per V^T row (s_kv rounded up to 16)
     size_t off_vt = 0;     // e4m3: workspace offset of V^T
@@ -285,6 +286,13 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
     } else {
         pl.n_blocks = p.T_q / rows_per_cta + p.B;
     }
+    // d = 64 under a narrow band (windows on both sides, a causal mask counting as a right
+    // window of 0; a query tile's allowed keys span at most 384): an item sees a few key
+    // tiles and its chain of waits sets the pace, so take 64-key tiles and run two CTAs per
+    // SM (twice the query tiles in flight)
+    if (p.d == 64 && p.dtype != FA_DTYPE_E4M3 && pl.n_splits == 1 && p.left >= 0 && p.right >= 0 &&
+        (long)p.left + p.right + p.P <= 384)
+        pl.kt = 64;
     if (p.dtype == FA_DTYPE_E4M3) {  // V^T [B][h_kv][d][s_pad] after the partials
         pl.s_pad = (p.s_kv + 15) / 16 * 16;
         pl.off_vt = pl.ws_bytes;
@@ -443,7 +451,7 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     const int tokens_k = p.cu_q ? p.T_k : p.s_kv;
     const int bdim = p.cu_q ? 1 : p.B;
     CUtensorMap tk, tv;
-    const int kv_box = (pl.path == FwdPath::kDecode || p.d >= 192) ? 64 : 128;
+    const int kv_box = (pl.path == FwdPath::kDecode || p.d >= 192) ? 64 : pl.kt;
     // a paged cache is a [num_pages][page_size][h_kv][d] pool: the map's key and outer
     // dimensions are the row within a page and the page
     const int kv_rows = p.block_table ? p.page_size : tokens_k;
@@ -513,10 +521,12 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.split_tiles = pl.split_tiles;
     a.unit_major = pl.unit_major;
     a.tokens = pl.tokens;
+    a.kt = pl.kt;
     {
         const long items = p.cu_q ? (long)pl.n_blocks * p.h_kv : (long)pl.n_blocks * pl.n_splits * p.h_kv * p.B;
+        const long slots = (long)sm_count() * (pl.kt == 64 ? 2 : 1);
         a.n_items = (int)items;
-        a.n_ctas = (int)(items < sm_count() ? items : sm_count());
+        a.n_ctas = (int)(items < slots ? items : slots);
         a.snake = (!p.cu_q && p.causal && !pl.unit_major) ? 1 : 0;
     }
     a.o = reinterpret_cast<uint16_t*>(o);

@@ -53,14 +53,30 @@ constexpr int kThreadsFwd = 384;
 // of every 4 column pairs of an unmasked tile, this many take the polynomial exp2
 constexpr int kExpPolyPairs = FA_FWD_EXP_POLY_PAIRS;
 
-template <int D>
+// KT keys per key tile: 128, or 64 at d = 64 for narrow bands (sliding windows), where an
+// item sees only a few key tiles and its chain of waits, not the tensor pipe, sets the pace.
+// With 64-key tiles the tensor memory of a CTA halves to 256 columns and its shared memory
+// to about 100 KB, so two CTAs share an SM and twice as many query tiles are in flight.
+template <int D, int KT>
 struct FwdCfg {
+    static_assert(KT == 128 || (KT == 64 && D == 64), "64-key tiles only at d = 64");
     static constexpr int KCH = D / 64;                  // 64-column chunks of a row
-    static constexpr int TILE_BYTES = 128 * D * 2;      // one Q / K / V tile (128 rows)
-    static constexpr int CHUNK_BYTES = 128 * 128;       // one [128 rows][64 cols] chunk
+    static constexpr int TILE_BYTES = 128 * D * 2;      // one Q tile (128 rows)
+    static constexpr int CHUNK_BYTES = 128 * 128;       // one [128 rows][64 cols] chunk of Q
+    static constexpr int KV_BYTES = KT * D * 2;         // one K / V tile (KT rows)
+    static constexpr int KV_CHUNK = KT * 128;           // one [KT rows][64 cols] chunk of K / V
     static constexpr int STAGES = (D == 64) ? 4 : 2;
-    static constexpr int TMEM_COLS = 512;
-    // TMEM columns: S_k at 128k, O_k at 256 + 128k
+    static constexpr int TMEM_COLS = KT == 128 ? 512 : 256;
+    static constexpr int CTAS_PER_SM = KT == 128 ? 1 : 2;
+    // TMEM columns: S_k at KT k (P_k is written over its first KT / 2), O_k at 2 KT + OW k
+    static constexpr int OW = KT == 128 ? 128 : D;
+    __host__ __device__ static constexpr uint32_t s_col(int k) { return (uint32_t)(KT * k); }
+    __host__ __device__ static constexpr uint32_t o_col(int k) { return (uint32_t)(2 * KT + OW * k); }
+    // registers per thread after setmaxnreg: producer / MMA / TMEM owner / scheduler group,
+    // and the two softmax groups; 128 REG_LOW + 256 REG_HIGH stays within what the CTA is
+    // launched with (checked before every launch)
+    static constexpr int REG_LOW = KT == 128 ? 56 : 48;
+    static constexpr int REG_HIGH = KT == 128 ? 224 : 96;
 };
 
 // One decoded work item, as the scheduler warp hands it to the other roles.
@@ -75,14 +91,15 @@ constexpr int kItemSlots = 3;
 // arrivals that free an item slot: producer, MMA issuer and the eight softmax warps
 constexpr int kItemReaders = 10;
 
-template <int D>
+template <int D, int KT>
 struct __align__(1024) FwdSmem {
-    uint8_t q[2][FwdCfg<D>::TILE_BYTES];
-    uint8_t k[FwdCfg<D>::STAGES][FwdCfg<D>::TILE_BYTES];
-    uint8_t v[FwdCfg<D>::STAGES][FwdCfg<D>::TILE_BYTES];
+    using C = FwdCfg<D, KT>;
+    uint8_t q[2][C::TILE_BYTES];
+    uint8_t k[C::STAGES][C::KV_BYTES];
+    uint8_t v[C::STAGES][C::KV_BYTES];
     uint64_t q_full;
-    uint64_t k_full[FwdCfg<D>::STAGES], k_empty[FwdCfg<D>::STAGES];
-    uint64_t v_full[FwdCfg<D>::STAGES], v_empty[FwdCfg<D>::STAGES];
+    uint64_t k_full[C::STAGES], k_empty[C::STAGES];
+    uint64_t v_full[C::STAGES], v_empty[C::STAGES];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
     uint64_t q_empty;
     uint64_t drain;
@@ -93,13 +110,14 @@ struct __align__(1024) FwdSmem {
     int abort_flag;
 };
 
-template <int D, bool F16>
-__global__ void __launch_bounds__(kThreadsFwd, 1)
+template <int D, bool F16, int KT>
+__global__ void __launch_bounds__(kThreadsFwd, FwdCfg<D, KT>::CTAS_PER_SM)
     fwd_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, KT>;
     extern __shared__ uint8_t smem_raw[];
-    FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    FwdSmem<D, KT>& s =
+        *reinterpret_cast<FwdSmem<D, KT>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Problem& p = a.p;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -147,11 +165,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-    // registers: 384 x 168 at launch; the producer/MMA group hands part of its share to
-    // the two softmax groups (128 x 56 + 256 x 224 = 64512).  The change is made
-    // at the top of each warp group's branch so the register allocator sees it on every path.
+    // registers: 384 x 168 at launch (one CTA per SM; 384 x 80 with two); the producer/MMA
+    // group hands part of its share to the two softmax groups (128 x 56 + 256 x 224 = 64512;
+    // 128 x 48 + 256 x 96 = 30720).  The change is made at the top of each warp group's
+    // branch so the register allocator sees it on every path.
     if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" :: "n"(C::REG_LOW) : "memory");
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
@@ -187,16 +206,16 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     const int st = gt % C::STAGES;
                     const uint32_t ph = (gt / C::STAGES) & 1;
                     int krow, kouter;
-                    kv_tile_coord(p, sv, j * BN, krow, kouter);
+                    kv_tile_coord(p, sv, j * KT, krow, kouter);
                     if (!(ok = twait(tr, kBKEmpty, &s.k_empty[st], ph ^ 1, ab))) break;
-                    mbar_expect_tx(&s.k_full[st], C::TILE_BYTES);
+                    mbar_expect_tx(&s.k_full[st], C::KV_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
-                        tma_load_4d(&s.k[st][c * C::CHUNK_BYTES], &tmk, &s.k_full[st], c * 64, g, krow, kouter);
+                        tma_load_4d(&s.k[st][c * C::KV_CHUNK], &tmk, &s.k_full[st], c * 64, g, krow, kouter);
                     ++k_issued;
                     if (!(ok = twait(tr, kBVEmpty, &s.v_empty[st], ph ^ 1, ab))) break;
-                    mbar_expect_tx(&s.v_full[st], C::TILE_BYTES);
+                    mbar_expect_tx(&s.v_full[st], C::KV_BYTES);
                     for (int c = 0; c < C::KCH; ++c)
-                        tma_load_4d(&s.v[st][c * C::CHUNK_BYTES], &tmv, &s.v_full[st], c * 64, g, krow, kouter);
+                        tma_load_4d(&s.v[st][c * C::KV_CHUNK], &tmv, &s.v_full[st], c * 64, g, krow, kouter);
                     ++v_issued;
                 }
             }
@@ -220,21 +239,22 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         if (lane == 0) {
             Tracer tr;
             tr.init(a.trace, 1);
-            constexpr uint32_t idS = idesc_16(128, BN, false, false, F16);
+            constexpr uint32_t idS = idesc_16(128, KT, false, false, F16);
             constexpr uint32_t idO = idesc_16(128, D, false, true, F16);
-            constexpr uint32_t kStageStep = (uint32_t)C::TILE_BYTES >> 4;  // descriptor units per stage
+            constexpr uint32_t kStageStep = (uint32_t)C::KV_BYTES >> 4;  // descriptor units per stage
             // a descriptor's start-address field is addr >> 4 in its low bits, so stepping
             // through a tile is a plain add to a base descriptor (no carry: addr < 256 KB)
             const uint64_t qd0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
             const uint64_t qd1 = sdesc_sw128(smem_u32(s.q[1]), 16, 1024);
             const uint64_t kd_base = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
-            const uint64_t vd_base = sdesc_sw128(smem_u32(s.v[0]), C::CHUNK_BYTES, 1024);
+            const uint64_t vd_base = sdesc_sw128(smem_u32(s.v[0]), C::KV_CHUNK, 1024);
             auto issue_s = [&](uint64_t qd, uint32_t scol, uint64_t kd) {
                 if constexpr (D == 128) mma_ss_kk16_x8(tmem + scol, qd, kd, idS, 0u);
                 else mma_ss_kk16_x4(tmem + scol, qd, kd, idS, 0u);
             };
             auto issue_pv = [&](uint32_t ocol, uint32_t pcol, uint64_t vd, uint32_t acc0) {
-                mma_ts_lin_mn_x8(tmem + ocol, tmem + pcol, vd, idO, acc0);
+                if constexpr (KT == 128) mma_ts_lin_mn_x8(tmem + ocol, tmem + pcol, vd, idO, acc0);
+                else mma_ts_lin_mn_x4(tmem + ocol, tmem + pcol, vd, idO, acc0);
             };
             uint32_t pc0 = 0, pc1 = 0;  // P tiles consumed per query tile
             uint32_t oc0 = 0, oc1 = 0;  // O tiles completed per query tile (o_full commits)
@@ -263,11 +283,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         tc_fence_after();
                         const uint64_t kd0 = kd_base + (uint64_t)(st0 * kStageStep);
                         if (u0 >= ta0 && u0 < ta1) {
-                            issue_s(qd0, 0, kd0);
+                            issue_s(qd0, C::s_col(0), kd0);
                             tc_commit(&s.s_full[0]);
                         }
                         if (u0 >= tb0 && u0 < tb1) {
-                            issue_s(qd1, 128, kd0);
+                            issue_s(qd1, C::s_col(1), kd0);
                             tc_commit(&s.s_full[1]);
                         }
                         tc_commit(&s.k_empty[st0]);
@@ -295,7 +315,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         if (ok && j == ta0 && oc0 > 0) ok = twait(tr, kBOFree, &s.o_free[0], (oc0 - 1) & 1, ab);
                         tc_fence_after();
                         if (ok) {
-                            issue_pv(256, 0, vd, j > ta0 ? 1u : 0u);
+                            issue_pv(C::o_col(0), C::s_col(0), vd, j > ta0 ? 1u : 0u);
                             if (j == ta1 - 1) {
                                 tc_commit(&s.o_full[0]);
                                 ++oc0;
@@ -307,7 +327,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         tc_fence_after();
                         k_ready = true;
                         if (ok) {
-                            issue_s(qd0, 0, kd1);
+                            issue_s(qd0, C::s_col(0), kd1);
                             tc_commit(&s.s_full[0]);
                         }
                     }
@@ -318,7 +338,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                         if (ok && j == tb0 && oc1 > 0) ok = twait(tr, kBOFree, &s.o_free[1], (oc1 - 1) & 1, ab);
                         tc_fence_after();
                         if (ok) {
-                            issue_pv(384, 128, vd, j > tb0 ? 1u : 0u);
+                            issue_pv(C::o_col(1), C::s_col(1), vd, j > tb0 ? 1u : 0u);
                             if (j == tb1 - 1) {
                                 tc_commit(&s.o_full[1]);
                                 ++oc1;
@@ -332,7 +352,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                             k_ready = true;
                         }
                         if (ok) {
-                            issue_s(qd1, 128, kd1);
+                            issue_s(qd1, C::s_col(1), kd1);
                             tc_commit(&s.s_full[1]);
                         }
                     }
@@ -365,7 +385,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         bool ok = true;
         for (int idx = blockIdx.x, step = first_step(a.snake); idx < a.n_items;
              idx += step, step = 2 * (int)gridDim.x - step) {
-            FwdItem w = fwd_item(a, idx);
+            FwdItem w = fwd_item(a, idx, KT);
             if (!w.live) continue;
             const int slot = n % kItemSlots;
             if (n >= kItemSlots) {
@@ -392,8 +412,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 if (a.tokens) {
                     lo_min = __reduce_min_sync(0xffffffffu, lo_min);
                     hi_max = __reduce_max_sync(0xffffffffu, hi_max);
-                    w.ti[k].t0 = lo_min <= hi_max ? lo_min / BN : 0;
-                    w.ti[k].t1 = lo_min <= hi_max ? hi_max / BN + 1 : 0;
+                    w.ti[k].t0 = lo_min <= hi_max ? lo_min / KT : 0;
+                    w.ti[k].t1 = lo_min <= hi_max ? hi_max / KT + 1 : 0;
                 }
             }
             if (a.tokens) {
@@ -443,13 +463,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         }
     }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" :: "n"(C::REG_HIGH) : "memory");
         // ================= softmax: one thread per row =================
         const int k = (warp - 4) >> 2;           // query tile
         const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-        const uint32_t tS = tmem + lane_base + 128 * k;
-        const uint32_t tO = tmem + lane_base + 256 + 128 * k;
+        const uint32_t tS = tmem + lane_base + C::s_col(k);
+        const uint32_t tO = tmem + lane_base + C::o_col(k);
         const float c = p.scale_log2;
         uint32_t scount = 0, ocount = 0;  // S tiles and O tiles received (carried across items)
         bool ok = true;
@@ -484,18 +504,19 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             }
             ++scount;
             tc_fence_after();
-            // one TMEM read of the whole S row (128 fp32 columns)
-            const int j0 = j * BN;
-            const bool edge = (j0 < jlo || j0 + BN - 1 > jhi);
-            uint32_t sr[128];
-            tmem_ld_32x32b_x128(tS, sr);
+            // one TMEM read of the whole S row (KT fp32 columns)
+            const int j0 = j * KT;
+            const bool edge = (j0 < jlo || j0 + KT - 1 > jhi);
+            uint32_t sr[KT];
+            if constexpr (KT == 128) tmem_ld_32x32b_x128(tS, sr);
+            else tmem_ld_32x32b_x64(tS, sr);
             if (edge) {
                 // the row's allowed columns [lo, hi] of this tile (a row without keys has
-                // lo > 127 and hi < 0) as a bit mask per 32-column chunk, applied without
+                // lo > KT - 1 and hi < 0) as a bit mask per 32-column chunk, applied without
                 // branches: one bit test and one select per element
                 const int lo = jlo - j0, hi = jhi - j0;
 #pragma unroll
-                for (int cb = 0; cb < BN; cb += 32) {
+                for (int cb = 0; cb < KT; cb += 32) {
                     const int c0 = max(lo - cb, 0), c1 = min(hi - cb, 31);
                     const uint32_t keep = c0 > c1 ? 0u : (0xffffffffu >> (31 - c1)) & (0xffffffffu << c0);
 #pragma unroll
@@ -505,7 +526,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             }
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int cc = 0; cc < BN; cc += 4) {
+            for (int cc = 0; cc < KT; cc += 4) {
                 mx0 = max3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
                 mx1 = max3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
             }
@@ -520,8 +541,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 l *= alpha;
                 rescale = true;
             }
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O_k row *= alpha (warp-wide TMEM access; alpha = 1 on the other lanes)
+            // O_k row *= alpha (warp-wide TMEM access; alpha = 1 on the other lanes); with
+            // 64-key tiles after P is out of the registers (the softmax has fewer of them), the
+            // P V that accumulates into O_k waits for p_full below
+            auto rescale_o = [&]() {
 #pragma unroll
                 for (int cb = 0; cb < D; cb += 32) {
                     uint32_t orr[32];
@@ -530,7 +553,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                     for (int t = 0; t < 32; ++t) orr[t] = __float_as_uint(__uint_as_float(orr[t]) * alpha);
                     tmem_st_32x32b_x32(tO + cb, orr);
                 }
-            }
+            };
+            if (KT == 128 && __any_sync(0xffffffffu, rescale)) rescale_o();
             // P = exp2(S*c - m) as 16-bit pairs (the inputs' type), packed in place (slot cc/2 is already consumed).
             // On tiles without masked entries a fraction of the exponentials runs on the FMA
             // pipe (exp2_poly2) to share the load with the MUFU unit.
@@ -539,7 +563,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             const float2 c2 = make_float2(c, c), nb2 = make_float2(-base, -base);
             float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int cc = 0; cc < BN; cc += 2) {
+            for (int cc = 0; cc < KT; cc += 2) {
                 float2 xv = __ffma2_rn(make_float2(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), c2, nb2);
                 float2 pv;
                 if (kExpPolyPairs > 0 && ((cc >> 1) & 3) < kExpPolyPairs && poly_ok) {
@@ -553,8 +577,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 sr[cc / 2] = pack16<F16>(pv.x, pv.y);
             }
             const float sum = sum2.x + sum2.y;
-            tmem_st_32x32b_x64(tS, sr);
+            if constexpr (KT == 128) tmem_st_32x32b_x64(tS, sr);
+            else tmem_st_32x32b_x32(tS, sr);
             l += sum;
+            if (KT == 64 && __any_sync(0xffffffffu, rescale)) rescale_o();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.p_full[k]);
@@ -653,15 +679,29 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 
 }  // namespace
 
+template <int D, bool F16, int KT>
+static cudaError_t launch_fwd_k(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t st) {
+    using C = FwdCfg<D, KT>;
+    const size_t smem = sizeof(FwdSmem<D, KT>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, F16, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // the warp groups' setmaxnreg shares must fit in the registers the CTA is launched with
+    // (an increase beyond them would never be granted)
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, fwd_kernel<D, F16, KT>)) != cudaSuccess) return e;
+    if (fa.numRegs * kThreadsFwd < 128 * C::REG_LOW + 256 * C::REG_HIGH) return cudaErrorLaunchOutOfResources;
+    if (a.n_items <= 0 || a.n_ctas <= 0) return cudaSuccess;
+    fwd_kernel<D, F16, KT><<<(unsigned)a.n_ctas, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
+    return cudaGetLastError();
+}
+
 template <int D, bool F16>
 static cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t st) {
-    const size_t smem = sizeof(FwdSmem<D>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (a.n_items <= 0 || a.n_ctas <= 0) return cudaSuccess;
-    fwd_kernel<D, F16><<<(unsigned)a.n_ctas, kThreadsFwd, smem, st>>>(a, tq, tk, tv);
-    return cudaGetLastError();
+    if constexpr (D == 64)
+        if (a.kt == 64) return launch_fwd_k<D, F16, 64>(a, tq, tk, tv, st);
+    return launch_fwd_k<D, F16, 128>(a, tq, tk, tv, st);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

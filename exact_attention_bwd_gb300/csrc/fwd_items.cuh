@@ -18,6 +18,7 @@ struct TileInfo {
 // One work item: the two query tiles [2 blk P, 2 blk P + 2P) of key/value head g of a
 // sequence (and one key split in split mode), numbered heaviest first: the key/value head
 // (and batch) vary fastest, the query block slowest, latest (longest causal band) first.
+// Key tiles are `bn` keys long (BN unless the kernel takes shorter ones).
 struct FwdItem {
     SeqView sv;
     Band band;
@@ -27,7 +28,7 @@ struct FwdItem {
     bool live;   // false for an idle block of a packed batch
 };
 
-__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx, int bn = BN) {
     const Problem& p = a.p;
     FwdItem w;
     int seq, blk;
@@ -76,7 +77,7 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx) {
         w.ti[k].active = w.ti[k].s0 < w.sv.nq;
         const int i1 = min(w.ti[k].s0 + p.P, w.sv.nq) - 1;
         if (w.ti[k].active) {
-            kv_tile_range(w.band, w.ti[k].s0, i1, BN, w.ti[k].t0, w.ti[k].t1);
+            kv_tile_range(w.band, w.ti[k].s0, i1, bn, w.ti[k].t0, w.ti[k].t1);
             if (a.n_splits > 1) {
                 w.ti[k].t0 = max(w.ti[k].t0, w.split * a.split_tiles);
                 w.ti[k].t1 = min(w.ti[k].t1, (w.split + 1) * a.split_tiles);

@@ -46,6 +46,8 @@ struct FwdArgs {
     int snake;         // their rounds alternate direction (items heaviest first: dense causal)
     int tokens;        // packed batch with queries and keys packed alike: query tiles run over
                        // the packed token axis and may hold several sequences (d <= 128 kernel)
+    int kt;            // keys per key tile of the d <= 128 kernel: 128, or 64 (d = 64 with a
+                       // narrow band: two CTAs per SM)
     uint16_t* o;       // [tokens, h_q, d] bf16, or fp16 for fp16 inputs
     float* lse;        // [B, h_q, s_q] or [h_q, T_q]; may be null
     float* o_part;     // split mode: [n_splits, rows, d] fp32
