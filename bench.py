@@ -488,12 +488,13 @@ def measure_workload(dev, name, steps=5, warmup=2, bwd_flags=0, dtype="bf16", ch
 
 
 def measure_d256(dev):
-    """fwd and fwd+bwd at head dim 256, with the backward's own rate against the bf16 peak.
-    Run last among the GPU sections; a failure is recorded in the section, not raised."""
+    """fwd and fwd+bwd at head dims 256 and 192 (the wide-head kernels), with the backward's
+    own rate against the bf16 peak.  Run last among the GPU sections; a failure is recorded
+    in the section, not raised."""
     from exact_attention_bwd_gb300 import binding as fa
     pk = peaks()
     out = {}
-    for name in ("d256_s8192_causal", "d256_s4096"):
+    for name in ("d256_s8192_causal", "d256_s4096", "d192_s8192_causal"):
         try:
             r = measure_workload(dev, name, check_status=True)
             ff = metrics.fwd_flops(inputs.workload(name))

@@ -150,6 +150,9 @@ WORKLOADS = {
                               causal=True, window=(-1, -1), sinks=False, varlen=False),
     "d256_s4096": dict(wid=6, variant=1, B=4, s_q=4096, s_kv=4096, h_q=16, h_kv=16, d=256,
                        causal=False, window=(-1, -1), sinks=False, varlen=False),
+    # head dim 192 (the padded size between 128 and 256), same token count
+    "d192_s8192_causal": dict(wid=6, variant=2, B=2, s_q=8192, s_kv=8192, h_q=16, h_kv=16, d=192,
+                              causal=True, window=(-1, -1), sinks=False, varlen=False),
     # decode / chunked prefill against a long cache
     **{f"decode_d{d}_sq{sq}": dict(wid=5, variant=(0 if d == 128 else 2) + (0 if sq == 1 else 1),
                                    B=64, s_q=sq, s_kv=32768, h_q=32, h_kv=8, d=d, causal=True,
