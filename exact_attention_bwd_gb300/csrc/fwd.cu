@@ -601,6 +601,9 @@ __global__ void __launch_bounds__(kThreadsFwd, FwdCfg<D, KT>::CTAS_PER_SM)
             tc_fence_after();
         }
         const bool split_mode = a.n_splits > 1;
+        // 32-byte stores where the base allows (the rows, 128 or more bytes, keep the alignment)
+        const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
+        const bool part_al32 = (reinterpret_cast<uintptr_t>(a.o_part) & 31u) == 0;
         float oscale = 0.f, lse = -INFINITY;
         if (!split_mode && p.sinks && row_valid) {
             const float s2 = sink2;
@@ -633,22 +636,46 @@ __global__ void __launch_bounds__(kThreadsFwd, FwdCfg<D, KT>::CTAS_PER_SM)
             if (lane == 0) mbar_arrive(&s.o_free[k]);
             if (row_valid) {
                 if (!split_mode) {
-                    uint4* orow = reinterpret_cast<uint4*>(a.o + (token_row(p, sv, i) * p.h_q + h) * D);
+                    uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D;
+                    if (o_al32) {
+                        // 32-byte stores (half the instructions; each row is 128 or 256 bytes)
 #pragma unroll
-                    for (int t = 0; t < D / 8; ++t) {
-                        uint4 wv;
-                        wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
-                        wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
-                        wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
-                        wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
-                        orow[t] = wv;
+                        for (int t = 0; t < D / 16; ++t) {
+                            uint32_t wv[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                wv[u] = pack16<F16>(__uint_as_float(orr[16 * t + 2 * u]) * oscale,
+                                                    __uint_as_float(orr[16 * t + 2 * u + 1]) * oscale);
+                            st_global_v8(orow + 16 * t, wv);
+                        }
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < D / 8; ++t) {
+                            uint4 wv;
+                            wv.x = pack16<F16>(__uint_as_float(orr[8 * t + 0]) * oscale, __uint_as_float(orr[8 * t + 1]) * oscale);
+                            wv.y = pack16<F16>(__uint_as_float(orr[8 * t + 2]) * oscale, __uint_as_float(orr[8 * t + 3]) * oscale);
+                            wv.z = pack16<F16>(__uint_as_float(orr[8 * t + 4]) * oscale, __uint_as_float(orr[8 * t + 5]) * oscale);
+                            wv.w = pack16<F16>(__uint_as_float(orr[8 * t + 6]) * oscale, __uint_as_float(orr[8 * t + 7]) * oscale);
+                            reinterpret_cast<uint4*>(orow)[t] = wv;
+                        }
                     }
                 } else {
-                    float4* op = reinterpret_cast<float4*>(a.o_part + ((long)split * nrows + prow) * D);
+                    float* op = a.o_part + ((long)split * nrows + prow) * D;
+                    if (part_al32) {
 #pragma unroll
-                    for (int t = 0; t < D / 4; ++t)
-                        op[t] = make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
+                        for (int t = 0; t < D / 8; ++t) {
+                            uint32_t wv[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) wv[u] = __float_as_uint(__uint_as_float(orr[8 * t + u]) * oscale);
+                            st_global_v8(op + 8 * t, wv);
+                        }
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < D / 4; ++t)
+                            reinterpret_cast<float4*>(op)[t] =
+                                make_float4(__uint_as_float(orr[4 * t]) * oscale, __uint_as_float(orr[4 * t + 1]) * oscale,
                                             __uint_as_float(orr[4 * t + 2]) * oscale, __uint_as_float(orr[4 * t + 3]) * oscale);
+                    }
                 }
             }
             tr.mark(kMEpilogueDone);
