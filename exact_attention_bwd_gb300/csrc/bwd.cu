@@ -586,6 +586,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         // ================= compute groups =================
         const int cg = (warp - 4) >> 2;            // column group
         const int wq = warp & 3;
+        const bool dkv_al32 = ((reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) & 31u) == 0;
         const int jr = (wq << 5) | lane;           // key row of this thread (TMEM lane)
         const uint32_t lane_base = (uint32_t)(wq << 5) << 16;
         const float c = p.scale_log2;
@@ -740,7 +741,25 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 #pragma unroll
                 for (int t = 0; t < D / 2; ++t) vv[t] = kk[t] = 0u;
             }
-            if (row_ok) {
+            if (row_ok && dkv_al32) {
+                // 32-byte stores (the half rows are 64 or 128 bytes)
+                uint16_t* dvp = a.dv + (krow * p.h_kv + bk.g) * D + (D / 2) * cg;
+                uint16_t* dkp = a.dk + (krow * p.h_kv + bk.g) * D + (D / 2) * cg;
+                const float mul = p.scale;
+#pragma unroll
+                for (int t = 0; t < D / 32; ++t) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        w[u] = pack16<F16>(__uint_as_float(vv[16 * t + 2 * u]), __uint_as_float(vv[16 * t + 2 * u + 1]));
+                    st_global_v8(dvp + 16 * t, w);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        w[u] = pack16<F16>(__uint_as_float(kk[16 * t + 2 * u]) * mul,
+                                           __uint_as_float(kk[16 * t + 2 * u + 1]) * mul);
+                    st_global_v8(dkp + 16 * t, w);
+                }
+            } else if (row_ok) {
                 uint4* dvp = reinterpret_cast<uint4*>(a.dv + (krow * p.h_kv + bk.g) * D + (D / 2) * cg);
                 uint4* dkp = reinterpret_cast<uint4*>(a.dk + (krow * p.h_kv + bk.g) * D + (D / 2) * cg);
                 const float mul = p.scale;

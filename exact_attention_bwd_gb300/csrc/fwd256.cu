@@ -325,6 +325,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
             tc_fence_after();
         }
         const bool split_mode = a.n_splits > 1;
+        const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;  // rows keep the alignment (D * 2 bytes)
         float oscale = 0.f, lse = -INFINITY;
         if (!split_mode && p.sinks && row_valid) {
             const float s2 = p.sinks[h] * kLog2e;
@@ -355,7 +356,19 @@ __global__ void __launch_bounds__(kThreads256, 1)
                 for (int t = 0; t < 32; ++t) orr[t] = 0u;
             }
             if (!row_valid) continue;
-            if (!split_mode) {
+            if (!split_mode && o_al32) {
+                // 32-byte stores (a 32-column chunk of the row is 64 bytes)
+                uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    uint32_t wv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        wv[u] = pack16<F16>(__uint_as_float(orr[16 * t + 2 * u]) * oscale,
+                                            __uint_as_float(orr[16 * t + 2 * u + 1]) * oscale);
+                    st_global_v8(orow + 16 * t, wv);
+                }
+            } else if (!split_mode) {
                 uint16_t* orow = a.o + (token_row(p, sv, i) * p.h_q + h) * D + cb;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
