@@ -387,11 +387,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     mbar_arrive(&s.dq_free);
                     if (DET && !dq_turn_wait(cnt, need, ab)) { ok = false; break; }
                     // for each query row the 32 lanes of a warp add to 32 consecutive floats
+                    // (the accumulator lines are kept in L2 ahead of streamed data: each is added to
+                    // by every key block that sees the tile)
                     float* acc = a.dq_acc + trow * D + tl;
+                    const uint64_t keep = policy_evict_last();
 #pragma unroll
-                    for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)r * D, __uint_as_float(qa[r]));
+                    for (int r = 0; r < 64; ++r) red_add_hint(acc + (long)r * D, __uint_as_float(qa[r]), keep);
 #pragma unroll
-                    for (int r = 0; r < 64; ++r) atomicAdd(acc + (long)(64 + r) * D, __uint_as_float(qb[r]));
+                    for (int r = 0; r < 64; ++r) red_add_hint(acc + (long)(64 + r) * D, __uint_as_float(qb[r]), keep);
                 } else {
                     uint32_t qv[D];
                     tmem_ld_32x32b_x64(tmem + lane_base + C::C_DQ, qv);
@@ -452,9 +455,19 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                         // frees while the previous block still runs
                         if (kv_issued > 0 && !(ok = twait(tr, kBDkvFull, &s.dkv_full, (kv_issued - 1) & 1, ab))) break;
                         mbar_expect_tx(&s.kv_full, 2 * C::TILE);
+                        // a block's K and V are read once: at d = 128 they leave L2 first (measured
+                        // faster there, slightly slower at d = 64)
+                        const uint64_t once = policy_evict_first();
                         for (int c = 0; c < C::KCH; ++c) {
-                            tma_load_4d(s.k + c * C::CHUNK, &tmk, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0, bk.sv.tma_b);
-                            tma_load_4d(s.v + c * C::CHUNK, &tmv, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0, bk.sv.tma_b);
+                            if constexpr (D == 128) {
+                                tma_load_4d_hint(s.k + c * C::CHUNK, &tmk, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0,
+                                                 bk.sv.tma_b, once);
+                                tma_load_4d_hint(s.v + c * C::CHUNK, &tmv, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0,
+                                                 bk.sv.tma_b, once);
+                            } else {
+                                tma_load_4d(s.k + c * C::CHUNK, &tmk, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0, bk.sv.tma_b);
+                                tma_load_4d(s.v + c * C::CHUNK, &tmv, &s.kv_full, c * 64, bk.g, bk.sv.k0 + bk.j0, bk.sv.tma_b);
+                            }
                         }
                         ++kv_issued;
                     }
