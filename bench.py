@@ -352,7 +352,9 @@ def run_e2e(args, fa, kw, ins, outs, flops, world, dev):
     memory, runs fa_fwd + fa_bwd, and copies its results (O, LSE, dQ, dK, dV) back to pinned
     host memory.  Steps are pipelined the way a serving or training loop would run them:
     copies on their own streams, two device sets of inputs and outputs, so step i+1's input
-    copy and step i-1's result copy overlap step i's kernels.  The timed region runs from
+    copy and step i-1's result copy overlap step i's kernels; within a step the forward
+    starts once Q, K, V have landed (dO gates the backward) and O, LSE leave while the
+    backward runs.  The timed region runs from
     the first step's first input copy to the last step's last result copy (pipeline fill
     and drain included)."""
     import torch
@@ -367,7 +369,9 @@ def run_e2e(args, fa, kw, ins, outs, flops, world, dev):
                 torch.empty_like(v)] for _ in range(2)]
     dsk = None if kw.get("sinks") is None else torch.empty_like(kw["sinks"])
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_qkv = [torch.cuda.Event() for _ in range(2)]  # Q, K, V of the set have landed
+    ev_in = [torch.cuda.Event() for _ in range(2)]   # ... and dO
+    ev_fwd = [torch.cuda.Event() for _ in range(2)]  # the forward has written O, LSE
     ev_cmp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
@@ -379,21 +383,30 @@ def run_e2e(args, fa, kw, ins, outs, flops, world, dev):
                     s_in.wait_event(ev_cmp[b])  # step it-2 has consumed this input set
                 if it == 0 and t0 is not None:
                     t0.record(s_in)
-                for dst, src in zip(dev_in[b], host_in):
+                for dst, src in zip(dev_in[b][:3], host_in[:3]):
                     dst.copy_(src, non_blocking=True)
+                ev_qkv[b].record(s_in)
+                dev_in[b][3].copy_(host_in[3], non_blocking=True)
                 ev_in[b].record(s_in)
             with torch.cuda.stream(s_cmp):
-                s_cmp.wait_event(ev_in[b])
+                # the forward needs Q, K, V only; dO (the last input copy) gates the backward
+                s_cmp.wait_event(ev_qkv[b])
                 if it >= 2:
                     s_cmp.wait_event(ev_out[b])  # step it-2's results have left this output set
                 qb, kb, vb, dob = dev_in[b]
                 ob, lb, dqb, dkb, dvb = dev_out[b]
                 fa.forward(qb, kb, vb, **kw, out=ob, lse=lb, workspace=ws_f)
+                ev_fwd[b].record(s_cmp)
+                s_cmp.wait_event(ev_in[b])
                 fa.backward(qb, kb, vb, ob, lb, dob, **kw, workspace=ws_b, grads=(dqb, dkb, dvb, dsk))
                 ev_cmp[b].record(s_cmp)
             with torch.cuda.stream(s_out):
+                # O and LSE leave while the backward runs; the gradients after it
+                s_out.wait_event(ev_fwd[b])
+                for dst, src in zip(host_out[:2], dev_out[b][:2]):
+                    dst.copy_(src, non_blocking=True)
                 s_out.wait_event(ev_cmp[b])
-                for dst, src in zip(host_out, dev_out[b]):
+                for dst, src in zip(host_out[2:], dev_out[b][2:]):
                     dst.copy_(src, non_blocking=True)
                 ev_out[b].record(s_out)
                 if it == n - 1 and t1 is not None:
