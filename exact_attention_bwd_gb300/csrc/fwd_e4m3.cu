@@ -47,35 +47,41 @@ struct __align__(1024) Smem8 {
 static_assert(sizeof(Smem8) + 1024 <= 232448, "e4m3 forward shared memory exceeds 227 KB");
 
 // ------------------------------------------------------------------------------------------
-// V -> V^T pre-pass: one CTA per (128-key block, kv head, batch); 16 KB through shared
-// memory; keys past s_kv are written as zeros up to s_pad (a multiple of 16).
+// V -> V^T pre-pass: one CTA of 4 warps per (128-key block, kv head, batch), no shared
+// memory.  Warp w takes bytes [32w, 32w + 32) of d, lane l keys 4l .. 4l + 3 of the block:
+// each key's 32 bytes come in with two 16-byte loads, every 4 x 4 byte block (4 keys x 4
+// values of d) is transposed in registers with byte permutes, and each of the lane's 32
+// d rows gets one 4-byte word, so a warp store writes 128 consecutive bytes of a V^T row.
+// Keys past s_kv are written as zeros up to s_pad (a multiple of 16).
 // ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) transpose_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+__global__ void __launch_bounds__(128) transpose_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
                                                           int s_kv, int h_kv, int s_pad) {
-    __shared__ uint8_t tile[128][132];  // [key][d], padded rows
-    const int k0 = blockIdx.x * 128, g = blockIdx.y, b = blockIdx.z;
-    for (int idx = threadIdx.x; idx < 128 * 8; idx += 256) {
-        const int key = idx >> 3, c = idx & 7;
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (k0 + key < s_kv)
-            x = *reinterpret_cast<const uint4*>(v + (((long)b * s_kv + k0 + key) * h_kv + g) * 128 + 16 * c);
-        uint32_t* t = reinterpret_cast<uint32_t*>(&tile[key][16 * c]);
-        t[0] = x.x;
-        t[1] = x.y;
-        t[2] = x.z;
-        t[3] = x.w;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < 128 * 8; idx += 256) {
-        const int dr = idx >> 3, c = idx & 7;  // d row, 16-key chunk
-        if (k0 + 16 * c >= s_pad) continue;
-        uint32_t w[4];
+    const int g = blockIdx.y, b = blockIdx.z;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int key0 = blockIdx.x * 128 + 4 * lane;  // first of the lane's four keys
+    if (key0 >= s_pad) return;
+    uint32_t x[4][8];  // [key][word]: bytes 4 j .. 4 j + 3 of the warp's 32 values of d
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            w[q] = (uint32_t)tile[16 * c + 4 * q][dr] | ((uint32_t)tile[16 * c + 4 * q + 1][dr] << 8) |
-                   ((uint32_t)tile[16 * c + 4 * q + 2][dr] << 16) | ((uint32_t)tile[16 * c + 4 * q + 3][dr] << 24);
-        *reinterpret_cast<uint4*>(vt + (((long)b * h_kv + g) * 128 + dr) * s_pad + k0 + 16 * c) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 4; ++i) {
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+        if (key0 + i < s_kv) {
+            const uint4* src = reinterpret_cast<const uint4*>(v + (((long)b * s_kv + key0 + i) * h_kv + g) * 128 + 32 * w);
+            lo = src[0];
+            hi = src[1];
+        }
+        x[i][0] = lo.x, x[i][1] = lo.y, x[i][2] = lo.z, x[i][3] = lo.w;
+        x[i][4] = hi.x, x[i][5] = hi.y, x[i][6] = hi.z, x[i][7] = hi.w;
+    }
+    uint8_t* dst = vt + (((long)b * h_kv + g) * 128 + 32 * w) * s_pad + key0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        // rows 4j .. 4j+3 of the warp's d range, keys key0 .. key0+3 (lowest byte first)
+        const uint32_t t0 = __byte_perm(x[0][j], x[1][j], 0x5140), t1 = __byte_perm(x[2][j], x[3][j], 0x5140);
+        const uint32_t t2 = __byte_perm(x[0][j], x[1][j], 0x7362), t3 = __byte_perm(x[2][j], x[3][j], 0x7362);
+        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 0) * s_pad) = __byte_perm(t0, t1, 0x5410);
+        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 1) * s_pad) = __byte_perm(t0, t1, 0x7632);
+        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 2) * s_pad) = __byte_perm(t2, t3, 0x5410);
+        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 3) * s_pad) = __byte_perm(t2, t3, 0x7632);
     }
 }
 
@@ -516,7 +522,7 @@ cudaError_t launch_transpose_v_e4m3(const uint8_t* v, uint8_t* vt, int B, int s_
                                     cudaStream_t st) {
     if (B <= 0 || s_pad <= 0) return cudaSuccess;
     dim3 grid((unsigned)cdiv(s_pad, 128), (unsigned)h_kv, (unsigned)B);
-    transpose_v_kernel<<<grid, 256, 0, st>>>(v, vt, s_kv, h_kv, s_pad);
+    transpose_v_kernel<<<grid, 128, 0, st>>>(v, vt, s_kv, h_kv, s_pad);
     return cudaGetLastError();
 }
 
