@@ -196,6 +196,7 @@ struct FwdPlan {
     int unit_major = 0;
     int tokens = 0;        // packed batch with cu_seqlens_q == cu_seqlens_k: token tiles
     int kt = 128;          // keys per key tile of the d <= 128 kernel (64: two CTAs per SM)
+    int tail_units = 0, tail_k = 0, tail_split_tiles = 0;  // tail split (d = 192 / 256)
     size_t part_rows = 0;  // rows of the split partials
     int s_pad = 0;         // e4m3: keys per V^T row (s_kv rounded up to 16)
     size_t off_vt = 0;     // e4m3: workspace offset of V^T
@@ -274,6 +275,36 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
         // few queries against a long key range: every query block does about the same work,
         // so launch the blocks of one (batch, kv head) together and let them share K/V in L2
         pl.unit_major = (p.s_q * 4 <= p.s_kv) ? 1 : 0;
+        // Tail split (d = 192 / 256: one CTA per item, one CTA per SM).  Such items all take
+        // about as long, so a last partial wave of CTAs leaves the other SMs idle for a
+        // whole item; the last units' items are cut into k key ranges instead (k chosen so
+        // that the pieces fill the last wave best) and their rows merged by the combine.
+        if (p.d >= 192 && pl.n_splits == 1 && pl.unit_major && p.left < 0 && tiles >= 64) {
+            const long units = (long)p.h_kv * p.B, items = units * pl.n_blocks, slots = sm_count();
+            const long rem = items % slots;
+            if (items > slots && rem > 0) {
+                const long tail_units = (rem + pl.n_blocks - 1) / pl.n_blocks;
+                const long tail = tail_units * pl.n_blocks;
+                // the tail's duration in whole items: ceil(k tail / slots) / k (1 without a split)
+                double best = (double)((tail + slots - 1) / slots);
+                int best_k = 1;
+                for (int k = 2; k <= 8; ++k) {
+                    const double len = (double)((k * tail + slots - 1) / slots) / k;
+                    if (len < best - 1e-9) {
+                        best = len;
+                        best_k = k;
+                    }
+                }
+                if (best_k > 1 && best <= 0.8) {
+                    pl.tail_units = (int)tail_units;
+                    pl.tail_k = best_k;
+                    pl.tail_split_tiles = (tiles + best_k - 1) / best_k;
+                    pl.part_rows = (size_t)tail_units * p.G * p.s_q;
+                    pl.ws_bytes = kStatusBytes + align256(pl.part_rows * best_k * p.d * 4) +
+                                  align256(pl.part_rows * best_k * 4);
+                }
+            }
+        }
         if (pl.n_splits > 1) {
             pl.part_rows = (size_t)p.B * p.h_q * p.s_q;
             pl.ws_bytes = kStatusBytes + align256(pl.part_rows * pl.n_splits * p.d * 4) +
@@ -462,7 +493,8 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         return FA_ERR_CUDA;
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     float* o_part = reinterpret_cast<float*>(ws + kStatusBytes);
-    float* lse_part = reinterpret_cast<float*>(ws + kStatusBytes + align256(pl.part_rows * pl.n_splits * p.d * 4));
+    const int part_splits = pl.tail_k > 1 ? pl.tail_k : pl.n_splits;  // pieces per row in the partials
+    float* lse_part = reinterpret_cast<float*>(ws + kStatusBytes + align256(pl.part_rows * part_splits * p.d * 4));
 
     if (pl.path == FwdPath::kDecode) {
         DecodeArgs a{};
@@ -522,6 +554,10 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.unit_major = pl.unit_major;
     a.tokens = pl.tokens;
     a.kt = pl.kt;
+    a.tail_k = pl.tail_k;
+    a.tail_split_tiles = pl.tail_split_tiles;
+    a.tail_item0 = pl.tail_k > 1 ? (p.h_kv * p.B - pl.tail_units) * pl.n_blocks : 0;
+    a.tail_row0 = pl.tail_k > 1 ? (long)(p.h_kv * p.B - pl.tail_units) * p.G * p.s_q : 0;
     {
         const long items = p.cu_q ? (long)pl.n_blocks * p.h_kv : (long)pl.n_blocks * pl.n_splits * p.h_kv * p.B;
         const long slots = (long)sm_count() * (pl.kt == 64 ? 2 : 1);
@@ -542,10 +578,12 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
         return p.dtype == FA_DTYPE_E4M3 ? launch_fwd_e4m3(a, tq, tk, tv, st) : launch_fwd(a, tq, tk, tv, st);
     });
     if (e != cudaSuccess) return FA_ERR_CUDA;
-    if (pl.n_splits > 1) {
+    if (pl.n_splits > 1 || pl.tail_k > 1) {
         CombineArgs c{};
         c.p = p;
-        c.n_splits = pl.n_splits;
+        c.n_splits = pl.n_splits > 1 ? pl.n_splits : pl.tail_k;
+        c.row0 = pl.tail_k > 1 ? a.tail_row0 : 0;
+        c.nrows = pl.tail_k > 1 ? (long)pl.part_rows : 0;
         c.o_part = o_part;
         c.lse_part = lse_part;
         c.o = reinterpret_cast<uint16_t*>(o);

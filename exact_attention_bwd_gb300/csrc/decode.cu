@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3) combine_kernel(const Co
     const Problem& p = a.p;
     // an earlier kernel of the call failed: its partials are incomplete, write nothing
     if (a.status && *reinterpret_cast<volatile const int*>(a.status) != 0) return;
-    const long nrows = (long)p.B * p.h_q * p.s_q;
+    const long nrows = a.nrows ? a.nrows : (long)p.B * p.h_q * p.s_q;  // rows of the partials
     const int lane = threadIdx.x & 31, l = lane % L;
     const long row0 = (((long)blockIdx.x * kCombineWarps + threadIdx.x / 32) * (32 / L) + lane / L) * RL;
     const int n = a.n_splits;
@@ -384,8 +384,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3) combine_kernel(const Co
     }
 #pragma unroll
     for (int q = 0; q < RL; ++q) {
-        const long row = row0 + q;
-        if (row >= nrows) break;
+        if (row0 + q >= nrows) break;
+        const long row = a.row0 + row0 + q;  // the output row
         const int i = (int)(row % p.s_q);
         const int h = (int)((row / p.s_q) % p.h_q);
         const int b = (int)(row / ((long)p.s_q * p.h_q));
@@ -448,7 +448,7 @@ int decode_ctas_per_sm(int d, int rows) { return (d >= 192 || rows > 4) ? 1 : 2;
 
 template <int D>
 static cudaError_t launch_combine_d(const CombineArgs& a, cudaStream_t st) {
-    const long nrows = (long)a.p.B * a.p.h_q * a.p.s_q;
+    const long nrows = a.nrows ? a.nrows : (long)a.p.B * a.p.h_q * a.p.s_q;
     const long rows_per_block = CombineCfg<D>::ROWS_PER_BLOCK;
     const long blocks = (nrows + rows_per_block - 1) / rows_per_block;
     if (blocks == 0) return cudaSuccess;

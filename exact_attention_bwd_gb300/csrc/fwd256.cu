@@ -68,11 +68,23 @@ __global__ void __launch_bounds__(kThreads256, 1)
     if (a.status && *reinterpret_cast<volatile int*>(a.status) != 0) return;
 
     // ---------------- work unit ----------------
-    // 1-D grid, heaviest work first (see the d <= 128 kernel)
+    // 1-D grid, heaviest work first (see the d <= 128 kernel); the last (batch, kv head)
+    // units may be cut into tail_k key ranges each (the tail split, see FwdArgs)
     int g, seq, blk, split = 0;
+    bool tail = false;
     {
         const int idx = blockIdx.x;
-        if (p.cu_q) {
+        if (a.tail_k > 1 && idx >= a.tail_item0) {
+            const int t = idx - a.tail_item0;
+            const int per_unit = a.n_blocks * a.tail_k;
+            const int unit = a.tail_item0 / a.n_blocks + t / per_unit;
+            const int x = t % per_unit;
+            g = unit % p.h_kv;
+            seq = unit / p.h_kv;
+            split = x % a.tail_k;
+            blk = a.n_blocks - 1 - x / a.tail_k;
+            tail = true;
+        } else if (p.cu_q) {
             g = idx % p.h_kv;
             blk = idx / p.h_kv;
             seq = owner_sequence(p.cu_q, p.B, blk, p.P);
@@ -94,9 +106,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const Band band{sv.nk - sv.nq, p.left, p.right, sv.nk};
     int t0, t1;
     kv_tile_range(band, s0, min(s0 + p.P, sv.nq) - 1, BN, t0, t1);
-    if (a.n_splits > 1) {
-        t0 = max(t0, split * a.split_tiles);
-        t1 = min(t1, (split + 1) * a.split_tiles);
+    if (a.n_splits > 1 || tail) {
+        const int st = tail ? a.tail_split_tiles : a.split_tiles;
+        t0 = max(t0, split * st);
+        t1 = min(t1, (split + 1) * st);
         if (t1 < t0) t1 = t0;
     }
     const int ntiles = t1 - t0;
@@ -324,7 +337,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
             ok = __all_sync(0xffffffffu, w);
             tc_fence_after();
         }
-        const bool split_mode = a.n_splits > 1;
+        const bool split_mode = a.n_splits > 1 || tail;
         const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;  // rows keep the alignment (D * 2 bytes)
         float oscale = 0.f, lse = -INFINITY;
         if (!split_mode && p.sinks && row_valid) {
@@ -338,8 +351,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
             oscale = 1.f / l;
             lse = (m_used + log2f(l)) * kLn2;
         }
-        const long nrows = (long)p.B * p.h_q * p.s_q;
-        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;
+        // the partials' rows: all B h_q s_q rows, or (tail split) those from tail_row0 on
+        const long row_base = tail ? a.tail_row0 : 0;
+        const long nrows = (long)p.B * p.h_q * p.s_q - row_base;
+        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i - row_base;
         if (row_valid) {
             if (!split_mode) {
                 if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
@@ -407,7 +422,8 @@ static cudaError_t launch_fwd_wide(const FwdArgs& a, const CUtensorMap& tq, cons
     auto kernel = a.p.dtype == FA_DTYPE_F16 ? fwd256_kernel<D, true> : fwd256_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long n = a.p.cu_q ? (long)a.n_blocks * a.p.h_kv : (long)a.n_blocks * a.n_splits * a.p.h_kv * a.p.B;
+    long n = a.p.cu_q ? (long)a.n_blocks * a.p.h_kv : (long)a.n_blocks * a.n_splits * a.p.h_kv * a.p.B;
+    if (a.tail_k > 1) n = a.tail_item0 + (n - a.tail_item0) * a.tail_k;
     kernel<<<(unsigned)n, kThreads256, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
 }

@@ -48,6 +48,12 @@ struct FwdArgs {
                        // the packed token axis and may hold several sequences (d <= 128 kernel)
     int kt;            // keys per key tile of the d <= 128 kernel: 128, or 64 (d = 64 with a
                        // narrow band: two CTAs per SM)
+    // tail split (d = 192 / 256, dense, one CTA per item): items from tail_item0 on (whole
+    // (batch, kv head) units, the last ones) are each cut into tail_k key ranges of
+    // tail_split_tiles tiles that write partials of rows [tail_row0, B h_q s_q) for the
+    // combine; the other items write final outputs.  tail_k = 0: no tail split.
+    int tail_item0, tail_k, tail_split_tiles;
+    long tail_row0;
     uint16_t* o;       // [tokens, h_q, d] bf16, or fp16 for fp16 inputs
     float* lse;        // [B, h_q, s_q] or [h_q, T_q]; may be null
     float* o_part;     // split mode: [n_splits, rows, d] fp32
@@ -77,6 +83,8 @@ struct DecodeArgs {
 struct CombineArgs {
     Problem p;
     int n_splits;
+    long row0, nrows;  // the rows merged: [row0, row0 + nrows) of B h_q s_q (nrows = 0: all);
+                       // the partials hold these rows only, from index 0
     const float* o_part;
     const float* lse_part;
     uint16_t* o;       // bf16 or fp16 (as the inputs)

@@ -195,3 +195,31 @@ def test_decode_full(d, s_q):
         check_lse(f"LSE b{b} g{g}", lse[b, hs].cpu().numpy(), rl[0])
     del k, v
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("d,sinks", [(256, False), (256, True), (192, False)])
+def test_wide_head_tail_split(d, sinks):
+    """B=40, h_q=32, h_kv=8, s_q=64, s_kv=4096 causal cache at d = 192 / 256: 640 one-CTA
+    items over the GB300's 152 SMs leave a last wave of 32; the planner then cuts the last
+    16 (batch, kv head) units' items into key ranges merged by the combine (the tail split).
+    Whole units on both sides of that boundary, and the first and last, against the oracle."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    B, s_q, s_kv, h_q, h_kv = 40, 64, 4096, 32, 8
+    G = h_q // h_kv
+    w = inputs.make(dict(wid=32, variant=d + int(sinks), B=B, s_q=s_q, s_kv=s_kv, h_q=h_q, h_kv=h_kv, d=d,
+                         causal=True, window=(-1, -1), sinks=sinks, varlen=False))
+    dv = dev_inputs(w)
+    o, lse, ws = fa.forward(dv["q"], dv["k"], dv["v"], causal=True, softmax_scale=w["scale"], sinks=dv["sinks"])
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == 0
+    for unit in (0, 303, 304, 319):
+        b, g = divmod(unit, h_kv)
+        hs = slice(g * G, (g + 1) * G)
+        qq = inputs.bf16_to_f64(w["q"][b:b + 1, :, hs])
+        kk = inputs.bf16_to_f64(w["k"][b:b + 1, :, g:g + 1])
+        vv = inputs.bf16_to_f64(w["v"][b:b + 1, :, g:g + 1])
+        sk = None if w["sinks"] is None else w["sinks"][hs].astype(np.float64)
+        ro, rl, _ = oracle.fwd(qq, kk, vv, scale=w["scale"], causal=True, sinks=sk)
+        check(f"O unit {unit}", from_dev(o[b:b + 1, :, hs]), ro)
+        check_lse(f"LSE unit {unit}", lse[b, hs].cpu().numpy(), rl[0])
