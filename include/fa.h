@@ -181,7 +181,9 @@ typedef struct fa_params {
 
 /* Bytes of workspace fa_fwd / fa_bwd need for these parameters (>= 256: the first
  * 256 bytes hold the device status word).  Returns 0 when the parameters are
- * invalid or unsupported. */
+ * invalid or unsupported.  The forward's plan (key splits, and the split of a last
+ * partial wave of work at d = 192 / 256) follows the current device's SM count, so the
+ * size is queried with the device that will run the call current. */
 size_t fa_fwd_workspace_size(const fa_params *p);
 size_t fa_bwd_workspace_size(const fa_params *p);
 

@@ -62,6 +62,8 @@ CASES = [
     dict(d=128, s_q=650, s_kv=200, h_q=4, h_kv=4),
     dict(d=128, lengths=[17, 283, 128, 0, 1, 0, 300, 129]),
     dict(d=64, lengths=[400, 3, 0, 250], h_q=8, h_kv=2, causal=False, window=(50, 20), sinks=True),
+    # dense grouped-query window at d = 64: the forward's 64-key tiles, two CTAs per SM
+    dict(d=64, s_q=700, s_kv=700, h_q=16, h_kv=2, causal=True, window=(127, 0), sinks=True),
 ]
 
 
