@@ -328,7 +328,8 @@ def run_ours(args):
     if not args.no_sweep:
         line["workloads"] = {n: measure_workload(dev, n) for n in SWEEP + OTHER}
         line["deterministic_bwd"] = {n: measure_workload(dev, n, bwd_flags=fa.FA_FLAG_DETERMINISTIC)
-                                     for n in ("sweep_s8192_causal", "sweep_s2048", "gqa_window_causal", "varlen")}
+                                     for n in ("sweep_s8192_causal", "sweep_s2048", "gqa_window_causal", "varlen",
+                                               "d256_s8192_causal")}
         line["f16"] = {n: measure_workload(dev, n, dtype="f16")
                        for n in ("sweep_s8192_causal", "sweep_s8192", "sweep_s2048", "gqa_window_causal", "varlen")}
         line["e4m3_fwd"] = {n: measure_fp8(dev, n) for n in ("sweep_s8192_causal", "sweep_s8192", "sweep_s16384",

@@ -350,7 +350,6 @@ struct BwdPlan {
 fa_status plan_bwd(const Problem& p, unsigned flags, BwdPlan& pl) {
     pl = BwdPlan();
     if (!supported_d(p.d)) return FA_ERR_UNSUPPORTED;
-    if (p.d >= 192 && (flags & FA_FLAG_DETERMINISTIC)) return FA_ERR_UNSUPPORTED;  // fixed dQ order: d <= 128
     if (p.block_table) return FA_ERR_UNSUPPORTED;  // paged caches: forward only
     if (p.dtype == FA_DTYPE_E4M3) return FA_ERR_UNSUPPORTED;      // e4m3: forward only
     const long rows_total = p.cu_q ? (long)p.T_q : (long)p.B * p.s_q;

@@ -861,7 +861,25 @@ __device__ __forceinline__ void block_qtiles64(const Problem& p, const SeqView& 
     qt1 = (i_hi >= i_lo) ? i_hi / p.P + 1 : 0;
 }
 
-template <int D, bool F16>
+// dq_predecessors for the 64-key blocks of the wide-head kernel.
+__device__ __forceinline__ int dq_predecessors64(const Problem& p, const SeqView& sv, const Band& band, DqOrder& o,
+                                                 int t) {
+    while (o.next * kKeys256 < sv.nk) {
+        int a0, a1;
+        block_qtiles64(p, sv, band, o.next, a0, a1);
+        if (a1 > a0) {
+            if (a0 > t) break;
+            ++o.n;
+        }
+        ++o.next;
+    }
+    return o.n;
+}
+
+// DET: the fixed dQ order of the d <= 128 kernel (DqOrder): a sequence's later 64-key
+// blocks take lower CTA indices, and the compute group adds its two dQ^T halves into query
+// tile t only after every later block that sees t has added (one count per warp).
+template <int D, bool F16, bool DET>
 __global__ void __launch_bounds__(kThreadsBwd256, 1)
     bwd256_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
@@ -885,6 +903,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
         if (p.cu_q) {
             g = idx % p.h_kv;
             blk = idx / p.h_kv;
+            if (DET) blk = a.n_kvblocks - 1 - blk;
             seq = owner_sequence(p.cu_k, p.B, blk, kKeys256);
             blk -= p.cu_k[seq] / kKeys256 + seq;
         } else {
@@ -892,6 +911,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
             band_order(idx, p.h_kv * p.B, a.n_bands, a.n_kvblocks, unit, blk);
             g = unit % p.h_kv;
             seq = unit / p.h_kv;
+            if (DET) blk = a.n_kvblocks - 1 - blk;
         }
     }
     const SeqView sv = seq_view(p, seq);
@@ -1062,6 +1082,8 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
         const float c = p.scale_log2;
         bool ok = true;
         int ndq = 0;
+        DqOrder order;  // DET: the later blocks examined so far
+        order.next = blk + 1;
         Tracer tr;
         tr.init(warp == 4 ? a.trace : nullptr, 2);
         tr.item(blockIdx.x);
@@ -1116,6 +1138,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
             mbar_arrive(&s.pds_full);
             tr.mark(kMSoftmaxDone);
             // ---- dQ^T halves: lane = column of d within the half, columns = query rows ----
+            int* cnt = DET ? a.dq_count + (long)g * a.n_qtiles + tbase + t : nullptr;
             for (int h = 0; h < 2; ++h) {
                 {
                     const bool w = twait(tr, kBDqFull, &s.dq_full, ndq & 1, ab);
@@ -1128,6 +1151,10 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 tmem_ld_32x32b_x64(tmem + lane_base + C_DQ + 64, qb);
                 tc_fence_before();
                 mbar_arrive(&s.dq_free);
+                if (DET && h == 0 && !dq_turn_wait(cnt, 4 * dq_predecessors64(p, sv, band, order, t), ab)) {
+                    ok = false;
+                    break;
+                }
                 // for each query row the 32 lanes of a warp add to 32 consecutive floats
                 // (at d = 192 the second half's lanes 64..127 hold the zero padding rows)
                 if (128 * h + r < D) {
@@ -1140,6 +1167,7 @@ __global__ void __launch_bounds__(kThreadsBwd256, 1)
                 tr.mark(kMDqReduced);
             }
             if (!ok) break;
+            if constexpr (DET) dq_turn_done(cnt);
         }
         // ---- epilogue: dV, dK of the block's 64 keys (lane = column of d within a half) ----
         if (nsteps > 0 && ok) {
@@ -1360,11 +1388,11 @@ static cudaError_t launch_main_d(const BwdArgs& a, const CUtensorMap& tq, const 
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool DET>
 static cudaError_t launch_main256(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem256);
-    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd256_kernel<D, true> : bwd256_kernel<D, false>;
+    auto kernel = a.p.dtype == FA_DTYPE_F16 ? bwd256_kernel<D, true, DET> : bwd256_kernel<D, false, DET>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long n = (long)a.n_kvblocks * a.p.h_kv * (a.p.cu_q ? 1 : a.p.B);
@@ -1376,10 +1404,11 @@ cudaError_t launch_bwd_main(const BwdArgs& a, const CUtensorMap& tq, const CUten
                             const CUtensorMap& tdo, cudaStream_t st) {
     switch (a.p.d) {
         case 192:
-            // the fixed dQ order is not built at d = 192 / 256 (the planner refuses the flag)
-            return a.dq_count ? cudaErrorInvalidValue : launch_main256<192>(a, tq, tk, tv, tdo, st);
+            return a.dq_count ? launch_main256<192, true>(a, tq, tk, tv, tdo, st)
+                              : launch_main256<192, false>(a, tq, tk, tv, tdo, st);
         case 256:
-            return a.dq_count ? cudaErrorInvalidValue : launch_main256<256>(a, tq, tk, tv, tdo, st);
+            return a.dq_count ? launch_main256<256, true>(a, tq, tk, tv, tdo, st)
+                              : launch_main256<256, false>(a, tq, tk, tv, tdo, st);
         case 64:
             if (a.dq_count) return launch_main_d<64, true, false>(a, tq, tk, tv, tdo, st);
             return a.tokens ? launch_main_d<64, false, true>(a, tq, tk, tv, tdo, st)

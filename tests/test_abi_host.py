@@ -106,9 +106,6 @@ def test_workspace_too_small():
 def test_backward_rejects():
     assert call_bwd(params(sinks=0x3000), dsinks=None) == fa.FA_ERR_INVALID_ARG
     assert call_bwd(params(d=160)) == fa.FA_ERR_UNSUPPORTED
-    # d = 192 and 256 have no fixed-order (deterministic) dQ
-    assert call_bwd(params(d=256, flags=fa.FA_FLAG_DETERMINISTIC)) == fa.FA_ERR_UNSUPPORTED
-    assert call_bwd(params(d=192, flags=fa.FA_FLAG_DETERMINISTIC)) == fa.FA_ERR_UNSUPPORTED
     assert call_bwd(params(h_q=3, h_kv=2)) == fa.FA_ERR_INVALID_ARG
     assert call_bwd(params(), q=MISAL) == fa.FA_ERR_INVALID_ARG
 
@@ -291,3 +288,15 @@ def test_d256_backward_workspace():
     align = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert fa.fa_bwd_workspace_size(p) == 256 + 2 * align(stat) + align(2 * tiles * 128 * 256 * 4)
     assert call_bwd(p, ws_bytes=16) == fa.FA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("d", [64, 128, 192, 256])
+def test_deterministic_workspace_adds_tile_counters(d):
+    """FA_FLAG_DETERMINISTIC (every head dimension) adds one int32 turn counter per (key/value
+    head, query tile) to the backward's workspace."""
+    def align(x):
+        return (x + 255) // 256 * 256
+    p0 = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=d)
+    p1 = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=d, flags=fa.FA_FLAG_DETERMINISTIC)
+    tiles = 2 * ((300 + 63) // 64)  # P = 64 positions per tile (G = 2)
+    assert fa.fa_bwd_workspace_size(p1) == fa.fa_bwd_workspace_size(p0) + align(2 * tiles * 4)

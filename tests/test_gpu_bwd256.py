@@ -62,13 +62,3 @@ CASES = [
 @pytest.mark.parametrize("i", range(len(CASES)))
 def test_backward_d256(i):
     compare(case(i, **CASES[i]))
-
-
-def test_deterministic_flag_refused():
-    from exact_attention_bwd_gb300 import binding as fa
-    from gpu_helpers import dev_inputs
-    w = case(50, B=1, s_q=130, s_kv=130)
-    d = dev_inputs(w)
-    o, lse, _ = fa.forward(d["q"], d["k"], d["v"], causal=True)
-    with pytest.raises(fa.FaError):
-        fa.backward(d["q"], d["k"], d["v"], o, lse, d["dout"], causal=True, flags=fa.FA_FLAG_DETERMINISTIC)

@@ -81,13 +81,3 @@ def test_decode_and_chunked_prefill_d192(s_q):
 
 def test_decode_d192_sinks_window():
     compare(case(30, B=3, s_q=1, s_kv=1500, h_q=8, h_kv=2, causal=False, window=(300, 0), sinks=True), bwd=False)
-
-
-def test_deterministic_flag_refused_d192():
-    from exact_attention_bwd_gb300 import binding as fa
-    from gpu_helpers import dev_inputs
-    w = case(50, B=1, s_q=130, s_kv=130)
-    d = dev_inputs(w)
-    o, lse, _ = fa.forward(d["q"], d["k"], d["v"], causal=True)
-    with pytest.raises(fa.FaError):
-        fa.backward(d["q"], d["k"], d["v"], o, lse, d["dout"], causal=True, flags=fa.FA_FLAG_DETERMINISTIC)

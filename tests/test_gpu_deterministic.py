@@ -4,7 +4,7 @@ With the flag, dQ is summed over key blocks in a fixed order and the sink gradie
 fixed per-head reduction, so two runs on the same inputs give the same bits (the pages'
 deterministic backward option, vllm-project/flash-attention README, changelog 2.4).  The
 results must still match the fp64 oracle like the default backward, and agree with it
-within the same tolerance.  The shapes cover d = 64 and 128, causal and window bands
+within the same tolerance.  The shapes cover d = 64, 128, 192 and 256, causal and window bands
 (whose key blocks see different query-tile ranges, so the order has gaps and ends),
 grouped-query heads, packed batches with empty sequences, and the benchmark's full size.
 """
@@ -56,6 +56,11 @@ CASES = [
     dict(d=128, s_q=650, s_kv=200, h_q=4, h_kv=4, causal=True),
     dict(d=128, lengths=[17, 283, 128, 0, 1, 0, 300, 129], h_q=4, h_kv=2),
     dict(d=64, lengths=[400, 3, 0, 250], h_q=8, h_kv=2, causal=False, window=(50, 20), sinks=True),
+    # the wide-head kernel (64-key blocks)
+    dict(d=256),
+    dict(d=192, causal=False, window=(130, 40), h_q=8, h_kv=2, sinks=True),
+    dict(d=256, lengths=[17, 283, 128, 0, 1, 0, 300, 129], h_q=4, h_kv=2),
+    dict(d=192, s_q=200, s_kv=650, h_q=6, h_kv=2),
 ]
 
 
