@@ -64,7 +64,7 @@
  *    (FA_FLAG_VALIDATE_CU) or a timeout leaves the outputs of the rest of the call
  *    unwritten.
  *  - Supported: bf16 and fp16 (and e4m3 for the forward at d = 128, see below); head dim d in
- *    {64, 128, 192, 256} for the forward and the backward (FA_FLAG_DETERMINISTIC: d <= 128);
+ *    {64, 128, 192, 256} for the forward and the backward (FA_FLAG_DETERMINISTIC included);
  *    h_q / h_kv <= 128.  d = 192 is one of the head sizes the pages pad to (dew-flash-attn
  *    PyPI page, the FA3 head-dim padding to 64 / 128 / 192 / 256).
  *    Anything else returns FA_ERR_UNSUPPORTED.
@@ -140,8 +140,8 @@ typedef enum fa_status {
  * vllm-project/flash-attention README (changelog 2.4).  A key block's CTA waits (bounded,
  * like every wait: FA_ERR_TIMEOUT) for the later blocks' contributions, which the launch
  * puts at lower CTA indices; slower than the default, markedly so without a causal mask.
- * The sink gradient is summed in a fixed order with or without the flag.  d <= 128 only:
- * with d = 256 fa_bwd returns FA_ERR_UNSUPPORTED. */
+ * The sink gradient is summed in a fixed order with or without the flag.  Every head
+ * dimension (at d = 192 / 256 the key blocks are 64 keys). */
 #define FA_FLAG_DETERMINISTIC 4u
 
 typedef struct fa_params {
