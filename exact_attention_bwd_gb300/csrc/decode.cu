@@ -382,13 +382,33 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 3) combine_kernel(const Co
             m[q] = mn;
         }
     }
+    // (batch, head, position) of the lane group's first output row; the next rows follow by
+    // carrying (rows are ordered batch, head, position)
+    int i, h, b;
+    {
+        const long row = a.row0 + row0;
+        if (row < 0x7fffffffL) {
+            const unsigned r = (unsigned)row, hb = r / (unsigned)p.s_q;
+            i = (int)(r - hb * (unsigned)p.s_q);
+            b = (int)(hb / (unsigned)p.h_q);
+            h = (int)(hb - (unsigned)b * (unsigned)p.h_q);
+        } else {
+            i = (int)(row % p.s_q);
+            h = (int)((row / p.s_q) % p.h_q);
+            b = (int)(row / ((long)p.s_q * p.h_q));
+        }
+    }
 #pragma unroll
     for (int q = 0; q < RL; ++q) {
         if (row0 + q >= nrows) break;
+        if (q > 0 && ++i == p.s_q) {
+            i = 0;
+            if (++h == p.h_q) {
+                h = 0;
+                ++b;
+            }
+        }
         const long row = a.row0 + row0 + q;  // the output row
-        const int i = (int)(row % p.s_q);
-        const int h = (int)((row / p.s_q) % p.h_q);
-        const int b = (int)(row / ((long)p.s_q * p.h_q));
         const float sink = p.sinks ? p.sinks[h] : -INFINITY;
         const float m_all = fmaxf(m[q], sink);
         const float sc = m[q] == -INFINITY ? 0.f : __expf(m[q] - m_all);
