@@ -34,6 +34,7 @@ struct __align__(1024) DecSmem {
     uint8_t k[DecCfg<D, RG>::STAGES][DecCfg<D, RG>::TILE];
     uint8_t v[DecCfg<D, RG>::STAGES][DecCfg<D, RG>::TILE];
     float mw[kComputeWarps][4 * RG], lw[kComputeWarps][4 * RG];
+    float4 pbuf[kComputeWarps][KPW];  // a warp's P of the current tile: [key][row of the group]
     uint64_t full[DecCfg<D, RG>::STAGES], empty[DecCfg<D, RG>::STAGES];
     int abort_flag;
 };
@@ -102,6 +103,11 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
     j_end = sv.nq > 0 ? min(j_end, band.hi(sv.nq - 1) + 1) : 0;
     const int t_begin = j_begin / BK;
     const int n_tiles = j_end > j_begin ? (j_end - 1) / BK + 1 - t_begin : 0;
+    // keys every query row may see, whether its position is used or not (the band bounds are
+    // monotone in the position, positions 0 .. s_q - 1): a tile inside [in_lo, in_hi] needs
+    // no per-key mask
+    const int in_lo = max(j_begin, band.lo(p.s_q - 1));
+    const int in_hi = min(j_end - 1, band.hi(0));
 
     Abort ab{&s.abort_flag, a.status, p.wait_ns};
     if (tid == 0) {
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
                 if (!__all_sync(0xffffffffu, w)) break;
             }
             const int jw = (t_begin + t) * BK + KPW * warp;  // first key of this warp
+            const bool interior = (t_begin + t) * BK >= in_lo && (t_begin + t) * BK + BK - 1 <= in_hi;
             float kv[KPW][EPL];
 #pragma unroll
             for (int k = 0; k < KPW; ++k) load_row_slice<EPL, C::CHUNK, F16>(s.k[st], KPW * warp + k, e0, kv[k]);
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
                 }
                 const int r = 4 * rg + rr;
                 float sc = v32[0];
-                {
+                if (!interior || r >= R) {
                     const int i = r / p.G;
                     const bool keep = r < R && j >= j_begin && j < j_end && j >= band.lo(i) && j <= band.hi(i);
                     if (!keep) sc = -INFINITY;
@@ -215,31 +222,46 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
                 const float m_old = (rr == 0) ? m[4 * rg] : (rr == 1) ? m[4 * rg + 1] : (rr == 2) ? m[4 * rg + 2] : m[4 * rg + 3];
-                const float m_new = fmaxf(m_old, mt);
+                // the running max moves only when it grows by more than 2^8 (exact: every
+                // exponential stays below 256 and the final division uses the same max)
+                const bool grow = m_old == -INFINITY ? mt > -INFINITY : mt > m_old + 8.f;
+                const bool any_grow = __any_sync(0xffffffffu, grow);
+                const float m_new = grow ? mt : m_old;
                 const float base = (m_new == -INFINITY) ? 0.f : m_new;
                 const float pr = ex2(sc - base);
-                const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - base);
                 float ps = pr;
                 ps += __shfl_xor_sync(0xffffffffu, ps, 4);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 8);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                // every lane takes the new state of the group's 4 rows from lanes 0..3
+                if (any_grow) {
+                    // some row's max moved: every lane takes the new state of the group's 4 rows
+                    // from lanes 0..3 and rescales its accumulators
+                    const float alpha = (m_old == -INFINITY) ? 0.f : (grow ? ex2(m_old - base) : 1.f);
 #pragma unroll
-                for (int r4 = 0; r4 < 4; ++r4) {
-                    const float al = __shfl_sync(0xffffffffu, alpha, r4);
-                    m[4 * rg + r4] = __shfl_sync(0xffffffffu, m_new, r4);
-                    l[4 * rg + r4] = l[4 * rg + r4] * al + __shfl_sync(0xffffffffu, ps, r4);
+                    for (int r4 = 0; r4 < 4; ++r4) {
+                        const float al = __shfl_sync(0xffffffffu, alpha, r4);
+                        m[4 * rg + r4] = __shfl_sync(0xffffffffu, m_new, r4);
+                        l[4 * rg + r4] = l[4 * rg + r4] * al + __shfl_sync(0xffffffffu, ps, r4);
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc[4 * rg + r4][e] *= al;
+                        for (int e = 0; e < EPL; ++e) acc[4 * rg + r4][e] *= al;
+                    }
+                } else {
+#pragma unroll
+                    for (int r4 = 0; r4 < 4; ++r4) l[4 * rg + r4] += __shfl_sync(0xffffffffu, ps, r4);
                 }
+                // P of the warp's 8 keys to every lane: lane 4k + r holds (key k, row r)
+                reinterpret_cast<float*>(s.pbuf[warp])[lane] = pr;
+                __syncwarp();
                 // O += P V over the warp's 8 keys
 #pragma unroll
                 for (int k = 0; k < KPW; ++k) {
                     float vv[EPL];
                     load_row_slice<EPL, C::CHUNK, F16>(s.v[st], KPW * warp + k, e0, vv);
+                    const float4 p4 = s.pbuf[warp][k];
+                    const float pk4[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
                     for (int r4 = 0; r4 < 4; ++r4) {
-                        const float pk = __shfl_sync(0xffffffffu, pr, 4 * k + r4);
+                        const float pk = pk4[r4];
 #pragma unroll
                         for (int e = 0; e < EPL; e += 2) {
                             const float2 o2 = __ffma2_rn(make_float2(pk, pk), make_float2(vv[e], vv[e + 1]),
@@ -249,6 +271,7 @@ __global__ void __launch_bounds__(kThreadsDec, DecCfg<D, RG>::MIN_BLOCKS)
                         }
                     }
                 }
+                __syncwarp();  // pbuf is rewritten by the next row group or tile
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.empty[st]);
