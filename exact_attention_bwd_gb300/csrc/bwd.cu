@@ -401,11 +401,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                     tc_fence_before();
                     mbar_arrive(&s.dq_free);
                     if (DET && !dq_turn_wait(cnt, need, ab)) { ok = false; break; }
-                    float4* acc = reinterpret_cast<float4*>(a.dq_acc + (trow + tl) * D);
+                    float* acc = a.dq_acc + (trow + tl) * D;
+                    const uint64_t keep = policy_evict_last();
 #pragma unroll
                     for (int t4 = 0; t4 < D / 4; ++t4)
-                        atomicAdd(acc + t4, make_float4(__uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
-                                                        __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3])));
+                        red_add4_hint(acc + 4 * t4, __uint_as_float(qv[4 * t4]), __uint_as_float(qv[4 * t4 + 1]),
+                                      __uint_as_float(qv[4 * t4 + 2]), __uint_as_float(qv[4 * t4 + 3]), keep);
                 }
                 if constexpr (DET) dq_turn_done(cnt);
                 tr.mark(kMDqReduced);

@@ -157,6 +157,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void red_add_hint(float* p, float v, uint64_t pol) {
     asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
 }
+// Four consecutive fp32 reductions (16-byte aligned) under an L2 cache policy.
+__device__ __forceinline__ void red_add4_hint(float* p, float a, float b, float c, float d, uint64_t pol) {
+    asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d), "l"(pol)
+                 : "memory");
+}
 // tma_load_4d under an L2 cache policy.
 __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
                                                  int c2, int c3, uint64_t pol) {
