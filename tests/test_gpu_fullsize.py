@@ -223,3 +223,60 @@ def test_wide_head_tail_split(d, sinks):
         ro, rl, _ = oracle.fwd(qq, kk, vv, scale=w["scale"], causal=True, sinks=sk)
         check(f"O unit {unit}", from_dev(o[b:b + 1, :, hs]), ro)
         check_lse(f"LSE unit {unit}", lse[b, hs].cpu().numpy(), rl[0])
+
+
+def test_offsets_beyond_int32_elements():
+    """Q, O, dO and dQ of more than 2^31 elements (B=1, s=140000, h_q=128, h_kv=32, d=128:
+    2.29e9 each, 4.6 GB in bf16; the fp32 dQ accumulator 9.2 GB), with a causal (127, 0)
+    window so the whole call stays short (groups of 4 query heads: with 16, the dK and dV
+    of the first keys, which sum 16 heads' rows of nearly one-hot P, exceed the absolute
+    bound already in an exact bf16-operand emulation).  Every address the kernels form past element 2^31
+    must be 64-bit.  A query row sees its 128 nearest keys and a key is seen by the 128 rows
+    after it, so a block of rows together with the 127 keys before it is an exact
+    sub-problem (bottom-right alignment keeps the diagonal) for O, LSE and dQ of its rows
+    and for dK, dV of its own keys; blocks at the start, across element 2^31 and at the end
+    are checked."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    B, s, h_q, h_kv, d = 1, 140000, 128, 32, 128
+    G = h_q // h_kv
+    assert s * h_q * d > 2 ** 31
+    window = (127, 0)
+    seed = lambda t: inputs.seed_of(34, 0, t)  # noqa: E731
+    q = inputs.normal_bf16_torch(seed(inputs.Q), (B, s, h_q, d), "cuda")
+    k = inputs.normal_bf16_torch(seed(inputs.K), (B, s, h_kv, d), "cuda")
+    v = inputs.normal_bf16_torch(seed(inputs.V), (B, s, h_kv, d), "cuda")
+    do = inputs.normal_bf16_torch(seed(inputs.DO), (B, s, h_q, d), "cuda")
+    scale = 1.0 / np.sqrt(d)
+    kw = dict(causal=True, window=window, softmax_scale=scale)
+    o, lse, ws = fa.forward(q, k, v, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == 0
+    del ws
+    dq, dk, dv, _, ws2 = fa.backward(q, k, v, o, lse, do, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws2) == 0
+    del ws2
+    torch.cuda.empty_cache()
+    edge = 2 ** 31 // (h_q * d)  # the position whose first element is element 2^31
+    for i0, g in [(0, 0), (edge - 100, 3), (s - 200, h_kv - 1)]:
+        i1 = i0 + 200
+        j0 = max(0, i0 - 127)
+        hs = slice(g * G, (g + 1) * G)
+        qq, dd = (from_dev(t[:, i0:i1, hs]) for t in (q, do))
+        kk, vv = (from_dev(t[:, j0:i1, g:g + 1]) for t in (k, v))
+        okw = dict(scale=scale, causal=True, window=window)
+        ro, rl, _ = oracle.fwd(qq, kk, vv, **okw)
+        rdq, rdk, rdv, _ = oracle.bwd(qq, kk, vv, dd, **okw)
+        check(f"O rows {i0}", from_dev(o[:, i0:i1, hs]), ro)
+        check_lse(f"LSE rows {i0}", lse[0, hs, i0:i1].cpu().numpy(), rl[0])
+        check(f"dQ rows {i0}", from_dev(dq[:, i0:i1, hs]), rdq)
+        # keys of the block that no row after i1 sees
+        kb = i0 - j0
+        check(f"dK keys {i0}", from_dev(dk[:, i0:i1 - 127, g:g + 1]), rdk[:, kb:kb + 200 - 127])
+        check(f"dV keys {i0}", from_dev(dv[:, i0:i1 - 127, g:g + 1]), rdv[:, kb:kb + 200 - 127])
+        if i1 == s:  # the last block's keys are all seen only by the block's rows
+            check("dK last keys", from_dev(dk[:, i0:, g:g + 1]), rdk[:, kb:])
+            check("dV last keys", from_dev(dv[:, i0:, g:g + 1]), rdv[:, kb:])
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
