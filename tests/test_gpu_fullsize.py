@@ -225,30 +225,39 @@ def test_wide_head_tail_split(d, sinks):
         check_lse(f"LSE unit {unit}", lse[b, hs].cpu().numpy(), rl[0])
 
 
-def test_offsets_beyond_int32_elements():
-    """Q, O, dO and dQ of more than 2^31 elements (B=1, s=140000, h_q=128, h_kv=32, d=128:
+@pytest.mark.parametrize("packed", [False, True], ids=["dense", "packed"])
+def test_offsets_beyond_int32_elements(packed):
+    """Q, O, dO and dQ of more than 2^31 elements (s=140000 tokens, h_q=128, h_kv=32, d=128:
     2.29e9 each, 4.6 GB in bf16; the fp32 dQ accumulator 9.2 GB), with a causal (127, 0)
     window so the whole call stays short (groups of 4 query heads: with 16, the dK and dV
     of the first keys, which sum 16 heads' rows of nearly one-hot P, exceed the absolute
-    bound already in an exact bf16-operand emulation).  Every address the kernels form past element 2^31
-    must be 64-bit.  A query row sees its 128 nearest keys and a key is seen by the 128 rows
-    after it, so a block of rows together with the 127 keys before it is an exact
-    sub-problem (bottom-right alignment keeps the diagonal) for O, LSE and dQ of its rows
-    and for dK, dV of its own keys; blocks at the start, across element 2^31 and at the end
-    are checked."""
+    bound already in an exact bf16-operand emulation).  Every address the kernels form past
+    element 2^31 must be 64-bit.  Dense: one batch of 140000 positions; packed: the same
+    tokens as sequences of 60000, 0 and 80000 (one offsets array for queries and keys, so
+    the token-tile path).  A query row sees its 128 nearest keys of its sequence and a key
+    is seen by the 128 rows after it, so a block of rows together with the up to 127 keys
+    before it is an exact sub-problem (bottom-right alignment keeps the diagonal) for O,
+    LSE and dQ of its rows and for dK, dV of its own keys; blocks at the start, across
+    element 2^31 and at the end are checked (packed: also at the third sequence's start)."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
-    B, s, h_q, h_kv, d = 1, 140000, 128, 32, 128
+    s, h_q, h_kv, d = 140000, 128, 32, 128
     G = h_q // h_kv
     assert s * h_q * d > 2 ** 31
     window = (127, 0)
     seed = lambda t: inputs.seed_of(34, 0, t)  # noqa: E731
-    q = inputs.normal_bf16_torch(seed(inputs.Q), (B, s, h_q, d), "cuda")
-    k = inputs.normal_bf16_torch(seed(inputs.K), (B, s, h_kv, d), "cuda")
-    v = inputs.normal_bf16_torch(seed(inputs.V), (B, s, h_kv, d), "cuda")
-    do = inputs.normal_bf16_torch(seed(inputs.DO), (B, s, h_q, d), "cuda")
+    q = inputs.normal_bf16_torch(seed(inputs.Q), (1, s, h_q, d), "cuda")
+    k = inputs.normal_bf16_torch(seed(inputs.K), (1, s, h_kv, d), "cuda")
+    v = inputs.normal_bf16_torch(seed(inputs.V), (1, s, h_kv, d), "cuda")
+    do = inputs.normal_bf16_torch(seed(inputs.DO), (1, s, h_q, d), "cuda")
     scale = 1.0 / np.sqrt(d)
     kw = dict(causal=True, window=window, softmax_scale=scale)
+    starts = [0]
+    if packed:
+        cu = torch.tensor([0, 60000, 60000, s], dtype=torch.int32, device="cuda")
+        kw.update(cu_q=cu, cu_k=cu)
+        starts = [0, 60000]
+        q, k, v, do = (t[0] for t in (q, k, v, do))
     o, lse, ws = fa.forward(q, k, v, **kw)
     torch.cuda.synchronize()
     assert fa.device_status(ws) == 0
@@ -258,10 +267,15 @@ def test_offsets_beyond_int32_elements():
     assert fa.device_status(ws2) == 0
     del ws2
     torch.cuda.empty_cache()
+    if packed:  # back to the dense [1, s, h, d] / [1, h, s] views for the checks
+        q, k, v, do, o, dq, dk, dv = (t.unsqueeze(0) for t in (q, k, v, do, o, dq, dk, dv))
+        lse = lse.unsqueeze(0)
     edge = 2 ** 31 // (h_q * d)  # the position whose first element is element 2^31
-    for i0, g in [(0, 0), (edge - 100, 3), (s - 200, h_kv - 1)]:
+    blocks = [(0, 0), (edge - 100, 3), (s - 200, h_kv - 1)] + ([(60000, 17)] if packed else [])
+    for i0, g in blocks:
         i1 = i0 + 200
-        j0 = max(0, i0 - 127)
+        start = max(x for x in starts if x <= i0)
+        j0 = max(start, i0 - 127)
         hs = slice(g * G, (g + 1) * G)
         qq, dd = (from_dev(t[:, i0:i1, hs]) for t in (q, do))
         kk, vv = (from_dev(t[:, j0:i1, g:g + 1]) for t in (k, v))
