@@ -222,6 +222,52 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
+def _check_tensors(q, named):
+    """Every tensor handed to the library: on q's CUDA device (the C ABI takes plain device
+    pointers; a host pointer there would be dereferenced by the kernels), contiguous (the
+    layouts are dense [B, S, H, D], [T, H, D] or the stated vectors), with the given element
+    type and element count or shape.  named: (name, tensor or None, dtype, shape or count)."""
+    import torch
+    if q.device.type != "cuda":
+        raise ValueError(f"q must be a CUDA tensor; it is on {q.device}")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    for name, t, dtype, want in named:
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}; every tensor must be on q's device {q.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}; it is {t.dtype}")
+        if isinstance(want, int):
+            if t.numel() != want:
+                raise ValueError(f"{name} must have {want} elements; it has {t.numel()}")
+        elif want is not None and tuple(t.shape) != tuple(want):
+            raise ValueError(f"{name} must have shape {tuple(want)}; it has {tuple(t.shape)}")
+
+
+def _vector_args(p, sinks, cu_q, cu_k, seqused_q, seqused_k):
+    """The optional per-head / per-sequence vectors of a call, for _check_tensors."""
+    import torch
+    i32, f32 = torch.int32, torch.float32
+    return [("sinks", sinks, f32, p.h_q), ("cu_q", cu_q, i32, p.B + 1), ("cu_k", cu_k, i32, p.B + 1),
+            ("seqused_q", seqused_q, i32, p.B), ("seqused_k", seqused_k, i32, p.B)]
+
+
+def _kv_shape(p, k, cu_q, block_table):
+    """The shape k must have: [B, s_kv, h_kv, d] dense, [T_k, h_kv, d] packed, or a page pool
+    [num_pages, page_size, h_kv, d]; B and d are q's (so no kernel reads past k's end)."""
+    if block_table is not None:
+        return (p.num_pages, p.page_size, p.h_kv, p.d)
+    if cu_q is not None:
+        return (p.s_kv, p.h_kv, p.d)
+    return (p.B, p.s_kv, p.h_kv, p.d)
+
+
 def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks=None, cu_q=None, cu_k=None,
             flags=0, out=None, lse=None, workspace=None, seqused_k=None, block_table=None, s_kv=None,
             descale=None, seqused_q=None, wait_limit_ns=0):
@@ -242,6 +288,15 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
                     cu_k=cu_k, flags=flags, seqused_k=seqused_k, block_table=block_table, s_kv=s_kv,
                     dtype=_type_code(q.dtype), q_descale=dq_, k_descale=dk_, v_descale=dv_,
                     seqused_q=seqused_q, wait_limit_ns=wait_limit_ns)
+    lse_shape = (p.B, p.h_q, p.s_q) if cu_q is None else (p.h_q, p.s_q)
+    _check_tensors(q, [("k", k, None, _kv_shape(p, k, cu_q, block_table)), ("v", v, None, k.shape),
+                       ("out", out, torch.bfloat16 if fp8 else q.dtype, q.shape), ("lse", lse, torch.float32, lse_shape),
+                       ("workspace", workspace, torch.uint8, None),
+                       ("block_table", block_table, torch.int32, None if block_table is None else
+                        (p.B, p.max_blocks_per_seq)),
+                       ("q_descale", dq_, torch.float32, p.B * p.h_kv), ("k_descale", dk_, torch.float32, p.B * p.h_kv),
+                       ("v_descale", dv_, torch.float32, p.B * p.h_kv)]
+                   + _vector_args(p, sinks, cu_q, cu_k, seqused_q, seqused_k))
     nbytes = fa_fwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_fwd_workspace_size")
@@ -250,8 +305,7 @@ def forward(q, k, v, *, causal=False, window=(-1, -1), softmax_scale=None, sinks
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16 if fp8 else q.dtype, device=q.device)
     if lse is None:
-        shape = (p.B, p.h_q, p.s_q) if cu_q is None else (p.h_q, p.s_q)
-        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     rc = fa_fwd(p, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream())
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
@@ -276,6 +330,15 @@ def backward(q, k, v, o, lse, dout, *, causal=False, window=(-1, -1), softmax_sc
     p = make_params(q, k, causal=causal, window=window, softmax_scale=softmax_scale, sinks=sinks, cu_q=cu_q,
                     cu_k=cu_k, flags=flags, seqused_q=seqused_q, seqused_k=seqused_k, dtype=_type_code(q.dtype),
                     wait_limit_ns=wait_limit_ns)
+    lse_shape = (p.B, p.h_q, p.s_q) if cu_q is None else (p.h_q, p.s_q)
+    g = (None, None, None, None) if grads is None else tuple(grads)
+    _check_tensors(q, [("k", k, None, _kv_shape(p, k, cu_q, None)), ("v", v, None, k.shape), ("o", o, None, q.shape),
+                       ("lse", lse, torch.float32, lse_shape), ("dout", dout, None, q.shape),
+                       ("dq", g[0], None, q.shape), ("dk", g[1], None, k.shape), ("dv", g[2], None, k.shape),
+                       ("dsinks", g[3], torch.float32, p.h_q), ("workspace", workspace, torch.uint8, None)]
+                   + _vector_args(p, sinks, cu_q, cu_k, seqused_q, seqused_k))
+    if lse is None:
+        raise ValueError("the backward needs the forward's lse")
     nbytes = fa_bwd_workspace_size(p)
     if nbytes == 0:
         raise FaError(FA_ERR_UNSUPPORTED, "fa_bwd_workspace_size")

@@ -300,3 +300,14 @@ def test_deterministic_workspace_adds_tile_counters(d):
     p1 = params(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=d, flags=fa.FA_FLAG_DETERMINISTIC)
     tiles = 2 * ((300 + 63) // 64)  # P = 64 positions per tile (G = 2)
     assert fa.fa_bwd_workspace_size(p1) == fa.fa_bwd_workspace_size(p0) + align(2 * tiles * 4)
+
+
+def test_binding_rejects_host_tensors():
+    """The library takes device pointers only: host tensors never reach it (no CPU path)."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 8, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.forward(q, q, q)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.backward(q, q, q, q, lse, q)
