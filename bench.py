@@ -523,8 +523,9 @@ def measure_d256(dev):
 
 def measure_fp8(dev, name, steps=8, warmup=3):
     """Forward with e4m3 inputs (same shapes; stored values N(0, 32^2) rounded to e4m3 with
-    per-(batch, kv head) descales): the whole fa_fwd call (V transpose + kernel) by CUDA
-    events, L2 flushed before every timed call; TFLOPS with the same FLOP convention."""
+    per-(batch, kv head) descales): the whole fa_fwd call by CUDA events and the kernel
+    alone by the library's own events, L2 flushed before every timed call; TFLOPS with the
+    same FLOP convention."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
     w = inputs.workload(name)

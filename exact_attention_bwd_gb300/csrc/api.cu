@@ -198,8 +198,6 @@ struct FwdPlan {
     int kt = 128;          // keys per key tile of the d <= 128 kernel (64: two CTAs per SM)
     int tail_units = 0, tail_k = 0, tail_split_tiles = 0;  // tail split (d = 192 / 256)
     size_t part_rows = 0;  // rows of the split partials
-    int s_pad = 0;         // e4m3: keys per V^T row (s_kv rounded up to 16)
-    size_t off_vt = 0;     // e4m3: workspace offset of V^T
     size_t off_trace = 0;  // trace builds: the per-role event records (tensor-core path)
     size_t ws_bytes = kStatusBytes;
 };
@@ -324,11 +322,6 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
     if (p.d == 64 && p.dtype != FA_DTYPE_E4M3 && pl.n_splits == 1 && p.left >= 0 && p.right >= 0 &&
         (long)p.left + p.right + p.P <= 384)
         pl.kt = 64;
-    if (p.dtype == FA_DTYPE_E4M3) {  // V^T [B][h_kv][d][s_pad] after the partials
-        pl.s_pad = (p.s_kv + 15) / 16 * 16;
-        pl.off_vt = pl.ws_bytes;
-        pl.ws_bytes += align256((size_t)p.B * p.h_kv * p.d * pl.s_pad);
-    }
 #ifdef FA_TRACE
     pl.off_trace = pl.ws_bytes;
     pl.ws_bytes += align256(kTraceBytes);
@@ -521,28 +514,21 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     FwdArgs a{};
     CUtensorMap tq;
     if (p.dtype == FA_DTYPE_E4M3) {
-        // Q, K: [b][s][h][128] bytes; V^T: [b][h_kv][128][s_pad] bytes, built here from V
+        // Q, K, V: [b][s][h][128] bytes (the kernel transposes each V tile in shared memory)
         const cuuint64_t dq[4] = {128, (cuuint64_t)p.h_q, (cuuint64_t)p.s_q, (cuuint64_t)p.B};
         const cuuint64_t sq[3] = {128, (cuuint64_t)p.h_q * 128, (cuuint64_t)p.s_q * p.h_q * 128};
         const cuuint32_t bq[4] = {128, (cuuint32_t)p.G, (cuuint32_t)p.P, 1};
         const cuuint64_t dk[4] = {128, (cuuint64_t)p.h_kv, (cuuint64_t)p.s_kv, (cuuint64_t)p.B};
         const cuuint64_t sk[3] = {128, (cuuint64_t)p.h_kv * 128, (cuuint64_t)p.s_kv * p.h_kv * 128};
         const cuuint32_t bk[4] = {128, 1, 128, 1};
-        uint8_t* vt = ws + pl.off_vt;
-        const cuuint64_t dv[4] = {(cuuint64_t)p.s_kv, 128, (cuuint64_t)p.h_kv, (cuuint64_t)p.B};
-        const cuuint64_t sv[3] = {(cuuint64_t)pl.s_pad, (cuuint64_t)pl.s_pad * 128, (cuuint64_t)pl.s_pad * 128 * p.h_kv};
-        const cuuint32_t bv[4] = {128, 128, 1, 1};
-        CUtensorMap tk8, tvt;
-        if (!encode_u8_4d(&tq, q, dq, sq, bq) || !encode_u8_4d(&tk8, k, dk, sk, bk) || !encode_u8_4d(&tvt, vt, dv, sv, bv))
+        CUtensorMap tk8, tv8;
+        if (!encode_u8_4d(&tq, q, dq, sq, bq) || !encode_u8_4d(&tk8, k, dk, sk, bk) || !encode_u8_4d(&tv8, v, dk, sk, bk))
             return FA_ERR_CUDA;
-        cudaError_t e = launch_transpose_v_e4m3(reinterpret_cast<const uint8_t*>(v), vt, p.B, p.s_kv, p.h_kv, pl.s_pad,
-                                                st);
-        if (e != cudaSuccess) return FA_ERR_CUDA;
         a.q_descale = in->q_descale;
         a.k_descale = in->k_descale;
         a.v_descale = in->v_descale;
         tk = tk8;
-        tv = tvt;
+        tv = tv8;
     } else if (!encode_bhsd(&tq, q, p.d, p.h_q, tokens_q, bdim, p.G, p.P, f16)) {
         return FA_ERR_CUDA;
     }

@@ -13,12 +13,15 @@
 //    memory, so the S tile is free as soon as the softmax has read it into registers and
 //    the next S = Q K^T is issued while the softmax still works: the softmax warps run back
 //    to back instead of waiting for each P V to finish.
-//  - Both GEMMs use K-major operands only: V is transposed to V^T [b][h][d][keys] by a
-//    pre-pass kernel, so P V reads V^T tiles exactly as S = Q K^T reads K tiles.
-//  - A 128-element e4m3 row is one 128-byte swizzle atom: Q, K, V^T and P tiles are 16 KB.
+//  - Both GEMMs use K-major operands only: each V tile arrives by TMA as it is stored
+//    ([keys][d], like K) into a staging slot, and warps 2 and 3 transpose it into a V^T tile
+//    ([d][keys]) of the ring the MMA reads, so P V reads V^T tiles exactly as S = Q K^T reads
+//    K tiles (no pass over V in memory).
+//  - A 128-element e4m3 row is one 128-byte swizzle atom: Q, K, V, V^T and P tiles are 16 KB.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
-// warps 4..7 and 8..11 the softmax of query tiles 0 and 1 (one thread per row).
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2 and 3 the V
+// transpose (warp 2 also owns the TMEM allocation), warps 4..7 and 8..11 the softmax of
+// query tiles 0 and 1 (one thread per row).
 #include "fwd_items.cuh"
 
 namespace fa {
@@ -26,15 +29,19 @@ namespace {
 
 constexpr int kThreads8 = 384;
 constexpr int kTile8 = 128 * 128;  // bytes of one e4m3 tile (128 rows of 128 bytes)
-constexpr int kStages8 = 4;
+constexpr int kStagesK = 4;   // K ring
+constexpr int kStagesVt = 2;  // V^T ring (written by the transpose warps)
+constexpr int kStagesV = 2;   // V staging ring (written by TMA)
 
 struct __align__(1024) Smem8 {
     uint8_t q[2][kTile8];
-    uint8_t k[kStages8][kTile8];
-    uint8_t vt[kStages8][kTile8];  // V^T tiles: [128 d rows][128 keys]
-    uint8_t p[2][2][kTile8];       // [query tile][buffer]: P rows of 128 keys
+    uint8_t k[kStagesK][kTile8];
+    uint8_t vt[kStagesVt][kTile8];  // V^T tiles: [128 d rows][128 keys]
+    uint8_t v[kStagesV][kTile8];    // V tiles as stored: [128 keys][128 d]
+    uint8_t p[2][2][kTile8];        // [query tile][buffer]: P rows of 128 keys
     uint64_t q_full, q_empty;
-    uint64_t k_full[kStages8], k_empty[kStages8], v_full[kStages8], v_empty[kStages8];
+    uint64_t k_full[kStagesK], k_empty[kStagesK], v_full[kStagesVt], v_empty[kStagesVt];
+    uint64_t vin_full[kStagesV], vin_empty[kStagesV];
     uint64_t s_full[2], s_free[2];
     uint64_t p_full[2][2], p_free[2][2];
     uint64_t o_full[2], o_free[2];
@@ -47,41 +54,37 @@ struct __align__(1024) Smem8 {
 static_assert(sizeof(Smem8) + 1024 <= 232448, "e4m3 forward shared memory exceeds 227 KB");
 
 // ------------------------------------------------------------------------------------------
-// V -> V^T pre-pass: one CTA of 4 warps per (128-key block, kv head, batch), no shared
-// memory.  Warp w takes bytes [32w, 32w + 32) of d, lane l keys 4l .. 4l + 3 of the block:
-// each key's 32 bytes come in with two 16-byte loads, every 4 x 4 byte block (4 keys x 4
-// values of d) is transposed in registers with byte permutes, and each of the lane's 32
-// d rows gets one 4-byte word, so a warp store writes 128 consecutive bytes of a V^T row.
-// Keys past s_kv are written as zeros up to s_pad (a multiple of 16).
+// V -> V^T inside the CTA: warp w (0 or 1) of the two transpose warps takes the 16-byte units
+// U = 4w .. 4w + 3 of d, lane l the keys 4l .. 4l + 3.  For each U the lane loads its four
+// keys' 16 bytes (one 16-byte load per key row of the swizzled V tile), transposes each of
+// the four 4 x 4 byte blocks in registers with byte permutes and stores one 4-byte word into
+// each of the 16 d rows of the V^T tile, so a warp store covers one whole 128-byte row.
 // ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) transpose_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
-                                                          int s_kv, int h_kv, int s_pad) {
-    const int g = blockIdx.y, b = blockIdx.z;
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int key0 = blockIdx.x * 128 + 4 * lane;  // first of the lane's four keys
-    if (key0 >= s_pad) return;
-    uint32_t x[4][8];  // [key][word]: bytes 4 j .. 4 j + 3 of the warp's 32 values of d
+__device__ __forceinline__ void transpose_v_tile(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt, int w,
+                                                 int lane) {
+#pragma unroll 1
+    for (int U = 4 * w; U < 4 * w + 4; ++U) {
+        uint32_t x[4][4];  // [key 4 lane + i][word c]: bytes 16 U + 4 c .. + 3 of d
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (key0 + i < s_kv) {
-            const uint4* src = reinterpret_cast<const uint4*>(v + (((long)b * s_kv + key0 + i) * h_kv + g) * 128 + 32 * w);
-            lo = src[0];
-            hi = src[1];
+        for (int i = 0; i < 4; ++i) {
+            const int key = 4 * lane + i;
+            const uint4 u = *reinterpret_cast<const uint4*>(v + key * 128 + ((U ^ (key & 7)) << 4));
+            x[i][0] = u.x, x[i][1] = u.y, x[i][2] = u.z, x[i][3] = u.w;
         }
-        x[i][0] = lo.x, x[i][1] = lo.y, x[i][2] = lo.z, x[i][3] = lo.w;
-        x[i][4] = hi.x, x[i][5] = hi.y, x[i][6] = hi.z, x[i][7] = hi.w;
-    }
-    uint8_t* dst = vt + (((long)b * h_kv + g) * 128 + 32 * w) * s_pad + key0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        // rows 4j .. 4j+3 of the warp's d range, keys key0 .. key0+3 (lowest byte first)
-        const uint32_t t0 = __byte_perm(x[0][j], x[1][j], 0x5140), t1 = __byte_perm(x[2][j], x[3][j], 0x5140);
-        const uint32_t t2 = __byte_perm(x[0][j], x[1][j], 0x7362), t3 = __byte_perm(x[2][j], x[3][j], 0x7362);
-        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 0) * s_pad) = __byte_perm(t0, t1, 0x5410);
-        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 1) * s_pad) = __byte_perm(t0, t1, 0x7632);
-        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 2) * s_pad) = __byte_perm(t2, t3, 0x5410);
-        *reinterpret_cast<uint32_t*>(dst + (long)(4 * j + 3) * s_pad) = __byte_perm(t2, t3, 0x7632);
+        for (int c = 0; c < 4; ++c) {
+            // d rows 16 U + 4 c + 0..3, keys 4 lane .. 4 lane + 3 (lowest byte first)
+            const uint32_t t0 = __byte_perm(x[0][c], x[1][c], 0x5140), t1 = __byte_perm(x[2][c], x[3][c], 0x5140);
+            const uint32_t t2 = __byte_perm(x[0][c], x[1][c], 0x7362), t3 = __byte_perm(x[2][c], x[3][c], 0x7362);
+            const uint32_t row_words[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632),
+                                           __byte_perm(t2, t3, 0x5410), __byte_perm(t2, t3, 0x7632)};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int d = 16 * U + 4 * c + m;
+                *reinterpret_cast<uint32_t*>(vt + d * 128 + (((lane >> 2) ^ (d & 7)) << 4) + 4 * (lane & 3)) =
+                    row_words[m];
+            }
+        }
     }
 }
 
@@ -93,7 +96,7 @@ __device__ __forceinline__ uint32_t sw128_unit(int r, int u) {
 
 __global__ void __launch_bounds__(kThreads8, 1)
     fwd_e4m3_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmvt) {
+                    const __grid_constant__ CUtensorMap tmv) {
     constexpr int D = 128;
     extern __shared__ uint8_t smem_raw[];
     Smem8& s = *reinterpret_cast<Smem8*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -107,11 +110,17 @@ __global__ void __launch_bounds__(kThreads8, 1)
         s.abort_flag = 0;
         mbar_init(&s.q_full, 1);
         mbar_init(&s.q_empty, 1);
-        for (int i = 0; i < kStages8; ++i) {
+        for (int i = 0; i < kStagesK; ++i) {
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.k_empty[i], 1);
-            mbar_init(&s.v_full[i], 1);
+        }
+        for (int i = 0; i < kStagesVt; ++i) {
+            mbar_init(&s.v_full[i], 2);  // one arrive per transpose warp
             mbar_init(&s.v_empty[i], 1);
+        }
+        for (int i = 0; i < kStagesV; ++i) {
+            mbar_init(&s.vin_full[i], 1);
+            mbar_init(&s.vin_empty[i], 2);
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&s.s_full[k], 1);
@@ -141,16 +150,16 @@ __global__ void __launch_bounds__(kThreads8, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-    // registers: 384 x 168 at launch; the producer/MMA group hands part of its share to
-    // the softmax groups (128 x 56 + 256 x 224 = 64512)
+    // registers: 384 x 168 at launch; the producer / MMA / transpose group hands part of
+    // its share to the softmax groups (128 x 72 + 256 x 216 = 64512)
     if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmvt);
+            tma_prefetch_desc(&tmv);
             const uint32_t qbox = (uint32_t)(p.P * p.G) * 128u;  // bytes of one Q box
             int gt = 0, n_q = 0, k_issued = 0, v_issued = 0;
             bool ok = true;
@@ -168,26 +177,28 @@ __global__ void __launch_bounds__(kThreads8, 1)
                         tma_load_4d(s.q[k], &tmq, &s.q_full, 0, w.g * p.G, w.sv.q0 + w.ti[k].s0, w.sv.tma_b);
                 ++n_q;
                 for (int j = w.u0; j < w.u1; ++j, ++gt) {
-                    const int st = gt % kStages8;
-                    const uint32_t ph = (gt / kStages8) & 1;
-                    if (!(ok = mbar_wait(&s.k_empty[st], ph ^ 1, ab))) break;
+                    const int st = gt % kStagesK;
+                    if (!(ok = mbar_wait(&s.k_empty[st], ((gt / kStagesK) & 1) ^ 1, ab))) break;
                     mbar_expect_tx(&s.k_full[st], kTile8);
                     tma_load_4d(s.k[st], &tmk, &s.k_full[st], 0, w.g, j * BN, w.sv.tma_b);
                     ++k_issued;
-                    if (!(ok = mbar_wait(&s.v_empty[st], ph ^ 1, ab))) break;
-                    mbar_expect_tx(&s.v_full[st], kTile8);
-                    tma_load_4d(s.vt[st], &tmvt, &s.v_full[st], j * BN, 0, w.g, w.sv.tma_b);
+                    const int sv = gt % kStagesV;
+                    if (!(ok = mbar_wait(&s.vin_empty[sv], ((gt / kStagesV) & 1) ^ 1, ab))) break;
+                    mbar_expect_tx(&s.vin_full[sv], kTile8);
+                    tma_load_4d(s.v[sv], &tmv, &s.vin_full[sv], 0, w.g, j * BN, w.sv.tma_b);
                     ++v_issued;
                 }
             }
-            for (int back = 1; back <= kStages8; ++back) {
+            for (int back = 1; back <= kStagesK; ++back) {
                 if (k_issued - back >= 0) {
                     const int i2 = k_issued - back;
-                    mbar_wait_quiet(&s.k_full[i2 % kStages8], (i2 / kStages8) & 1);
+                    mbar_wait_quiet(&s.k_full[i2 % kStagesK], (i2 / kStagesK) & 1);
                 }
+            }
+            for (int back = 1; back <= kStagesV; ++back) {
                 if (v_issued - back >= 0) {
                     const int i2 = v_issued - back;
-                    mbar_wait_quiet(&s.v_full[i2 % kStages8], (i2 / kStages8) & 1);
+                    mbar_wait_quiet(&s.vin_full[i2 % kStagesV], (i2 / kStagesV) & 1);
                 }
             }
             if (n_q > 0) mbar_wait_quiet(&s.q_full, (n_q - 1) & 1);
@@ -235,8 +246,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
                 tc_fence_after();
                 // prologue: S for the item's first key tile
                 {
-                    const int st0 = gt % kStages8;
-                    if (ok && (ok = mbar_wait(&s.k_full[st0], (gt / kStages8) & 1, ab))) {
+                    const int st0 = gt % kStagesK;
+                    if (ok && (ok = mbar_wait(&s.k_full[st0], (gt / kStagesK) & 1, ab))) {
                         tc_fence_after();
                         const uint64_t kd0 = kd_base + (uint64_t)(st0 * kStep);
                         for (int k = 0; ok && k < 2; ++k)
@@ -249,8 +260,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
                 for (int j = u0; ok && j < u1; ++j, ++it) {
                     // S for key tile j + 1 first: the softmax can go on while P V of tile j runs
                     if (j + 1 < u1) {
-                        const int st1 = (it + 1) % kStages8;
-                        if (!(ok = mbar_wait(&s.k_full[st1], ((it + 1) / kStages8) & 1, ab))) break;
+                        const int st1 = (it + 1) % kStagesK;
+                        if (!(ok = mbar_wait(&s.k_full[st1], ((it + 1) / kStagesK) & 1, ab))) break;
                         tc_fence_after();
                         const uint64_t kd1 = kd_base + (uint64_t)(st1 * kStep);
                         for (int k = 0; ok && k < 2; ++k)
@@ -259,8 +270,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
                         if (j + 2 == u1) tc_commit(&s.q_empty);  // the item's last S
                         tc_commit(&s.k_empty[st1]);
                     }
-                    const int st = it % kStages8;
-                    if (!(ok = mbar_wait(&s.v_full[st], (it / kStages8) & 1, ab))) break;
+                    const int st = it % kStagesVt;
+                    if (!(ok = mbar_wait(&s.v_full[st], (it / kStagesVt) & 1, ab))) break;
                     const uint64_t vd = vd_base + (uint64_t)(st * kStep);
                     for (int k = 0; ok && k < 2; ++k) {
                         if (j < t0[k] || j >= t1[k]) continue;
@@ -286,9 +297,35 @@ __global__ void __launch_bounds__(kThreads8, 1)
             tc_commit(&s.drain);
             mbar_wait_quiet(&s.drain, 0);
         }
+    } else {
+        // ================= V transpose (warps 2, 3) =================
+        const int wt = warp - 2;
+        int gt = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x, step = first_step(a.snake); ok && idx < a.n_items;
+             idx += step, step = 2 * (int)gridDim.x - step) {
+            const FwdItem w = fwd_item(a, idx);
+            if (!w.live || w.u1 <= w.u0) continue;
+            for (int j = w.u0; j < w.u1; ++j, ++gt) {
+                const int sv = gt % kStagesV, st = gt % kStagesVt;
+                {
+                    // the V tile has landed, and the P V that read this V^T slot last is done
+                    bool wv = mbar_wait(&s.vin_full[sv], (gt / kStagesV) & 1, ab);
+                    wv = wv && mbar_wait(&s.v_empty[st], ((gt / kStagesVt) & 1) ^ 1, ab);
+                    if (!__all_sync(0xffffffffu, wv)) { ok = false; break; }
+                }
+                transpose_v_tile(s.v[sv], s.vt[st], wt, lane);
+                fence_proxy_async_smem();  // the V^T words, for the tensor core's reads
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&s.vin_empty[sv]);
+                    mbar_arrive(&s.v_full[st]);
+                }
+            }
+        }
     }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
         // ================= softmax: one thread per row =================
         const int k = (warp - 4) >> 2;           // query tile
         const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
@@ -508,21 +545,13 @@ __global__ void __launch_bounds__(kThreads8, 1)
 
 }  // namespace
 
-cudaError_t launch_fwd_e4m3(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+cudaError_t launch_fwd_e4m3(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             cudaStream_t st) {
     const size_t smem = sizeof(Smem8) + 1024;
     cudaError_t e = cudaFuncSetAttribute(fwd_e4m3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (a.n_items <= 0 || a.n_ctas <= 0) return cudaSuccess;
-    fwd_e4m3_kernel<<<(unsigned)a.n_ctas, kThreads8, smem, st>>>(a, tq, tk, tvt);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_v_e4m3(const uint8_t* v, uint8_t* vt, int B, int s_kv, int h_kv, int s_pad,
-                                    cudaStream_t st) {
-    if (B <= 0 || s_pad <= 0) return cudaSuccess;
-    dim3 grid((unsigned)cdiv(s_pad, 128), (unsigned)h_kv, (unsigned)B);
-    transpose_v_kernel<<<grid, 128, 0, st>>>(v, vt, s_kv, h_kv, s_pad);
+    fwd_e4m3_kernel<<<(unsigned)a.n_ctas, kThreads8, smem, st>>>(a, tq, tk, tv);
     return cudaGetLastError();
 }
 

@@ -130,11 +130,8 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMa
                        cudaStream_t st);
 cudaError_t launch_fwd256(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t st);
-cudaError_t launch_fwd_e4m3(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+cudaError_t launch_fwd_e4m3(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             cudaStream_t st);
-// V [B, s_kv, h_kv, 128] e4m3 -> V^T [B, h_kv, 128, s_pad] (keys innermost, zero past s_kv)
-cudaError_t launch_transpose_v_e4m3(const uint8_t* v, uint8_t* vt, int B, int s_kv, int h_kv, int s_pad,
-                                    cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 int decode_rows_max(int d);                // query rows per key/value head the decode kernel takes

@@ -98,8 +98,8 @@
  * product, o is written as bf16 and lse (fp32) is that of the descaled problem.  Dense
  * tensors with d = 128 only (no cu_seqlens, no block_table; seqused_k, windows, causal and
  * sinks are supported); anything else returns FA_ERR_UNSUPPORTED, and fa_bwd rejects the
- * type.  The workspace also holds a transposed copy of v (h_kv * 128 bytes per key, keys
- * padded to 16).
+ * type.  The workspace is the bf16 forward's for the same shape (v is transposed tile by
+ * tile inside the kernel, not copied).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H

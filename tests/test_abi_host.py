@@ -188,11 +188,13 @@ def test_e4m3_forward_rejects(kw, code):
 
 
 def test_e4m3_workspace_and_backward():
-    # the forward's workspace holds V^T: B * h_kv * 128 bytes per key, keys padded to 16
+    # V is transposed tile by tile inside the kernel: the workspace is the bf16 forward's
+    # (the status word alone without key splits, plus the partials with them)
+    for kw in (dict(B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=128), dict(B=1, s_q=64, s_kv=32768, h_q=4, h_kv=1, d=128)):
+        assert fa.fa_fwd_workspace_size(params(dtype=fa.FA_DTYPE_E4M3, **kw)) == fa.fa_fwd_workspace_size(params(**kw))
     p = params(dtype=fa.FA_DTYPE_E4M3, B=2, s_q=300, s_kv=300, h_q=4, h_kv=2, d=128)
-    s_pad = -(-300 // 16) * 16
-    assert fa.fa_fwd_workspace_size(p) == 256 + (2 * 2 * 128 * s_pad + 255) // 256 * 256
-    assert call_fwd(p, ws_bytes=300) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_fwd_workspace_size(p) == 256
+    assert call_fwd(p, ws_bytes=100) == fa.FA_ERR_WORKSPACE
     assert call_bwd(p) == fa.FA_ERR_UNSUPPORTED
 
 
