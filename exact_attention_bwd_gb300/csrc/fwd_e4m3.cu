@@ -178,14 +178,16 @@ __global__ void __launch_bounds__(kThreads8, 1)
                 ++n_q;
                 for (int j = w.u0; j < w.u1; ++j, ++gt) {
                     const int st = gt % kStagesK;
+                    int row, outer;  // the key tile's map coordinates (dense or packed)
+                    kv_tile_coord(p, w.sv, j * BN, row, outer);
                     if (!(ok = mbar_wait(&s.k_empty[st], ((gt / kStagesK) & 1) ^ 1, ab))) break;
                     mbar_expect_tx(&s.k_full[st], kTile8);
-                    tma_load_4d(s.k[st], &tmk, &s.k_full[st], 0, w.g, j * BN, w.sv.tma_b);
+                    tma_load_4d(s.k[st], &tmk, &s.k_full[st], 0, w.g, row, outer);
                     ++k_issued;
                     const int sv = gt % kStagesV;
                     if (!(ok = mbar_wait(&s.vin_empty[sv], ((gt / kStagesV) & 1) ^ 1, ab))) break;
                     mbar_expect_tx(&s.vin_full[sv], kTile8);
-                    tma_load_4d(s.v[sv], &tmv, &s.vin_full[sv], 0, w.g, j * BN, w.sv.tma_b);
+                    tma_load_4d(s.v[sv], &tmv, &s.vin_full[sv], 0, w.g, row, outer);
                     ++v_issued;
                 }
             }

@@ -95,10 +95,10 @@
  * element, same layouts) and the true inputs are q * q_descale[b * h_kv + g] (likewise k,
  * v) for batch b and key/value head g; a NULL descale means 1.  S = Q K^T and O = P V run
  * on the fp8 tensor cores with fp32 accumulation, P is rounded to e4m3 for the second
- * product, o is written as bf16 and lse (fp32) is that of the descaled problem.  Dense
- * tensors with d = 128 only (no cu_seqlens, no block_table; seqused_k, windows, causal and
- * sinks are supported); anything else returns FA_ERR_UNSUPPORTED, and fa_bwd rejects the
- * type.  The workspace is the bf16 forward's for the same shape (v is transposed tile by
+ * product, o is written as bf16 and lse (fp32) is that of the descaled problem.  d = 128
+ * only, dense or packed (cu_seqlens; the descale index b is then the sequence), no
+ * block_table; seqused_k, windows, causal and sinks are supported; anything else returns
+ * FA_ERR_UNSUPPORTED, and fa_bwd rejects the type.  The workspace is the bf16 forward's for the same shape (v is transposed tile by
  * tile inside the kernel, not copied).
  */
 #ifndef FA_GB300_H

@@ -155,3 +155,47 @@ def test_fp8_cache_shape_sampled():
         ro, rl, emu = reference(sub)
         judge(o[b:b + 1], ro, emu)
         check_lse("LSE", lse[b:b + 1], rl)
+
+
+PACKED = [
+    dict(lq=[300, 0, 129, 1, 1000, 64], causal=True, sinks=True),
+    dict(lq=[100, 250, 17], lk=[300, 250, 40], causal=True, window=(64, 0)),
+    dict(lq=[2000, 3, 700], causal=False, window=(100, 30), h_q=16, h_kv=2),
+]
+
+
+@pytest.mark.parametrize("i", range(len(PACKED)))
+def test_fp8_packed_batch(i):
+    """Packed batches (cu_seqlens; empty and one-token sequences, s_q != s_kv per sequence):
+    each sequence against the oracle and the emulation run on it alone, judged together."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    kw = dict(PACKED[i])
+    lq = np.asarray(kw.pop("lq"))
+    lk = np.asarray(kw.pop("lk", lq))
+    B = len(lq)
+    c = case(60 + i, B=B, s_q=int(lq.max()), s_kv=int(lk.max()), **kw)
+    cu_q, cu_k = inputs.cu_seqlens(lq), inputs.cu_seqlens(lk)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    pack = lambda x, n: np.concatenate([x[b, :n[b]] for b in range(B)])  # noqa: E731
+    q, k, v = dev(pack(c["q"], lq)), dev(pack(c["k"], lk)), dev(pack(c["v"], lk))
+    tcq = dev(cu_q)
+    tck = tcq if np.array_equal(cu_q, cu_k) else dev(cu_k)
+    o, lse, ws = fa.forward(q, k, v, causal=c["causal"], window=c["window"], softmax_scale=c["scale"],
+                            sinks=None if c["sinks"] is None else dev(c["sinks"]), cu_q=tcq, cu_k=tck,
+                            descale=tuple(dev(x) for x in c["descale"]))
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK
+    o, lse = from_dev(o), lse.cpu().numpy().astype(np.float64)
+    got, ref, emu = [], [], []
+    for b in range(B):
+        if lq[b] == 0:
+            continue
+        sub = dict(c, B=1, s_q=int(lq[b]), s_kv=int(lk[b]), q=c["q"][b:b + 1, :lq[b]], k=c["k"][b:b + 1, :lk[b]],
+                   v=c["v"][b:b + 1, :lk[b]], descale=tuple(x.reshape(B, -1)[b:b + 1].ravel() for x in c["descale"]))
+        ro, rl, em = reference(sub)
+        got.append(o[cu_q[b]:cu_q[b + 1]])
+        ref.append(ro[0])
+        emu.append(em[0])
+        check_lse(f"LSE sequence {b}", lse[None, :, cu_q[b]:cu_q[b + 1]], rl)
+    judge(np.concatenate(got), np.concatenate(ref), np.concatenate(emu))
