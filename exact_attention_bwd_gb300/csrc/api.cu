@@ -139,8 +139,8 @@ fa_status normalise(const fa_params* in, Problem& p) {
     if (a.window_left < -1 || a.window_right < -1) return FA_ERR_INVALID_ARG;
     if (a.d % 8 != 0 || a.d > 256) return FA_ERR_UNSUPPORTED;
     if (a.dtype != FA_DTYPE_BF16 && a.dtype != FA_DTYPE_F16 && a.dtype != FA_DTYPE_E4M3) return FA_ERR_INVALID_ARG;
-    // e4m3: d = 128, dense or packed (no paged cache)
-    if (a.dtype == FA_DTYPE_E4M3 && (a.d != 128 || a.block_table)) return FA_ERR_UNSUPPORTED;
+    // e4m3: d = 128 (dense, packed or a paged cache)
+    if (a.dtype == FA_DTYPE_E4M3 && a.d != 128) return FA_ERR_UNSUPPORTED;
     std::memset(&p, 0, sizeof(p));
     p.B = a.B;
     p.s_q = a.s_q;
@@ -514,13 +514,13 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     FwdArgs a{};
     CUtensorMap tq;
     if (p.dtype == FA_DTYPE_E4M3) {
-        // Q, K, V: [b][s][h][128] bytes, or [1][T][h][128] packed (the kernel transposes each
-        // V tile in shared memory)
+        // Q, K, V: [b][s][h][128] bytes, [1][T][h][128] packed, or K, V a page pool
+        // [num_pages][page_size][h_kv][128] (the kernel transposes each V tile in shared memory)
         const cuuint64_t dq[4] = {128, (cuuint64_t)p.h_q, (cuuint64_t)tokens_q, (cuuint64_t)bdim};
         const cuuint64_t sq[3] = {128, (cuuint64_t)p.h_q * 128, (cuuint64_t)tokens_q * p.h_q * 128};
         const cuuint32_t bq[4] = {128, (cuuint32_t)p.G, (cuuint32_t)p.P, 1};
-        const cuuint64_t dk[4] = {128, (cuuint64_t)p.h_kv, (cuuint64_t)tokens_k, (cuuint64_t)bdim};
-        const cuuint64_t sk[3] = {128, (cuuint64_t)p.h_kv * 128, (cuuint64_t)tokens_k * p.h_kv * 128};
+        const cuuint64_t dk[4] = {128, (cuuint64_t)p.h_kv, (cuuint64_t)kv_rows, (cuuint64_t)kv_outer};
+        const cuuint64_t sk[3] = {128, (cuuint64_t)p.h_kv * 128, (cuuint64_t)kv_rows * p.h_kv * 128};
         const cuuint32_t bk[4] = {128, 1, 128, 1};
         CUtensorMap tk8, tv8;
         if (!encode_u8_4d(&tq, q, dq, sq, bq) || !encode_u8_4d(&tk8, k, dk, sk, bk) || !encode_u8_4d(&tv8, v, dk, sk, bk))

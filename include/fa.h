@@ -96,9 +96,9 @@
  * v) for batch b and key/value head g; a NULL descale means 1.  S = Q K^T and O = P V run
  * on the fp8 tensor cores with fp32 accumulation, P is rounded to e4m3 for the second
  * product, o is written as bf16 and lse (fp32) is that of the descaled problem.  d = 128
- * only, dense or packed (cu_seqlens; the descale index b is then the sequence), no
- * block_table; seqused_k, windows, causal and sinks are supported; anything else returns
- * FA_ERR_UNSUPPORTED, and fa_bwd rejects the type.  The workspace is the bf16 forward's for the same shape (v is transposed tile by
+ * only, dense, packed (cu_seqlens; the descale index b is then the sequence) or with a
+ * paged k / v cache; seqused_k, windows, causal and sinks are supported; anything else
+ * returns FA_ERR_UNSUPPORTED, and fa_bwd rejects the type.  The workspace is the bf16 forward's for the same shape (v is transposed tile by
  * tile inside the kernel, not copied).
  */
 #ifndef FA_GB300_H

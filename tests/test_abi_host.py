@@ -178,19 +178,21 @@ def test_deterministic_workspace():
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=fa.FA_DTYPE_E4M3, d=64), fa.FA_ERR_UNSUPPORTED),        # e4m3: d = 128 only
     (dict(dtype=fa.FA_DTYPE_E4M3, d=256), fa.FA_ERR_UNSUPPORTED),
-    (dict(dtype=fa.FA_DTYPE_E4M3, block_table=0x4000, page_size=128, max_blocks_per_seq=2, num_pages=4),
-     fa.FA_ERR_UNSUPPORTED),
     (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
 ])
 def test_e4m3_forward_rejects(kw, code):
     assert call_fwd(params(**kw)) == code
 
 
-def test_e4m3_packed_is_planned():
-    # packed e4m3 batches are planned like bf16 ones, without token tiles
+def test_e4m3_packed_and_paged_are_planned():
+    # packed e4m3 batches are planned like bf16 ones, without token tiles; paged caches too
     p = params(dtype=fa.FA_DTYPE_E4M3, B=3, s_q=700, s_kv=700, cu_seqlens_q=0x2000, cu_seqlens_k=0x2000)
     assert fa.fa_fwd_workspace_size(p) > 0
     assert call_bwd(p) == fa.FA_ERR_UNSUPPORTED
+    kw = dict(B=2, s_q=64, s_kv=1000, block_table=0x4000, page_size=256, max_blocks_per_seq=4, num_pages=8)
+    assert fa.fa_fwd_workspace_size(params(dtype=fa.FA_DTYPE_E4M3, **kw)) == fa.fa_fwd_workspace_size(params(**kw))
+    bad = dict(kw, page_size=64)
+    assert fa.fa_fwd_workspace_size(params(dtype=fa.FA_DTYPE_E4M3, **bad)) == 0
 
 
 def test_e4m3_workspace_and_backward():

@@ -199,3 +199,39 @@ def test_fp8_packed_batch(i):
         emu.append(em[0])
         check_lse(f"LSE sequence {b}", lse[None, :, cu_q[b]:cu_q[b + 1]], rl)
     judge(np.concatenate(got), np.concatenate(ref), np.concatenate(emu))
+
+
+@pytest.mark.parametrize("s_q,used", [(1, False), (64, True)])
+def test_fp8_paged_cache(s_q, used):
+    """A paged e4m3 cache (256-key pages in a seeded order, spare pages in the pool, a
+    logical length that is not a multiple of the page size): the same bits as the dense
+    cache (same kernel, same tile order), and the oracle by the same rule."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    B, s_kv, ps = 3, 1000, 256
+    c = case(70 + s_q, B=B, s_q=s_q, s_kv=s_kv, h_q=8, h_kv=2, causal=True, used=used)
+    mb = -(-s_kv // ps)
+    n_pages = B * mb + 3
+    table = inputs.page_table(inputs.seed_of(WID, 70 + s_q, 20), B, mb, n_pages)
+
+    def pool_of(x):
+        pool = np.zeros((n_pages, ps, c["h_kv"], 128), np.uint8)
+        for b in range(B):
+            for blk in range(mb):
+                seg = x[b, blk * ps:(blk + 1) * ps]
+                pool[table[b, blk], :seg.shape[0]] = seg
+        return pool
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    kw = dict(causal=True, window=c["window"], softmax_scale=c["scale"], descale=tuple(dev(x) for x in c["descale"]),
+              seqused_k=None if c["used"] is None else dev(c["used"]))
+    q = dev(c["q"])
+    o_p, lse_p, ws = fa.forward(q, dev(pool_of(c["k"])), dev(pool_of(c["v"])), block_table=dev(table), s_kv=s_kv,
+                                **kw)
+    o_d, lse_d, ws2 = fa.forward(q, dev(c["k"]), dev(c["v"]), **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK and fa.device_status(ws2) == fa.FA_OK
+    assert torch.equal(o_p.view(torch.int16), o_d.view(torch.int16))
+    assert torch.equal(lse_p.view(torch.int32), lse_d.view(torch.int32))
+    ro, rl, emu = reference(c)
+    judge(from_dev(o_p), ro, emu)
+    check_lse("LSE", lse_p.cpu().numpy().astype(np.float64), rl)
