@@ -235,3 +235,34 @@ def test_fp8_paged_cache(s_q, used):
     ro, rl, emu = reference(c)
     judge(from_dev(o_p), ro, emu)
     check_lse("LSE", lse_p.cpu().numpy().astype(np.float64), rl)
+
+
+def test_fp8_seqused_q_and_k():
+    """Partly filled query and key slots (seqused_q, seqused_k; a slot with no queries): the
+    used rows of each batch entry against the oracle and the emulation on the used part
+    alone (bottom-right alignment follows the used counts)."""
+    import torch
+    from exact_attention_bwd_gb300 import binding as fa
+    B = 3
+    c = case(80, B=B, s_q=64, s_kv=1000, h_q=8, h_kv=2, causal=True)
+    used_q = np.array([64, 10, 0], np.int32)
+    used_k = np.array([1000, 500, 300], np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    o, lse, ws = fa.forward(dev(c["q"]), dev(c["k"]), dev(c["v"]), causal=True, softmax_scale=c["scale"],
+                            descale=tuple(dev(x) for x in c["descale"]), seqused_q=dev(used_q), seqused_k=dev(used_k))
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK
+    o, lse = from_dev(o), lse.cpu().numpy().astype(np.float64)
+    got, ref, emu = [], [], []
+    for b in range(B):
+        if used_q[b] == 0:
+            continue
+        sub = dict(c, B=1, s_q=int(used_q[b]), s_kv=int(used_k[b]), q=c["q"][b:b + 1, :used_q[b]],
+                   k=c["k"][b:b + 1, :used_k[b]], v=c["v"][b:b + 1, :used_k[b]],
+                   descale=tuple(x.reshape(B, -1)[b:b + 1].ravel() for x in c["descale"]))
+        ro, rl, em = reference(sub)
+        got.append(o[b, :used_q[b]])
+        ref.append(ro[0])
+        emu.append(em[0])
+        check_lse(f"LSE[{b}]", lse[b:b + 1, :, :used_q[b]], rl)
+    judge(np.concatenate(got), np.concatenate(ref), np.concatenate(emu))
