@@ -115,6 +115,8 @@ CASES = [
     dict(B=2, s_q=1, s_kv=3000, causal=True),       # decode shape: split keys
     dict(B=1, s_q=64, s_kv=2100, causal=True),      # chunked prefill: split keys
     dict(B=3, s_q=64, s_kv=1000, causal=True, used=True),
+    dict(B=2, s_q=1, s_kv=3000, causal=True, sinks=True, h_q=16, h_kv=2),  # split keys, sinks in the combine
+    dict(B=1, s_q=64, s_kv=2100, causal=False, window=(500, 0), sinks=True),
 ]
 
 
