@@ -273,11 +273,16 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
         // few queries against a long key range: every query block does about the same work,
         // so launch the blocks of one (batch, kv head) together and let them share K/V in L2
         pl.unit_major = (p.s_q * 4 <= p.s_kv) ? 1 : 0;
-        // Tail split (d = 192 / 256: one CTA per item, one CTA per SM).  Such items all take
-        // about as long, so a last partial wave of CTAs leaves the other SMs idle for a
-        // whole item; the last units' items are cut into k key ranges instead (k chosen so
-        // that the pieces fill the last wave best) and their rows merged by the combine.
-        if (p.d >= 192 && pl.n_splits == 1 && pl.unit_major && p.left < 0 && tiles >= 64) {
+        // Tail split.  Where every item takes about as long (few queries against a long key
+        // range), a last partial round of items leaves the other SMs idle for a whole item;
+        // the last units' items are cut into k key ranges instead (k chosen so that the
+        // pieces fill the last round best) and their rows merged by the combine.  d = 192 /
+        // 256 (one CTA per item and per SM) takes it in place of no split; d <= 128 (the
+        // persistent kernel, bf16 / fp16) in place of splitting every unit's keys, when it is
+        // as short, since only the tail's rows then go through the fp32 partials.
+        const bool wide = p.d >= 192;
+        const bool tail_ok = wide ? pl.n_splits == 1 : (pl.n_splits > 1 && p.dtype != FA_DTYPE_E4M3);
+        if (tail_ok && pl.unit_major && p.left < 0 && tiles >= (wide ? 64 : 8)) {
             const long units = (long)p.h_kv * p.B, items = units * pl.n_blocks, slots = sm_count();
             const long rem = items % slots;
             if (items > slots && rem > 0) {
@@ -293,7 +298,15 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
                         best_k = k;
                     }
                 }
-                if (best_k > 1 && best <= 0.8) {
+                bool take = best_k > 1 && best <= 0.8;
+                if (take && !wide) {
+                    // against every unit split n_splits ways: ceil(n items / slots) / n items
+                    const double full = (double)((pl.n_splits * items + slots - 1) / slots) / pl.n_splits;
+                    take = (double)((items - tail + slots - 1) / slots) + best <= full + 1e-9;
+                }
+                if (take) {
+                    pl.n_splits = 1;
+                    pl.split_tiles = 0;
                     pl.tail_units = (int)tail_units;
                     pl.tail_k = best_k;
                     pl.tail_split_tiles = (tiles + best_k - 1) / best_k;
@@ -545,7 +558,8 @@ fa_status fa_fwd(const fa_params* in, const void* q, const void* k, const void* 
     a.tail_item0 = pl.tail_k > 1 ? (p.h_kv * p.B - pl.tail_units) * pl.n_blocks : 0;
     a.tail_row0 = pl.tail_k > 1 ? (long)(p.h_kv * p.B - pl.tail_units) * p.G * p.s_q : 0;
     {
-        const long items = p.cu_q ? (long)pl.n_blocks * p.h_kv : (long)pl.n_blocks * pl.n_splits * p.h_kv * p.B;
+        long items = p.cu_q ? (long)pl.n_blocks * p.h_kv : (long)pl.n_blocks * pl.n_splits * p.h_kv * p.B;
+        if (pl.tail_k > 1) items = a.tail_item0 + (items - a.tail_item0) * pl.tail_k;  // the tail's pieces
         const long slots = (long)sm_count() * (pl.kt == 64 ? 2 : 1);
         a.n_items = (int)items;
         a.n_ctas = (int)(items < slots ? items : slots);

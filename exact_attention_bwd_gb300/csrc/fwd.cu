@@ -83,6 +83,7 @@ struct FwdCfg {
 struct ItemInfo {
     int idx, end;       // item index; end = 1: no more items for this CTA
     int g, split, b;    // key/value head, key split, batch or sequence
+    int tail;           // 1: a tail-split piece (rows to the partials from tail_row0 on)
     int q0, k0, tma_b;  // first query / key row of the sequence, outer TMA coordinate
     int u0, u1;         // union key-tile range of the two tiles (u1 <= u0: none)
     int s0[2], t0[2], t1[2];  // first query position and key-tile range of each tile
@@ -433,6 +434,7 @@ __global__ void __launch_bounds__(kThreadsFwd, FwdCfg<D, KT>::CTAS_PER_SM)
                 it.end = 0;
                 it.g = w.g;
                 it.split = w.split;
+                it.tail = w.tail ? 1 : 0;
                 it.b = w.sv.b;
                 it.q0 = w.sv.q0;
                 it.k0 = w.sv.k0;
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(kThreadsFwd, FwdCfg<D, KT>::CTAS_PER_SM)
             ok = __all_sync(0xffffffffu, wt);
             tc_fence_after();
         }
-        const bool split_mode = a.n_splits > 1;
+        const bool split_mode = a.n_splits > 1 || itm.tail;
         // 32-byte stores where the base allows (the rows, 128 or more bytes, keep the alignment)
         const bool o_al32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
         const bool part_al32 = (reinterpret_cast<uintptr_t>(a.o_part) & 31u) == 0;
@@ -616,8 +618,11 @@ __global__ void __launch_bounds__(kThreadsFwd, FwdCfg<D, KT>::CTAS_PER_SM)
             oscale = 1.f / l;
             lse = (m_used + log2f(l)) * kLn2;
         }
-        const long nrows = (long)p.B * p.h_q * p.s_q;
-        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;  // split-mode row (dense only)
+        // split-mode rows (dense only): all B h_q s_q rows, or (tail split) those from
+        // tail_row0 on
+        const long row_base = itm.tail ? a.tail_row0 : 0;
+        const long nrows = (long)p.B * p.h_q * p.s_q - row_base;
+        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i - row_base;
         if (row_valid) {
             if (!split_mode) {
                 if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;

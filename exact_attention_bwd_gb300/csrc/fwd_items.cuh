@@ -26,6 +26,7 @@ struct FwdItem {
     TileInfo ti[2];
     int u0, u1;  // union key-tile range of the two tiles
     bool live;   // false for an idle block of a packed batch
+    bool tail;   // a piece of a tail-split unit: its rows go to the partials
 };
 
 __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx, int bn = BN) {
@@ -33,6 +34,7 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx, int bn = 
     FwdItem w;
     int seq, blk;
     w.split = 0;
+    w.tail = false;
     if (p.cu_q && a.tokens) {
         // token tiles: query tile k of block blk holds packed rows [(2 blk + k) P, + P), whatever
         // sequences they belong to; key coordinates are packed rows too.  The key-tile ranges
@@ -51,7 +53,19 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx, int bn = 
         w.live = blk * 2 * p.P < p.T_q;
         return w;
     }
-    if (p.cu_q) {
+    if (a.tail_k > 1 && idx >= a.tail_item0) {
+        // tail split (dense, unit-major): the last units' items, each cut into tail_k key
+        // ranges, numbered unit by unit after the whole items
+        const int t = idx - a.tail_item0;
+        const int per_unit = a.n_blocks * a.tail_k;
+        const int unit = a.tail_item0 / a.n_blocks + t / per_unit;
+        const int x = t % per_unit;
+        w.g = unit % p.h_kv;
+        seq = unit / p.h_kv;
+        w.split = x % a.tail_k;
+        blk = a.n_blocks - 1 - x / a.tail_k;
+        w.tail = true;
+    } else if (p.cu_q) {
         w.g = idx % p.h_kv;
         const int bs = 2 * p.P;
         blk = idx / p.h_kv;
@@ -78,9 +92,10 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int idx, int bn = 
         const int i1 = min(w.ti[k].s0 + p.P, w.sv.nq) - 1;
         if (w.ti[k].active) {
             kv_tile_range(w.band, w.ti[k].s0, i1, bn, w.ti[k].t0, w.ti[k].t1);
-            if (a.n_splits > 1) {
-                w.ti[k].t0 = max(w.ti[k].t0, w.split * a.split_tiles);
-                w.ti[k].t1 = min(w.ti[k].t1, (w.split + 1) * a.split_tiles);
+            if (a.n_splits > 1 || w.tail) {
+                const int st = w.tail ? a.tail_split_tiles : a.split_tiles;
+                w.ti[k].t0 = max(w.ti[k].t0, w.split * st);
+                w.ti[k].t1 = min(w.ti[k].t1, (w.split + 1) * st);
                 if (w.ti[k].t1 < w.ti[k].t0) w.ti[k].t1 = w.ti[k].t0;
             }
         } else {
