@@ -278,10 +278,10 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
         // the last units' items are cut into k key ranges instead (k chosen so that the
         // pieces fill the last round best) and their rows merged by the combine.  d = 192 /
         // 256 (one CTA per item and per SM) takes it in place of no split; d <= 128 (the
-        // persistent kernel, bf16 / fp16) in place of splitting every unit's keys, when it is
-        // as short, since only the tail's rows then go through the fp32 partials.
+        // persistent kernels, 16-bit and e4m3) in place of splitting every unit's keys, when it
+        // is as short, since only the tail's rows then go through the fp32 partials.
         const bool wide = p.d >= 192;
-        const bool tail_ok = wide ? pl.n_splits == 1 : (pl.n_splits > 1 && p.dtype != FA_DTYPE_E4M3);
+        const bool tail_ok = wide ? pl.n_splits == 1 : pl.n_splits > 1;
         if (tail_ok && pl.unit_major && p.left < 0 && tiles >= (wide ? 64 : 8)) {
             const long units = (long)p.h_kv * p.B, items = units * pl.n_blocks, slots = sm_count();
             const long rem = items % slots;

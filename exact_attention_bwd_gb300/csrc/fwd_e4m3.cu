@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
             tc_fence_after();
         }
         const float vds = a.v_descale ? a.v_descale[(long)sv.b * p.h_kv + g] : 1.f;
-        const bool split_mode = a.n_splits > 1;
+        const bool split_mode = a.n_splits > 1 || w.tail;
         float oscale = 0.f, lse = -INFINITY;
         if (!split_mode && p.sinks && row_valid) {
             const float s2 = p.sinks[h] * kLog2e;
@@ -485,8 +485,10 @@ __global__ void __launch_bounds__(kThreads8, 1)
             oscale = vds / l;
             lse = (m_used + log2f(l)) * kLn2;
         }
-        const long nrows = (long)p.B * p.h_q * p.s_q;
-        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i;
+        // split-mode rows: all B h_q s_q rows, or (tail split) those from tail_row0 on
+        const long row_base = w.tail ? a.tail_row0 : 0;
+        const long nrows = (long)p.B * p.h_q * p.s_q - row_base;
+        const long prow = ((long)sv.b * p.h_q + h) * p.s_q + i - row_base;
         if (row_valid) {
             if (!split_mode) {
                 if (a.lse) a.lse[lse_index(p, sv, i, h)] = lse;
