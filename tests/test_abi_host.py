@@ -321,3 +321,22 @@ def test_binding_rejects_host_tensors():
         fa.forward(q, q, q)
     with pytest.raises(ValueError, match="CUDA"):
         fa.backward(q, q, q, q, lse, q)
+
+
+def test_tail_split_plans():
+    """The forward planner's tail split, by its workspace (status word + fp32 partials of
+    the tail rows).  Without a device the planner counts 152 SMs, the GB300's count.  The
+    d = 128 chunked-prefill shape (512 items of one unit each, a last round of 56) cuts the
+    last 56 units into 8 key ranges instead of splitting every unit in two; d = 256 (1024
+    items, two per unit, a last wave of 112) cuts the last 56 units into 4; with 8 batch
+    entries (64 items, under one round) every unit's keys stay split (7 ways)."""
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+
+    def ws(d, k, rows):
+        return 256 + al(rows * k * d * 4) + al(rows * k * 4)
+    kw = dict(s_q=64, s_kv=32768, h_q=32, h_kv=8, causal=1)
+    assert fa.fa_fwd_workspace_size(params(B=64, d=128, **kw)) == ws(128, 8, 56 * 4 * 64)
+    assert fa.fa_fwd_workspace_size(params(B=64, d=256, **kw)) == ws(256, 4, 56 * 4 * 64)
+    assert fa.fa_fwd_workspace_size(params(B=8, d=128, **kw)) == ws(128, 7, 8 * 32 * 64)
+    # e4m3 takes the same plans as bf16
+    assert fa.fa_fwd_workspace_size(params(B=64, d=128, dtype=fa.FA_DTYPE_E4M3, **kw)) == ws(128, 8, 56 * 4 * 64)
