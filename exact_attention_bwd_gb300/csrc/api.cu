@@ -278,10 +278,11 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
         // the last units' items are cut into k key ranges instead (k chosen so that the
         // pieces fill the last round best) and their rows merged by the combine.  d = 192 /
         // 256 (one CTA per item and per SM) takes it in place of no split; d <= 128 (the
-        // persistent kernels, 16-bit and e4m3) in place of splitting every unit's keys, when it
-        // is as short, since only the tail's rows then go through the fp32 partials.
+        // persistent kernels, 16-bit and e4m3) in place of splitting every unit's keys when it
+        // is as short (only the tail's rows then go through the fp32 partials), or in place of
+        // no split when it is shorter.
         const bool wide = p.d >= 192;
-        const bool tail_ok = wide ? pl.n_splits == 1 : pl.n_splits > 1;
+        const bool tail_ok = wide ? pl.n_splits == 1 : true;
         if (tail_ok && pl.unit_major && p.left < 0 && tiles >= (wide ? 64 : 8)) {
             const long units = (long)p.h_kv * p.B, items = units * pl.n_blocks, slots = sm_count();
             const long rem = items % slots;
@@ -300,9 +301,13 @@ fa_status plan_fwd(const Problem& p, unsigned flags, FwdPlan& pl) {
                 }
                 bool take = best_k > 1 && best <= 0.8;
                 if (take && !wide) {
-                    // against every unit split n_splits ways: ceil(n items / slots) / n items
-                    const double full = (double)((pl.n_splits * items + slots - 1) / slots) / pl.n_splits;
-                    take = (double)((items - tail + slots - 1) / slots) + best <= full + 1e-9;
+                    // in item-rounds, against every unit split n ways (ceil(n items / slots) / n)
+                    // or against no split (ceil(items / slots))
+                    const double mine = (double)((items - tail + slots - 1) / slots) + best;
+                    if (pl.n_splits > 1)
+                        take = mine <= (double)((pl.n_splits * items + slots - 1) / slots) / pl.n_splits + 1e-9;
+                    else
+                        take = mine < (double)((items + slots - 1) / slots) - 1e-9;
                 }
                 if (take) {
                     pl.n_splits = 1;

@@ -268,3 +268,25 @@ def test_fp8_seqused_q_and_k():
         emu.append(em[0])
         check_lse(f"LSE[{b}]", lse[b:b + 1, :, :used_q[b]], rl)
     judge(np.concatenate(got), np.concatenate(ref), np.concatenate(emu))
+
+
+def test_fp8_tail_split():
+    """B=40 (batch, kv head) units of s_q=64 rows against s_kv=2048 keys: 320 items over the
+    GB300's 152 SMs leave a last round of 16, whose units the planner cuts into key ranges
+    merged by the combine (the tail split).  Units on both sides of the boundary, and the
+    first and last, against the oracle by the same rule."""
+    c = case(90, B=40, s_q=64, s_kv=2048, h_q=32, h_kv=8, causal=True, sinks=True)
+    o, lse = run_gpu(c)
+    got, ref, emu = [], [], []
+    for unit in (0, 303, 304, 319):
+        b, g = divmod(unit, 8)
+        hs = slice(4 * g, 4 * g + 4)
+        sub = dict(c, B=1, h_q=4, h_kv=1, q=c["q"][b:b + 1, :, hs], k=c["k"][b:b + 1, :, g:g + 1],
+                   v=c["v"][b:b + 1, :, g:g + 1], sinks=c["sinks"][hs],
+                   descale=tuple(x.reshape(40, 8)[b:b + 1, g:g + 1].ravel() for x in c["descale"]))
+        ro, rl, em = reference(sub)
+        got.append(o[b:b + 1, :, hs])
+        ref.append(ro)
+        emu.append(em)
+        check_lse(f"LSE unit {unit}", lse[b:b + 1, hs], rl)
+    judge(np.concatenate(got), np.concatenate(ref), np.concatenate(emu))

@@ -197,12 +197,14 @@ def test_decode_full(d, s_q):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("d,sinks", [(256, False), (256, True), (192, False)])
-def test_wide_head_tail_split(d, sinks):
-    """B=40, h_q=32, h_kv=8, s_q=64, s_kv=4096 causal cache at d = 192 / 256: 640 one-CTA
-    items over the GB300's 152 SMs leave a last wave of 32; the planner then cuts the last
-    16 (batch, kv head) units' items into key ranges merged by the combine (the tail split).
-    Whole units on both sides of that boundary, and the first and last, against the oracle."""
+@pytest.mark.parametrize("d,sinks", [(256, False), (256, True), (192, False), (128, True), (64, False)])
+def test_tail_split(d, sinks):
+    """B=40, h_q=32, h_kv=8, s_q=64, s_kv=4096 causal cache: at d = 192 / 256, 640 one-CTA
+    items over the GB300's 152 SMs leave a last wave of 32; at d = 64 / 128 (the persistent
+    kernel, one item per unit), 320 items leave a last round of 16.  The planner then cuts
+    the last 16 (batch, kv head) units' items into key ranges merged by the combine (the
+    tail split).  Whole units on both sides of that boundary, and the first and last,
+    against the oracle."""
     import torch
     from exact_attention_bwd_gb300 import binding as fa
     B, s_q, s_kv, h_q, h_kv = 40, 64, 4096, 32, 8
