@@ -338,5 +338,12 @@ def test_tail_split_plans():
     assert fa.fa_fwd_workspace_size(params(B=64, d=128, **kw)) == ws(128, 8, 56 * 4 * 64)
     assert fa.fa_fwd_workspace_size(params(B=64, d=256, **kw)) == ws(256, 4, 56 * 4 * 64)
     assert fa.fa_fwd_workspace_size(params(B=8, d=128, **kw)) == ws(128, 7, 8 * 32 * 64)
+    # no key split planned (B=40 against 4096 keys: 320 items, a last round of 16): the last
+    # 16 units are cut 8 ways (2 + 1/8 rounds instead of 3), at d = 64 and 128
+    kw40 = dict(B=40, s_q=64, s_kv=4096, h_q=32, h_kv=8, causal=1)
+    for d in (64, 128):
+        assert fa.fa_fwd_workspace_size(params(d=d, **kw40)) == ws(d, 8, 16 * 4 * 64)
+    # the headline shape (no split, no tail): the status word alone
+    assert fa.fa_fwd_workspace_size(params(B=2, s_q=8192, s_kv=8192, h_q=16, h_kv=16, d=128, causal=1)) == 256
     # e4m3 takes the same plans as bf16
     assert fa.fa_fwd_workspace_size(params(B=64, d=128, dtype=fa.FA_DTYPE_E4M3, **kw)) == ws(128, 8, 56 * 4 * 64)
